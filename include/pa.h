@@ -1,0 +1,217 @@
+/*
+ * pa.h -- C ABI of the GB300 paged-KV step library (libpa.so).
+ *
+ * One continuous-batching engine step, data plane only, as traced on the
+ * page "vLLM 推理流程分析" (§5.1.2 _prepare_inputs, §6.1-6.3 attention dispatch,
+ * FlashAttention path and KV-cache write):
+ *
+ *   pa_plan          host: validate the step's metadata and build the work
+ *                    decomposition every layer of the step reuses;
+ *   pa_slot_mapping  device: slot of every scheduled token;
+ *   pa_write_kv      device: scatter the new K/V rows into the paged caches;
+ *   pa_attention     device: causal GQA attention of every scheduled query
+ *                    token over its request's context, read through the block
+ *                    table; decode rows, chunked-prefill/extend rows, prefix
+ *                    hits and the shared-prefix (cascade) route.
+ *
+ * Data types: every tensor element is IEEE bfloat16, passed as raw 16-bit
+ * patterns; metadata is int32 except slot_mapping (int64).  All layouts are
+ * dense row-major:
+ *   q, out              [T][Hq][D]
+ *   key, value (new)    [T][Hkv][D]
+ *   key_cache,
+ *   value_cache         [num_blocks][block_size][Hkv][D]     (§6.2 layout)
+ *   block_table         [num_reqs][max_blocks_per_req]
+ * T is the number of scheduled tokens of the step (query_start_loc[num_reqs]).
+ * Query head h reads kv head h / (Hq / Hkv).  Query token i of request r is
+ * at absolute position num_computed_tokens[r] + i and attends to keys
+ * 0..position (bottom-right causal alignment).
+ *
+ * Supported: head_dim 64 or 128, block_size 16, Hq % Hkv == 0 with the group
+ * size Hq/Hkv a power of two up to 16, num_blocks * 16 < 2^31.  Other shapes
+ * return PA_ERR_UNSUPPORTED.
+ *
+ * Ownership: the caller allocates and owns every device buffer (q, caches,
+ * block table, out, slot mapping, workspace).  A plan is host memory owned by
+ * the library from pa_plan until pa_plan_destroy.  Device entry points only
+ * enqueue work on the given stream (a cudaStream_t; NULL = the legacy default
+ * stream) and never synchronise, except pa_check_device_errors.  Errors come
+ * back as a status; nothing aborts, traps or throws across the ABI.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARGUMENT = 1,   /* malformed metadata or pointer; nothing enqueued */
+    PA_ERR_UNSUPPORTED = 2,        /* well-formed but outside the supported shapes    */
+    PA_ERR_CUDA = 3,               /* a CUDA runtime call failed                      */
+    PA_ERR_DEVICE_CHECK = 4,       /* a kernel recorded an error in the error word    */
+    PA_ERR_WORKSPACE_TOO_SMALL = 5 /* workspace smaller than pa_plan reported         */
+} pa_status;
+
+/* Bits a kernel may set in the device error word (see pa_check_device_errors). */
+#define PA_DEVERR_SLOT_RANGE   0x1  /* pa_write_kv: slot >= number of cache slots      */
+#define PA_DEVERR_BLOCK_RANGE  0x2  /* pa_attention: block id outside [0, num_blocks)  */
+#define PA_DEVERR_TIMEOUT      0x4  /* a bounded wait inside a kernel gave up          */
+
+typedef struct pa_plan_s pa_plan_t;
+
+/*
+ * The step's metadata, as CommonAttentionMetadata carries it ("vLLM 推理流程分析"
+ * §5.1.3) plus the scheduler's common-prefix count (§4.4).  All arrays are
+ * HOST memory, read during pa_plan only.
+ */
+typedef struct {
+    int32_t num_reqs;              /* R >= 0                                          */
+    int32_t num_heads_q;           /* Hq                                              */
+    int32_t num_heads_kv;          /* Hkv                                             */
+    int32_t head_dim;              /* D: 64 or 128                                    */
+    int32_t block_size;            /* tokens per cache block: 16                      */
+    int32_t num_blocks;            /* physical blocks in each cache                   */
+    int32_t max_blocks_per_req;    /* block_table row stride                          */
+    const int32_t *query_start_loc;      /* [R+1]: 0, then running sums of the
+                                            scheduled token counts (§5.1.2)         */
+    const int32_t *seq_lens;             /* [R]: context length after this step    */
+    const int32_t *num_computed_tokens;  /* [R]: must equal seq_len - q_len          */
+    const int32_t *block_table_host;     /* optional [R][max_blocks_per_req] host
+                                            copy; enables block-id range checks and
+                                            the common-prefix equality check       */
+    int32_t num_common_prefix_blocks;    /* n >= 0: the first n blocks of every
+                                            request with query tokens are the same
+                                            physical blocks and fully computed
+                                            (n*16 <= num_computed_tokens[r]); n > 0
+                                            selects the cascade route              */
+    float softmax_scale;           /* scores are softmax_scale * <q, k>; must be > 0   */
+    int32_t num_sms;               /* SMs to plan for; 0 = query the current device    */
+} pa_batch_desc;
+
+/* Work decomposition of a plan (for tests, benchmarks and launch counts). */
+typedef struct {
+    int32_t num_tokens;            /* T                                               */
+    int32_t num_decode_rows;       /* requests with exactly one query token           */
+    int32_t num_extend_rows;       /* requests with more than one query token         */
+    int32_t num_decode_ctas;       /* persistent CTAs of the split-KV decode kernel   */
+    int32_t num_decode_items;      /* (request, key range, head group) segments       */
+    int32_t num_extend_tiles;      /* 128-row tiles of the tensor-core kernel         */
+    int32_t num_prefix_tiles;      /* of which: shared-prefix (cascade) tiles         */
+    int32_t num_partial_slots;     /* (token, partition) partial results              */
+    int32_t num_merge_rows;        /* tokens whose output is merged from partials     */
+    int32_t kernels_per_call;      /* kernel launches one pa_attention call makes     */
+    int64_t decode_kv_bytes;       /* K+V bytes the decode rows must read             */
+    int64_t prefix_kv_bytes;       /* K+V bytes of the shared prefix (read once)      */
+    double  extend_flops;          /* 4*D*Hq * visible (query, key) pairs, extend     */
+    double  prefix_flops;          /* the same for the shared-prefix tiles            */
+} pa_plan_info;
+
+/*
+ * Validate the step's metadata and build its plan.
+ *   desc              the step (host arrays, read only during this call)
+ *   out               receives the plan on PA_OK (NULL otherwise)
+ *   workspace_bytes   receives the device workspace size pa_attention needs
+ * Returns PA_ERR_INVALID_ARGUMENT for: a NULL pointer, R < 0, non-positive
+ * head counts or num_blocks, Hq % Hkv != 0, query_start_loc[0] != 0 or a
+ * decreasing query_start_loc, num_computed + q_len != seq_len, a context
+ * needing more than max_blocks_per_req blocks, a non-positive or non-finite
+ * softmax_scale, a block id out of range in block_table_host, or a violated
+ * common-prefix precondition.  PA_ERR_UNSUPPORTED for shapes listed above.
+ * Host-only (no CUDA call) unless num_sms == 0.
+ */
+pa_status pa_plan(const pa_batch_desc *desc, pa_plan_t **out, size_t *workspace_bytes);
+
+/* Release a plan.  Never waits for the device: the plan's pinned staging
+ * buffer goes back to a library pool and is reused only after its last
+ * host->device copy has completed.  NULL is ignored. */
+void pa_plan_destroy(pa_plan_t *plan);
+
+/* Fill *info with the plan's work decomposition. */
+pa_status pa_plan_get_info(const pa_plan_t *plan, pa_plan_info *info);
+
+/*
+ * slot_mapping[t] for every scheduled token ("vLLM 推理流程分析" §5.1.2,
+ * block_table.compute_slot_mapping; "vLLM 源码完全拆解（十六）", third
+ * walk-through): token i of request r has position p = num_computed[r] + i
+ * and slot = block_table[r][p / block_size] * block_size + p % block_size.
+ * All pointers are DEVICE memory: query_start_loc [R+1], num_computed [R],
+ * block_table [R][max_blocks_per_req], slot_mapping [T] (written).  The
+ * metadata must be the same that pa_plan accepted.
+ */
+pa_status pa_slot_mapping(const int32_t *query_start_loc, const int32_t *num_computed,
+                          const int32_t *block_table, int32_t num_reqs, int32_t num_tokens,
+                          int32_t max_blocks_per_req, int32_t block_size,
+                          int64_t *slot_mapping, void *stream);
+
+/*
+ * The KV-cache write ("vLLM 推理流程分析" §6.3, reshape_and_cache_flash):
+ * for every t with slot_mapping[t] >= 0, row slot_mapping[t] of key_cache and
+ * value_cache (viewed as [num_slots][Hkv*D]) becomes a bit copy of key[t] and
+ * value[t].  Negative slots are skipped.  A slot >= num_slots is skipped and
+ * sets PA_DEVERR_SLOT_RANGE in *device_error_word when that is non-NULL.
+ * Duplicate non-negative slots in one call are invalid input (which copy wins
+ * is unspecified).  All buffers are DEVICE memory, 16-byte aligned:
+ * key/value [T][Hkv][D], slot_mapping [T], caches [num_slots/16][16][Hkv][D].
+ * Must be enqueued before pa_attention of the same step on the same stream
+ * (write first, then attend: §6.1).
+ */
+pa_status pa_write_kv(const void *key, const void *value, const int64_t *slot_mapping,
+                      int32_t num_tokens, int32_t num_heads_kv, int32_t head_dim,
+                      void *key_cache, void *value_cache, int64_t num_slots,
+                      int32_t *device_error_word, void *stream);
+
+/*
+ * Causal GQA attention of the step ("vLLM 推理流程分析" §6.2,
+ * flash_attn_varlen_func(q, key_cache, value_cache, cu_seqlens_q, seqlen_k,
+ * block_table, softmax_scale, causal=True)).
+ *   plan          from pa_plan for this step (may be reused by every layer)
+ *   q             DEVICE bf16 [T][Hq][D]
+ *   key_cache,
+ *   value_cache   DEVICE bf16 [num_blocks][16][Hkv][D], already holding this
+ *                 step's new rows (pa_write_kv enqueued earlier)
+ *   block_table   DEVICE int32 [R][max_blocks_per_req]; entries past a
+ *                 request's last needed block are never read
+ *   out           DEVICE bf16 [T][Hq][D], written for every scheduled token
+ *   workspace     DEVICE scratch of at least the size pa_plan reported, 256-byte
+ *                 aligned.  Its first 4 bytes are the device error word: zero it
+ *                 once before first use; kernels only ever OR bits into it.
+ * The result depends only on the metadata and the logical contents: physical
+ * block placement does not change a single bit of it.  Slots past seq_len in a
+ * request's last block are never used (their contents may be anything,
+ * including NaN).  Returns PA_ERR_WORKSPACE_TOO_SMALL, PA_ERR_INVALID_ARGUMENT
+ * (NULL or misaligned pointer) or PA_ERR_CUDA (launch failure).
+ */
+pa_status pa_attention(const pa_plan_t *plan, const void *q, const void *key_cache,
+                       const void *value_cache, const int32_t *block_table, void *out,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Read and clear the device error word (the first 4 bytes of a workspace, or
+ * any int32 the caller passed to pa_write_kv).  Synchronises the stream.
+ * *bits (optional) receives the PA_DEVERR_* bits seen.  Returns PA_OK when no
+ * bit was set, PA_ERR_DEVICE_CHECK otherwise, PA_ERR_CUDA if the read failed.
+ */
+pa_status pa_check_device_errors(int32_t *device_error_word, int32_t *bits, void *stream);
+
+/*
+ * Optional per-kernel timing.  While enabled, every pa_attention call with
+ * this plan records CUDA events around each kernel it launches.
+ * pa_plan_kernel_times waits for those events and returns, per kernel kind
+ * (0 decode, 1 extend/prefix, 2 merge, 3 metadata copy), the summed
+ * milliseconds and the launch count since timing was enabled.
+ */
+pa_status pa_plan_enable_timing(pa_plan_t *plan, int32_t enable);
+pa_status pa_plan_kernel_times(pa_plan_t *plan, double ms_total[4], int32_t launches[4]);
+
+/* Static description of a status code. */
+const char *pa_status_string(pa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H */

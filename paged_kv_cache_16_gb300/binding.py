@@ -1,0 +1,263 @@
+"""ctypes binding of libpa.so: argument marshalling only.
+
+Every function here forwards to the C ABI declared in ``include/pa.h`` with
+the same name; device tensors are passed as raw pointers (``data_ptr()``)
+and streams as ``cudaStream_t`` handles.  No step of the computation runs in
+Python: if the compiled library is missing, loading fails with an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import build as _build
+
+PA_OK = 0
+PA_ERR_INVALID_ARGUMENT = 1
+PA_ERR_UNSUPPORTED = 2
+PA_ERR_CUDA = 3
+PA_ERR_DEVICE_CHECK = 4
+PA_ERR_WORKSPACE_TOO_SMALL = 5
+
+PA_DEVERR_SLOT_RANGE = 0x1
+PA_DEVERR_BLOCK_RANGE = 0x2
+PA_DEVERR_TIMEOUT = 0x4
+
+# symbols include/pa.h declares (checked by the CPU tests)
+EXPORTED = ("pa_plan", "pa_plan_destroy", "pa_plan_get_info", "pa_slot_mapping", "pa_write_kv",
+            "pa_attention", "pa_check_device_errors", "pa_plan_enable_timing",
+            "pa_plan_kernel_times", "pa_status_string")
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+class BatchDesc(ctypes.Structure):
+    _fields_ = [
+        ("num_reqs", ctypes.c_int32),
+        ("num_heads_q", ctypes.c_int32),
+        ("num_heads_kv", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int32),
+        ("max_blocks_per_req", ctypes.c_int32),
+        ("query_start_loc", ctypes.POINTER(ctypes.c_int32)),
+        ("seq_lens", ctypes.POINTER(ctypes.c_int32)),
+        ("num_computed_tokens", ctypes.POINTER(ctypes.c_int32)),
+        ("block_table_host", ctypes.POINTER(ctypes.c_int32)),
+        ("num_common_prefix_blocks", ctypes.c_int32),
+        ("softmax_scale", ctypes.c_float),
+        ("num_sms", ctypes.c_int32),
+    ]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [
+        ("num_tokens", ctypes.c_int32),
+        ("num_decode_rows", ctypes.c_int32),
+        ("num_extend_rows", ctypes.c_int32),
+        ("num_decode_ctas", ctypes.c_int32),
+        ("num_decode_items", ctypes.c_int32),
+        ("num_extend_tiles", ctypes.c_int32),
+        ("num_prefix_tiles", ctypes.c_int32),
+        ("num_partial_slots", ctypes.c_int32),
+        ("num_merge_rows", ctypes.c_int32),
+        ("kernels_per_call", ctypes.c_int32),
+        ("decode_kv_bytes", ctypes.c_int64),
+        ("prefix_kv_bytes", ctypes.c_int64),
+        ("extend_flops", ctypes.c_double),
+        ("prefix_flops", ctypes.c_double),
+    ]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return _build.LIBRARY
+
+
+def load(path: str | None = None, build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libpa.so (optionally building it first)."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or _build.LIBRARY
+    if not os.path.exists(p):
+        if build_if_missing:
+            p = _build.build()
+        else:
+            raise RuntimeError(f"libpa.so not built ({p}); run paged_kv_cache_16_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_status_string.argtypes = [ctypes.c_int]
+    lib.pa_plan.restype = ctypes.c_int
+    lib.pa_plan.argtypes = [ctypes.POINTER(BatchDesc), ctypes.POINTER(vp), ctypes.POINTER(sz)]
+    lib.pa_plan_destroy.restype = None
+    lib.pa_plan_destroy.argtypes = [vp]
+    lib.pa_plan_get_info.restype = ctypes.c_int
+    lib.pa_plan_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
+    lib.pa_slot_mapping.restype = ctypes.c_int
+    lib.pa_slot_mapping.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
+    lib.pa_write_kv.restype = ctypes.c_int
+    lib.pa_write_kv.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, i64, vp, vp]
+    lib.pa_attention.restype = ctypes.c_int
+    lib.pa_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.pa_check_device_errors.restype = ctypes.c_int
+    lib.pa_check_device_errors.argtypes = [vp, i32p, vp]
+    lib.pa_plan_enable_timing.restype = ctypes.c_int
+    lib.pa_plan_enable_timing.argtypes = [vp, i32]
+    lib.pa_plan_kernel_times.restype = ctypes.c_int
+    lib.pa_plan_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_double), i32p]
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().pa_status_string(int(status)).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def _check(status: int, what: str):
+    if status != PA_OK:
+        raise PaError(status, what)
+
+
+def _ptr(t) -> int | None:
+    """Raw device/host address of a tensor (or None)."""
+    if t is None:
+        return None
+    return int(t.data_ptr())
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+@dataclass
+class Plan:
+    handle: int
+    workspace_bytes: int
+    _keep: tuple  # host arrays referenced while pa_plan runs
+
+    def info(self) -> dict:
+        pi = PlanInfo()
+        _check(load().pa_plan_get_info(self.handle, ctypes.byref(pi)), "pa_plan_get_info")
+        return pi.as_dict()
+
+    def enable_timing(self, on: bool = True):
+        _check(load().pa_plan_enable_timing(self.handle, 1 if on else 0), "pa_plan_enable_timing")
+
+    def kernel_times(self):
+        ms = (ctypes.c_double * 4)()
+        n = (ctypes.c_int32 * 4)()
+        _check(load().pa_plan_kernel_times(self.handle, ms, n), "pa_plan_kernel_times")
+        return list(ms), list(n)
+
+    def destroy(self):
+        if self.handle:
+            load().pa_plan_destroy(self.handle)
+            self.handle = 0
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:  # noqa: BLE001 -- interpreter shutdown
+            pass
+
+
+def make_desc(*, num_heads_q, num_heads_kv, head_dim, num_blocks, query_start_loc, seq_lens,
+              num_computed_tokens, block_table_host=None, max_blocks_per_req=None,
+              num_common_prefix_blocks=0, softmax_scale, num_sms=0, block_size=16):
+    qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    nc = np.ascontiguousarray(num_computed_tokens, dtype=np.int32)
+    bt = None if block_table_host is None else np.ascontiguousarray(block_table_host, dtype=np.int32)
+    if max_blocks_per_req is None:
+        max_blocks_per_req = bt.shape[1] if bt is not None else 1
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    d = BatchDesc()
+    d.num_reqs = len(sl)
+    d.num_heads_q = num_heads_q
+    d.num_heads_kv = num_heads_kv
+    d.head_dim = head_dim
+    d.block_size = block_size
+    d.num_blocks = num_blocks
+    d.max_blocks_per_req = int(max_blocks_per_req)
+    d.query_start_loc = qsl.ctypes.data_as(i32p)
+    d.seq_lens = sl.ctypes.data_as(i32p)
+    d.num_computed_tokens = nc.ctypes.data_as(i32p)
+    d.block_table_host = bt.ctypes.data_as(i32p) if bt is not None else ctypes.cast(None, i32p)
+    d.num_common_prefix_blocks = int(num_common_prefix_blocks)
+    d.softmax_scale = float(softmax_scale)
+    d.num_sms = int(num_sms)
+    return d, (qsl, sl, nc, bt)
+
+
+def pa_plan(**kw) -> Plan:
+    """Validate the step's metadata and build its plan (see pa.h)."""
+    d, keep = make_desc(**kw)
+    handle = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    _check(load().pa_plan(ctypes.byref(d), ctypes.byref(handle), ctypes.byref(ws)), "pa_plan")
+    return Plan(handle.value, ws.value, keep)
+
+
+def pa_plan_status(**kw) -> int:
+    """Status code pa_plan returns for this descriptor (plan discarded)."""
+    d, keep = make_desc(**kw)
+    handle = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    st = load().pa_plan(ctypes.byref(d), ctypes.byref(handle), ctypes.byref(ws))
+    if st == PA_OK:
+        load().pa_plan_destroy(handle.value)
+    return st
+
+
+def pa_slot_mapping(query_start_loc, num_computed, block_table, num_tokens: int, slot_mapping,
+                    block_size: int = 16, stream=None):
+    _check(load().pa_slot_mapping(_ptr(query_start_loc), _ptr(num_computed), _ptr(block_table),
+                                  int(num_computed.numel()), int(num_tokens), int(block_table.shape[1]),
+                                  int(block_size), _ptr(slot_mapping), _stream(stream)), "pa_slot_mapping")
+
+
+def pa_write_kv(key, value, slot_mapping, key_cache, value_cache, device_error_word=None, stream=None):
+    T, hkv, d = key.shape
+    num_slots = key_cache.shape[0] * key_cache.shape[1]
+    _check(load().pa_write_kv(_ptr(key), _ptr(value), _ptr(slot_mapping), T, hkv, d, _ptr(key_cache),
+                              _ptr(value_cache), num_slots, _ptr(device_error_word), _stream(stream)),
+           "pa_write_kv")
+
+
+def pa_attention(plan: Plan, q, key_cache, value_cache, block_table, out, workspace, stream=None):
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().pa_attention(plan.handle, _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_table),
+                               _ptr(out), _ptr(workspace), nbytes, _stream(stream)), "pa_attention")
+
+
+def pa_check_device_errors(word, stream=None) -> int:
+    """Read and clear a device error word; returns the PA_DEVERR_* bits seen."""
+    bits = ctypes.c_int32(0)
+    st = load().pa_check_device_errors(_ptr(word), ctypes.byref(bits), _stream(stream))
+    if st not in (PA_OK, PA_ERR_DEVICE_CHECK):
+        raise PaError(st, "pa_check_device_errors")
+    return int(bits.value)

@@ -1,0 +1,311 @@
+// Split-KV decode attention: one query token per request, keys streamed
+// block by block from the paged caches.
+//
+// Shape of the work (page "vLLM 推理流程分析" §6.2 / §10.2: a decode query
+// reads every earlier K/V row through the block table; page
+// "vLLM 源码完全拆解（十六）", third walk-through: stable softmax over the
+// pages, partition partials (m, l, o) merged afterwards).
+//
+// GB300 mapping:
+//  * persistent CTAs, one per SM; the planner cuts the concatenation of all
+//    decode requests' key blocks into equal contiguous runs, one per CTA, so
+//    every SM streams the same number of bytes (runs that split a request
+//    produce partials for the merge kernel);
+//  * one CTA serves HG kv heads; a producer warp streams each 16-token block
+//    as HG x (D/64) TMA boxes of [16 rows][64 dims] (128-byte swizzle) for K
+//    and for V into an NS-stage mbarrier ring;
+//  * one consumer warp per kv head: the G query heads of the group form the
+//    rows of a 16x16 bf16 MMA tile (G <= 16), so each K/V row loaded from HBM
+//    is used by all G heads; S = Q K^T and O += P V run on the tensor cores
+//    (mma.sync), the online softmax in fp32 registers with quad shuffles.
+#include "dev.cuh"
+
+namespace pa {
+namespace {
+
+using namespace dev;
+
+template <int D, int HG>
+struct DecodeCfg {
+    static constexpr int NH = D / 64;                      // 128-byte column halves
+    static constexpr int BOX = 16 * 128;                   // one [16][64] bf16 box
+    static constexpr int TSTAGE = HG * NH * BOX;           // K (or V) bytes per block
+    static constexpr int STAGE = decode_stage_bytes(D, HG);
+    static constexpr int NS = decode_stages(D, HG);
+    static constexpr int THREADS = decode_threads(HG);
+    static constexpr int SMEM = decode_smem_bytes(D, HG);
+};
+
+template <int D, int HG>
+__global__ void __launch_bounds__((HG + 1) * 32, 1)
+decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+              const DecodeParams p) {
+    using C = DecodeCfg<D, HG>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int abort_flag;
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;           // stages, 1024-aligned
+    const uint32_t bar0 = base + C::NS * C::STAGE;           // full_k | full_v | empty
+    auto full_k = [&](int s) { return bar0 + 8u * s; };
+    auto full_v = [&](int s) { return bar0 + 8u * (C::NS + s); };
+    auto empty = [&](int s) { return bar0 + 8u * (2 * C::NS + s); };
+    auto stage = [&](int s) { return base + static_cast<uint32_t>(s) * C::STAGE; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < C::NS; ++s) {
+            mbar_init(full_k(s), 1);
+            mbar_init(full_v(s), 1);
+            mbar_init(empty(s), HG);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int item_begin = p.cta_begin[blockIdx.x];
+    const int item_end = p.cta_begin[blockIdx.x + 1];
+
+    if (warp == HG) {
+        // ------------------------------------------------------ producer --
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+        }
+        int issued = 0;
+        bool ok = true;
+        for (int it = item_begin; it < item_end && ok; ++it) {
+            const DecodeItem item = p.items[it];
+            const int32_t *bt = p.block_table + static_cast<int64_t>(item.req) * p.max_blocks;
+            const int h0 = item.head_group * HG;
+            for (int pg = item.page_begin; pg < item.page_end; ++pg) {
+                const int s = issued % C::NS;
+                const int n = issued / C::NS;
+                if (n > 0 && !warp_wait(empty(s), (n & 1) ^ 1, &abort_flag)) {
+                    if (lane == 0) raise_abort(&abort_flag, p.err, kErrTimeout);
+                    ok = false;
+                    break;
+                }
+                const int32_t blk = bt[pg];
+                const bool valid = blk >= 0 && blk < p.num_blocks;
+                if (lane == 0) {
+                    if (valid) {
+                        mbar_arrive_expect_tx(full_k(s), C::TSTAGE);
+                        mbar_arrive_expect_tx(full_v(s), C::TSTAGE);
+                    } else {
+                        atomicOr(p.err, kErrBlockRange);
+                        mbar_arrive(full_k(s));
+                        mbar_arrive(full_v(s));
+                    }
+                }
+                __syncwarp();
+                if (valid && lane < 2 * HG * C::NH) {
+                    const int tensor = lane / (HG * C::NH);
+                    const int idx = lane % (HG * C::NH);
+                    const uint32_t dst = stage(s) + tensor * C::TSTAGE + idx * C::BOX;
+                    const uint32_t bar = tensor ? full_v(s) : full_k(s);
+                    tma_load_3d(dst, tensor ? &tm_v : &tm_k, (idx % C::NH) * 64, h0 + idx / C::NH,
+                                blk * kBlockSize, bar);
+                }
+                ++issued;
+            }
+        }
+        // Never leave the CTA with TMA writes in flight.
+        if (lane == 0) {
+            for (int k = issued - 1; k >= 0 && k >= issued - C::NS; --k) {
+                const int s = k % C::NS, n = k / C::NS;
+                if (!mbar_wait(full_k(s), n & 1, nullptr) || !mbar_wait(full_v(s), n & 1, nullptr))
+                    atomicOr(p.err, kErrTimeout);
+            }
+        }
+    } else {
+        // ------------------------------------------------------ consumers --
+        const int g = lane >> 2;   // MMA row group: query heads g and g + 8
+        const int t4 = lane & 3;
+        const int G = p.group;
+        int consumed = 0;
+        bool ok = true;
+        for (int it = item_begin; it < item_end && ok; ++it) {
+            const DecodeItem item = p.items[it];
+            const int kvh = item.head_group * HG + warp;
+            const uint16_t *qrow = p.q + (static_cast<int64_t>(item.token) * p.num_heads_q + kvh * G) * D;
+            uint32_t qf[D / 16][4];
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int c = kk * 16 + 2 * t4;
+                qf[kk][0] = g < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + g * D + c)) : 0u;
+                qf[kk][1] = g + 8 < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + (g + 8) * D + c)) : 0u;
+                qf[kk][2] = g < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + g * D + c + 8)) : 0u;
+                qf[kk][3] = g + 8 < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + (g + 8) * D + c + 8)) : 0u;
+            }
+            float o[D / 8][4];
+#pragma unroll
+            for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+            float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+            for (int pg = item.page_begin; pg < item.page_end; ++pg, ++consumed) {
+                const int s = consumed % C::NS;
+                const uint32_t par = (consumed / C::NS) & 1;
+                if (!warp_wait(full_k(s), par, &abort_flag)) {
+                    if (lane == 0) raise_abort(&abort_flag, p.err, kErrTimeout);
+                    ok = false;
+                    break;
+                }
+                const uint32_t kb = stage(s) + warp * C::NH * C::BOX;
+                const uint32_t vb = kb + C::TSTAGE;
+                // S = Q K^T over this block's 16 keys (two n-tiles of 8 keys)
+                float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int mi = lane >> 3;
+                    const int key = (mi >> 1) * 8 + (lane & 7);
+                    const int chunk = (kk % 4) * 2 + (mi & 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4(sw128(kb + (kk / 4) * C::BOX, key, chunk), b0, b1, b2, b3);
+                    mma_bf16_16816(sc[0], qf[kk], b0, b1);
+                    mma_bf16_16816(sc[1], qf[kk], b2, b3);
+                }
+                // mask keys past the context, scale to log2 units
+                const int key0 = pg * kBlockSize;
+                const int valid_keys = item.key_end - key0;  // >= 1
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int key = j * 8 + 2 * t4 + (e & 1);
+                        sc[j][e] = key < valid_keys ? sc[j][e] * p.scale_log2 : -INFINITY;
+                    }
+                float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+                float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                // Rescale only when the running maximum grows by more than 2^8;
+                // otherwise keep the stale reference (weights stay <= 256).
+                const bool need0 = mx0 > m0 + 8.f;
+                const bool need1 = mx1 > m1 + 8.f;
+                float a0 = 1.f, a1 = 1.f;
+                if (need0) { a0 = ex2(m0 - mx0); m0 = mx0; l0 *= a0; }
+                if (need1) { a1 = ex2(m1 - mx1); m1 = mx1; l1 *= a1; }
+                if (__any_sync(0xffffffffu, need0 || need1)) {
+#pragma unroll
+                    for (int j = 0; j < D / 8; ++j) {
+                        o[j][0] *= a0; o[j][1] *= a0; o[j][2] *= a1; o[j][3] *= a1;
+                    }
+                }
+                const float r0 = m0 == -INFINITY ? 0.f : m0;
+                const float r1 = m1 == -INFINITY ? 0.f : m1;
+                uint32_t pa[4];
+                pa[0] = pack_bf16x2(ex2(sc[0][0] - r0), ex2(sc[0][1] - r0));
+                pa[1] = pack_bf16x2(ex2(sc[0][2] - r1), ex2(sc[0][3] - r1));
+                pa[2] = pack_bf16x2(ex2(sc[1][0] - r0), ex2(sc[1][1] - r0));
+                pa[3] = pack_bf16x2(ex2(sc[1][2] - r1), ex2(sc[1][3] - r1));
+                l0 += bf16_lo(pa[0]) + bf16_hi(pa[0]) + bf16_lo(pa[2]) + bf16_hi(pa[2]);
+                l1 += bf16_lo(pa[1]) + bf16_hi(pa[1]) + bf16_lo(pa[3]) + bf16_hi(pa[3]);
+
+                if (!warp_wait(full_v(s), par, &abort_flag)) {
+                    if (lane == 0) raise_abort(&abort_flag, p.err, kErrTimeout);
+                    ok = false;
+                    break;
+                }
+                if (valid_keys < kBlockSize) {
+                    // rows past the context may hold anything (even NaN); zero
+                    // them so that 0-weight * row stays 0 inside the MMA
+                    const int bad = kBlockSize - valid_keys;
+                    for (int i = lane; i < bad * C::NH * 8; i += 32) {
+                        const int row = valid_keys + i / (C::NH * 8);
+                        const int half = (i / 8) % C::NH;
+                        const int ch = i % 8;
+                        const uint32_t a = vb + half * C::BOX + row * 128 + ch * 16;
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                // O += P V
+#pragma unroll
+                for (int np = 0; np < D / 16; ++np) {
+                    const int mi = lane >> 3;
+                    const int key = (mi & 1) * 8 + (lane & 7);
+                    const int chunk = 2 * np + (mi >> 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4_trans(sw128(vb + (chunk / 8) * C::BOX, key, chunk % 8), b0, b1, b2, b3);
+                    mma_bf16_16816(o[2 * np], pa, b0, b1);
+                    mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty(s));
+            }
+            if (!ok) break;
+            // ------------------------------------------------ finalize --
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+            const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
+            const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+            const int h_row0 = kvh * G + g, h_row1 = kvh * G + g + 8;
+            if (item.part < 0) {
+                uint16_t *orow = p.out + static_cast<int64_t>(item.token) * p.num_heads_q * D;
+#pragma unroll
+                for (int j = 0; j < D / 8; ++j) {
+                    const int d = j * 8 + 2 * t4;
+                    if (g < G)
+                        *reinterpret_cast<uint32_t *>(orow + h_row0 * D + d) = pack_bf16x2(o[j][0] * inv0, o[j][1] * inv0);
+                    if (g + 8 < G)
+                        *reinterpret_cast<uint32_t *>(orow + h_row1 * D + d) = pack_bf16x2(o[j][2] * inv1, o[j][3] * inv1);
+                }
+            } else {
+                const int64_t slot = static_cast<int64_t>(p.part_offset[item.token * p.n_groups + item.head_group]) + item.part;
+                float *op = p.o_part + slot * p.num_heads_q * D;
+#pragma unroll
+                for (int j = 0; j < D / 8; ++j) {
+                    const int d = j * 8 + 2 * t4;
+                    if (g < G)
+                        *reinterpret_cast<float2 *>(op + h_row0 * D + d) = make_float2(o[j][0] * inv0, o[j][1] * inv0);
+                    if (g + 8 < G)
+                        *reinterpret_cast<float2 *>(op + h_row1 * D + d) = make_float2(o[j][2] * inv1, o[j][3] * inv1);
+                }
+                if (t4 == 0) {
+                    if (g < G) p.ml_part[slot * p.num_heads_q + h_row0] = make_float2(m0, l0);
+                    if (g + 8 < G) p.ml_part[slot * p.num_heads_q + h_row1] = make_float2(m1, l1);
+                }
+            }
+        }
+    }
+    __syncthreads();
+}
+
+template <int D, int HG>
+cudaError_t launch_t(int num_ctas, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                     const DecodeParams &p, cudaStream_t stream) {
+    using C = DecodeCfg<D, HG>;
+    static bool configured = false;  // attribute is per function, set once per process
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, HG>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    decode_kernel<D, HG><<<num_ctas, C::THREADS, C::SMEM, stream>>>(tm_k, tm_v, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+#define PA_DECODE_CASES(X) \
+    X(64, 1) X(64, 2) X(64, 4) X(64, 8) X(128, 1) X(128, 2) X(128, 4) X(128, 8)
+
+cudaError_t launch_decode(int head_dim, int hg, int num_ctas, const CUtensorMap &tm_k,
+                          const CUtensorMap &tm_v, const DecodeParams &p, cudaStream_t stream) {
+    if (num_ctas <= 0) return cudaSuccess;
+#define X(d, h) \
+    if (head_dim == d && hg == h) return launch_t<d, h>(num_ctas, tm_k, tm_v, p, stream);
+    PA_DECODE_CASES(X)
+#undef X
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

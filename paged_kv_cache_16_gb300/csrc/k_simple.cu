@@ -1,0 +1,144 @@
+// Bandwidth-trivial kernels of the step: slot mapping, the KV-cache scatter
+// and the merge of partition partials.
+#include "dev.cuh"
+
+namespace pa {
+namespace {
+
+// slot of every scheduled token ("vLLM 推理流程分析" §5.1.2 compute_slot_mapping):
+// the request is found by binary search over query_start_loc.
+__global__ void slot_mapping_kernel(const int32_t *__restrict__ qsl,
+                                    const int32_t *__restrict__ num_computed,
+                                    const int32_t *__restrict__ block_table, int32_t num_reqs,
+                                    int32_t num_tokens, int32_t max_blocks, int32_t block_size,
+                                    int64_t *__restrict__ slots) {
+    const int32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= num_tokens) return;
+    int32_t lo = 0, hi = num_reqs - 1;  // last r with qsl[r] <= t
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (qsl[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int32_t pos = num_computed[lo] + (t - qsl[lo]);
+    const int32_t blk = block_table[static_cast<int64_t>(lo) * max_blocks + pos / block_size];
+    slots[t] = static_cast<int64_t>(blk) * block_size + pos % block_size;
+}
+
+// reshape_and_cache ("vLLM 推理流程分析" §6.3): one thread moves one 16-byte
+// chunk of one token's key row and the same chunk of its value row.
+// Consecutive threads touch consecutive chunks, so loads and stores coalesce.
+__global__ void write_kv_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                                const int64_t *__restrict__ slots, int64_t total_chunks,
+                                int32_t chunks_per_row, uint4 *__restrict__ key_cache,
+                                uint4 *__restrict__ value_cache, int64_t num_slots,
+                                int32_t *err) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+         i < total_chunks; i += stride) {
+        const int64_t t = i / chunks_per_row;
+        const int32_t c = static_cast<int32_t>(i - t * chunks_per_row);
+        const int64_t slot = __ldg(slots + t);
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (err != nullptr && c == 0) atomicOr(err, kErrSlotRange);
+            continue;
+        }
+        const uint4 kv = __ldcs(key + i);
+        const uint4 vv = __ldcs(value + i);
+        key_cache[slot * chunks_per_row + c] = kv;
+        value_cache[slot * chunks_per_row + c] = vv;
+    }
+}
+
+// Merge of partition partials (page "vLLM 源码完全拆解（十六）", third
+// walk-through: per-partition (m_r, l_r, o_r) combined with exponential
+// rescaling).  One warp per (token, query head); m is in log2 units.
+template <int D>
+__global__ void merge_kernel(MergeParams p) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= p.num_rows * p.max_heads) return;
+    const MergeRow row = p.rows[warp / p.max_heads];
+    const int hi = warp % p.max_heads;
+    if (hi >= row.hq_count) return;
+    const int h = row.hq_begin + hi;
+    constexpr int V = D / 32;  // floats per lane
+    float m = -INFINITY;
+    for (int s = 0; s < row.count; ++s) {
+        const float2 ml = p.ml_part[static_cast<int64_t>(row.slot0 + s) * p.num_heads_q + h];
+        if (ml.y > 0.f) m = fmaxf(m, ml.x);
+    }
+    float acc[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] = 0.f;
+    float total = 0.f;
+    for (int s = 0; s < row.count; ++s) {
+        const int64_t slot = row.slot0 + s;
+        const float2 ml = p.ml_part[slot * p.num_heads_q + h];
+        if (!(ml.y > 0.f)) continue;
+        const float w = dev::ex2(ml.x - m) * ml.y;
+        total += w;
+        const float *o = p.o_part + (slot * p.num_heads_q + h) * D + lane * V;
+        if constexpr (V == 4) {
+            const float4 x = *reinterpret_cast<const float4 *>(o);
+            acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+        } else {
+            const float2 x = *reinterpret_cast<const float2 *>(o);
+            acc[0] += w * x.x; acc[1] += w * x.y;
+        }
+    }
+    const float inv = total > 0.f ? 1.f / total : 0.f;
+    uint16_t *dst = p.out + (static_cast<int64_t>(row.token) * p.num_heads_q + h) * D + lane * V;
+    if constexpr (V == 4) {
+        uint2 packed;
+        packed.x = dev::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        packed.y = dev::pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2 *>(dst) = packed;
+    } else {
+        *reinterpret_cast<uint32_t *>(dst) = dev::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_slot_mapping(const int32_t *qsl, const int32_t *num_computed,
+                                const int32_t *block_table, int32_t num_reqs, int32_t num_tokens,
+                                int32_t max_blocks, int32_t block_size, int64_t *slots,
+                                cudaStream_t stream) {
+    if (num_tokens <= 0) return cudaSuccess;
+    const int threads = 256;
+    const int blocks = (num_tokens + threads - 1) / threads;
+    slot_mapping_kernel<<<blocks, threads, 0, stream>>>(qsl, num_computed, block_table, num_reqs,
+                                                        num_tokens, max_blocks, block_size, slots);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_write_kv(const void *key, const void *value, const int64_t *slots,
+                            int32_t num_tokens, int32_t row_elems, void *key_cache,
+                            void *value_cache, int64_t num_slots, int32_t *err,
+                            cudaStream_t stream) {
+    if (num_tokens <= 0) return cudaSuccess;
+    const int32_t chunks_per_row = row_elems * 2 / 16;
+    const int64_t total = static_cast<int64_t>(num_tokens) * chunks_per_row;
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    if (blocks > 152 * 16) blocks = 152 * 16;  // grid-stride beyond ~16 waves of CTAs
+    write_kv_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), slots, total,
+        chunks_per_row, static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache),
+        num_slots, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_merge(int head_dim, const MergeParams &p, cudaStream_t stream) {
+    if (p.num_rows <= 0) return cudaSuccess;
+    const int64_t warps = static_cast<int64_t>(p.num_rows) * p.max_heads;
+    const int threads = 256;
+    const unsigned blocks = static_cast<unsigned>((warps * 32 + threads - 1) / threads);
+    if (head_dim == 128) merge_kernel<128><<<blocks, threads, 0, stream>>>(p);
+    else if (head_dim == 64) merge_kernel<64><<<blocks, threads, 0, stream>>>(p);
+    else return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,649 @@
+// C ABI of the paged-KV step: metadata validation and planning (host), and
+// the enqueueing of the device kernels.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+using namespace pa;
+
+struct pa_plan_s {
+    // step shape
+    int32_t R = 0, Hq = 0, Hkv = 0, D = 0, num_blocks = 0, max_blocks = 0;
+    int32_t T = 0, G = 0, HG = 1, n_groups = 1, num_sms = 0;
+    int32_t n_prefix = 0;         // num_common_prefix_blocks (cascade when > 0)
+    int32_t prefix_req = -1;      // block-table row of the shared prefix
+    int32_t prefix_splits = 0;
+    float scale_log2 = 0.f;
+    // work lists
+    std::vector<int32_t> part_offset;   // [T * n_groups]
+    std::vector<int32_t> cta_begin;     // [ncta + 1]
+    std::vector<DecodeItem> items;
+    std::vector<ExtendTile> tiles;
+    std::vector<MergeRow> merges;
+    int32_t num_slots = 0;
+    // workspace layout
+    size_t off_part = 0, off_cta = 0, off_items = 0, off_tiles = 0, off_merges = 0;
+    size_t blob_bytes = 0, off_opart = 0, off_ml = 0, ws_bytes = 0;
+    std::vector<uint8_t> blob;          // host image of the metadata blob
+    void *pinned = nullptr;             // pinned staging copy used for async uploads
+    size_t pinned_cap = 0;
+    cudaEvent_t upload_evt = nullptr;   // recorded after each upload from `pinned`
+    pa_plan_info info{};
+    // timing
+    bool timing = false;
+    std::vector<cudaEvent_t> ev_start[4], ev_stop[4];
+    std::mutex mu;
+};
+
+namespace {
+
+constexpr size_t kHeader = 256;
+
+// Pinned staging buffers for the per-call metadata upload, recycled across
+// plans.  A plan takes a buffer on its first pa_attention call and hands it
+// back when destroyed; the buffer is given out again only after the last copy
+// from it has completed on the device (its event has fired), so destroying a
+// plan never waits and never frees pinned memory on the hot path.
+class StagingPool {
+  public:
+    bool acquire(size_t bytes, void **ptr, size_t *cap, cudaEvent_t *ev) {
+        std::lock_guard<std::mutex> lock(mu_);
+        for (size_t i = 0; i < free_.size(); ++i) {
+            if (free_[i].cap >= bytes && cudaEventQuery(free_[i].ev) == cudaSuccess) {
+                *ptr = free_[i].ptr;
+                *cap = free_[i].cap;
+                *ev = free_[i].ev;
+                free_.erase(free_.begin() + static_cast<long>(i));
+                return true;
+            }
+        }
+        const size_t rounded = align(bytes, size_t(64) << 10);
+        if (cudaMallocHost(ptr, rounded) != cudaSuccess) return false;
+        if (cudaEventCreateWithFlags(ev, cudaEventDisableTiming) != cudaSuccess) {
+            cudaFreeHost(*ptr);
+            return false;
+        }
+        *cap = rounded;
+        return true;
+    }
+    void release(void *ptr, size_t cap, cudaEvent_t ev) {
+        std::lock_guard<std::mutex> lock(mu_);
+        free_.push_back({ptr, cap, ev});
+        if (free_.size() > kMaxFree) {  // bound the pool: retire the oldest
+            Buf old = free_.front();
+            free_.erase(free_.begin());
+            cudaEventSynchronize(old.ev);
+            cudaEventDestroy(old.ev);
+            cudaFreeHost(old.ptr);
+        }
+    }
+
+  private:
+    struct Buf {
+        void *ptr;
+        size_t cap;
+        cudaEvent_t ev;
+    };
+    static size_t align(size_t x, size_t a) { return (x + a - 1) / a * a; }
+    static constexpr size_t kMaxFree = 32;
+    std::mutex mu_;
+    std::vector<Buf> free_;
+};
+
+StagingPool &staging() {
+    static StagingPool *pool = new StagingPool();  // never destroyed: outlives CUDA teardown
+    return *pool;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int heads_per_group(int hkv) {
+    for (int hg = kMaxDecodeHeads; hg > 1; hg >>= 1)
+        if (hkv % hg == 0) return hg;
+    return 1;
+}
+
+// cuTensorMapEncodeTiled from the driver, fetched once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 3-D bf16 tensor map over [outer][mid][D] with a box of [box_outer][box_mid][64]
+// and 128-byte swizzling.
+bool make_map(CUtensorMap *tm, const void *ptr, uint64_t d, uint64_t mid, uint64_t outer,
+              uint32_t box_mid, uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {d, mid, outer};
+    cuuint64_t strides[2] = {d * 2, mid * d * 2};
+    cuuint32_t box[3] = {64, box_mid, box_outer};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+pa_status validate(const pa_batch_desc *d) {
+    if (d->num_reqs < 0 || d->num_heads_q <= 0 || d->num_heads_kv <= 0 || d->num_blocks <= 0 ||
+        d->max_blocks_per_req <= 0 || d->block_size <= 0 || d->head_dim <= 0)
+        return PA_ERR_INVALID_ARGUMENT;
+    if (d->num_heads_q % d->num_heads_kv != 0) return PA_ERR_INVALID_ARGUMENT;
+    if (!(d->softmax_scale > 0.f) || !std::isfinite(d->softmax_scale)) return PA_ERR_INVALID_ARGUMENT;
+    if (d->num_common_prefix_blocks < 0 || d->num_sms < 0) return PA_ERR_INVALID_ARGUMENT;
+    if (d->query_start_loc == nullptr || (d->num_reqs > 0 && (d->seq_lens == nullptr ||
+                                                              d->num_computed_tokens == nullptr)))
+        return PA_ERR_INVALID_ARGUMENT;
+    const int32_t *qsl = d->query_start_loc;
+    if (qsl[0] != 0) return PA_ERR_INVALID_ARGUMENT;
+    for (int32_t r = 0; r < d->num_reqs; ++r) {
+        const int64_t q_len = static_cast<int64_t>(qsl[r + 1]) - qsl[r];
+        if (q_len < 0) return PA_ERR_INVALID_ARGUMENT;
+        if (d->seq_lens[r] < 0 || d->num_computed_tokens[r] < 0) return PA_ERR_INVALID_ARGUMENT;
+        if (static_cast<int64_t>(d->num_computed_tokens[r]) + q_len != d->seq_lens[r])
+            return PA_ERR_INVALID_ARGUMENT;
+        const int64_t need = (static_cast<int64_t>(d->seq_lens[r]) + d->block_size - 1) / d->block_size;
+        if (need > d->max_blocks_per_req) return PA_ERR_INVALID_ARGUMENT;
+        if (d->block_table_host) {
+            const int32_t *row = d->block_table_host + static_cast<int64_t>(r) * d->max_blocks_per_req;
+            for (int64_t b = 0; b < need; ++b)
+                if (row[b] < 0 || row[b] >= d->num_blocks) return PA_ERR_INVALID_ARGUMENT;
+        }
+    }
+    const int32_t n = d->num_common_prefix_blocks;
+    if (n > 0) {
+        if (n > d->max_blocks_per_req) return PA_ERR_INVALID_ARGUMENT;
+        int32_t ref = -1;
+        for (int32_t r = 0; r < d->num_reqs; ++r) {
+            if (qsl[r + 1] == qsl[r]) continue;
+            if (static_cast<int64_t>(n) * d->block_size > d->num_computed_tokens[r]) return PA_ERR_INVALID_ARGUMENT;
+            if (d->block_table_host) {
+                if (ref < 0) {
+                    ref = r;
+                    continue;
+                }
+                const int32_t *a = d->block_table_host + static_cast<int64_t>(ref) * d->max_blocks_per_req;
+                const int32_t *b = d->block_table_host + static_cast<int64_t>(r) * d->max_blocks_per_req;
+                for (int32_t i = 0; i < n; ++i)
+                    if (a[i] != b[i]) return PA_ERR_INVALID_ARGUMENT;
+            }
+        }
+    }
+    // supported shapes
+    if (d->block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+    if (d->head_dim != 64 && d->head_dim != 128) return PA_ERR_UNSUPPORTED;
+    const int G = d->num_heads_q / d->num_heads_kv;
+    if (!is_pow2(G) || G > 16) return PA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(d->num_blocks) * d->block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+// Cut the concatenated decode runs into ncta equal contiguous shares.
+void plan_decode(pa_plan_s *P, const pa_batch_desc *d, const std::vector<int32_t> &decode_rows,
+                 std::vector<int32_t> &pieces) {
+    struct Run { int32_t r, grp, pb, pe; };
+    std::vector<Run> runs;
+    const int32_t kb = P->n_prefix;  // first block of the suffix work
+    int64_t total = 0;
+    for (int grp = 0; grp < P->n_groups; ++grp)
+        for (int32_t r : decode_rows) {
+            const int32_t pe = (d->seq_lens[r] + kBlockSize - 1) / kBlockSize;
+            if (pe <= kb) continue;
+            runs.push_back({r, grp, kb, pe});
+            total += pe - kb;
+        }
+    pieces.assign(static_cast<size_t>(d->num_reqs) * P->n_groups, 0);
+    P->cta_begin.assign(1, 0);
+    if (total == 0) return;
+    const int cps = std::max(1, decode_ctas_per_sm_static(P->D, P->HG));
+    const int64_t min_pages = 4;
+    int64_t ncta = std::min<int64_t>(static_cast<int64_t>(P->num_sms) * cps, (total + min_pages - 1) / min_pages);
+    ncta = std::max<int64_t>(ncta, 1);
+    size_t run = 0;
+    int32_t cursor = runs.empty() ? 0 : runs[0].pb;
+    for (int64_t c = 0; c < ncta; ++c) {
+        int64_t quota = total / ncta + (c < total % ncta ? 1 : 0);
+        while (quota > 0 && run < runs.size()) {
+            const Run &R = runs[run];
+            const int32_t take = static_cast<int32_t>(std::min<int64_t>(quota, R.pe - cursor));
+            DecodeItem it{};
+            it.token = d->query_start_loc[R.r];
+            it.req = R.r;
+            it.page_begin = cursor;
+            it.page_end = cursor + take;
+            it.key_end = d->seq_lens[R.r];
+            it.head_group = R.grp;
+            it.part = pieces[static_cast<size_t>(R.r) * P->n_groups + R.grp]++;
+            P->items.push_back(it);
+            cursor += take;
+            quota -= take;
+            if (cursor >= R.pe) {
+                ++run;
+                if (run < runs.size()) cursor = runs[run].pb;
+            }
+        }
+        P->cta_begin.push_back(static_cast<int32_t>(P->items.size()));
+    }
+}
+
+pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d) {
+    P->R = d->num_reqs;
+    P->Hq = d->num_heads_q;
+    P->Hkv = d->num_heads_kv;
+    P->D = d->head_dim;
+    P->num_blocks = d->num_blocks;
+    P->max_blocks = d->max_blocks_per_req;
+    P->T = d->num_reqs > 0 ? d->query_start_loc[d->num_reqs] : 0;
+    P->G = P->Hq / P->Hkv;
+    P->HG = heads_per_group(P->Hkv);
+    P->n_groups = P->Hkv / P->HG;
+    P->scale_log2 = d->softmax_scale * 1.4426950408889634f;
+    P->num_sms = d->num_sms;
+    if (P->num_sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return PA_ERR_CUDA;
+    }
+    const int32_t *qsl = d->query_start_loc;
+    std::vector<int32_t> decode_rows, extend_rows;
+    for (int32_t r = 0; r < P->R; ++r) {
+        const int32_t q_len = qsl[r + 1] - qsl[r];
+        if (q_len == 1) decode_rows.push_back(r);
+        else if (q_len > 1) extend_rows.push_back(r);
+    }
+    const bool cascade = d->num_common_prefix_blocks > 0 && P->T > 0;
+    P->n_prefix = cascade ? d->num_common_prefix_blocks : 0;
+    const int32_t kb_keys = P->n_prefix * kBlockSize;
+    for (int32_t r = 0; r < P->R; ++r)
+        if (qsl[r + 1] > qsl[r]) { P->prefix_req = r; break; }
+
+    // ---------------------------------------------------- tensor-core tiles
+    const int tpt = kTileRows / P->G;   // tokens per 128-row tile
+    if (cascade) {
+        const int n_key_tiles = (kb_keys + kTileKeys - 1) / kTileKeys;
+        const int token_tiles = (P->T + tpt - 1) / tpt;
+        const int units = P->Hkv * token_tiles;
+        int splits = static_cast<int>(std::lround(static_cast<double>(P->num_sms) / units));
+        splits = std::max(1, std::min(splits, n_key_tiles));
+        const int chunk = (n_key_tiles + splits - 1) / splits;      // key tiles per split
+        splits = (n_key_tiles + chunk - 1) / chunk;
+        P->prefix_splits = splits;
+        for (int h = 0; h < P->Hkv; ++h)
+            for (int tt = 0; tt < token_tiles; ++tt)
+                for (int s = 0; s < splits; ++s) {
+                    ExtendTile t{};
+                    t.t0 = tt * tpt;
+                    t.n_tok = std::min(tpt, P->T - t.t0);
+                    t.req = P->prefix_req;
+                    t.pos0 = 0;
+                    t.key_begin = s * chunk * kTileKeys;
+                    t.key_end = std::min(kb_keys, (s + 1) * chunk * kTileKeys);
+                    t.kv_head = h;
+                    t.part = s;
+                    t.causal = 0;
+                    P->tiles.push_back(t);
+                }
+        P->info.num_prefix_tiles = static_cast<int32_t>(P->tiles.size());
+    }
+    for (int32_t r : extend_rows) {
+        const int32_t q_len = qsl[r + 1] - qsl[r];
+        for (int h = 0; h < P->Hkv; ++h)
+            for (int32_t m0 = 0; m0 < q_len; m0 += tpt) {
+                ExtendTile t{};
+                t.t0 = qsl[r] + m0;
+                t.n_tok = std::min(tpt, q_len - m0);
+                t.req = r;
+                t.pos0 = d->num_computed_tokens[r] + m0;
+                t.key_begin = kb_keys;
+                t.key_end = std::min(d->seq_lens[r], t.pos0 + t.n_tok);
+                t.kv_head = h;
+                t.part = cascade ? P->prefix_splits : -1;
+                t.causal = 1;
+                P->tiles.push_back(t);
+            }
+    }
+    // longest key ranges first: the last wave is made of short tiles
+    std::stable_sort(P->tiles.begin(), P->tiles.end(), [](const ExtendTile &a, const ExtendTile &b) {
+        return (a.key_end - a.key_begin) > (b.key_end - b.key_begin);
+    });
+
+    // ------------------------------------------------------------- decode
+    std::vector<int32_t> pieces;
+    plan_decode(P, d, decode_rows, pieces);
+
+    // ----------------------------------------------------- partial slots
+    std::vector<int32_t> count(static_cast<size_t>(P->T) * P->n_groups, 0);
+    for (int32_t r : decode_rows)
+        for (int grp = 0; grp < P->n_groups; ++grp) {
+            const int32_t k = pieces[static_cast<size_t>(r) * P->n_groups + grp];
+            count[static_cast<size_t>(qsl[r]) * P->n_groups + grp] =
+                cascade ? P->prefix_splits + k : (k > 1 ? k : 0);
+        }
+    if (cascade)
+        for (int32_t r : extend_rows)
+            for (int32_t t = qsl[r]; t < qsl[r + 1]; ++t)
+                for (int grp = 0; grp < P->n_groups; ++grp)
+                    count[static_cast<size_t>(t) * P->n_groups + grp] = P->prefix_splits + 1;
+    for (DecodeItem &it : P->items) {
+        const int32_t k = pieces[static_cast<size_t>(it.req) * P->n_groups + it.head_group];
+        if (cascade) it.part += P->prefix_splits;
+        else if (k == 1) it.part = -1;
+    }
+    P->part_offset.assign(count.size(), 0);
+    int64_t slots = 0;
+    for (size_t i = 0; i < count.size(); ++i) {
+        P->part_offset[i] = static_cast<int32_t>(slots);
+        slots += count[i];
+        if (count[i] > 0) {
+            MergeRow m{};
+            m.token = static_cast<int32_t>(i / P->n_groups);
+            m.slot0 = P->part_offset[i];
+            m.count = count[i];
+            m.hq_begin = static_cast<int32_t>(i % P->n_groups) * P->HG * P->G;
+            m.hq_count = P->HG * P->G;
+            P->merges.push_back(m);
+        }
+    }
+    if (slots > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    P->num_slots = static_cast<int32_t>(slots);
+
+    // ------------------------------------------------- workspace layout
+    size_t off = kHeader;
+    auto place = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 16); return o; };
+    P->off_part = place(P->part_offset.size() * sizeof(int32_t));
+    P->off_cta = place(P->cta_begin.size() * sizeof(int32_t));
+    P->off_items = place(P->items.size() * sizeof(DecodeItem));
+    P->off_tiles = place(P->tiles.size() * sizeof(ExtendTile));
+    P->off_merges = place(P->merges.size() * sizeof(MergeRow));
+    P->blob_bytes = off - kHeader;
+    off = align_up(off, 256);
+    P->off_opart = off;
+    off = align_up(off + static_cast<size_t>(P->num_slots) * P->Hq * P->D * sizeof(float), 256);
+    P->off_ml = off;
+    off = align_up(off + static_cast<size_t>(P->num_slots) * P->Hq * sizeof(float2), 256);
+    P->ws_bytes = off;
+    P->blob.assign(P->blob_bytes, 0);
+    auto put = [&](size_t at, const void *src, size_t n) {
+        if (n) std::memcpy(P->blob.data() + (at - kHeader), src, n);
+    };
+    put(P->off_part, P->part_offset.data(), P->part_offset.size() * sizeof(int32_t));
+    put(P->off_cta, P->cta_begin.data(), P->cta_begin.size() * sizeof(int32_t));
+    put(P->off_items, P->items.data(), P->items.size() * sizeof(DecodeItem));
+    put(P->off_tiles, P->tiles.data(), P->tiles.size() * sizeof(ExtendTile));
+    put(P->off_merges, P->merges.data(), P->merges.size() * sizeof(MergeRow));
+
+    // ------------------------------------------------------------- info
+    pa_plan_info &I = P->info;
+    I.num_tokens = P->T;
+    I.num_decode_rows = static_cast<int32_t>(decode_rows.size());
+    I.num_extend_rows = static_cast<int32_t>(extend_rows.size());
+    I.num_decode_ctas = static_cast<int32_t>(P->cta_begin.size()) - 1;
+    I.num_decode_items = static_cast<int32_t>(P->items.size());
+    I.num_extend_tiles = static_cast<int32_t>(P->tiles.size());
+    I.num_partial_slots = P->num_slots;
+    I.num_merge_rows = static_cast<int32_t>(P->merges.size());
+    I.kernels_per_call = (P->items.empty() ? 0 : 1) + (P->tiles.empty() ? 0 : 1) + (P->merges.empty() ? 0 : 1);
+    const int64_t row_bytes = static_cast<int64_t>(P->Hkv) * P->D * 2 * 2;   // K and V, bf16
+    for (int32_t r : decode_rows) I.decode_kv_bytes += (d->seq_lens[r] - kb_keys) * row_bytes;
+    I.prefix_kv_bytes = cascade ? kb_keys * row_bytes : 0;
+    double pairs = 0.0;
+    for (int32_t r : extend_rows) {
+        const int32_t q_len = qsl[r + 1] - qsl[r];
+        for (int32_t i = 0; i < q_len; ++i) pairs += d->num_computed_tokens[r] + i + 1 - kb_keys;
+    }
+    I.extend_flops = 4.0 * P->D * P->Hq * pairs;
+    I.prefix_flops = cascade ? 4.0 * P->D * P->Hq * static_cast<double>(P->T) * kb_keys : 0.0;
+    return PA_OK;
+}
+
+cudaError_t record(pa_plan_s *P, int kind, bool start, cudaStream_t stream) {
+    if (!P->timing) return cudaSuccess;
+    cudaEvent_t e;
+    cudaError_t err = cudaEventCreate(&e);
+    if (err != cudaSuccess) return err;
+    (start ? P->ev_start : P->ev_stop)[kind].push_back(e);
+    return cudaEventRecord(e, stream);
+}
+
+void clear_timing(pa_plan_s *P) {
+    for (int k = 0; k < 4; ++k) {
+        for (auto e : P->ev_start[k]) cudaEventDestroy(e);
+        for (auto e : P->ev_stop[k]) cudaEventDestroy(e);
+        P->ev_start[k].clear();
+        P->ev_stop[k].clear();
+    }
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char *pa_status_string(pa_status s) {
+    switch (s) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARGUMENT: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported shape";
+        case PA_ERR_CUDA: return "CUDA runtime error";
+        case PA_ERR_DEVICE_CHECK: return "device-side check failed";
+        case PA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    }
+    return "unknown status";
+}
+
+pa_status pa_plan(const pa_batch_desc *desc, pa_plan_t **out, size_t *workspace_bytes) {
+    if (out) *out = nullptr;
+    if (desc == nullptr || out == nullptr || workspace_bytes == nullptr) return PA_ERR_INVALID_ARGUMENT;
+    pa_status st = validate(desc);
+    if (st != PA_OK) return st;
+    pa_plan_s *P = new (std::nothrow) pa_plan_s();
+    if (!P) return PA_ERR_INVALID_ARGUMENT;
+    st = build_plan(P, desc);
+    if (st != PA_OK) {
+        delete P;
+        return st;
+    }
+    *out = P;
+    *workspace_bytes = P->ws_bytes;
+    return PA_OK;
+}
+
+void pa_plan_destroy(pa_plan_t *P) {
+    if (!P) return;
+    if (P->pinned) staging().release(P->pinned, P->pinned_cap, P->upload_evt);
+    clear_timing(P);
+    delete P;
+}
+
+pa_status pa_plan_get_info(const pa_plan_t *P, pa_plan_info *info) {
+    if (!P || !info) return PA_ERR_INVALID_ARGUMENT;
+    *info = P->info;
+    return PA_OK;
+}
+
+pa_status pa_slot_mapping(const int32_t *qsl, const int32_t *num_computed, const int32_t *block_table,
+                          int32_t num_reqs, int32_t num_tokens, int32_t max_blocks_per_req,
+                          int32_t block_size, int64_t *slot_mapping, void *stream) {
+    if (num_tokens < 0 || num_reqs < 0 || max_blocks_per_req <= 0 || block_size <= 0)
+        return PA_ERR_INVALID_ARGUMENT;
+    if (num_tokens == 0) return PA_OK;
+    if (num_reqs == 0 || !qsl || !num_computed || !block_table || !slot_mapping) return PA_ERR_INVALID_ARGUMENT;
+    cudaError_t e = launch_slot_mapping(qsl, num_computed, block_table, num_reqs, num_tokens, max_blocks_per_req,
+                                        block_size, slot_mapping, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_write_kv(const void *key, const void *value, const int64_t *slot_mapping, int32_t num_tokens,
+                      int32_t num_heads_kv, int32_t head_dim, void *key_cache, void *value_cache,
+                      int64_t num_slots, int32_t *device_error_word, void *stream) {
+    if (num_tokens < 0 || num_heads_kv <= 0 || head_dim <= 0 || num_slots < 0) return PA_ERR_INVALID_ARGUMENT;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !slot_mapping || !key_cache || !value_cache) return PA_ERR_INVALID_ARGUMENT;
+    const int64_t row_bytes = static_cast<int64_t>(num_heads_kv) * head_dim * 2;
+    if (row_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16))
+        return PA_ERR_INVALID_ARGUMENT;
+    cudaError_t e = launch_write_kv(key, value, slot_mapping, num_tokens, num_heads_kv * head_dim, key_cache,
+                                    value_cache, num_slots, device_error_word, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_attention(const pa_plan_t *plan, const void *q, const void *key_cache, const void *value_cache,
+                       const int32_t *block_table, void *out, void *workspace, size_t workspace_bytes,
+                       void *stream_) {
+    if (!plan) return PA_ERR_INVALID_ARGUMENT;
+    pa_plan_s *P = const_cast<pa_plan_s *>(plan);
+    if (P->T == 0) return PA_OK;
+    if (!q || !key_cache || !value_cache || !block_table || !out || !workspace) return PA_ERR_INVALID_ARGUMENT;
+    if (!aligned(workspace, 256) || !aligned(q, 16) || !aligned(out, 16) || !aligned(key_cache, 16) ||
+        !aligned(value_cache, 16) || !aligned(block_table, 4))
+        return PA_ERR_INVALID_ARGUMENT;
+    if (workspace_bytes < P->ws_bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    std::lock_guard<std::mutex> lock(P->mu);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+
+    // metadata upload (pinned, stream ordered)
+    if (P->blob_bytes) {
+        if (!P->pinned) {
+            if (!staging().acquire(P->blob_bytes, &P->pinned, &P->pinned_cap, &P->upload_evt)) return PA_ERR_CUDA;
+            std::memcpy(P->pinned, P->blob.data(), P->blob_bytes);
+        }
+        if (record(P, 3, true, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (cudaMemcpyAsync(ws + kHeader, P->pinned, P->blob_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+            return PA_ERR_CUDA;
+        if (record(P, 3, false, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (cudaEventRecord(P->upload_evt, stream) != cudaSuccess) return PA_ERR_CUDA;
+    }
+    int32_t *err = reinterpret_cast<int32_t *>(ws);
+    const int32_t *part_offset = reinterpret_cast<const int32_t *>(ws + P->off_part);
+    float *o_part = reinterpret_cast<float *>(ws + P->off_opart);
+    float2 *ml_part = reinterpret_cast<float2 *>(ws + P->off_ml);
+    uint16_t *out16 = static_cast<uint16_t *>(out);
+
+    CUtensorMap tm_k, tm_v;
+    const uint64_t rows = static_cast<uint64_t>(P->num_blocks) * kBlockSize;
+    if (!make_map(&tm_k, key_cache, P->D, P->Hkv, rows, 1, kBlockSize) ||
+        !make_map(&tm_v, value_cache, P->D, P->Hkv, rows, 1, kBlockSize))
+        return PA_ERR_CUDA;
+
+    if (!P->tiles.empty()) {
+        CUtensorMap tm_q;
+        if (!make_map(&tm_q, q, P->D, P->Hq, P->T, P->G, kTileRows / P->G)) return PA_ERR_CUDA;
+        ExtendParams ep{};
+        ep.out = out16;
+        ep.block_table = block_table;
+        ep.tiles = reinterpret_cast<const ExtendTile *>(ws + P->off_tiles);
+        ep.part_offset = part_offset;
+        ep.o_part = o_part;
+        ep.ml_part = ml_part;
+        ep.err = err;
+        ep.num_tiles = static_cast<int32_t>(P->tiles.size());
+        ep.max_blocks = P->max_blocks;
+        ep.num_blocks = P->num_blocks;
+        ep.num_heads_q = P->Hq;
+        ep.group = P->G;
+        ep.n_groups = P->n_groups;
+        ep.heads_per_group = P->HG;
+        ep.scale_log2 = P->scale_log2;
+        if (record(P, 1, true, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_extend(P->D, tm_q, tm_k, tm_v, ep, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (record(P, 1, false, stream) != cudaSuccess) return PA_ERR_CUDA;
+    }
+    if (!P->items.empty()) {
+        DecodeParams dp{};
+        dp.q = static_cast<const uint16_t *>(q);
+        dp.out = out16;
+        dp.block_table = block_table;
+        dp.items = reinterpret_cast<const DecodeItem *>(ws + P->off_items);
+        dp.cta_begin = reinterpret_cast<const int32_t *>(ws + P->off_cta);
+        dp.part_offset = part_offset;
+        dp.o_part = o_part;
+        dp.ml_part = ml_part;
+        dp.err = err;
+        dp.max_blocks = P->max_blocks;
+        dp.num_blocks = P->num_blocks;
+        dp.num_heads_q = P->Hq;
+        dp.group = P->G;
+        dp.n_groups = P->n_groups;
+        dp.scale_log2 = P->scale_log2;
+        const int ncta = static_cast<int>(P->cta_begin.size()) - 1;
+        if (record(P, 0, true, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_decode(P->D, P->HG, ncta, tm_k, tm_v, dp, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (record(P, 0, false, stream) != cudaSuccess) return PA_ERR_CUDA;
+    }
+    if (!P->merges.empty()) {
+        MergeParams mp{};
+        mp.out = out16;
+        mp.rows = reinterpret_cast<const MergeRow *>(ws + P->off_merges);
+        mp.o_part = o_part;
+        mp.ml_part = ml_part;
+        mp.num_rows = static_cast<int32_t>(P->merges.size());
+        mp.num_heads_q = P->Hq;
+        mp.max_heads = P->HG * P->G;
+        if (record(P, 2, true, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_merge(P->D, mp, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (record(P, 2, false, stream) != cudaSuccess) return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+pa_status pa_check_device_errors(int32_t *word, int32_t *bits, void *stream_) {
+    if (bits) *bits = 0;
+    if (!word) return PA_ERR_INVALID_ARGUMENT;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    int32_t host = 0;
+    if (cudaMemcpyAsync(&host, word, sizeof host, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaMemsetAsync(word, 0, sizeof host, stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (bits) *bits = host;
+    return host == 0 ? PA_OK : PA_ERR_DEVICE_CHECK;
+}
+
+pa_status pa_plan_enable_timing(pa_plan_t *P, int32_t enable) {
+    if (!P) return PA_ERR_INVALID_ARGUMENT;
+    std::lock_guard<std::mutex> lock(P->mu);
+    clear_timing(P);
+    P->timing = enable != 0;
+    return PA_OK;
+}
+
+pa_status pa_plan_kernel_times(pa_plan_t *P, double ms_total[4], int32_t launches[4]) {
+    if (!P || !ms_total || !launches) return PA_ERR_INVALID_ARGUMENT;
+    std::lock_guard<std::mutex> lock(P->mu);
+    for (int k = 0; k < 4; ++k) {
+        ms_total[k] = 0.0;
+        launches[k] = static_cast<int32_t>(P->ev_stop[k].size());
+        for (size_t i = 0; i < P->ev_stop[k].size(); ++i) {
+            if (cudaEventSynchronize(P->ev_stop[k][i]) != cudaSuccess) return PA_ERR_CUDA;
+            float ms = 0.f;
+            if (cudaEventElapsedTime(&ms, P->ev_start[k][i], P->ev_stop[k][i]) != cudaSuccess) return PA_ERR_CUDA;
+            ms_total[k] += ms;
+        }
+    }
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,150 @@
+// Internal work-list records shared by the host planner and the kernels.
+// Everything here is plain old data: the planner fills host arrays of these,
+// pa_attention copies them into the workspace, the kernels read them there.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace pa {
+
+constexpr int kBlockSize = 16;     // tokens per cache block
+constexpr int kTileKeys = 128;     // keys per tensor-core tile (8 blocks)
+constexpr int kTileRows = 128;     // query rows per tensor-core tile
+constexpr int kMaxDecodeHeads = 8; // kv heads one decode CTA serves
+
+// Split-KV decode kernel resources, shared by the planner (which sizes the
+// persistent grid without touching a device) and the kernel.
+constexpr int decode_stage_bytes(int d, int hg) { return 2 * hg * (d / 64) * 16 * 128; }
+constexpr int decode_stages(int d, int hg) {
+    return decode_stage_bytes(d, hg) * 4 <= 200 * 1024   ? 4
+           : decode_stage_bytes(d, hg) * 3 <= 200 * 1024 ? 3
+                                                          : 2;
+}
+constexpr int decode_threads(int hg) { return (hg + 1) * 32; }
+constexpr int decode_smem_bytes(int d, int hg) {
+    return decode_stages(d, hg) * decode_stage_bytes(d, hg) + 3 * decode_stages(d, hg) * 8 + 1024;
+}
+constexpr int kSmemPerSm = 233472;  // 228 KiB of shared memory per SM
+constexpr int decode_ctas_per_sm_static(int d, int hg) {
+    return (kSmemPerSm / (decode_smem_bytes(d, hg) + 1024)) < (2048 / decode_threads(hg))
+               ? (kSmemPerSm / (decode_smem_bytes(d, hg) + 1024))
+               : (2048 / decode_threads(hg));
+}
+
+// Device error word bits (mirrors PA_DEVERR_* of pa.h).
+constexpr int kErrSlotRange = 0x1;
+constexpr int kErrBlockRange = 0x2;
+constexpr int kErrTimeout = 0x4;
+
+// One contiguous run of one request's key blocks for one group of kv heads,
+// processed by one persistent CTA of the split-KV decode kernel.
+struct DecodeItem {
+    int32_t token;       // query row (q / out row)
+    int32_t req;         // block-table row
+    int32_t page_begin;  // first logical block of the run
+    int32_t page_end;    // one past the last logical block of the run
+    int32_t key_end;     // keys >= key_end are masked (= seq_len)
+    int32_t head_group;  // kv heads [head_group*HG, head_group*HG + HG)
+    int32_t part;        // partial index of this run (-1: write bf16 output)
+    int32_t pad;
+};
+
+// One tile of 128 query rows (tokens x G query heads of one kv head) against
+// the key range [key_begin, key_end) of one request's context.
+struct ExtendTile {
+    int32_t t0;          // first token of the tile
+    int32_t n_tok;       // tokens of the tile that belong to it (<= 128/G)
+    int32_t req;         // block-table row the keys are read through
+    int32_t pos0;        // absolute position of token t0 (causal bound)
+    int32_t key_begin;   // block aligned
+    int32_t key_end;
+    int32_t kv_head;
+    int32_t part;        // partial index (-1: write bf16 output)
+    int32_t causal;      // 0: every key of the range is visible (shared prefix)
+    int32_t pad[3];
+};
+
+// The query heads [hq_begin, hq_begin + hq_count) of one token whose output
+// is the merge of `count` partial results starting at partial slot `slot0`.
+struct MergeRow {
+    int32_t token;
+    int32_t slot0;
+    int32_t count;
+    int32_t hq_begin;
+    int32_t hq_count;
+    int32_t pad[3];
+};
+
+// Layout of the workspace:
+//   [0, 256)            error word and reserved
+//   meta blob           part_offset[T] | cta_begin[ncta+1] | DecodeItem[] |
+//                       ExtendTile[] | MergeRow[]        (each 16-byte aligned)
+//   o_part              float [num_slots][Hq][D]
+//   ml_part             float2 [num_slots][Hq]  (log2-domain max, sum)
+struct DecodeParams {
+    const uint16_t *q;
+    uint16_t *out;
+    const int32_t *block_table;
+    const DecodeItem *items;
+    const int32_t *cta_begin;   // [gridDim.x + 1] item ranges per CTA
+    const int32_t *part_offset; // [T][n_groups] first partial slot of (token, head group)
+    float *o_part;
+    float2 *ml_part;
+    int32_t *err;
+    int32_t max_blocks;
+    int32_t num_blocks;
+    int32_t num_heads_q;
+    int32_t group;              // G = Hq / Hkv
+    int32_t n_groups;           // kv-head groups (Hkv / heads per group)
+    float scale_log2;           // softmax_scale * log2(e)
+};
+
+struct ExtendParams {
+    uint16_t *out;
+    const int32_t *block_table;
+    const ExtendTile *tiles;
+    const int32_t *part_offset;
+    float *o_part;
+    float2 *ml_part;
+    int32_t *err;
+    int32_t num_tiles;
+    int32_t max_blocks;
+    int32_t num_blocks;
+    int32_t num_heads_q;
+    int32_t group;
+    int32_t n_groups;
+    int32_t heads_per_group;    // kv heads per head group (indexes part_offset)
+    float scale_log2;
+};
+
+struct MergeParams {
+    uint16_t *out;
+    const MergeRow *rows;
+    const float *o_part;
+    const float2 *ml_part;
+    int32_t num_rows;
+    int32_t num_heads_q;
+    int32_t max_heads;          // largest hq_count of any row
+};
+
+// Launchers (each returns the launch's cudaError_t).
+cudaError_t launch_slot_mapping(const int32_t *qsl, const int32_t *num_computed,
+                                const int32_t *block_table, int32_t num_reqs, int32_t num_tokens,
+                                int32_t max_blocks, int32_t block_size, int64_t *slots,
+                                cudaStream_t stream);
+cudaError_t launch_write_kv(const void *key, const void *value, const int64_t *slots,
+                            int32_t num_tokens, int32_t row_elems, void *key_cache,
+                            void *value_cache, int64_t num_slots, int32_t *err,
+                            cudaStream_t stream);
+// Decode kernel: head_dim D, heads per CTA hg.  Returns cudaErrorInvalidValue
+// for an unsupported (D, hg).
+cudaError_t launch_decode(int head_dim, int hg, int num_ctas, const CUtensorMap &tm_k,
+                          const CUtensorMap &tm_v, const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_extend(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                          const CUtensorMap &tm_v, const ExtendParams &p, cudaStream_t stream);
+cudaError_t launch_merge(int head_dim, const MergeParams &p, cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,203 @@
+"""The C ABI on the CPU: the library loads, exports what pa.h declares, and
+pa_plan validates metadata and decomposes work (no kernel is launched)."""
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+from paged_kv_cache_16_gb300 import binding, build, workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_symbols_exported(lib):
+    names = declared_functions()
+    assert "pa_attention" in names and "pa_plan" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in pa.h but not exported"
+    assert sorted(binding.EXPORTED) == names
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert binding.status_string(s)
+    assert binding.status_string(99) == "unknown status"
+
+
+def desc(batch, **over):
+    kw = dict(num_heads_q=batch.num_heads_q, num_heads_kv=batch.num_heads_kv, head_dim=batch.head_dim,
+              num_blocks=batch.num_blocks, query_start_loc=batch.query_start_loc, seq_lens=batch.seq_lens,
+              num_computed_tokens=batch.num_computed, block_table_host=batch.block_table,
+              num_common_prefix_blocks=batch.num_common_prefix_blocks, softmax_scale=batch.softmax_scale,
+              num_sms=152)
+    kw.update(over)
+    return kw
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return workloads.tiny("1B")
+
+
+def test_valid_plan(lib, tiny):
+    assert binding.pa_plan_status(**desc(tiny)) == binding.PA_OK
+
+
+@pytest.mark.parametrize("case", [
+    "qsl_start", "qsl_decreasing", "length_identity", "too_many_blocks", "block_id_range",
+    "block_id_negative", "heads_indivisible", "scale_zero", "scale_nan", "negative_prefix",
+    "prefix_not_computed", "prefix_not_shared", "zero_heads", "negative_sms"])
+def test_invalid_metadata(lib, tiny, case):
+    b = tiny
+    kw = desc(b)
+    qsl = b.query_start_loc.copy()
+    nc = b.num_computed.copy()
+    bt = b.block_table.copy()
+    if case == "qsl_start":
+        kw["query_start_loc"] = qsl + 1
+    elif case == "qsl_decreasing":
+        qsl[2] = qsl[3] + 1
+        kw["query_start_loc"] = qsl
+    elif case == "length_identity":
+        nc[1] += 1
+        kw["num_computed_tokens"] = nc
+    elif case == "too_many_blocks":
+        kw["block_table_host"] = bt[:, :1]
+    elif case == "block_id_range":
+        bt[0, 0] = b.num_blocks
+        kw["block_table_host"] = bt
+    elif case == "block_id_negative":
+        bt[3, 1] = -1
+        kw["block_table_host"] = bt
+    elif case == "heads_indivisible":
+        kw["num_heads_q"] = 5
+    elif case == "scale_zero":
+        kw["softmax_scale"] = 0.0
+    elif case == "scale_nan":
+        kw["softmax_scale"] = float("nan")
+    elif case == "negative_prefix":
+        kw["num_common_prefix_blocks"] = -1
+    elif case == "prefix_not_computed":
+        kw["num_common_prefix_blocks"] = 1     # requests with num_computed 0
+    elif case == "prefix_not_shared":
+        c = workloads.cascade(batch=4, lo=64, hi=80, num_blocks=400)
+        bt2 = c.block_table.copy()
+        bt2[2, [0, 1]] = bt2[2, [1, 0]]        # same ids, different order in one row
+        kw = desc(c, block_table_host=bt2)
+    elif case == "zero_heads":
+        kw["num_heads_kv"] = 0
+    elif case == "negative_sms":
+        kw["num_sms"] = -1
+    assert binding.pa_plan_status(**kw) == binding.PA_ERR_INVALID_ARGUMENT
+
+
+@pytest.mark.parametrize("over", [dict(head_dim=96), dict(block_size=32), dict(num_heads_q=6, num_heads_kv=2),
+                                  dict(num_heads_q=64, num_heads_kv=2)])
+def test_unsupported_shapes(lib, tiny, over):
+    kw = desc(tiny, **over)
+    if "block_size" in over:
+        # keep the metadata consistent with 32-token blocks
+        kw["block_table_host"] = tiny.block_table[:, :2]
+    assert binding.pa_plan_status(**kw) == binding.PA_ERR_UNSUPPORTED
+
+
+def test_mixed_batch_example_metadata(lib):
+    """The R0/R1/R2 worked example (decode, prefix-hit chunk, spec verify)."""
+    qsl = np.array([0, 1, 257, 260], np.int32)
+    seq = np.array([1025, 768, 603], np.int32)
+    nc = np.array([1024, 512, 600], np.int32)
+    kw = dict(num_heads_q=8, num_heads_kv=2, head_dim=128, num_blocks=200, query_start_loc=qsl, seq_lens=seq,
+              num_computed_tokens=nc, max_blocks_per_req=65, softmax_scale=0.1, num_sms=152)
+    plan = binding.pa_plan(**kw)
+    info = plan.info()
+    assert info["num_decode_rows"] == 1 and info["num_extend_rows"] == 2
+    # 256 + 3 query tokens, G = 4 -> 32 tokens per tile: 8 + 1 tiles per kv head
+    assert info["num_extend_tiles"] == 2 * (8 + 1)
+    bad = nc.copy()
+    bad[1] = 511
+    assert binding.pa_plan_status(**{**kw, "num_computed_tokens": bad}) == binding.PA_ERR_INVALID_ARGUMENT
+
+
+@pytest.mark.parametrize("maker", ["decode", "long", "mixed", "cascade", "cascade_off"])
+def test_plan_decomposition(lib, maker):
+    """Row classification, tile counts, byte and FLOP counts, cascade slots
+    and launch counts of the plan agree with the batch (host-side view)."""
+    if maker == "decode":
+        b = workloads.decode(batch=16, num_blocks=5000)
+    elif maker == "long":
+        b = workloads.long_context(batch=2, context=16384, num_blocks=2100)
+    elif maker == "mixed":
+        b = workloads.mixed(n_decode=24, n_shared=4, chunk=300, chunk_b_cached=500, lo=100, hi=900)
+    elif maker == "cascade":
+        b = workloads.cascade(batch=8, num_blocks=1000)
+    else:
+        b = workloads.cascade(batch=8, num_blocks=1000, use_cascade=False)
+    plan = binding.pa_plan(**desc(b))
+    info = plan.info()
+    q_lens = b.q_lens
+    n_prefix = b.num_common_prefix_blocks
+    kb = n_prefix * 16
+    dec = [r for r in range(b.num_reqs) if q_lens[r] == 1]
+    ext = [r for r in range(b.num_reqs) if q_lens[r] > 1]
+    assert info["num_decode_rows"] == len(dec) and info["num_extend_rows"] == len(ext)
+    row_bytes = b.num_heads_kv * b.head_dim * 4
+    assert info["decode_kv_bytes"] == sum((int(b.seq_lens[r]) - kb) * row_bytes for r in dec)
+    G = b.num_heads_q // b.num_heads_kv
+    tpt = 128 // G
+    n_ext_tiles = sum(math.ceil(q_lens[r] / tpt) for r in ext) * b.num_heads_kv
+    assert info["num_extend_tiles"] == n_ext_tiles + info["num_prefix_tiles"]
+    if n_prefix:
+        assert info["num_prefix_tiles"] > 0
+        assert info["prefix_kv_bytes"] == kb * row_bytes
+        assert info["num_merge_rows"] == b.num_tokens
+    else:
+        assert info["num_prefix_tiles"] == 0
+    assert plan.workspace_bytes % 256 == 0
+    assert info["kernels_per_call"] == (info["num_decode_items"] > 0) + (info["num_extend_tiles"] > 0) + \
+        (info["num_merge_rows"] > 0)
+    assert info["num_decode_ctas"] <= 152
+
+
+def test_plan_is_deterministic_and_placement_free(lib):
+    """The plan depends on lengths only: a different physical placement of
+    the same batch gives the same decomposition and workspace size."""
+    a = workloads.decode(batch=16, num_blocks=5000, seed=0)
+    b = workloads.decode(batch=16, num_blocks=5000, seed=0)
+    b_bt = np.random.default_rng(9).permutation(5000)[: a.block_table.size].reshape(a.block_table.shape)
+    pa = binding.pa_plan(**desc(a))
+    pb = binding.pa_plan(**desc(b, block_table_host=b_bt.astype(np.int32)))
+    assert pa.info() == pb.info() and pa.workspace_bytes == pb.workspace_bytes
+
+
+def test_empty_batch(lib):
+    kw = dict(num_heads_q=4, num_heads_kv=2, head_dim=64, num_blocks=4,
+              query_start_loc=np.zeros(1, np.int32), seq_lens=np.zeros(0, np.int32),
+              num_computed_tokens=np.zeros(0, np.int32), max_blocks_per_req=1, softmax_scale=0.125,
+              num_sms=152)
+    plan = binding.pa_plan(**kw)
+    assert plan.info()["num_tokens"] == 0 and plan.info()["kernels_per_call"] == 0
+
+
+def test_idle_requests_and_zero_lengths(lib):
+    """q_len = 0 rows (and a zero-length request) plan to no work."""
+    kw = dict(num_heads_q=4, num_heads_kv=2, head_dim=64, num_blocks=8,
+              query_start_loc=np.array([0, 0, 1, 1], np.int32), seq_lens=np.array([5, 3, 0], np.int32),
+              num_computed_tokens=np.array([5, 2, 0], np.int32), max_blocks_per_req=1,
+              softmax_scale=0.125, num_sms=152)
+    info = binding.pa_plan(**kw).info()
+    assert info["num_decode_rows"] == 1 and info["num_extend_rows"] == 0 and info["num_tokens"] == 1
