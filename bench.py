@@ -48,6 +48,9 @@ WORKLOADS = {
     "mixed": ("mixed continuous-batching step: 256 decodes seq_len U[1024,8192] (32 share a 1024-token "
               "prefix) + 2048-token chunk from 0 + 2048-token chunk over 4096 cached; Hq=32 Hkv=8 D=128",
               lambda seed, dev: workloads.mixed(seed=seed, device=dev, pool_device=dev)),
+    "prefill": ("the two chunked-prefill requests of the mixed step alone: a 2048-token chunk from 0 and a "
+                "2048-token chunk over 4096 cached tokens; Hq=32 Hkv=8 D=128",
+                lambda seed, dev: workloads.mixed(seed=seed, n_decode=0, n_shared=0, device=dev, pool_device=dev)),
     "long": ("long-context decode, 70B-shaped layer: 8 requests x 131072 tokens, Hq=64 Hkv=8 D=128",
              lambda seed, dev: workloads.long_context(seed=seed, device=dev, pool_device=dev)),
     "cascade": ("cascade shared-prefix decode: 128 decodes over a 4096-token common prefix "
