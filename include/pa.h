@@ -208,6 +208,48 @@ pa_status pa_check_device_errors(int32_t *device_error_word, int32_t *bits, void
 pa_status pa_plan_enable_timing(pa_plan_t *plan, int32_t enable);
 pa_status pa_plan_kernel_times(pa_plan_t *plan, double ms_total[4], int32_t launches[4]);
 
+/* Size in bytes of the library-owned scratch array pa_attention_no_alloc
+ * uses in place of a caller workspace (16 MiB per device). */
+#define PA_NO_ALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * pa_attention for callers that cannot allocate device memory.  The pages
+ * have no counterpart of this call; it exists for users of this library, not
+ * for the method.
+ *
+ * Who can't allocate: an engine that gives nearly all free device memory to
+ * its paged KV pool at start-up has no room for a per-step workspace, and a
+ * hot path that must not call cudaMalloc/cudaFree (they can synchronise the
+ * whole device) cannot create one on demand.  Such a caller passes the same
+ * inputs and output as to pa_attention but no workspace: the scratch is a
+ * library-owned device array of PA_NO_ALLOC_SCRATCH_BYTES, created on each
+ * device that loads the library's module holding it and kept until exit.
+ * This call allocates nothing: no cudaMalloc, cudaMallocHost, cudaFree, no
+ * pinned staging buffer (the metadata is copied from the plan's pageable host
+ * image, so the upload waits for the stream's earlier work), and it records
+ * no timing events.
+ *
+ *   plan, q, key_cache, value_cache, block_table, out   as for pa_attention
+ *   device_error_word  optional DEVICE int32: receives (overwritten, not ORed)
+ *                      this call's PA_DEVERR_* bits; read it with
+ *                      pa_check_device_errors
+ *   stream             cudaStream_t
+ * Returns PA_ERR_WORKSPACE_TOO_SMALL, before enqueueing anything, when the
+ * plan's workspace_bytes exceeds PA_NO_ALLOC_SCRATCH_BYTES; otherwise as
+ * pa_attention.
+ *
+ * The first call on a device (made with that device current) looks up the
+ * array's device address; make that first call before any stream capture.
+ * Every call on a device shares the one array and the array keeps the last
+ * call's contents: the error word is cleared by each call, everything else is
+ * rewritten before it is read.  Calls whose work can overlap on the GPU (on
+ * different streams, or from different host threads without ordering) race
+ * on the array and must be serialised by the caller.
+ */
+pa_status pa_attention_no_alloc(const pa_plan_t *plan, const void *q, const void *key_cache,
+                                const void *value_cache, const int32_t *block_table, void *out,
+                                int32_t *device_error_word, void *stream);
+
 /* Static description of a status code. */
 const char *pa_status_string(pa_status status);
 

@@ -29,7 +29,7 @@ PA_DEVERR_TIMEOUT = 0x4
 # symbols include/pa.h declares (checked by the CPU tests)
 EXPORTED = ("pa_plan", "pa_plan_destroy", "pa_plan_get_info", "pa_slot_mapping", "pa_write_kv",
             "pa_attention", "pa_check_device_errors", "pa_plan_enable_timing",
-            "pa_plan_kernel_times", "pa_status_string")
+            "pa_plan_kernel_times", "pa_status_string", "pa_attention_no_alloc")
 
 
 class PaError(RuntimeError):
@@ -114,6 +114,8 @@ def load(path: str | None = None, build_if_missing: bool = False) -> ctypes.CDLL
     lib.pa_write_kv.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, i64, vp, vp]
     lib.pa_attention.restype = ctypes.c_int
     lib.pa_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.pa_attention_no_alloc.restype = ctypes.c_int
+    lib.pa_attention_no_alloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
     lib.pa_check_device_errors.restype = ctypes.c_int
     lib.pa_check_device_errors.argtypes = [vp, i32p, vp]
     lib.pa_plan_enable_timing.restype = ctypes.c_int
@@ -252,6 +254,18 @@ def pa_attention(plan: Plan, q, key_cache, value_cache, block_table, out, worksp
     nbytes = workspace.numel() * workspace.element_size()
     _check(load().pa_attention(plan.handle, _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_table),
                                _ptr(out), _ptr(workspace), nbytes, _stream(stream)), "pa_attention")
+
+
+def pa_attention_no_alloc(plan: Plan, q, key_cache, value_cache, block_table, out, device_error_word=None,
+                          stream=None):
+    """pa_attention with the library's fixed scratch array instead of a workspace
+    (for callers that cannot allocate device memory; see pa.h)."""
+    _check(load().pa_attention_no_alloc(plan.handle, _ptr(q), _ptr(key_cache), _ptr(value_cache),
+                                        _ptr(block_table), _ptr(out), _ptr(device_error_word), _stream(stream)),
+           "pa_attention_no_alloc")
+
+
+NO_ALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def pa_check_device_errors(word, stream=None) -> int:

@@ -10,42 +10,48 @@
 #include <cudaTypedefs.h>
 
 #include "../../include/pa.h"
-#include "pa_internal.h"
+#include "plan.h"
 
 using namespace pa;
 
-struct pa_plan_s {
-    // step shape
-    int32_t R = 0, Hq = 0, Hkv = 0, D = 0, num_blocks = 0, max_blocks = 0;
-    int32_t T = 0, G = 0, HG = 1, n_groups = 1, num_sms = 0;
-    int32_t n_prefix = 0;         // num_common_prefix_blocks (cascade when > 0)
-    int32_t prefix_req = -1;      // block-table row of the shared prefix
-    int32_t prefix_splits = 0;
-    float scale_log2 = 0.f;
-    // work lists
-    std::vector<int32_t> part_offset;   // [T * n_groups]
-    std::vector<int32_t> cta_begin;     // [ncta + 1]
-    std::vector<DecodeItem> items;
-    std::vector<ExtendTile> tiles;
-    std::vector<MergeRow> merges;
-    int32_t num_slots = 0;
-    // workspace layout
-    size_t off_part = 0, off_cta = 0, off_items = 0, off_tiles = 0, off_merges = 0;
-    size_t blob_bytes = 0, off_opart = 0, off_ml = 0, ws_bytes = 0;
-    std::vector<uint8_t> blob;          // host image of the metadata blob
-    void *pinned = nullptr;             // pinned staging copy used for async uploads
-    size_t pinned_cap = 0;
-    cudaEvent_t upload_evt = nullptr;   // recorded after each upload from `pinned`
-    pa_plan_info info{};
-    // timing
-    bool timing = false;
-    std::vector<cudaEvent_t> ev_start[4], ev_stop[4];
-    std::mutex mu;
-};
+namespace pa {
+
+// cuTensorMapEncodeTiled from the driver, fetched once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 3-D bf16 tensor map over [outer][mid][D] with a box of [box_outer][box_mid][64]
+// and 128-byte swizzling.
+bool make_map(CUtensorMap *tm, const void *ptr, uint64_t d, uint64_t mid, uint64_t outer,
+              uint32_t box_mid, uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {d, mid, outer};
+    cuuint64_t strides[2] = {d * 2, mid * d * 2};
+    cuuint32_t box[3] = {64, box_mid, box_outer};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace pa
 
 namespace {
 
-constexpr size_t kHeader = 256;
+constexpr size_t kHeader = kWorkspaceHeader;
 
 // Pinned staging buffers for the per-call metadata upload, recycled across
 // plans.  A plan takes a buffer on its first pa_attention call and hands it
@@ -111,37 +117,6 @@ int heads_per_group(int hkv) {
     for (int hg = kMaxDecodeHeads; hg > 1; hg >>= 1)
         if (hkv % hg == 0) return hg;
     return 1;
-}
-
-// cuTensorMapEncodeTiled from the driver, fetched once through the runtime.
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// 3-D bf16 tensor map over [outer][mid][D] with a box of [box_outer][box_mid][64]
-// and 128-byte swizzling.
-bool make_map(CUtensorMap *tm, const void *ptr, uint64_t d, uint64_t mid, uint64_t outer,
-              uint32_t box_mid, uint32_t box_outer) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {d, mid, outer};
-    cuuint64_t strides[2] = {d * 2, mid * d * 2};
-    cuuint32_t box[3] = {64, box_mid, box_outer};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
-                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
 }
 
 pa_status validate(const pa_batch_desc *d) {

@@ -1,0 +1,49 @@
+// The plan object behind the opaque pa_plan_t of pa.h (host only), and the
+// host helpers the entry points share.
+#pragma once
+#include <mutex>
+#include <vector>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+struct pa_plan_s {
+    // step shape
+    int32_t R = 0, Hq = 0, Hkv = 0, D = 0, num_blocks = 0, max_blocks = 0;
+    int32_t T = 0, G = 0, HG = 1, n_groups = 1, num_sms = 0;
+    int32_t n_prefix = 0;         // num_common_prefix_blocks (cascade when > 0)
+    int32_t prefix_req = -1;      // block-table row of the shared prefix
+    int32_t prefix_splits = 0;
+    float scale_log2 = 0.f;
+    // work lists
+    std::vector<int32_t> part_offset;   // [T * n_groups]
+    std::vector<int32_t> cta_begin;     // [ncta + 1]
+    std::vector<pa::DecodeItem> items;
+    std::vector<pa::ExtendTile> tiles;
+    std::vector<pa::MergeRow> merges;
+    int32_t num_slots = 0;
+    // workspace layout
+    size_t off_part = 0, off_cta = 0, off_items = 0, off_tiles = 0, off_merges = 0;
+    size_t blob_bytes = 0, off_opart = 0, off_ml = 0, ws_bytes = 0;
+    std::vector<uint8_t> blob;          // host image of the metadata blob
+    void *pinned = nullptr;             // pinned staging copy used for async uploads
+    size_t pinned_cap = 0;
+    cudaEvent_t upload_evt = nullptr;   // recorded after each upload from `pinned`
+    pa_plan_info info{};
+    // timing
+    bool timing = false;
+    std::vector<cudaEvent_t> ev_start[4], ev_stop[4];
+    std::mutex mu;
+};
+
+namespace pa {
+
+constexpr size_t kWorkspaceHeader = 256;  // error word + reserved, then the metadata blob
+
+// 3-D bf16 tensor map over [outer][mid][D] with a box of [box_outer][box_mid][64]
+// and 128-byte swizzling (false if the driver entry point is unavailable or
+// the encoding is rejected).
+bool make_map(CUtensorMap *tm, const void *ptr, uint64_t d, uint64_t mid, uint64_t outer, uint32_t box_mid,
+              uint32_t box_outer);
+
+}  // namespace pa
