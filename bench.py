@@ -64,7 +64,10 @@ WORKLOADS = {
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # dominant kernel from one ncu capture, valid only while the kernel source is
 # unchanged (sha256 of the file).  Filled in from profiles/.
-TRAFFIC = {}
+TRAFFIC = {
+    # (kernel, workload, source sha) -> bytes per launch; profiles/decode_kernel_decode-workload.md
+    ("decode", "decode", "2c4247d3e0dff9f8"): 645_201_152,
+}
 KERNEL_SOURCES = {"decode": "paged_kv_cache_16_gb300/csrc/k_decode.cu",
                   "extend": "paged_kv_cache_16_gb300/csrc/k_extend.cu"}
 
