@@ -100,7 +100,7 @@ typedef struct {
     int32_t num_extend_rows;       /* requests with more than one query token         */
     int32_t num_decode_ctas;       /* persistent CTAs of the split-KV decode kernel   */
     int32_t num_decode_items;      /* (request, key range, head group) segments       */
-    int32_t num_extend_tiles;      /* 128-row tiles of the tensor-core kernel         */
+    int32_t num_extend_tiles;      /* CTA tiles (<= 256 rows) of the tensor-core kernel */
     int32_t num_prefix_tiles;      /* of which: shared-prefix (cascade) tiles         */
     int32_t num_partial_slots;     /* (token, partition) partial results              */
     int32_t num_merge_rows;        /* tokens whose output is merged from partials     */

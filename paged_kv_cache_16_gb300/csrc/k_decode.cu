@@ -79,7 +79,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const DecodeItem item = p.items[it];
             const int32_t *bt = p.block_table + static_cast<int64_t>(item.req) * p.max_blocks;
             const int h0 = item.head_group * HG;
+            int32_t blk_lane = 0;       // block id of page (window + lane), 32 pages at a time
+            int window = item.page_begin - 32;
             for (int pg = item.page_begin; pg < item.page_end; ++pg) {
+                if (pg - window >= 32) {
+                    window = pg;
+                    blk_lane = pg + lane < item.page_end ? bt[pg + lane] : 0;
+                }
                 const int s = issued % C::NS;
                 const int n = issued / C::NS;
                 if (n > 0 && !warp_wait(empty(s), (n & 1) ^ 1, &abort_flag)) {
@@ -87,7 +93,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     ok = false;
                     break;
                 }
-                const int32_t blk = bt[pg];
+                const int32_t blk = __shfl_sync(0xffffffffu, blk_lane, pg - window);
                 const bool valid = blk >= 0 && blk < p.num_blocks;
                 if (lane == 0) {
                     if (valid) {

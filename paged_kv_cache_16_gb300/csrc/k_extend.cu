@@ -1,27 +1,33 @@
-// Extend / chunked-prefill attention tile on the 5th-generation tensor cores
+// Extend / chunked-prefill attention on the 5th-generation tensor cores
 // (tcgen05, accumulators in tensor memory), and the shared-prefix stage of
 // the cascade route.
 //
 // What one CTA computes (page "vLLM 推理流程分析" §6.2: varlen causal
 // attention through block_table; §10.1: a token sees itself and earlier
 // tokens; §5.1.2: positions = num_computed + offset in the chunk):
-//   128 query rows = 128/G consecutive tokens x the G query heads of one kv
-//   head, against keys [key_begin, key_end) of one request's context, read
-//   through the block table in tiles of 128 keys (8 blocks).  Row (i, g) at
-//   absolute position pos0 + i sees key j iff j <= pos0 + i (causal tiles);
-//   shared-prefix tiles see their whole key range.
+//   up to 256 query rows = 2 sub-tiles of 128 rows, each 128/G consecutive
+//   tokens x the G query heads of one kv head, against keys
+//   [key_begin, key_end) of one request's context, read through the block
+//   table in tiles of 128 keys (8 blocks).  Row (i, g) at absolute position
+//   pos0 + i sees key j iff j <= pos0 + i (causal tiles); shared-prefix tiles
+//   see their whole key range.  Both sub-tiles share every K/V tile loaded.
 //
-// Per 128-key tile:  S = Q K^T   (tcgen05.mma, M=128 N=128 K=D, S in TMEM)
-//                    P = exp2(S*scale*log2e - m)  (4 softmax warps, one row each)
-//                    O += P V    (tcgen05.mma, M=128 N=D K=128, O in TMEM)
+// Per 128-key tile and sub-tile t:
+//   S_t = Q_t K^T        tcgen05.mma M=128 N=128 K=D, A and B from shared memory
+//   P_t = exp2(S_t*scale*log2e - m)   softmax warpgroup t, one row per thread,
+//                        written back to tensor memory over S_t as bf16 pairs
+//   O_t += P_t V         tcgen05.mma M=128 N=D K=128, A from tensor memory
 // Warp roles: warp 0 TMA producer (Q once, K/V blocks into a 2-stage ring),
-// warp 1 MMA issuer (one thread) and TMEM owner, warps 2-5 softmax,
-// correction and epilogue.  S is double-buffered in TMEM so the QK^T of tile
-// j+1 overlaps the softmax of tile j.  The running max is only moved (and O
-// rescaled) when it grows by more than 2^8, which keeps every weight <= 256.
+// warp 1 MMA issuer (one thread) and tensor-memory owner, warps 2-5 softmax
+// of sub-tile 0, warps 6-9 softmax of sub-tile 1.  The MMA thread alternates
+// between the sub-tiles, so the tensor core works on one while the other's
+// softmax runs.  The running max only moves (and O is rescaled) when it
+// grows by more than 2^8, which keeps every weight <= 256.
 //
+// Tensor memory (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256)
+// (P_t in the first 64 columns of S_t), O_0 [256,256+D), O_1 [384,384+D).
 // Shared memory tiles are 128-byte-swizzled [rows][64 elements] halves:
-//   Q  (A, K-major), K (B, K-major), P (A, K-major), V (B, MN-major).
+// Q_t (A, K-major), K (B, K-major), V (B, MN-major).
 #include "dev.cuh"
 
 namespace pa {
@@ -33,19 +39,20 @@ template <int D>
 struct ExtCfg {
     static constexpr int NH = D / 64;
     static constexpr int HALF = 128 * 128;            // [128 rows][64] bf16 half tile
-    static constexpr int QB = NH * HALF;              // Q tile bytes
+    static constexpr int QB = NH * HALF;              // one Q sub-tile
     static constexpr int KVB = NH * HALF;             // K (or V) tile bytes per stage
-    static constexpr int PB = 2 * HALF;               // P tile: 128 rows x 128 keys
     static constexpr int NS = 2;
-    static constexpr int THREADS = 192;
-    static constexpr int TILE_SMEM = QB + NS * 2 * KVB + PB;
-    // keep one CTA per SM: it owns all 512 TMEM columns
+    static constexpr int THREADS = 320;
+    static constexpr int TILE_SMEM = 2 * QB + NS * 2 * KVB;
+    // one CTA per SM: it owns all 512 tensor-memory columns
     static constexpr int SMEM = (TILE_SMEM + 2048 < 120 * 1024) ? 120 * 1024 : TILE_SMEM + 2048;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t COL_O = 256;
     static constexpr uint32_t IDESC_QK = idesc_bf16(128, 128, false, false);
     static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
 };
+
+__device__ __forceinline__ uint32_t col_s(int t) { return static_cast<uint32_t>(t) * 128u; }
+__device__ __forceinline__ uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(t) * 128u; }
 
 // barrier indices
 enum : int {
@@ -53,16 +60,15 @@ enum : int {
     B_KFULL = 1,   // +stage
     B_VFULL = 3,   // +stage
     B_KVEMPTY = 5, // +stage
-    B_SFULL = 7,   // +buffer
-    B_SFREE = 9,   // +buffer
-    B_PFULL = 11,
-    B_ODONE = 12,
+    B_SFULL = 7,   // +sub-tile
+    B_PFULL = 9,   // +sub-tile
+    B_ODONE = 11,  // +sub-tile
     B_DRAIN = 13,
     NUM_BARS = 14
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
 extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const ExtendParams p) {
     using C = ExtCfg<D>;
@@ -72,17 +78,30 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     __shared__ __align__(8) uint64_t bars[NUM_BARS];
 
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-    const uint32_t q_s = base;
-    auto k_s = [&](int s) { return base + C::QB + static_cast<uint32_t>(s) * 2 * C::KVB; };
+    auto q_s = [&](int t) { return base + static_cast<uint32_t>(t) * C::QB; };
+    auto k_s = [&](int s) { return base + 2 * C::QB + static_cast<uint32_t>(s) * 2 * C::KVB; };
     auto v_s = [&](int s) { return k_s(s) + C::KVB; };
-    const uint32_t p_s = base + C::QB + C::NS * 2 * C::KVB;
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const ExtendTile tile = p.tiles[blockIdx.x];
     const int G = p.group;
-    const int n_tiles = (tile.key_end - tile.key_begin + kTileKeys - 1) / kTileKeys;
+    const int tpt = kTileRows / G;                    // tokens per 128-row sub-tile
+    // key tiles each sub-tile needs (0 for an empty sub-tile)
+    int n_sub[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int first = t * tpt;
+        if (first >= tile.n_tok) {
+            n_sub[t] = 0;
+            continue;
+        }
+        const int last = min(tile.n_tok, first + tpt);   // one past the sub-tile's last token
+        const int kend = tile.causal ? min(tile.key_end, tile.pos0 + last) : tile.key_end;
+        n_sub[t] = (kend - tile.key_begin + kTileKeys - 1) / kTileKeys;
+    }
+    const int n_tiles = max(n_sub[0], n_sub[1]);
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -92,12 +111,11 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mbar_init(bar(B_VFULL + s), 1);
             mbar_init(bar(B_KVEMPTY + s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(B_SFULL + b), 1);
-            mbar_init(bar(B_SFREE + b), 128);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(bar(B_SFULL + t), 1);
+            mbar_init(bar(B_PFULL + t), 128);
+            mbar_init(bar(B_ODONE + t), 1);
         }
-        mbar_init(bar(B_PFULL), 128);
-        mbar_init(bar(B_ODONE), 1);
         mbar_init(bar(B_DRAIN), 1);
         fence_barrier_init();
     }
@@ -112,15 +130,18 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
     if (warp == 0) {
         // -------------------------------------------------------- producer --
+        const int n_q = n_sub[1] > 0 ? 2 : 1;
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(bar(B_Q), C::QB);
+            mbar_arrive_expect_tx(bar(B_Q), n_q * C::QB);
         }
         __syncwarp();
-        if (lane < C::NH)
-            tma_load_3d(q_s + lane * C::HALF, &tm_q, lane * 64, tile.kv_head * G, tile.t0, bar(B_Q));
+        if (lane < n_q * C::NH) {
+            const int t = lane / C::NH, half = lane % C::NH;
+            tma_load_3d(q_s(t) + half * C::HALF, &tm_q, half * 64, tile.kv_head * G, tile.t0 + t * tpt, bar(B_Q));
+        }
         const int32_t *bt = p.block_table + static_cast<int64_t>(tile.req) * p.max_blocks;
         int issued = 0;
         for (int j = 0; j < n_tiles; ++j) {
@@ -175,125 +196,161 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // ------------------------------------------------------ MMA issuer --
         if (lane == 0) {
             bool ok = mbar_wait(bar(B_Q), 0, &abort_flag);
-            tc_fence_after();
-            auto pv = [&](int jj) -> bool {
-                const int s = jj % C::NS;
-                if (!mbar_wait(bar(B_PFULL), jj & 1, &abort_flag)) return false;
-                if (!mbar_wait(bar(B_VFULL + s), (jj / C::NS) & 1, &abort_flag)) return false;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kTileKeys / 16; ++kk) {
-                    const uint64_t a = sdesc_sw128(p_s + (kk / 4) * C::HALF + (kk % 4) * 32, 16, 1024);
-                    const uint64_t b = sdesc_sw128(v_s(s) + kk * 2048, C::HALF, 1024);
-                    tc_mma(tmem + C::COL_O, a, b, C::IDESC_PV, (jj > 0 || kk > 0) ? 1u : 0u);
-                }
-                tc_commit(bar(B_ODONE));
-                tc_commit(bar(B_KVEMPTY + s));
-                return true;
-            };
-            for (int j = 0; j < n_tiles && ok; ++j) {
+            auto qk = [&](int t, int j) {
                 const int s = j % C::NS;
-                const int sb = j & 1;
-                ok = mbar_wait(bar(B_KFULL + s), (j / C::NS) & 1, &abort_flag);
-                if (ok && j >= 2) ok = mbar_wait(bar(B_SFREE + sb), ((j >> 1) - 1) & 1, &abort_flag);
-                if (!ok) break;
-                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a = sdesc_sw128(q_s + (kk / 4) * C::HALF + (kk % 4) * 32, 16, 1024);
+                    const uint64_t a = sdesc_sw128(q_s(t) + (kk / 4) * C::HALF + (kk % 4) * 32, 16, 1024);
                     const uint64_t b = sdesc_sw128(k_s(s) + (kk / 4) * C::HALF + (kk % 4) * 32, 16, 1024);
-                    tc_mma(tmem + sb * 128, a, b, C::IDESC_QK, kk > 0 ? 1u : 0u);
+                    tc_mma(tmem + col_s(t), a, b, C::IDESC_QK, kk > 0 ? 1u : 0u);
                 }
-                tc_commit(bar(B_SFULL + sb));
-                if (j >= 1) ok = pv(j - 1);
+                tc_commit(bar(B_SFULL + t));
+            };
+            auto pv = [&](int t, int j) -> bool {
+                if (!mbar_wait(bar(B_PFULL + t), j & 1, &abort_flag)) return false;
+                tc_fence_after();
+                const int s = j % C::NS;
+#pragma unroll
+                for (int kk = 0; kk < kTileKeys / 16; ++kk) {
+                    const uint64_t b = sdesc_sw128(v_s(s) + kk * 2048, C::HALF, 1024);
+                    tc_mma_ts(tmem + col_o(t), tmem + col_s(t) + kk * 8, b, C::IDESC_PV,
+                              (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                return true;
+            };
+            if (ok && n_tiles > 0) {
+                ok = mbar_wait(bar(B_KFULL), 0, &abort_flag);
+                tc_fence_after();
+                if (ok && n_sub[0] > 0) qk(0, 0);
+                if (ok && n_sub[1] > 0) qk(1, 0);
             }
-            if (ok && n_tiles > 0) ok = pv(n_tiles - 1);
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const int s = j % C::NS;
+                const int s1 = (j + 1) % C::NS;
+                const uint32_t par1 = ((j + 1) / C::NS) & 1;
+                ok = mbar_wait(bar(B_VFULL + s), (j / C::NS) & 1, &abort_flag);
+#pragma unroll
+                for (int t = 0; t < 2 && ok; ++t) {
+                    if (j >= n_sub[t]) continue;
+                    ok = pv(t, j);
+                    if (!ok) break;
+                    if (j + 1 < n_sub[t]) {
+                        ok = mbar_wait(bar(B_KFULL + s1), par1, &abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        qk(t, j + 1);   // overwrites S_t: issued after the PV that reads P_t
+                    } else {
+                        tc_commit(bar(B_ODONE + t));
+                    }
+                }
+                if (ok) tc_commit(bar(B_KVEMPTY + s));
+            }
             if (!ok) raise_abort(&abort_flag, p.err, kErrTimeout);
-            // every MMA of this CTA must finish before TMEM is released
+            // every MMA of this CTA must finish before tensor memory is released
             tc_commit(bar(B_DRAIN));
             if (!mbar_wait(bar(B_DRAIN), 0, nullptr)) atomicOr(p.err, kErrTimeout);
         }
         __syncwarp();
     } else {
         // ------------------------------------------- softmax + epilogue --
-        const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
+        const int t = (warp - 2) / 4;            // sub-tile of this warpgroup
+        const int quarter = warp & 3;            // tensor-memory lanes 32*quarter .. +31
         const int row = quarter * 32 + lane;
         const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        const int i = row / G;
+        const int i = t * tpt + row / G;         // token of this row within the tile
         const int gq = row % G;
         const bool tok_valid = i < tile.n_tok;
         const int pos_lim = tile.causal ? tile.pos0 + i + 1 : 0x7fffffff;  // keys < pos_lim
+        const int row_end = min(tile.key_end, pos_lim);
+        const int n_mine = n_sub[t];
+        const int zero_owner_last = n_sub[0] == n_tiles ? 0 : 1;  // who zeroes the last V tile
         float m = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            const int sb = j & 1;
-            const int s = j % C::NS;
-            if (!warp_wait(bar(B_SFULL + sb), (j >> 1) & 1, &abort_flag)) { ok = false; break; }
+        for (int j = 0; j < n_mine; ++j) {
+            if (!warp_wait(bar(B_SFULL + t), j & 1, &abort_flag)) { ok = false; break; }
             tc_fence_after();
-            uint32_t sr[128];
-            tmem_ld32(t_row + sb * 128 + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            tmem_ld32(t_row + sb * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-            tmem_ld32(t_row + sb * 128 + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
-            tmem_ld32(t_row + sb * 128 + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(bar(B_SFREE + sb));
-
             const int kt0 = tile.key_begin + j * kTileKeys;
-            const int lim = min(tile.key_end, pos_lim) - kt0;   // columns < lim are visible
+            const int lim = row_end - kt0;       // columns < lim are visible
+            const bool full_row = lim >= kTileKeys;
+            // pass 1: row max of the raw scores, 32 columns at a time
             float mx = -INFINITY;
+#pragma unroll 1
+            for (int c0 = 0; c0 < kTileKeys; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(t_row + col_s(t) + c0, v);
+                tmem_wait_ld();
+                if (full_row) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                const float v = c < lim ? __uint_as_float(sr[c]) * p.scale_log2 : -INFINITY;
-                sr[c] = __float_as_uint(v);
-                mx = fmaxf(mx, v);
+                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (c0 + e < lim) mx = fmaxf(mx, __uint_as_float(v[e]));
+                }
             }
-            const bool need = mx > m + 8.f;
+            const float mxs = mx * p.scale_log2;
+            const bool need = mxs > m + 8.f;
             float alpha = 1.f;
             if (need) {
-                alpha = ex2(m - mx);
-                m = mx;
+                alpha = ex2(m - mxs);
+                m = mxs;
                 l *= alpha;
             }
-            const float ref = m == -INFINITY ? 0.f : m;
-            if (j >= 1) {
-                // PV of the previous tile must be done: O is final for it and
-                // the P buffer is free again
-                if (!warp_wait(bar(B_ODONE), (j - 1) & 1, &abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, need)) {
+            const float nref = m == -INFINITY ? 0.f : -m;
+            // pass 2: P = exp2(s*scale - m) as bf16 pairs, written over the
+            // first 64 columns of S (64 score columns -> 32 P columns at a
+            // time; every score column is read before it is overwritten)
 #pragma unroll 1
-                    for (int c = 0; c < D; c += 32) {
-                        uint32_t orr[32];
-                        tmem_ld32(t_row + C::COL_O + c, orr);
-                        tmem_wait_ld();
+            for (int h = 0; h < 2; ++h) {
+                uint32_t a[32], b[32], w[32];
+                tmem_ld32(t_row + col_s(t) + h * 64, a);
+                tmem_ld32(t_row + col_s(t) + h * 64 + 32, b);
+                tmem_wait_ld();
+                if (full_row) {
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-                        tmem_st32(t_row + C::COL_O + c, orr);
+                    for (int e = 0; e < 16; ++e) {
+                        const float p0 = ex2(fmaf(__uint_as_float(a[2 * e]), p.scale_log2, nref));
+                        const float p1 = ex2(fmaf(__uint_as_float(a[2 * e + 1]), p.scale_log2, nref));
+                        const float p2 = ex2(fmaf(__uint_as_float(b[2 * e]), p.scale_log2, nref));
+                        const float p3 = ex2(fmaf(__uint_as_float(b[2 * e + 1]), p.scale_log2, nref));
+                        l += (p0 + p1) + (p2 + p3);
+                        w[e] = pack_bf16x2(p0, p1);
+                        w[16 + e] = pack_bf16x2(p2, p3);
                     }
-                    tmem_wait_st();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int c = h * 64 + 2 * e;
+                        const float p0 = c < lim ? ex2(fmaf(__uint_as_float(a[2 * e]), p.scale_log2, nref)) : 0.f;
+                        const float p1 = c + 1 < lim ? ex2(fmaf(__uint_as_float(a[2 * e + 1]), p.scale_log2, nref)) : 0.f;
+                        const float p2 = c + 32 < lim ? ex2(fmaf(__uint_as_float(b[2 * e]), p.scale_log2, nref)) : 0.f;
+                        const float p3 = c + 33 < lim ? ex2(fmaf(__uint_as_float(b[2 * e + 1]), p.scale_log2, nref)) : 0.f;
+                        l += (p0 + p1) + (p2 + p3);
+                        w[e] = pack_bf16x2(p0, p1);
+                        w[16 + e] = pack_bf16x2(p2, p3);
+                    }
+                }
+                tmem_st32(t_row + col_s(t) + h * 32, w);
+            }
+            if (j >= 1 && __any_sync(0xffffffffu, need)) {
+                // O_t holds the tiles before j (their PV completed before S_t(j) did)
+#pragma unroll 1
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t orr[32];
+                    tmem_ld32(t_row + col_o(t) + c, orr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                    tmem_st32(t_row + col_o(t) + c, orr);
                 }
             }
-            // P row -> shared memory (bf16, 128-byte swizzled, K-major)
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    w[e] = pack_bf16x2(ex2(__uint_as_float(sr[c * 8 + 2 * e]) - ref),
-                                       ex2(__uint_as_float(sr[c * 8 + 2 * e + 1]) - ref));
-                    l += bf16_lo(w[e]) + bf16_hi(w[e]);
-                }
-                const uint32_t a = sw128(p_s + (c / 8) * C::HALF, row, c % 8);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[0]), "r"(w[1]),
-                             "r"(w[2]), "r"(w[3])
-                             : "memory");
-            }
+            tmem_wait_st();
             // value rows past the end of the key range may hold anything
             // (unwritten slots, stale blocks, NaN): zero them so that
             // 0 * row stays 0 inside the MMA
             const int valid_keys = tile.key_end - kt0;
-            if (valid_keys < kTileKeys) {
+            if (valid_keys < kTileKeys && j == n_tiles - 1 && t == zero_owner_last) {
+                const int s = j % C::NS;
                 if (!warp_wait(bar(B_VFULL + s), (j / C::NS) & 1, &abort_flag)) { ok = false; break; }
                 if (row >= valid_keys) {
 #pragma unroll
@@ -301,34 +358,33 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
                         for (int ch = 0; ch < 8; ++ch) {
                             const uint32_t a = v_s(s) + h * C::HALF + row * 128 + ch * 16;
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0)
-                                         : "memory");
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
                         }
                 }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bar(B_PFULL));
+            mbar_arrive(bar(B_PFULL + t));
         }
         if (!ok) raise_abort(&abort_flag, p.err, kErrTimeout);
         // ----------------------------------------------------- epilogue --
-        if (ok && n_tiles > 0 && warp_wait(bar(B_ODONE), (n_tiles - 1) & 1, &abort_flag)) {
+        if (ok && n_mine > 0 && warp_wait(bar(B_ODONE + t), 0, &abort_flag)) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const int t = tile.t0 + i;
+            const int tok = tile.t0 + i;
             const int h = tile.kv_head * G + gq;
             int64_t slot = -1;
             if (tile.part >= 0 && tok_valid)
-                slot = static_cast<int64_t>(p.part_offset[t * p.n_groups + tile.kv_head / p.heads_per_group]) +
+                slot = static_cast<int64_t>(p.part_offset[tok * p.n_groups + tile.kv_head / p.heads_per_group]) +
                        tile.part;
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
                 uint32_t orr[32];
-                tmem_ld32(t_row + C::COL_O + c, orr);
+                tmem_ld32(t_row + col_o(t) + c, orr);
                 tmem_wait_ld();
                 if (!tok_valid) continue;
                 if (tile.part < 0) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + (static_cast<int64_t>(t) * p.num_heads_q + h) * D + c);
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + (static_cast<int64_t>(tok) * p.num_heads_q + h) * D + c);
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint4 w;
@@ -347,7 +403,7 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
             }
             if (tok_valid && tile.part >= 0) p.ml_part[slot * p.num_heads_q + h] = make_float2(m, l);
-        } else if (n_tiles > 0) {
+        } else if (n_mine > 0) {
             raise_abort(&abort_flag, p.err, kErrTimeout);
         }
         tc_fence_before();

@@ -254,7 +254,7 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d) {
         if (qsl[r + 1] > qsl[r]) { P->prefix_req = r; break; }
 
     // ---------------------------------------------------- tensor-core tiles
-    const int tpt = kTileRows / P->G;   // tokens per 128-row tile
+    const int tpt = 2 * (kTileRows / P->G);   // tokens per CTA tile: two 128-row sub-tiles
     if (cascade) {
         const int n_key_tiles = (kb_keys + kTileKeys - 1) / kTileKeys;
         const int token_tiles = (P->T + tpt - 1) / tpt;

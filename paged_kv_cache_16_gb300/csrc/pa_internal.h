@@ -12,7 +12,7 @@ namespace pa {
 
 constexpr int kBlockSize = 16;     // tokens per cache block
 constexpr int kTileKeys = 128;     // keys per tensor-core tile (8 blocks)
-constexpr int kTileRows = 128;     // query rows per tensor-core tile
+constexpr int kTileRows = 128;     // query rows per tensor-core sub-tile (two per CTA)
 constexpr int kMaxDecodeHeads = 8; // kv heads one decode CTA serves
 
 // Split-KV decode kernel resources, shared by the planner (which sizes the
@@ -52,11 +52,12 @@ struct DecodeItem {
     int32_t pad;
 };
 
-// One tile of 128 query rows (tokens x G query heads of one kv head) against
-// the key range [key_begin, key_end) of one request's context.
+// One CTA tile of up to 256 query rows (2 x 128/G consecutive tokens x the
+// G query heads of one kv head) against the key range [key_begin, key_end)
+// of one request's context.
 struct ExtendTile {
     int32_t t0;          // first token of the tile
-    int32_t n_tok;       // tokens of the tile that belong to it (<= 128/G)
+    int32_t n_tok;       // tokens of the tile that belong to it (<= 256/G)
     int32_t req;         // block-table row the keys are read through
     int32_t pos0;        // absolute position of token t0 (causal bound)
     int32_t key_begin;   // block aligned

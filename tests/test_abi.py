@@ -126,8 +126,8 @@ def test_mixed_batch_example_metadata(lib):
     plan = binding.pa_plan(**kw)
     info = plan.info()
     assert info["num_decode_rows"] == 1 and info["num_extend_rows"] == 2
-    # 256 + 3 query tokens, G = 4 -> 32 tokens per tile: 8 + 1 tiles per kv head
-    assert info["num_extend_tiles"] == 2 * (8 + 1)
+    # 256 + 3 query tokens, G = 4 -> 64 tokens per CTA tile: 4 + 1 tiles per kv head
+    assert info["num_extend_tiles"] == 2 * (4 + 1)
     bad = nc.copy()
     bad[1] = 511
     assert binding.pa_plan_status(**{**kw, "num_computed_tokens": bad}) == binding.PA_ERR_INVALID_ARGUMENT
@@ -158,7 +158,7 @@ def test_plan_decomposition(lib, maker):
     row_bytes = b.num_heads_kv * b.head_dim * 4
     assert info["decode_kv_bytes"] == sum((int(b.seq_lens[r]) - kb) * row_bytes for r in dec)
     G = b.num_heads_q // b.num_heads_kv
-    tpt = 128 // G
+    tpt = 2 * (128 // G)        # tokens per CTA tile (two 128-row sub-tiles)
     n_ext_tiles = sum(math.ceil(q_lens[r] / tpt) for r in ext) * b.num_heads_kv
     assert info["num_extend_tiles"] == n_ext_tiles + info["num_prefix_tiles"]
     if n_prefix:
