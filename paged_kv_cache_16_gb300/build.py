@@ -37,13 +37,19 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra_flags=(), output: str | None = None) -> str:
+    """Compile every csrc/*.cu (in parallel) and link libpa.so.
+
+    ``extra_flags`` go to every nvcc compile; ``output`` builds elsewhere than
+    the package's _build/libpa.so (objects land next to it)."""
+    library = output or LIBRARY
+    if not force and output is None and not extra_flags and up_to_date():
         return LIBRARY
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    build_dir = os.path.dirname(library)
+    os.makedirs(build_dir, exist_ok=True)
     procs, objs = [], []
     for src in sources():
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         cmd = [NVCC, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
@@ -58,10 +64,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    tmp = LIBRARY + f".tmp{os.getpid()}"
+    tmp = library + f".tmp{os.getpid()}"
     subprocess.run([NVCC, *ARCH, "-shared", "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIBRARY)
-    return LIBRARY
+    os.replace(tmp, library)
+    return library
 
 
 if __name__ == "__main__":

@@ -72,6 +72,34 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Like mbar_wait but never suspends the thread (non-blocking test_wait in a
+// spin): for the single thread that issues the tensor-core MMAs, where the
+// wake-up latency of a suspended wait shows up as tensor-core idle time.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+#pragma unroll 1
+    for (int i = 0; i < 1024; ++i)
+        if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t start = global_timer();
+#pragma unroll 1
+    while (true) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if (abort_flag != nullptr && *abort_flag) return false;
+        if (global_timer() - start > kWaitLimitNs) return false;
+    }
+}
+
 // mbar_wait by every lane of a warp, with one warp-wide answer: either all
 // lanes go on or all stop (keeps later warp-collective instructions legal).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
@@ -136,6 +164,24 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// 2^x on the FMA pipe, for x <= 2^22 (inputs below -120 give ~2^-120):
+// x = n + f with n = round(x) and f in [-1/2, 1/2]; 2^f from a degree-3
+// polynomial fitted for minimum relative error (coefficients printed by
+// csrc/gen_exp2_poly.py, max relative error 7.5e-5); n is added to the
+// exponent field of the polynomial's value as an integer.
+__device__ __forceinline__ float ex2_fma(float x) {
+    constexpr float kRound = 12582912.f;          // 1.5 * 2^23
+    x = fmaxf(x, -120.f);
+    const float y = x + kRound;                   // integer part in the low mantissa bits
+    const float f = x - (y - kRound);
+    float p = 0.05517132207751274f;
+    p = fmaf(p, f, 0.24261054396629333f);
+    p = fmaf(p, f, 0.6932609677314758f);
+    p = fmaf(p, f, 0.9999281167984009f);
+    // (bits of y) << 23 == n << 23: the low 9 bits of kRound's pattern are 0
+    return __int_as_float(__float_as_int(p) + (__float_as_int(y) << 23));
 }
 
 // ---------------------------------------------- legacy warp MMA (mma.sync) --

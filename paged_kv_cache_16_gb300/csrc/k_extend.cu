@@ -17,7 +17,7 @@
 //   P_t = exp2(S_t*scale*log2e - m)   softmax warpgroup t, one row per thread,
 //                        written back to tensor memory over S_t as bf16 pairs
 //   O_t += P_t V         tcgen05.mma M=128 N=D K=128, A from tensor memory
-// Warp roles: warp 0 TMA producer (Q once, K/V blocks into a 2-stage ring),
+// Warp roles: warp 0 TMA producer (Q once, K and V blocks into 2-stage rings),
 // warp 1 MMA issuer (one thread) and tensor-memory owner, warps 2-5 softmax
 // of sub-tile 0, warps 6-9 softmax of sub-tile 1.  The MMA thread alternates
 // between the sub-tiles, so the tensor core works on one while the other's
@@ -51,20 +51,30 @@ struct ExtCfg {
     static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
 };
 
+// Every kFmaExpEvery-th exponential of the softmax is evaluated on the FMA
+// pipe (ex2_fma) instead of the special-function unit (0 = never).
+#ifndef PA_FMA_EXP_EVERY
+#define PA_FMA_EXP_EVERY 0
+#endif
+constexpr int kFmaExpEvery = PA_FMA_EXP_EVERY;
+
 __device__ __forceinline__ uint32_t col_s(int t) { return static_cast<uint32_t>(t) * 128u; }
 __device__ __forceinline__ uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(t) * 128u; }
 
-// barrier indices
+// barrier indices.  K and V stages are released separately: a K stage as
+// soon as the QK^T MMAs reading it finish, a V stage after the PV MMAs, so the
+// next K tile is loaded while the current tile's softmax and PV still run.
 enum : int {
     B_Q = 0,
     B_KFULL = 1,   // +stage
     B_VFULL = 3,   // +stage
-    B_KVEMPTY = 5, // +stage
-    B_SFULL = 7,   // +sub-tile
-    B_PFULL = 9,   // +sub-tile
-    B_ODONE = 11,  // +sub-tile
-    B_DRAIN = 13,
-    NUM_BARS = 14
+    B_KEMPTY = 5,  // +stage
+    B_VEMPTY = 7,  // +stage
+    B_SFULL = 9,   // +sub-tile
+    B_PFULL = 11,  // +sub-tile
+    B_ODONE = 13,  // +sub-tile
+    B_DRAIN = 15,
+    NUM_BARS = 16
 };
 
 template <int D>
@@ -109,7 +119,8 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int s = 0; s < C::NS; ++s) {
             mbar_init(bar(B_KFULL + s), 1);
             mbar_init(bar(B_VFULL + s), 1);
-            mbar_init(bar(B_KVEMPTY + s), 1);
+            mbar_init(bar(B_KEMPTY + s), 1);
+            mbar_init(bar(B_VEMPTY + s), 1);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(bar(B_SFULL + t), 1);
@@ -143,14 +154,10 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tma_load_3d(q_s(t) + half * C::HALF, &tm_q, half * 64, tile.kv_head * G, tile.t0 + t * tpt, bar(B_Q));
         }
         const int32_t *bt = p.block_table + static_cast<int64_t>(tile.req) * p.max_blocks;
-        int issued = 0;
+        int issued[2] = {0, 0};   // K and V tiles whose loads were issued
         for (int j = 0; j < n_tiles; ++j) {
             const int s = j % C::NS;
             const int n = j / C::NS;
-            if (n > 0 && !warp_wait(bar(B_KVEMPTY + s), (n & 1) ^ 1, &abort_flag)) {
-                if (lane == 0) raise_abort(&abort_flag, p.err, kErrTimeout);
-                break;
-            }
             const int kt0 = tile.key_begin + j * kTileKeys;
             const int pages = min(8, (tile.key_end - kt0 + kBlockSize - 1) / kBlockSize);
             int32_t blk = 0;
@@ -160,42 +167,46 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 valid = blk >= 0 && blk < p.num_blocks;
             }
             const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-            if (lane == 0) {
-                if (__popc(vmask) != pages) atomicOr(p.err, kErrBlockRange);
-                const uint32_t bytes = __popc(vmask) * kBlockSize * 128 * C::NH;
-                mbar_arrive_expect_tx(bar(B_KFULL + s), bytes);
-                mbar_arrive_expect_tx(bar(B_VFULL + s), bytes);
-            }
-            __syncwarp();
-            static_assert(2 * 8 * C::NH <= 32, "one TMA box per lane");
-            {
-                const int tensor = lane / (8 * C::NH);
-                const int rem = lane % (8 * C::NH);
-                const int page = rem / C::NH;
-                const int half = rem % C::NH;
-                const int32_t b = __shfl_sync(0xffffffffu, blk, page);  // every lane takes part
-                if (lane < 2 * 8 * C::NH && ((vmask >> page) & 1u)) {
-                    const uint32_t dst = (tensor ? v_s(s) : k_s(s)) + half * C::HALF + page * 2048;
-                    tma_load_3d(dst, tensor ? &tm_v : &tm_k, half * 64, tile.kv_head, b * kBlockSize,
-                                bar(tensor ? B_VFULL + s : B_KFULL + s));
+            const uint32_t bytes = __popc(vmask) * kBlockSize * 128 * C::NH;
+            if (lane == 0 && __popc(vmask) != pages) atomicOr(p.err, kErrBlockRange);
+            static_assert(8 * C::NH <= 32, "one TMA box per lane");
+            const int page = lane / C::NH;
+            const int half = lane % C::NH;
+            const int32_t b = __shfl_sync(0xffffffffu, blk, page & 7);  // every lane takes part
+            const bool mine = lane < 8 * C::NH && ((vmask >> page) & 1u);
+            bool ok = true;
+#pragma unroll
+            for (int tensor = 0; tensor < 2; ++tensor) {
+                const int empty = tensor ? B_VEMPTY : B_KEMPTY;
+                const int full = tensor ? B_VFULL : B_KFULL;
+                if (n > 0 && !warp_wait(bar(empty + s), (n & 1) ^ 1, &abort_flag)) {
+                    if (lane == 0) raise_abort(&abort_flag, p.err, kErrTimeout);
+                    ok = false;
+                    break;
                 }
+                if (lane == 0) mbar_arrive_expect_tx(bar(full + s), bytes);
+                __syncwarp();
+                if (mine)
+                    tma_load_3d((tensor ? v_s(s) : k_s(s)) + half * C::HALF + page * 2048, tensor ? &tm_v : &tm_k,
+                                half * 64, tile.kv_head, b * kBlockSize, bar(full + s));
+                ++issued[tensor];
             }
-            ++issued;
+            if (!ok) break;
         }
         if (lane == 0) {
             // no TMA write may outlive the CTA
             if (!mbar_wait(bar(B_Q), 0, nullptr)) atomicOr(p.err, kErrTimeout);
-            for (int k = issued - 1; k >= 0 && k >= issued - C::NS; --k) {
-                const int s = k % C::NS, n = k / C::NS;
-                if (!mbar_wait(bar(B_KFULL + s), n & 1, nullptr) ||
-                    !mbar_wait(bar(B_VFULL + s), n & 1, nullptr))
-                    atomicOr(p.err, kErrTimeout);
-            }
+            for (int tensor = 0; tensor < 2; ++tensor)
+                for (int k = issued[tensor] - 1; k >= 0 && k >= issued[tensor] - C::NS; --k) {
+                    const int s = k % C::NS, n = k / C::NS;
+                    if (!mbar_wait(bar((tensor ? B_VFULL : B_KFULL) + s), n & 1, nullptr))
+                        atomicOr(p.err, kErrTimeout);
+                }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer --
         if (lane == 0) {
-            bool ok = mbar_wait(bar(B_Q), 0, &abort_flag);
+            bool ok = mbar_wait_spin(bar(B_Q), 0, &abort_flag);
             auto qk = [&](int t, int j) {
                 const int s = j % C::NS;
 #pragma unroll
@@ -207,7 +218,7 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 tc_commit(bar(B_SFULL + t));
             };
             auto pv = [&](int t, int j) -> bool {
-                if (!mbar_wait(bar(B_PFULL + t), j & 1, &abort_flag)) return false;
+                if (!mbar_wait_spin(bar(B_PFULL + t), j & 1, &abort_flag)) return false;
                 tc_fence_after();
                 const int s = j % C::NS;
 #pragma unroll
@@ -219,31 +230,39 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 return true;
             };
             if (ok && n_tiles > 0) {
-                ok = mbar_wait(bar(B_KFULL), 0, &abort_flag);
+                ok = mbar_wait_spin(bar(B_KFULL), 0, &abort_flag);
                 tc_fence_after();
                 if (ok && n_sub[0] > 0) qk(0, 0);
                 if (ok && n_sub[1] > 0) qk(1, 0);
+                if (ok) tc_commit(bar(B_KEMPTY));          // K tile 0 read by both QK^T
             }
             for (int j = 0; j < n_tiles && ok; ++j) {
                 const int s = j % C::NS;
                 const int s1 = (j + 1) % C::NS;
                 const uint32_t par1 = ((j + 1) / C::NS) & 1;
-                ok = mbar_wait(bar(B_VFULL + s), (j / C::NS) & 1, &abort_flag);
+                bool k_next_ready = false;
+                ok = mbar_wait_spin(bar(B_VFULL + s), (j / C::NS) & 1, &abort_flag);
 #pragma unroll
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (j >= n_sub[t]) continue;
                     ok = pv(t, j);
                     if (!ok) break;
                     if (j + 1 < n_sub[t]) {
-                        ok = mbar_wait(bar(B_KFULL + s1), par1, &abort_flag);
-                        if (!ok) break;
+                        if (!k_next_ready) {
+                            ok = mbar_wait_spin(bar(B_KFULL + s1), par1, &abort_flag);
+                            if (!ok) break;
+                            k_next_ready = true;
+                        }
                         tc_fence_after();
                         qk(t, j + 1);   // overwrites S_t: issued after the PV that reads P_t
                     } else {
                         tc_commit(bar(B_ODONE + t));
                     }
                 }
-                if (ok) tc_commit(bar(B_KVEMPTY + s));
+                if (ok) {
+                    tc_commit(bar(B_VEMPTY + s));                      // V tile j read by both PV
+                    if (j + 1 < n_tiles) tc_commit(bar(B_KEMPTY + s1));  // K tile j+1 read by both QK^T
+                }
             }
             if (!ok) raise_abort(&abort_flag, p.err, kErrTimeout);
             // every MMA of this CTA must finish before tensor memory is released
@@ -271,24 +290,27 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tc_fence_after();
             const int kt0 = tile.key_begin + j * kTileKeys;
             const int lim = row_end - kt0;       // columns < lim are visible
-            const bool full_row = lim >= kTileKeys;
-            // pass 1: row max of the raw scores, 32 columns at a time
-            float mx = -INFINITY;
-#pragma unroll 1
-            for (int c0 = 0; c0 < kTileKeys; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(t_row + col_s(t) + c0, v);
-                tmem_wait_ld();
-                if (full_row) {
+            // the whole S row in registers: four loads, one wait
+            uint32_t sr[128];
+            tmem_ld32(t_row + col_s(t) + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tmem_ld32(t_row + col_s(t) + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            tmem_ld32(t_row + col_s(t) + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[64]));
+            tmem_ld32(t_row + col_s(t) + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[96]));
+            tmem_wait_ld();
+            if (lim < kTileKeys) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (c0 + e < lim) mx = fmaxf(mx, __uint_as_float(v[e]));
-                }
+                for (int c = 0; c < 128; ++c)
+                    if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
             }
-            const float mxs = mx * p.scale_log2;
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; c += 4) {
+                mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
+                mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
+                mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
+                mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+            }
+            const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
             const bool need = mxs > m + 8.f;
             float alpha = 1.f;
             if (need) {
@@ -297,41 +319,26 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 l *= alpha;
             }
             const float nref = m == -INFINITY ? 0.f : -m;
-            // pass 2: P = exp2(s*scale - m) as bf16 pairs, written over the
-            // first 64 columns of S (64 score columns -> 32 P columns at a
-            // time; every score column is read before it is overwritten)
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                uint32_t a[32], b[32], w[32];
-                tmem_ld32(t_row + col_s(t) + h * 64, a);
-                tmem_ld32(t_row + col_s(t) + h * 64 + 32, b);
-                tmem_wait_ld();
-                if (full_row) {
+            // P = exp2(s*scale - m) as bf16 pairs, packed in place (entry e
+            // takes columns 2e and 2e+1, which are read before entry e is
+            // written), then stored over the first 64 columns of S
+            float l0 = 0.f, l1 = 0.f;
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float p0 = ex2(fmaf(__uint_as_float(a[2 * e]), p.scale_log2, nref));
-                        const float p1 = ex2(fmaf(__uint_as_float(a[2 * e + 1]), p.scale_log2, nref));
-                        const float p2 = ex2(fmaf(__uint_as_float(b[2 * e]), p.scale_log2, nref));
-                        const float p3 = ex2(fmaf(__uint_as_float(b[2 * e + 1]), p.scale_log2, nref));
-                        l += (p0 + p1) + (p2 + p3);
-                        w[e] = pack_bf16x2(p0, p1);
-                        w[16 + e] = pack_bf16x2(p2, p3);
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int c = h * 64 + 2 * e;
-                        const float p0 = c < lim ? ex2(fmaf(__uint_as_float(a[2 * e]), p.scale_log2, nref)) : 0.f;
-                        const float p1 = c + 1 < lim ? ex2(fmaf(__uint_as_float(a[2 * e + 1]), p.scale_log2, nref)) : 0.f;
-                        const float p2 = c + 32 < lim ? ex2(fmaf(__uint_as_float(b[2 * e]), p.scale_log2, nref)) : 0.f;
-                        const float p3 = c + 33 < lim ? ex2(fmaf(__uint_as_float(b[2 * e + 1]), p.scale_log2, nref)) : 0.f;
-                        l += (p0 + p1) + (p2 + p3);
-                        w[e] = pack_bf16x2(p0, p1);
-                        w[16 + e] = pack_bf16x2(p2, p3);
-                    }
-                }
-                tmem_st32(t_row + col_s(t) + h * 32, w);
+            for (int e = 0; e < 64; ++e) {
+                // one exponential in kFmaExpEvery goes to the FMA pipe, the
+                // rest to the special-function unit, to balance the two
+                const float x0 = fmaf(__uint_as_float(sr[2 * e]), p.scale_log2, nref);
+                const float x1 = fmaf(__uint_as_float(sr[2 * e + 1]), p.scale_log2, nref);
+                const float p0 = ex2(x0);
+                const float p1 = (kFmaExpEvery > 0 && (2 * e + 1) % kFmaExpEvery == kFmaExpEvery - 1)
+                                     ? ex2_fma(x1) : ex2(x1);
+                l0 += p0;
+                l1 += p1;
+                sr[e] = pack_bf16x2(p0, p1);
             }
+            l += l0 + l1;
+            tmem_st32(t_row + col_s(t) + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tmem_st32(t_row + col_s(t) + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
             if (j >= 1 && __any_sync(0xffffffffu, need)) {
                 // O_t holds the tiles before j (their PV completed before S_t(j) did)
 #pragma unroll 1
