@@ -66,7 +66,9 @@ WORKLOADS = {
 # unchanged (sha256 of the file).  Filled in from profiles/.
 TRAFFIC = {
     # (kernel, workload, source sha) -> bytes per launch; profiles/decode_kernel_decode-workload.md
-    ("decode", "decode", "2c4247d3e0dff9f8"): 645_201_152,
+    ("decode", "decode", "556c55355d272fd6"): 644_464_640,
+    # profiles/extend_kernel_prefill-workload.md
+    ("extend", "prefill", "ac26b38d115f117e"): 73_388_800,
 }
 KERNEL_SOURCES = {"decode": "paged_kv_cache_16_gb300/csrc/k_decode.cu",
                   "extend": "paged_kv_cache_16_gb300/csrc/k_extend.cu"}

@@ -215,6 +215,55 @@ __device__ __forceinline__ uint32_t sw128(uint32_t base, uint32_t row, uint32_t 
     return base + row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
+// ------------------------------------------------------------ partials --
+// Merge of partition partials for one query head, by one warp (page
+// "vLLM 源码完全拆解（十六）", third walk-through: local (m_r, l_r, o_r)
+// combined with exponential rescaling; m in log2 units here):
+//   m = max m_r,  w_r = 2^(m_r - m) l_r,  out = sum w_r o_r / sum w_r.
+// Partials are read in slot order, so the result does not depend on which
+// CTA or kernel performs the merge.
+template <int D>
+__device__ __forceinline__ void merge_head(uint16_t *out_row, const float *o_part, const float2 *ml_part,
+                                           int64_t slot0, int count, int num_heads_q, int h, int lane) {
+    constexpr int V = D / 32;
+    float m = -INFINITY;
+    for (int s = 0; s < count; ++s) {
+        const float2 ml = __ldcg(ml_part + (slot0 + s) * num_heads_q + h);
+        if (ml.y > 0.f) m = fmaxf(m, ml.x);
+    }
+    float acc[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) acc[v] = 0.f;
+    float total = 0.f;
+    for (int s = 0; s < count; ++s) {
+        const int64_t slot = slot0 + s;
+        const float2 ml = __ldcg(ml_part + slot * num_heads_q + h);
+        if (!(ml.y > 0.f)) continue;
+        const float w = ex2(ml.x - m) * ml.y;
+        total += w;
+        const float *o = o_part + (slot * num_heads_q + h) * D + lane * V;
+        // L2 loads: partials written by other SMs in this same launch must
+        // not be served from a stale L1 line
+        if constexpr (V == 4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4 *>(o));
+            acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
+        } else {
+            const float2 x = __ldcg(reinterpret_cast<const float2 *>(o));
+            acc[0] += w * x.x; acc[1] += w * x.y;
+        }
+    }
+    const float inv = total > 0.f ? 1.f / total : 0.f;
+    uint16_t *dst = out_row + static_cast<int64_t>(h) * D + lane * V;
+    if constexpr (V == 4) {
+        uint2 packed;
+        packed.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        packed.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2 *>(dst) = packed;
+    } else {
+        *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+}
+
 // ---------------------------------------------------------------- tcgen05 --
 // Shared-memory matrix descriptor, 128-byte swizzle.  Start address, leading
 // and stride byte offsets in 16-byte units; descriptor version 1 (bits 46-47);

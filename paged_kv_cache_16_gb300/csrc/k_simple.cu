@@ -61,42 +61,8 @@ __global__ void merge_kernel(MergeParams p) {
     const MergeRow row = p.rows[warp / p.max_heads];
     const int hi = warp % p.max_heads;
     if (hi >= row.hq_count) return;
-    const int h = row.hq_begin + hi;
-    constexpr int V = D / 32;  // floats per lane
-    float m = -INFINITY;
-    for (int s = 0; s < row.count; ++s) {
-        const float2 ml = p.ml_part[static_cast<int64_t>(row.slot0 + s) * p.num_heads_q + h];
-        if (ml.y > 0.f) m = fmaxf(m, ml.x);
-    }
-    float acc[V];
-#pragma unroll
-    for (int v = 0; v < V; ++v) acc[v] = 0.f;
-    float total = 0.f;
-    for (int s = 0; s < row.count; ++s) {
-        const int64_t slot = row.slot0 + s;
-        const float2 ml = p.ml_part[slot * p.num_heads_q + h];
-        if (!(ml.y > 0.f)) continue;
-        const float w = dev::ex2(ml.x - m) * ml.y;
-        total += w;
-        const float *o = p.o_part + (slot * p.num_heads_q + h) * D + lane * V;
-        if constexpr (V == 4) {
-            const float4 x = *reinterpret_cast<const float4 *>(o);
-            acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
-        } else {
-            const float2 x = *reinterpret_cast<const float2 *>(o);
-            acc[0] += w * x.x; acc[1] += w * x.y;
-        }
-    }
-    const float inv = total > 0.f ? 1.f / total : 0.f;
-    uint16_t *dst = p.out + (static_cast<int64_t>(row.token) * p.num_heads_q + h) * D + lane * V;
-    if constexpr (V == 4) {
-        uint2 packed;
-        packed.x = dev::pack_bf16x2(acc[0] * inv, acc[1] * inv);
-        packed.y = dev::pack_bf16x2(acc[2] * inv, acc[3] * inv);
-        *reinterpret_cast<uint2 *>(dst) = packed;
-    } else {
-        *reinterpret_cast<uint32_t *>(dst) = dev::pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    }
+    dev::merge_head<D>(p.out + static_cast<int64_t>(row.token) * p.num_heads_q * D, p.o_part, p.ml_part,
+                       row.slot0, row.count, p.num_heads_q, row.hq_begin + hi, lane);
 }
 
 }  // namespace
