@@ -45,6 +45,8 @@
 #define ORACLE_BAD_BLOCK 2
 #define ORACLE_NO_MEMORY 3
 
+double oracle_e4m3_value(uint8_t code);
+
 /* bf16 -> double, exact: a bf16 pattern is the top half of an IEEE binary32. */
 static double bf16_to_double(uint16_t bits) {
     uint32_t w = ((uint32_t)bits) << 16;
@@ -117,6 +119,83 @@ int oracle_write_kv(int32_t num_tokens, int32_t num_heads_kv, int32_t head_dim,
     return status;
 }
 
+/*
+ * FP8 KV cache ("vLLM 推理流程分析" §6.3: reshape_and_cache_flash takes
+ * kv_cache_dtype, k_scale and v_scale and converts to FP8 when the cache is
+ * quantised).  Reading: the cache holds OCP E4M3 codes (1 sign, 4 exponent
+ * bits with bias 7, 3 mantissa bits; largest finite 448, no infinities,
+ * S.1111.111 is NaN) of x / scale, with one float scale per tensor; a read
+ * returns code_value * scale.  The quotient is formed in IEEE binary32 (the
+ * precision the write kernel uses), then rounded to the nearest E4M3 value,
+ * ties to even, saturating to +-448.
+ */
+double oracle_e4m3_value(uint8_t code) {
+    int sign = (code >> 7) & 1;
+    int e = (code >> 3) & 0xF;
+    int m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);              /* subnormal: m * 2^-9 */
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+uint8_t oracle_e4m3_encode(float x) {
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    if (isinf(x)) return (uint8_t)(sign | 0x7E);     /* saturates like any large value */
+    double a = fabs((double)x);
+    if (a == 0.0) return sign;
+    /* spacing of the E4M3 grid around a: 2^-9 below the smallest normal
+     * 2^-6, else 2^(exponent - 3) */
+    int ex;
+    frexp(a, &ex);                                    /* a = f * 2^ex, f in [0.5, 1) */
+    int e = ex - 1;                                   /* floor(log2(a)) */
+    double quantum = e < -6 ? ldexp(1.0, -9) : ldexp(1.0, e - 3);
+    double v = rint(a / quantum) * quantum;           /* nearest, ties to even */
+    if (v > 448.0) v = 448.0;                         /* saturate to the largest finite */
+    if (v == 0.0) return sign;
+    frexp(v, &ex);
+    e = ex - 1;
+    uint8_t bits;
+    if (e < -6) {
+        bits = (uint8_t)(v / ldexp(1.0, -9));         /* subnormal mantissa */
+    } else {
+        int mant = (int)((v / ldexp(1.0, e) - 1.0) * 8.0);
+        bits = (uint8_t)(((e + 7) << 3) | mant);
+    }
+    return (uint8_t)(sign | bits);
+}
+
+static float fp8_quotient(uint16_t bits, float scale) {
+    return (float)bf16_to_double(bits) / scale;       /* binary32 division */
+}
+
+/* Step 2 with an FP8 cache: caches are [num_slots][Hkv*D] E4M3 codes. */
+int oracle_write_kv_fp8(int32_t num_tokens, int32_t num_heads_kv, int32_t head_dim,
+                        const uint16_t *key, const uint16_t *value, const int64_t *slot_mapping,
+                        uint8_t *key_cache, uint8_t *value_cache, int64_t num_slots,
+                        float k_scale, float v_scale) {
+    int status = ORACLE_OK;
+    int64_t row = (int64_t)num_heads_kv * head_dim;
+    for (int32_t t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_slots) { status = ORACLE_BAD_BLOCK; continue; }
+        for (int64_t e = 0; e < row; ++e) {
+            key_cache[slot * row + e] = oracle_e4m3_encode(fp8_quotient(key[(int64_t)t * row + e], k_scale));
+            value_cache[slot * row + e] = oracle_e4m3_encode(fp8_quotient(value[(int64_t)t * row + e], v_scale));
+        }
+    }
+    return status;
+}
+
+/* Dequantise FP8 caches into the double values attention reads
+ * (code_value * scale), so the attention of step 3 applies unchanged. */
+void oracle_dequantize_fp8(int64_t n, const uint8_t *codes, double scale, double *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_value(codes[i]) * scale;
+}
+
 /* Metadata check shared by the attention entry points: q_len from the
  * prefix sums ("vLLM 源码完全拆解（十六）", fourth walk-through: c_i tokens of
  * request i, query_start_loc its prefix sum) and seq_len = num_computed +
@@ -142,16 +221,22 @@ static int check_metadata(int32_t num_reqs, const int32_t *qsl, const int32_t *s
  * [0,1,2] -> block table -> physical [7,12,19]). */
 static int gather_context(int32_t r, int32_t length, int32_t num_heads_kv, int32_t head_dim,
                           int32_t block_size, int32_t num_blocks, const int32_t *block_table,
-                          int32_t max_blocks_per_req, const uint16_t *key_cache,
-                          const uint16_t *value_cache, float *k_ctx, float *v_ctx) {
+                          int32_t max_blocks_per_req, const void *key_cache,
+                          const void *value_cache, int kv_fp8, float *k_ctx, float *v_ctx) {
     int64_t row = (int64_t)num_heads_kv * head_dim;
     for (int32_t j = 0; j < length; ++j) {
         int32_t physical = block_table[(int64_t)r * max_blocks_per_req + j / block_size];
         if (physical < 0 || physical >= num_blocks) return ORACLE_BAD_BLOCK;
         int64_t slot = (int64_t)physical * block_size + j % block_size;
         for (int64_t e = 0; e < row; ++e) {
-            k_ctx[(int64_t)j * row + e] = (float)bf16_to_double(key_cache[slot * row + e]);
-            v_ctx[(int64_t)j * row + e] = (float)bf16_to_double(value_cache[slot * row + e]);
+            /* an E4M3 code's value is exact in binary32; its scale is applied
+             * in fp64 by the caller */
+            k_ctx[(int64_t)j * row + e] = kv_fp8
+                ? (float)oracle_e4m3_value(((const uint8_t *)key_cache)[slot * row + e])
+                : (float)bf16_to_double(((const uint16_t *)key_cache)[slot * row + e]);
+            v_ctx[(int64_t)j * row + e] = kv_fp8
+                ? (float)oracle_e4m3_value(((const uint8_t *)value_cache)[slot * row + e])
+                : (float)bf16_to_double(((const uint16_t *)value_cache)[slot * row + e]);
         }
     }
     return ORACLE_OK;
@@ -207,15 +292,16 @@ static void attend_range(const double *qv, const float *k_ctx, const float *v_ct
  * out:  [T][Hq][D] doubles, normalised output o (rows not chosen untouched).
  * out_m, out_l: optional [T][Hq] doubles receiving the partial's m and l.
  */
-int oracle_attention_range(int32_t num_reqs, int32_t num_heads_q, int32_t num_heads_kv,
-                           int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                           int32_t max_blocks_per_req, const int32_t *query_start_loc,
-                           const int32_t *seq_lens, const int32_t *num_computed,
-                           const int32_t *block_table, double softmax_scale,
-                           const uint16_t *q, const uint16_t *key_cache,
-                           const uint16_t *value_cache, const int32_t *rows, int32_t n_rows,
-                           int32_t key_begin_override, int32_t key_end_override,
-                           double *out, double *out_m, double *out_l) {
+static int attention_core(int32_t num_reqs, int32_t num_heads_q, int32_t num_heads_kv,
+                          int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                          int32_t max_blocks_per_req, const int32_t *query_start_loc,
+                          const int32_t *seq_lens, const int32_t *num_computed,
+                          const int32_t *block_table, double softmax_scale,
+                          const uint16_t *q, const void *key_cache, const void *value_cache,
+                          int kv_fp8, double k_scale, double v_scale,
+                          const int32_t *rows, int32_t n_rows,
+                          int32_t key_begin_override, int32_t key_end_override,
+                          double *out, double *out_m, double *out_l) {
     if (num_heads_kv <= 0 || num_heads_q % num_heads_kv != 0) return ORACLE_BAD_METADATA;
     int st = check_metadata(num_reqs, query_start_loc, seq_lens, num_computed,
                             max_blocks_per_req, block_size);
@@ -247,7 +333,7 @@ int oracle_attention_range(int32_t num_reqs, int32_t num_heads_q, int32_t num_he
         if (!k_ctx || !v_ctx) { free(k_ctx); free(v_ctx); status = ORACLE_NO_MEMORY; break; }
         status = gather_context(r, length, num_heads_kv, head_dim, block_size, num_blocks,
                                 block_table, max_blocks_per_req, key_cache, value_cache,
-                                k_ctx, v_ctx);
+                                kv_fp8, k_ctx, v_ctx);
         if (status == ORACLE_OK) {
             int64_t pairs = (int64_t)q_len * num_heads_q;
 #pragma omp parallel
@@ -271,10 +357,13 @@ int oracle_attention_range(int32_t num_reqs, int32_t num_heads_q, int32_t num_he
                     const uint16_t *qrow = q + ((int64_t)t * num_heads_q + h) * head_dim;
                     for (int32_t d = 0; d < head_dim; ++d) qv[d] = bf16_to_double(qrow[d]);
                     double m, l;
+                    /* k = code * k_scale and v = code * v_scale (both 1 for bf16):
+                     * the key scale joins the softmax scale, the value scale
+                     * multiplies the normalised output */
                     attend_range(qv, k_ctx, v_ctx, kb, ke, h / group, num_heads_kv, head_dim,
-                                 softmax_scale, scores, &m, &l, ov);
+                                 softmax_scale * k_scale, scores, &m, &l, ov);
                     double *orow = out + ((int64_t)t * num_heads_q + h) * head_dim;
-                    for (int32_t d = 0; d < head_dim; ++d) orow[d] = ov[d];
+                    for (int32_t d = 0; d < head_dim; ++d) orow[d] = ov[d] * v_scale;
                     if (out_m) out_m[(int64_t)t * num_heads_q + h] = m;
                     if (out_l) out_l[(int64_t)t * num_heads_q + h] = l;
                 }
@@ -288,6 +377,36 @@ int oracle_attention_range(int32_t num_reqs, int32_t num_heads_q, int32_t num_he
     }
     free(wanted);
     return status;
+}
+
+int oracle_attention_range(int32_t num_reqs, int32_t num_heads_q, int32_t num_heads_kv,
+                           int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                           int32_t max_blocks_per_req, const int32_t *query_start_loc,
+                           const int32_t *seq_lens, const int32_t *num_computed,
+                           const int32_t *block_table, double softmax_scale,
+                           const uint16_t *q, const uint16_t *key_cache,
+                           const uint16_t *value_cache, const int32_t *rows, int32_t n_rows,
+                           int32_t key_begin_override, int32_t key_end_override,
+                           double *out, double *out_m, double *out_l) {
+    return attention_core(num_reqs, num_heads_q, num_heads_kv, head_dim, block_size, num_blocks,
+                          max_blocks_per_req, query_start_loc, seq_lens, num_computed, block_table,
+                          softmax_scale, q, key_cache, value_cache, 0, 1.0, 1.0, rows, n_rows,
+                          key_begin_override, key_end_override, out, out_m, out_l);
+}
+
+/* Step 3 over FP8 caches ([num_blocks][block_size][Hkv][D] E4M3 codes):
+ * every key and value is its code's value times k_scale / v_scale. */
+int oracle_attention_fp8(int32_t num_reqs, int32_t num_heads_q, int32_t num_heads_kv,
+                         int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                         int32_t max_blocks_per_req, const int32_t *query_start_loc,
+                         const int32_t *seq_lens, const int32_t *num_computed,
+                         const int32_t *block_table, double softmax_scale, const uint16_t *q,
+                         const uint8_t *key_cache, const uint8_t *value_cache, float k_scale,
+                         float v_scale, const int32_t *rows, int32_t n_rows, double *out) {
+    return attention_core(num_reqs, num_heads_q, num_heads_kv, head_dim, block_size, num_blocks,
+                          max_blocks_per_req, query_start_loc, seq_lens, num_computed, block_table,
+                          softmax_scale, q, key_cache, value_cache, 1, (double)k_scale,
+                          (double)v_scale, rows, n_rows, -1, -1, out, NULL, NULL);
 }
 
 /* The full causal attention of step 3. */

@@ -94,6 +94,19 @@ class Oracle:
         L.oracle_merge_partials.restype = None
         L.oracle_merge_partials.argtypes = [ctypes.c_int32, ctypes.c_int32, _f64p, _f64p, _f64p,
                                             _f64p, _f64p, _f64p]
+        _u8p = ctypes.POINTER(ctypes.c_uint8)
+        L.oracle_e4m3_value.restype = ctypes.c_double
+        L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_encode.restype = ctypes.c_uint8
+        L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        L.oracle_write_kv_fp8.restype = ctypes.c_int
+        L.oracle_write_kv_fp8.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _u16p, _u16p, _i64p,
+                                          _u8p, _u8p, ctypes.c_int64, ctypes.c_float, ctypes.c_float]
+        L.oracle_attention_fp8.restype = ctypes.c_int
+        L.oracle_attention_fp8.argtypes = [
+            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+            ctypes.c_int32, ctypes.c_int32, _i32p, _i32p, _i32p, _i32p, ctypes.c_double,
+            _u16p, _u8p, _u8p, ctypes.c_float, ctypes.c_float, _i32p, ctypes.c_int32, _f64p]
         L.oracle_check_common_prefix.restype = ctypes.c_int
         L.oracle_check_common_prefix.argtypes = [ctypes.c_int32, _i32p, _i32p, _i32p,
                                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]
@@ -184,6 +197,66 @@ class Oracle:
         return int(self.lib.oracle_check_common_prefix(
             len(nc), _ptr(qsl, _i32p), _ptr(nc, _i32p), _ptr(bt, _i32p), bt.shape[1],
             block_size, int(num_common_prefix_blocks)))
+
+    # -- FP8 (E4M3) cache ---------------------------------------------------
+    def e4m3_value(self, code: int) -> float:
+        return self.lib.oracle_e4m3_value(int(code) & 0xFF)
+
+    def e4m3_encode(self, x: float) -> int:
+        return int(self.lib.oracle_e4m3_encode(float(x)))
+
+    def write_kv_fp8(self, key, value, slot_mapping, key_cache, value_cache, k_scale: float,
+                     v_scale: float) -> int:
+        key = np.ascontiguousarray(key, dtype=np.uint16)
+        value = np.ascontiguousarray(value, dtype=np.uint16)
+        slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+        assert key_cache.dtype == np.uint8 and key_cache.flags["C_CONTIGUOUS"]
+        assert value_cache.dtype == np.uint8 and value_cache.flags["C_CONTIGUOUS"]
+        T, hkv, d = key.shape
+        num_slots = key_cache.shape[0] * key_cache.shape[1]
+        u8 = ctypes.POINTER(ctypes.c_uint8)
+        return int(self.lib.oracle_write_kv_fp8(T, hkv, d, _ptr(key, _u16p), _ptr(value, _u16p),
+                                                _ptr(slots, _i64p), _ptr(key_cache, u8), _ptr(value_cache, u8),
+                                                num_slots, float(k_scale), float(v_scale)))
+
+    def attention_fp8(self, *, query_start_loc, seq_lens, num_computed, block_table, q, key_cache,
+                      value_cache, softmax_scale: float, k_scale: float, v_scale: float, rows=None):
+        qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+        sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        nc = np.ascontiguousarray(num_computed, dtype=np.int32)
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        kc = np.ascontiguousarray(key_cache, dtype=np.uint8)
+        vc = np.ascontiguousarray(value_cache, dtype=np.uint8)
+        T, hq, d = q.shape
+        num_blocks, block_size, hkv, d2 = kc.shape
+        assert d == d2 and vc.shape == kc.shape
+        out = np.full((T, hq, d), np.nan, dtype=np.float64)
+        rows_arr = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+        n_rows = 0 if rows_arr is None else len(rows_arr)
+        u8 = ctypes.POINTER(ctypes.c_uint8)
+        st = self.lib.oracle_attention_fp8(
+            len(sl), hq, hkv, d, block_size, num_blocks, bt.shape[1], _ptr(qsl, _i32p), _ptr(sl, _i32p),
+            _ptr(nc, _i32p), _ptr(bt, _i32p), float(softmax_scale), _ptr(q, _u16p), _ptr(kc, u8),
+            _ptr(vc, u8), float(k_scale), float(v_scale), _ptr(rows_arr, _i32p), n_rows, _ptr(out, _f64p))
+        if st != OK:
+            raise OracleError(f"attention_fp8 status {st}")
+        return out
+
+    def step_fp8(self, *, query_start_loc, seq_lens, num_computed, block_table, q, key, value,
+                 key_cache, value_cache, softmax_scale: float, k_scale: float, v_scale: float, rows=None):
+        """FP8 cache: write (quantising), then attend (dequantising)."""
+        kc = np.array(key_cache, dtype=np.uint8, copy=True, order="C")
+        vc = np.array(value_cache, dtype=np.uint8, copy=True, order="C")
+        block_size = kc.shape[1]
+        slots = self.slot_mapping(query_start_loc, num_computed, block_table, block_size)
+        st = self.write_kv_fp8(key, value, slots, kc, vc, k_scale, v_scale)
+        if st != OK:
+            raise OracleError(f"write_fp8 status {st}")
+        out = self.attention_fp8(query_start_loc=query_start_loc, seq_lens=seq_lens, num_computed=num_computed,
+                                 block_table=block_table, q=q, key_cache=kc, value_cache=vc,
+                                 softmax_scale=softmax_scale, k_scale=k_scale, v_scale=v_scale, rows=rows)
+        return kc, vc, slots, out
 
     # -- the whole step: write, then attend ---------------------------------
     def step(self, *, query_start_loc, seq_lens, num_computed, block_table, q, key, value,

@@ -389,3 +389,100 @@ def run_all(orc):
         except Exception:  # noqa: BLE001 -- any failure counts
             failed.append(pin.__name__)
     return failed
+
+
+# ------------------------------------------------------------ FP8 (E4M3) --
+
+def pin_e4m3_codes(orc):
+    """Code <-> value pairs fixed by the E4M3 definition (golden/e4m3_codes.txt)."""
+    for value, code in read_table("e4m3_codes.txt"):
+        v, c = float(value), int(code, 16)
+        assert orc.e4m3_encode(v) == c, (value, hex(orc.e4m3_encode(v)))
+        got = orc.e4m3_value(c)
+        assert got == v and math.copysign(1.0, got) == math.copysign(1.0, v), (code, got)
+
+
+def pin_e4m3_round_trip_and_order(orc):
+    """Every finite code survives decode -> encode; magnitudes grow with the
+    code; the sign bit mirrors the value; 0x7F / 0xFF are NaN."""
+    prev = -1.0
+    for c in range(0x7F):
+        v = orc.e4m3_value(c)
+        assert orc.e4m3_encode(v) == c, hex(c)
+        assert orc.e4m3_encode(-v) == (c | 0x80), hex(c)
+        assert v > prev or (c == 0 and v == 0.0), hex(c)
+        prev = v
+    assert math.isnan(orc.e4m3_value(0x7F)) and math.isnan(orc.e4m3_value(0xFF))
+
+
+def pin_e4m3_rounding(orc):
+    """Nearest value, ties to the even mantissa, saturation at 448."""
+    assert orc.e4m3_encode(1.0625) == 0x38          # halfway 1.0 / 1.125 -> even (1.0)
+    assert orc.e4m3_encode(1.1875) == 0x3A          # halfway 1.125 / 1.25 -> even (1.25)
+    assert orc.e4m3_encode(1.06) == 0x38 and orc.e4m3_encode(1.07) == 0x39   # either side of 1.0625
+    assert orc.e4m3_encode(1.5 * 2 ** -9) == 0x02   # subnormal tie -> even
+    assert orc.e4m3_encode(2 ** -11) == 0x00        # below half the smallest subnormal
+    assert orc.e4m3_encode(0.99 * 2 ** -6) == 0x08  # rounds up into the normal range
+    for big in (449.0, 463.9, 464.0, 500.0, 1e6, float("inf")):
+        assert orc.e4m3_encode(big) == 0x7E and orc.e4m3_encode(-big) == 0xFE, big
+    assert orc.e4m3_encode(float("nan")) == 0x7F
+
+
+def pin_fp8_write_scales(orc):
+    """The FP8 write stores the code of x / scale, K and V with their own scale."""
+    nb, bs, hkv, d = 2, 16, 1, 64
+    kc = np.zeros((nb, bs, hkv, d), np.uint8)
+    vc = np.zeros((nb, bs, hkv, d), np.uint8)
+    key = to_bf16_bits(np.full((3, hkv, d), 2.0))
+    val = to_bf16_bits(np.full((3, hkv, d), -3.0))
+    slots = np.array([5, -1, 20], np.int64)
+    assert orc.write_kv_fp8(key, val, slots, kc, vc, 0.5, 2.0) == 0
+    flat_k, flat_v = kc.reshape(-1, d), vc.reshape(-1, d)
+    assert np.all(flat_k[5] == 0x48) and np.all(flat_k[20] == 0x48)      # 2 / 0.5 = 4
+    assert np.all(flat_v[5] == 0xBC) and np.all(flat_v[20] == 0xBC)      # -3 / 2 = -1.5
+    untouched = [i for i in range(nb * bs) if i not in (5, 20)]
+    assert not flat_k[untouched].any() and not flat_v[untouched].any()
+
+
+def _fp8_case(seed):
+    """Tiny FP8 batch and a bf16 batch holding exactly its dequantised values
+    (a power-of-two scale keeps every code_value * scale exact in bf16)."""
+    rng = _rng(seed)
+    case = Case(rng, hq=4, hkv=2, d=64, q_lens=[1, 9, 1], seq_lens=[37, 9, 20])
+    codes_k = rng.integers(0, 256, size=case.kc.shape).astype(np.uint8)
+    codes_v = rng.integers(0, 256, size=case.vc.shape).astype(np.uint8)
+    for codes in (codes_k, codes_v):      # no NaN codes
+        codes[(codes & 0x7F) == 0x7F] = 0x3A
+    return case, codes_k, codes_v
+
+
+def pin_fp8_attention_is_dequantised_attention(orc):
+    """Attention over FP8 caches equals attention over the dequantised values."""
+    case, ck, cv = _fp8_case(30)
+    ks, vs = 0.25, 0.5
+    vals_k = np.vectorize(orc.e4m3_value)(ck) * ks
+    vals_v = np.vectorize(orc.e4m3_value)(cv) * vs
+    kw = dict(query_start_loc=case.qsl, seq_lens=case.seq_lens.astype(np.int32),
+              num_computed=case.num_computed.astype(np.int32), block_table=case.block_table,
+              q=to_bf16_bits(case.q), softmax_scale=case.scale)
+    got = orc.attention_fp8(key_cache=ck, value_cache=cv, k_scale=ks, v_scale=vs, **kw)
+    want = orc.attention(key_cache=to_bf16_bits(vals_k), value_cache=to_bf16_bits(vals_v), **kw)
+    assert np.allclose(got, want, rtol=0, atol=1e-12)
+
+
+def pin_fp8_scale_roles(orc):
+    """k_scale acts as a softmax temperature, v_scale multiplies the output."""
+    case, ck, cv = _fp8_case(31)
+    kw = dict(query_start_loc=case.qsl, seq_lens=case.seq_lens.astype(np.int32),
+              num_computed=case.num_computed.astype(np.int32), block_table=case.block_table,
+              q=to_bf16_bits(case.q), key_cache=ck, value_cache=cv)
+    a = orc.attention_fp8(softmax_scale=case.scale, k_scale=0.02, v_scale=1.0, **kw)
+    b = orc.attention_fp8(softmax_scale=case.scale * 2, k_scale=0.01, v_scale=1.0, **kw)
+    c = orc.attention_fp8(softmax_scale=case.scale, k_scale=0.02, v_scale=3.0, **kw)
+    assert np.allclose(a, b, rtol=1e-12, atol=1e-12)
+    assert np.allclose(c, 3.0 * a, rtol=1e-12, atol=1e-12)
+    d = orc.attention_fp8(softmax_scale=case.scale, k_scale=0.04, v_scale=1.0, **kw)
+    assert not np.allclose(a, d)
+
+
+PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -41,6 +41,13 @@ MUTANTS = [
      "if (0) return ORACLE_BAD_METADATA;"),
     ("length_identity_unchecked", "if (num_computed[r] + q_len != seq_lens[r]) return ORACLE_BAD_METADATA;",
      "if (0) return ORACLE_BAD_METADATA;"),
+    ("e4m3_ties_away", "double v = rint(a / quantum) * quantum;", "double v = round(a / quantum) * quantum;"),
+    ("e4m3_no_saturation", "if (v > 448.0) v = 448.0;", "if (0) v = 448.0;"),
+    ("e4m3_wrong_bias", "else v = ldexp(1.0 + m / 8.0, e - 7);", "else v = ldexp(1.0 + m / 8.0, e - 8);"),
+    ("fp8_scale_multiplied", "return (float)bf16_to_double(bits) / scale;", "return (float)bf16_to_double(bits) * scale;"),
+    ("fp8_key_scale_dropped", "softmax_scale * k_scale, scores, &m, &l, ov);", "softmax_scale, scores, &m, &l, ov);"),
+    ("fp8_value_scale_dropped", "for (int32_t d = 0; d < head_dim; ++d) orow[d] = ov[d] * v_scale;",
+     "for (int32_t d = 0; d < head_dim; ++d) orow[d] = ov[d];"),
     ("query_head_transposed", "const uint16_t *qrow = q + ((int64_t)t * num_heads_q + h) * head_dim;",
      "const uint16_t *qrow = q + ((int64_t)t * num_heads_q + (num_heads_q - 1 - h)) * head_dim;"),
 ]
