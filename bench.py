@@ -41,24 +41,25 @@ L2_FLUSH_BYTES = 256 << 20
 WORKLOADS = {
     "decode": ("decode-only Llama-3-8B-shaped layer: 64 requests x 1 token, seq_len U[512,4096], "
                "Hq=32 Hkv=8 D=128 bf16, block_size 16, 20000-block permuted pool",
-               lambda seed, dev: workloads.decode(seed=seed, device=dev, pool_device=dev)),
+               lambda seed, dev, kv: workloads.decode(seed=seed, device=dev, pool_device=dev, kv_cache_dtype=kv)),
     "tiny": ("tiny mixed step (reading 1B): Hq=4 Hkv=2 D=64, 2 decodes + 8-token chunk over 9 cached + "
              "33-token prefill, 64-block pool",
-             lambda seed, dev: workloads.tiny("1B", seed=seed, device=dev)),
+             lambda seed, dev, kv: workloads.tiny("1B", seed=seed, device=dev)),
     "mixed": ("mixed continuous-batching step: 256 decodes seq_len U[1024,8192] (32 share a 1024-token "
               "prefix) + 2048-token chunk from 0 + 2048-token chunk over 4096 cached; Hq=32 Hkv=8 D=128",
-              lambda seed, dev: workloads.mixed(seed=seed, device=dev, pool_device=dev)),
+              lambda seed, dev, kv: workloads.mixed(seed=seed, device=dev, pool_device=dev, kv_cache_dtype=kv)),
     "prefill": ("the two chunked-prefill requests of the mixed step alone: a 2048-token chunk from 0 and a "
                 "2048-token chunk over 4096 cached tokens; Hq=32 Hkv=8 D=128",
-                lambda seed, dev: workloads.mixed(seed=seed, n_decode=0, n_shared=0, device=dev, pool_device=dev)),
+                lambda seed, dev, kv: workloads.mixed(seed=seed, n_decode=0, n_shared=0, device=dev, pool_device=dev,
+                                                        kv_cache_dtype=kv)),
     "long": ("long-context decode, 70B-shaped layer: 8 requests x 131072 tokens, Hq=64 Hkv=8 D=128",
-             lambda seed, dev: workloads.long_context(seed=seed, device=dev, pool_device=dev)),
+             lambda seed, dev, kv: workloads.long_context(seed=seed, device=dev, pool_device=dev, kv_cache_dtype=kv)),
     "cascade": ("cascade shared-prefix decode: 128 decodes over a 4096-token common prefix "
                 "(num_common_prefix_blocks=256) + private suffixes U[64,1024]; Hq=32 Hkv=8 D=128",
-                lambda seed, dev: workloads.cascade(seed=seed, device=dev, pool_device=dev)),
+                lambda seed, dev, kv: workloads.cascade(seed=seed, device=dev, pool_device=dev, kv_cache_dtype=kv)),
     "cascade-off": ("the cascade workload on the plain route (num_common_prefix_blocks=0)",
-                    lambda seed, dev: workloads.cascade(seed=seed, device=dev, pool_device=dev,
-                                                        use_cascade=False)),
+                    lambda seed, dev, kv: workloads.cascade(seed=seed, device=dev, pool_device=dev,
+                                                            use_cascade=False, kv_cache_dtype=kv)),
 }
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the
@@ -194,10 +195,15 @@ def oracle_sample(batch, host, budget_s: float, seed: int = 0):
         a, b = int(batch.query_start_loc[r]), int(batch.query_start_loc[r + 1])
         rows = np.arange(a, b, dtype=np.int32)
         t0 = time.perf_counter()
-        orc.write_kv(host["key"][a:b], host["value"][a:b], slots[a:b], kc, vc)
-        orc.attention(query_start_loc=batch.query_start_loc, seq_lens=batch.seq_lens,
+        common = dict(query_start_loc=batch.query_start_loc, seq_lens=batch.seq_lens,
                       num_computed=batch.num_computed, block_table=batch.block_table, q=host["q"],
                       key_cache=kc, value_cache=vc, softmax_scale=batch.softmax_scale, rows=rows)
+        if batch.kv_cache_dtype == "fp8":
+            orc.write_kv_fp8(host["key"][a:b], host["value"][a:b], slots[a:b], kc, vc, batch.k_scale, batch.v_scale)
+            orc.attention_fp8(k_scale=batch.k_scale, v_scale=batch.v_scale, **common)
+        else:
+            orc.write_kv(host["key"][a:b], host["value"][a:b], slots[a:b], kc, vc)
+            orc.attention(**common)
         seconds += time.perf_counter() - t0
         tokens += b - a
         taken += 1
@@ -208,8 +214,10 @@ def oracle_sample(batch, host, budget_s: float, seed: int = 0):
 
 
 def host_copies(batch):
+    def cache(t):
+        return t.detach().cpu().numpy().copy() if t.dtype == torch.uint8 else np.array(bf16_bits(t))
     return {"q": bf16_bits(batch.q), "key": bf16_bits(batch.key), "value": bf16_bits(batch.value),
-            "kc": np.array(bf16_bits(batch.key_cache)), "vc": np.array(bf16_bits(batch.value_cache))}
+            "kc": cache(batch.key_cache), "vc": cache(batch.value_cache)}
 
 
 # ---------------------------------------------------------------- reference --
@@ -218,7 +226,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     desc, maker = WORKLOADS[args.workload]
-    batch = maker(args.seed, "cpu")
+    batch = maker(args.seed, "cpu", args.kv_dtype)
     host = host_copies(batch)
     per_step = max(0.02, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
@@ -256,7 +264,7 @@ def run_ours(args, world, rank, local):
     build.build()
     binding.load()
     desc, maker = WORKLOADS[args.workload]
-    batch = maker(args.seed + rank, dev)
+    batch = maker(args.seed + rank, dev, args.kv_dtype)
     T = batch.num_tokens
     st = DeviceStep(batch, dev)
     q, key, value = batch.q.to(dev), batch.key.to(dev), batch.value.to(dev)
@@ -402,9 +410,10 @@ def run_ours(args, world, rank, local):
         line = {
             "metric": METRIC, "value": tokens_all / (ms_all / 1e3), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_all, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if args.kv_dtype == "bf16" else "bf16 q/out, e4m3 kv",
             "data": "synthetic (seeded N(0,1) bf16 q/k/v and cache pool, seeded lengths and block permutation)",
             "config": {"workload": desc, "name": args.workload, "tokens_per_step": T, "seed": args.seed,
+                       "kv_cache_dtype": args.kv_dtype,
                        "l2": "flushed between timed steps (256 MiB write + read-back, outside the step events)",
                        "step": "pa_plan (host) + pa_slot_mapping + pa_write_kv + pa_attention",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -426,6 +435,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="decode")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
+                    help="KV cache element type (fp8 = E4M3 codes with per-tensor scales)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -27,9 +27,9 @@
  * at absolute position num_computed_tokens[r] + i and attends to keys
  * 0..position (bottom-right causal alignment).
  *
- * Supported: head_dim 64 or 128, block_size 16, Hq % Hkv == 0 with the group
- * size Hq/Hkv a power of two up to 16, num_blocks * 16 < 2^31.  Other shapes
- * return PA_ERR_UNSUPPORTED.
+ * Supported: head_dim 64 or 128 (128 only with FP8 caches), block_size 16,
+ * Hq % Hkv == 0 with the group size Hq/Hkv a power of two up to 16,
+ * num_blocks * 16 < 2^31.  Other shapes return PA_ERR_UNSUPPORTED.
  *
  * Ownership: the caller allocates and owns every device buffer (q, caches,
  * block table, out, slot mapping, workspace).  A plan is host memory owned by
@@ -91,7 +91,17 @@ typedef struct {
                                             selects the cascade route              */
     float softmax_scale;           /* scores are softmax_scale * <q, k>; must be > 0   */
     int32_t num_sms;               /* SMs to plan for; 0 = query the current device    */
+    int32_t kv_cache_dtype;        /* PA_KV_BF16 or PA_KV_FP8_E4M3                      */
+    float k_scale;                 /* FP8 caches: a key reads code_value * k_scale     */
+    float v_scale;                 /* FP8 caches: a value reads code_value * v_scale   */
 } pa_batch_desc;
+
+/* Element type of the K/V caches ("vLLM 推理流程分析" §6.3: kv_cache_dtype, FP8
+ * conversion with k_scale / v_scale).  FP8 caches hold one E4M3 code per
+ * element (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, largest finite
+ * 448, S.1111.111 = NaN) in the same [num_blocks][16][Hkv][D] layout. */
+#define PA_KV_BF16 0
+#define PA_KV_FP8_E4M3 1
 
 /* Work decomposition of a plan (for tests, benchmarks and launch counts). */
 typedef struct {
@@ -105,6 +115,8 @@ typedef struct {
     int32_t num_partial_slots;     /* (token, partition) partial results              */
     int32_t num_merge_rows;        /* tokens whose output is merged from partials     */
     int32_t kernels_per_call;      /* kernel launches one pa_attention call makes     */
+    int32_t num_dequant_blocks;    /* FP8: cache blocks the tensor-core tiles read,
+                                      expanded to bf16 in the workspace each call   */
     int64_t decode_kv_bytes;       /* K+V bytes the decode rows must read             */
     int64_t prefix_kv_bytes;       /* K+V bytes of the shared prefix (read once)      */
     double  extend_flops;          /* 4*D*Hq * visible (query, key) pairs, extend     */
@@ -120,8 +132,9 @@ typedef struct {
  * head counts or num_blocks, Hq % Hkv != 0, query_start_loc[0] != 0 or a
  * decreasing query_start_loc, num_computed + q_len != seq_len, a context
  * needing more than max_blocks_per_req blocks, a non-positive or non-finite
- * softmax_scale, a block id out of range in block_table_host, or a violated
- * common-prefix precondition.  PA_ERR_UNSUPPORTED for shapes listed above.
+ * softmax_scale, a block id out of range in block_table_host, a violated
+ * common-prefix precondition, an unknown kv_cache_dtype, or (FP8) a scale that
+ * is not finite and > 0.  PA_ERR_UNSUPPORTED for shapes listed above.
  * Host-only (no CUDA call) unless num_sms == 0.
  */
 pa_status pa_plan(const pa_batch_desc *desc, pa_plan_t **out, size_t *workspace_bytes);
@@ -166,14 +179,30 @@ pa_status pa_write_kv(const void *key, const void *value, const int64_t *slot_ma
                       int32_t *device_error_word, void *stream);
 
 /*
+ * The KV-cache write into FP8 caches ("vLLM 推理流程分析" §6.3: with an FP8
+ * kv_cache_dtype the write converts with k_scale / v_scale): element e of
+ * key[t] is stored as the E4M3 code of (float)key[t][e] / k_scale, the
+ * quotient formed in IEEE binary32 and rounded to the nearest E4M3 value, ties
+ * to even, saturating to +-448 (NaN stays NaN); values likewise with v_scale.
+ * Slots, skipping, the error word, ordering and alignment as for pa_write_kv;
+ * the caches are uint8 [num_slots/16][16][Hkv][D].  The scales must be finite
+ * and > 0 (else PA_ERR_INVALID_ARGUMENT).
+ */
+pa_status pa_write_kv_fp8(const void *key, const void *value, const int64_t *slot_mapping,
+                          int32_t num_tokens, int32_t num_heads_kv, int32_t head_dim,
+                          void *key_cache, void *value_cache, int64_t num_slots, float k_scale,
+                          float v_scale, int32_t *device_error_word, void *stream);
+
+/*
  * Causal GQA attention of the step ("vLLM 推理流程分析" §6.2,
  * flash_attn_varlen_func(q, key_cache, value_cache, cu_seqlens_q, seqlen_k,
  * block_table, softmax_scale, causal=True)).
  *   plan          from pa_plan for this step (may be reused by every layer)
  *   q             DEVICE bf16 [T][Hq][D]
  *   key_cache,
- *   value_cache   DEVICE bf16 [num_blocks][16][Hkv][D], already holding this
- *                 step's new rows (pa_write_kv enqueued earlier)
+ *   value_cache   DEVICE [num_blocks][16][Hkv][D] of the plan's kv_cache_dtype
+ *                 (bf16, or E4M3 codes read as code_value * k_scale / v_scale),
+ *                 already holding this step's new rows (written earlier)
  *   block_table   DEVICE int32 [R][max_blocks_per_req]; entries past a
  *                 request's last needed block are never read
  *   out           DEVICE bf16 [T][Hq][D], written for every scheduled token

@@ -22,6 +22,9 @@ PA_ERR_CUDA = 3
 PA_ERR_DEVICE_CHECK = 4
 PA_ERR_WORKSPACE_TOO_SMALL = 5
 
+PA_KV_BF16 = 0
+PA_KV_FP8_E4M3 = 1
+
 PA_DEVERR_SLOT_RANGE = 0x1
 PA_DEVERR_BLOCK_RANGE = 0x2
 PA_DEVERR_TIMEOUT = 0x4
@@ -29,7 +32,7 @@ PA_DEVERR_TIMEOUT = 0x4
 # symbols include/pa.h declares (checked by the CPU tests)
 EXPORTED = ("pa_plan", "pa_plan_destroy", "pa_plan_get_info", "pa_slot_mapping", "pa_write_kv",
             "pa_attention", "pa_check_device_errors", "pa_plan_enable_timing",
-            "pa_plan_kernel_times", "pa_status_string", "pa_attention_no_alloc")
+            "pa_plan_kernel_times", "pa_status_string", "pa_attention_no_alloc", "pa_write_kv_fp8")
 
 
 class PaError(RuntimeError):
@@ -54,6 +57,9 @@ class BatchDesc(ctypes.Structure):
         ("num_common_prefix_blocks", ctypes.c_int32),
         ("softmax_scale", ctypes.c_float),
         ("num_sms", ctypes.c_int32),
+        ("kv_cache_dtype", ctypes.c_int32),
+        ("k_scale", ctypes.c_float),
+        ("v_scale", ctypes.c_float),
     ]
 
 
@@ -69,6 +75,7 @@ class PlanInfo(ctypes.Structure):
         ("num_partial_slots", ctypes.c_int32),
         ("num_merge_rows", ctypes.c_int32),
         ("kernels_per_call", ctypes.c_int32),
+        ("num_dequant_blocks", ctypes.c_int32),
         ("decode_kv_bytes", ctypes.c_int64),
         ("prefix_kv_bytes", ctypes.c_int64),
         ("extend_flops", ctypes.c_double),
@@ -112,6 +119,8 @@ def load(path: str | None = None, build_if_missing: bool = False) -> ctypes.CDLL
     lib.pa_slot_mapping.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp, vp]
     lib.pa_write_kv.restype = ctypes.c_int
     lib.pa_write_kv.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, i64, vp, vp]
+    lib.pa_write_kv_fp8.restype = ctypes.c_int
+    lib.pa_write_kv_fp8.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, i64, ctypes.c_float, ctypes.c_float, vp, vp]
     lib.pa_attention.restype = ctypes.c_int
     lib.pa_attention.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.pa_attention_no_alloc.restype = ctypes.c_int
@@ -189,7 +198,8 @@ class Plan:
 
 def make_desc(*, num_heads_q, num_heads_kv, head_dim, num_blocks, query_start_loc, seq_lens,
               num_computed_tokens, block_table_host=None, max_blocks_per_req=None,
-              num_common_prefix_blocks=0, softmax_scale, num_sms=0, block_size=16):
+              num_common_prefix_blocks=0, softmax_scale, num_sms=0, block_size=16, kv_cache_dtype=0,
+              k_scale=1.0, v_scale=1.0):
     qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     nc = np.ascontiguousarray(num_computed_tokens, dtype=np.int32)
@@ -212,6 +222,9 @@ def make_desc(*, num_heads_q, num_heads_kv, head_dim, num_blocks, query_start_lo
     d.num_common_prefix_blocks = int(num_common_prefix_blocks)
     d.softmax_scale = float(softmax_scale)
     d.num_sms = int(num_sms)
+    d.kv_cache_dtype = int(kv_cache_dtype)
+    d.k_scale = float(k_scale)
+    d.v_scale = float(v_scale)
     return d, (qsl, sl, nc, bt)
 
 
@@ -248,6 +261,16 @@ def pa_write_kv(key, value, slot_mapping, key_cache, value_cache, device_error_w
     _check(load().pa_write_kv(_ptr(key), _ptr(value), _ptr(slot_mapping), T, hkv, d, _ptr(key_cache),
                               _ptr(value_cache), num_slots, _ptr(device_error_word), _stream(stream)),
            "pa_write_kv")
+
+
+def pa_write_kv_fp8(key, value, slot_mapping, key_cache, value_cache, k_scale: float, v_scale: float,
+                    device_error_word=None, stream=None):
+    """Quantising cache write into E4M3 caches (uint8 tensors)."""
+    T, hkv, d = key.shape
+    num_slots = key_cache.shape[0] * key_cache.shape[1]
+    _check(load().pa_write_kv_fp8(_ptr(key), _ptr(value), _ptr(slot_mapping), T, hkv, d, _ptr(key_cache),
+                                  _ptr(value_cache), num_slots, float(k_scale), float(v_scale),
+                                  _ptr(device_error_word), _stream(stream)), "pa_write_kv_fp8")
 
 
 def pa_attention(plan: Plan, q, key_cache, value_cache, block_table, out, workspace, stream=None):

@@ -25,27 +25,34 @@ namespace {
 
 using namespace dev;
 
-template <int D, int HG>
+template <int D, int HG, bool KV8>
 struct DecodeCfg {
-    static constexpr int NH = D / 64;                      // 128-byte column halves
-    static constexpr int BOX = 16 * 128;                   // one [16][64] bf16 box
+    static constexpr int EB = KV8 ? 1 : 2;                 // bytes per cache element
+    static constexpr int NH = D * EB / 128;                // 128-byte boxes per cache row
+    static constexpr int CPE = 128 / EB;                   // elements per box row
+    static constexpr int BOX = 16 * 128;                   // one [16 rows][128 B] box
     static constexpr int TSTAGE = HG * NH * BOX;           // K (or V) bytes per block
-    static constexpr int STAGE = decode_stage_bytes(D, HG);
-    static constexpr int NS = decode_stages(D, HG);
+    static constexpr int STAGE = decode_stage_bytes(D, HG, KV8);
+    static constexpr int NS = decode_stages(D, HG, KV8);
+    static constexpr int STAGING = decode_staging_bytes(D, HG, KV8);  // f16 V rows per warp (E4M3)
     static constexpr int THREADS = decode_threads(HG);
-    static constexpr int SMEM = decode_smem_bytes(D, HG);
+    static constexpr int SMEM = decode_smem_bytes(D, HG, KV8);
 };
 
-template <int D, int HG>
+// bf16 pair -> f16 pair (saturating at the largest finite f16)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) { return pack_f16x2_sat(bf16_lo(w), bf16_hi(w)); }
+
+template <int D, int HG, bool KV8>
 __global__ void __launch_bounds__((HG + 1) * 32, 1)
 decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const DecodeParams p) {
-    using C = DecodeCfg<D, HG>;
+    using C = DecodeCfg<D, HG, KV8>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ int abort_flag;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;           // stages, 1024-aligned
-    const uint32_t bar0 = base + C::NS * C::STAGE;           // full_k | full_v | empty
+    const uint32_t staging = base + C::NS * C::STAGE;        // E4M3: per-warp f16 V rows
+    const uint32_t bar0 = staging + C::STAGING;              // full_k | full_v | empty
     auto full_k = [&](int s) { return bar0 + 8u * s; };
     auto full_v = [&](int s) { return bar0 + 8u * (C::NS + s); };
     auto empty = [&](int s) { return bar0 + 8u * (2 * C::NS + s); };
@@ -111,7 +118,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     const int idx = lane % (HG * C::NH);
                     const uint32_t dst = stage(s) + tensor * C::TSTAGE + idx * C::BOX;
                     const uint32_t bar = tensor ? full_v(s) : full_k(s);
-                    tma_load_3d(dst, tensor ? &tm_v : &tm_k, (idx % C::NH) * 64, h0 + idx / C::NH,
+                    tma_load_3d(dst, tensor ? &tm_v : &tm_k, (idx % C::NH) * C::CPE, h0 + idx / C::NH,
                                 blk * kBlockSize, bar);
                 }
                 ++issued;
@@ -137,13 +144,30 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const int kvh = item.head_group * HG + warp;
             const uint16_t *qrow = p.q + (static_cast<int64_t>(item.token) * p.num_heads_q + kvh * G) * D;
             uint32_t qf[D / 16][4];
+            if constexpr (!KV8) {
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const int c = kk * 16 + 2 * t4;
-                qf[kk][0] = g < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + g * D + c)) : 0u;
-                qf[kk][1] = g + 8 < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + (g + 8) * D + c)) : 0u;
-                qf[kk][2] = g < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + g * D + c + 8)) : 0u;
-                qf[kk][3] = g + 8 < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + (g + 8) * D + c + 8)) : 0u;
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int c = kk * 16 + 2 * t4;
+                    qf[kk][0] = g < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + g * D + c)) : 0u;
+                    qf[kk][1] = g + 8 < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + (g + 8) * D + c)) : 0u;
+                    qf[kk][2] = g < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + g * D + c + 8)) : 0u;
+                    qf[kk][3] = g + 8 < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + (g + 8) * D + c + 8)) : 0u;
+                }
+            } else {
+                // f16 operands; the contraction index is permuted so that a
+                // lane's four k-values of a step are four adjacent key bytes:
+                // k = 2t,2t+1 <-> d = 16kk+4t+{0,1};  k = 2t+8,2t+9 <-> d = 16kk+4t+{2,3}
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int c = kk * 16 + 4 * t4;
+                    auto ld = [&](int row, int col) {
+                        return bf16x2_to_f16x2(__ldg(reinterpret_cast<const uint32_t *>(qrow + row * D + col)));
+                    };
+                    qf[kk][0] = g < G ? ld(g, c) : 0u;
+                    qf[kk][1] = g + 8 < G ? ld(g + 8, c) : 0u;
+                    qf[kk][2] = g < G ? ld(g, c + 2) : 0u;
+                    qf[kk][3] = g + 8 < G ? ld(g + 8, c + 2) : 0u;
+                }
             }
             float o[D / 8][4];
 #pragma unroll
@@ -162,15 +186,27 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 const uint32_t vb = kb + C::TSTAGE;
                 // S = Q K^T over this block's 16 keys (two n-tiles of 8 keys)
                 float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                if constexpr (!KV8) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const int mi = lane >> 3;
-                    const int key = (mi >> 1) * 8 + (lane & 7);
-                    const int chunk = (kk % 4) * 2 + (mi & 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4(sw128(kb + (kk / 4) * C::BOX, key, chunk), b0, b1, b2, b3);
-                    mma_bf16_16816(sc[0], qf[kk], b0, b1);
-                    mma_bf16_16816(sc[1], qf[kk], b2, b3);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const int mi = lane >> 3;
+                        const int key = (mi >> 1) * 8 + (lane & 7);
+                        const int chunk = (kk % 4) * 2 + (mi & 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldmatrix_x4(sw128(kb + (kk / 4) * C::BOX, key, chunk), b0, b1, b2, b3);
+                        mma_bf16_16816(sc[0], qf[kk], b0, b1);
+                        mma_bf16_16816(sc[1], qf[kk], b2, b3);
+                    }
+                } else {
+                    // keys g and g+8: the four codes d = 16kk+4t..+3 of each
+                    // (one 32-bit word, conflict-free across the warp)
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t w0 = lds_u32(sw128(kb, g, kk) + 4 * t4);
+                        const uint32_t w1 = lds_u32(sw128(kb, g + 8, kk) + 4 * t4);
+                        mma_f16_16816(sc[0], qf[kk], e4m3x2_to_f16x2(w0 & 0xFFFFu), e4m3x2_to_f16x2(w0 >> 16));
+                        mma_f16_16816(sc[1], qf[kk], e4m3x2_to_f16x2(w1 & 0xFFFFu), e4m3x2_to_f16x2(w1 >> 16));
+                    }
                 }
                 // mask keys past the context, scale to log2 units
                 const int key0 = pg * kBlockSize;
@@ -204,45 +240,94 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 const float r0 = m0 == -INFINITY ? 0.f : m0;
                 const float r1 = m1 == -INFINITY ? 0.f : m1;
                 uint32_t pa[4];
-                pa[0] = pack_bf16x2(ex2(sc[0][0] - r0), ex2(sc[0][1] - r0));
-                pa[1] = pack_bf16x2(ex2(sc[0][2] - r1), ex2(sc[0][3] - r1));
-                pa[2] = pack_bf16x2(ex2(sc[1][0] - r0), ex2(sc[1][1] - r0));
-                pa[3] = pack_bf16x2(ex2(sc[1][2] - r1), ex2(sc[1][3] - r1));
-                l0 += bf16_lo(pa[0]) + bf16_hi(pa[0]) + bf16_lo(pa[2]) + bf16_hi(pa[2]);
-                l1 += bf16_lo(pa[1]) + bf16_hi(pa[1]) + bf16_lo(pa[3]) + bf16_hi(pa[3]);
+                if constexpr (!KV8) {
+                    pa[0] = pack_bf16x2(ex2(sc[0][0] - r0), ex2(sc[0][1] - r0));
+                    pa[1] = pack_bf16x2(ex2(sc[0][2] - r1), ex2(sc[0][3] - r1));
+                    pa[2] = pack_bf16x2(ex2(sc[1][0] - r0), ex2(sc[1][1] - r0));
+                    pa[3] = pack_bf16x2(ex2(sc[1][2] - r1), ex2(sc[1][3] - r1));
+                    l0 += bf16_lo(pa[0]) + bf16_hi(pa[0]) + bf16_lo(pa[2]) + bf16_hi(pa[2]);
+                    l1 += bf16_lo(pa[1]) + bf16_hi(pa[1]) + bf16_lo(pa[3]) + bf16_hi(pa[3]);
+                } else {
+                    pa[0] = pack_f16x2(ex2(sc[0][0] - r0), ex2(sc[0][1] - r0));
+                    pa[1] = pack_f16x2(ex2(sc[0][2] - r1), ex2(sc[0][3] - r1));
+                    pa[2] = pack_f16x2(ex2(sc[1][0] - r0), ex2(sc[1][1] - r0));
+                    pa[3] = pack_f16x2(ex2(sc[1][2] - r1), ex2(sc[1][3] - r1));
+                    l0 += f16_lo(pa[0]) + f16_hi(pa[0]) + f16_lo(pa[2]) + f16_hi(pa[2]);
+                    l1 += f16_lo(pa[1]) + f16_hi(pa[1]) + f16_lo(pa[3]) + f16_hi(pa[3]);
+                }
 
                 if (!warp_wait(full_v(s), par, &abort_flag)) {
                     if (lane == 0) raise_abort(&abort_flag, p.err, kErrTimeout);
                     ok = false;
                     break;
                 }
-                if (valid_keys < kBlockSize) {
-                    // rows past the context may hold anything (even NaN); zero
-                    // them so that 0-weight * row stays 0 inside the MMA
-                    const int bad = kBlockSize - valid_keys;
-                    for (int i = lane; i < bad * C::NH * 8; i += 32) {
-                        const int row = valid_keys + i / (C::NH * 8);
-                        const int half = (i / 8) % C::NH;
-                        const int ch = i % 8;
-                        const uint32_t a = vb + half * C::BOX + row * 128 + ch * 16;
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
+                if constexpr (!KV8) {
+                    if (valid_keys < kBlockSize) {
+                        // rows past the context may hold anything (even NaN); zero
+                        // them so that 0-weight * row stays 0 inside the MMA
+                        const int bad = kBlockSize - valid_keys;
+                        for (int i = lane; i < bad * C::NH * 8; i += 32) {
+                            const int row = valid_keys + i / (C::NH * 8);
+                            const int half = (i / 8) % C::NH;
+                            const int ch = i % 8;
+                            const uint32_t a = vb + half * C::BOX + row * 128 + ch * 16;
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
                     }
-                    fence_proxy_async_smem();
+                    // O += P V
+#pragma unroll
+                    for (int np = 0; np < D / 16; ++np) {
+                        const int mi = lane >> 3;
+                        const int key = (mi & 1) * 8 + (lane & 7);
+                        const int chunk = 2 * np + (mi >> 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldmatrix_x4_trans(sw128(vb + (chunk / 8) * C::BOX, key, chunk % 8), b0, b1, b2, b3);
+                        mma_bf16_16816(o[2 * np], pa, b0, b1);
+                        mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty(s));
+                } else {
+                    // this head's value rows, E4M3 -> f16 into the warp's staging
+                    // rows ([16][64] halves, same swizzle as a bf16 box); rows
+                    // past the context become 0 (their codes may be NaN)
+                    const uint32_t stg = staging + warp * (16 * D * 2);
+#pragma unroll
+                    for (int i = 0; i < (16 * D / 16) / 32; ++i) {
+                        const int ci = lane + 32 * i;
+                        const int row = ci / (D / 16);
+                        const int c = ci % (D / 16);          // 16 codes: d = 16c .. 16c+15
+                        uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                        if (row < valid_keys) {
+                            const uint4 x = lds_v4(sw128(vb, row, c));
+                            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                w[2 * q] = e4m3x2_to_f16x2(xs[q] & 0xFFFFu);
+                                w[2 * q + 1] = e4m3x2_to_f16x2(xs[q] >> 16);
+                            }
+                        }
+                        const uint32_t hb = stg + (c >> 2) * C::BOX;
+                        sts_v4(sw128(hb, row, (c & 3) * 2), w[0], w[1], w[2], w[3]);
+                        sts_v4(sw128(hb, row, (c & 3) * 2 + 1), w[4], w[5], w[6], w[7]);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(empty(s));   // the E4M3 block is no longer read
+                    // O += P V (f16)
+#pragma unroll
+                    for (int np = 0; np < D / 16; ++np) {
+                        const int mi = lane >> 3;
+                        const int key = (mi & 1) * 8 + (lane & 7);
+                        const int chunk = 2 * np + (mi >> 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldmatrix_x4_trans(sw128(stg + (chunk / 8) * C::BOX, key, chunk % 8), b0, b1, b2, b3);
+                        mma_f16_16816(o[2 * np], pa, b0, b1);
+                        mma_f16_16816(o[2 * np + 1], pa, b2, b3);
+                    }
                     __syncwarp();
                 }
-                // O += P V
-#pragma unroll
-                for (int np = 0; np < D / 16; ++np) {
-                    const int mi = lane >> 3;
-                    const int key = (mi & 1) * 8 + (lane & 7);
-                    const int chunk = 2 * np + (mi >> 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4_trans(sw128(vb + (chunk / 8) * C::BOX, key, chunk % 8), b0, b1, b2, b3);
-                    mma_bf16_16816(o[2 * np], pa, b0, b1);
-                    mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty(s));
             }
             if (!ok) break;
             // ------------------------------------------------ finalize --
@@ -250,8 +335,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
             l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
             l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-            const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
-            const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+            const float inv0 = l0 > 0.f ? p.out_scale / l0 : 0.f;
+            const float inv1 = l1 > 0.f ? p.out_scale / l1 : 0.f;
             const int h_row0 = kvh * G + g, h_row1 = kvh * G + g + 8;
             if (item.part < 0) {
                 uint16_t *orow = p.out + static_cast<int64_t>(item.token) * p.num_heads_q * D;
@@ -284,31 +369,32 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     __syncthreads();
 }
 
-template <int D, int HG>
+template <int D, int HG, bool KV8>
 cudaError_t launch_t(int num_ctas, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                      const DecodeParams &p, cudaStream_t stream) {
-    using C = DecodeCfg<D, HG>;
+    using C = DecodeCfg<D, HG, KV8>;
     static bool configured = false;  // attribute is per function, set once per process
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, HG>,
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, HG, KV8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    decode_kernel<D, HG><<<num_ctas, C::THREADS, C::SMEM, stream>>>(tm_k, tm_v, p);
+    decode_kernel<D, HG, KV8><<<num_ctas, C::THREADS, C::SMEM, stream>>>(tm_k, tm_v, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-#define PA_DECODE_CASES(X) \
-    X(64, 1) X(64, 2) X(64, 4) X(64, 8) X(128, 1) X(128, 2) X(128, 4) X(128, 8)
+#define PA_DECODE_CASES(X)                                                                                  \
+    X(64, 1, false) X(64, 2, false) X(64, 4, false) X(64, 8, false) X(128, 1, false) X(128, 2, false)      \
+    X(128, 4, false) X(128, 8, false) X(128, 1, true) X(128, 2, true) X(128, 4, true) X(128, 8, true)
 
-cudaError_t launch_decode(int head_dim, int hg, int num_ctas, const CUtensorMap &tm_k,
+cudaError_t launch_decode(int head_dim, int hg, bool kv8, int num_ctas, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const DecodeParams &p, cudaStream_t stream) {
     if (num_ctas <= 0) return cudaSuccess;
-#define X(d, h) \
-    if (head_dim == d && hg == h) return launch_t<d, h>(num_ctas, tm_k, tm_v, p, stream);
+#define X(d, h, f) \
+    if (head_dim == d && hg == h && kv8 == f) return launch_t<d, h, f>(num_ctas, tm_k, tm_v, p, stream);
     PA_DECODE_CASES(X)
 #undef X
     return cudaErrorInvalidValue;

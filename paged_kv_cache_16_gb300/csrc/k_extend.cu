@@ -377,7 +377,7 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // ----------------------------------------------------- epilogue --
         if (ok && n_mine > 0 && warp_wait(bar(B_ODONE + t), 0, &abort_flag)) {
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = l > 0.f ? p.out_scale / l : 0.f;
             const int tok = tile.t0 + i;
             const int h = tile.kv_head * G + gq;
             int64_t slot = -1;

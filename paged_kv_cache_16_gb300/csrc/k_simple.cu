@@ -50,6 +50,81 @@ __global__ void write_kv_kernel(const uint4 *__restrict__ key, const uint4 *__re
     }
 }
 
+// reshape_and_cache into E4M3 caches ("vLLM 推理流程分析" §6.3, FP8 conversion
+// with k_scale / v_scale): one thread turns 16 bf16 elements of a token's key
+// row (and of its value row) into 16 codes, code = E4M3(bf16 / scale) with the
+// quotient rounded once in IEEE binary32.
+__device__ __forceinline__ uint4 quantize16(uint4 a, uint4 b, float scale) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint16_t lo = dev::pack_e4m3x2(__fdiv_rn(dev::bf16_lo(w[2 * i]), scale),
+                                             __fdiv_rn(dev::bf16_hi(w[2 * i]), scale));
+        const uint16_t hi = dev::pack_e4m3x2(__fdiv_rn(dev::bf16_lo(w[2 * i + 1]), scale),
+                                             __fdiv_rn(dev::bf16_hi(w[2 * i + 1]), scale));
+        o[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__global__ void write_kv_fp8_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
+                                    const int64_t *__restrict__ slots, int64_t total_chunks,
+                                    int32_t chunks_per_row, uint4 *__restrict__ key_cache,
+                                    uint4 *__restrict__ value_cache, int64_t num_slots, float k_scale,
+                                    float v_scale, int32_t *err) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_chunks; i += stride) {
+        const int64_t t = i / chunks_per_row;
+        const int32_t c = static_cast<int32_t>(i - t * chunks_per_row);
+        const int64_t slot = __ldg(slots + t);
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            if (err != nullptr && c == 0) atomicOr(err, kErrSlotRange);
+            continue;
+        }
+        key_cache[slot * chunks_per_row + c] = quantize16(__ldcs(key + 2 * i), __ldcs(key + 2 * i + 1), k_scale);
+        value_cache[slot * chunks_per_row + c] =
+            quantize16(__ldcs(value + 2 * i), __ldcs(value + 2 * i + 1), v_scale);
+    }
+}
+
+// E4M3 cache blocks read by the tensor-core tiles, expanded to bf16 scratch
+// blocks: the code values themselves (exact in bf16; the scales are applied
+// by the attention kernels).  One CTA per block.
+__device__ __forceinline__ void expand16(const uint4 codes, uint4 *dst) {
+    const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t h0 = dev::e4m3x2_to_f16x2(w[i] & 0xFFFFu);
+        const uint32_t h1 = dev::e4m3x2_to_f16x2(w[i] >> 16);
+        o[2 * i] = dev::pack_bf16x2(dev::f16_lo(h0), dev::f16_hi(h0));
+        o[2 * i + 1] = dev::pack_bf16x2(dev::f16_lo(h1), dev::f16_hi(h1));
+    }
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+__global__ void dequant_kernel(DequantParams p) {
+    const DequantItem it = p.items[blockIdx.x];
+    const int32_t src = p.block_table[static_cast<int64_t>(it.req) * p.max_blocks + it.block];
+    const int32_t chunks = p.block_elems / 16;
+    uint4 *kd = reinterpret_cast<uint4 *>(p.key_out + static_cast<int64_t>(it.dst) * p.block_elems);
+    uint4 *vd = reinterpret_cast<uint4 *>(p.value_out + static_cast<int64_t>(it.dst) * p.block_elems);
+    if (src < 0 || src >= p.num_blocks) {
+        if (threadIdx.x == 0) atomicOr(p.err, kErrBlockRange);
+        for (int32_t c = threadIdx.x; c < 2 * chunks; c += blockDim.x) kd[c] = vd[c] = make_uint4(0, 0, 0, 0);
+        return;
+    }
+    const uint4 *ks = reinterpret_cast<const uint4 *>(p.key_cache + static_cast<int64_t>(src) * p.block_elems);
+    const uint4 *vs = reinterpret_cast<const uint4 *>(p.value_cache + static_cast<int64_t>(src) * p.block_elems);
+    for (int32_t c = threadIdx.x; c < chunks; c += blockDim.x) {
+        expand16(__ldg(ks + c), kd + 2 * c);
+        expand16(__ldg(vs + c), vd + 2 * c);
+    }
+}
+
 // Merge of partition partials (page "vLLM 源码完全拆解（十六）", third
 // walk-through: per-partition (m_r, l_r, o_r) combined with exponential
 // rescaling).  One warp per (token, query head); m is in log2 units.
@@ -93,6 +168,27 @@ cudaError_t launch_write_kv(const void *key, const void *value, const int64_t *s
         static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), slots, total,
         chunks_per_row, static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache),
         num_slots, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_write_kv_fp8(const void *key, const void *value, const int64_t *slots, int32_t num_tokens,
+                                int32_t row_elems, void *key_cache, void *value_cache, int64_t num_slots,
+                                float k_scale, float v_scale, int32_t *err, cudaStream_t stream) {
+    if (num_tokens <= 0) return cudaSuccess;
+    const int32_t chunks_per_row = row_elems / 16;        // 16 codes per output chunk
+    const int64_t total = static_cast<int64_t>(num_tokens) * chunks_per_row;
+    const int threads = 256;
+    int64_t blocks = (total + threads - 1) / threads;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    write_kv_fp8_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+        static_cast<const uint4 *>(key), static_cast<const uint4 *>(value), slots, total, chunks_per_row,
+        static_cast<uint4 *>(key_cache), static_cast<uint4 *>(value_cache), num_slots, k_scale, v_scale, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const DequantParams &p, cudaStream_t stream) {
+    if (p.num_items <= 0) return cudaSuccess;
+    dequant_kernel<<<p.num_items, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

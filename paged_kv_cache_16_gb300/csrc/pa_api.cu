@@ -47,6 +47,20 @@ bool make_map(CUtensorMap *tm, const void *ptr, uint64_t d, uint64_t mid, uint64
     return r == CUDA_SUCCESS;
 }
 
+bool make_map_u8(CUtensorMap *tm, const void *ptr, uint64_t d, uint64_t mid, uint64_t outer, uint32_t box_mid,
+                 uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {d, mid, outer};
+    cuuint64_t strides[2] = {d, mid * d};
+    cuuint32_t box[3] = {128, box_mid, box_outer};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace pa
 
 namespace {
@@ -164,8 +178,13 @@ pa_status validate(const pa_batch_desc *d) {
             }
         }
     }
+    if (d->kv_cache_dtype != PA_KV_BF16 && d->kv_cache_dtype != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARGUMENT;
+    if (d->kv_cache_dtype == PA_KV_FP8_E4M3 &&
+        (!(d->k_scale > 0.f) || !std::isfinite(d->k_scale) || !(d->v_scale > 0.f) || !std::isfinite(d->v_scale)))
+        return PA_ERR_INVALID_ARGUMENT;
     // supported shapes
     if (d->block_size != kBlockSize) return PA_ERR_UNSUPPORTED;
+    if (d->kv_cache_dtype == PA_KV_FP8_E4M3 && d->head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (d->head_dim != 64 && d->head_dim != 128) return PA_ERR_UNSUPPORTED;
     const int G = d->num_heads_q / d->num_heads_kv;
     if (!is_pow2(G) || G > 16) return PA_ERR_UNSUPPORTED;
@@ -190,7 +209,7 @@ void plan_decode(pa_plan_s *P, const pa_batch_desc *d, const std::vector<int32_t
     pieces.assign(static_cast<size_t>(d->num_reqs) * P->n_groups, 0);
     P->cta_begin.assign(1, 0);
     if (total == 0) return;
-    const int cps = std::max(1, decode_ctas_per_sm_static(P->D, P->HG));
+    const int cps = std::max(1, decode_ctas_per_sm_static(P->D, P->HG, P->kv8));
     const int64_t min_pages = 4;
     int64_t ncta = std::min<int64_t>(static_cast<int64_t>(P->num_sms) * cps, (total + min_pages - 1) / min_pages);
     ncta = std::max<int64_t>(ncta, 1);
@@ -232,7 +251,9 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d) {
     P->G = P->Hq / P->Hkv;
     P->HG = heads_per_group(P->Hkv);
     P->n_groups = P->Hkv / P->HG;
-    P->scale_log2 = d->softmax_scale * 1.4426950408889634f;
+    P->kv8 = d->kv_cache_dtype == PA_KV_FP8_E4M3;
+    P->scale_log2 = d->softmax_scale * (P->kv8 ? d->k_scale : 1.f) * 1.4426950408889634f;
+    P->out_scale = P->kv8 ? d->v_scale : 1.f;
     P->num_sms = d->num_sms;
     if (P->num_sms == 0) {
         int dev = 0;
@@ -303,6 +324,34 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d) {
         return (a.key_end - a.key_begin) > (b.key_end - b.key_begin);
     });
 
+    // E4M3 caches: the tiles read bf16 copies of the blocks they touch, one
+    // scratch block-table row per request the tiles read through
+    if (P->kv8 && !P->tiles.empty()) {
+        std::vector<int32_t> row_of(static_cast<size_t>(P->R), -1), lo, hi, reqs;
+        for (const ExtendTile &t : P->tiles) {
+            int32_t &row = row_of[t.req];
+            if (row < 0) {
+                row = static_cast<int32_t>(reqs.size());
+                reqs.push_back(t.req);
+                lo.push_back(INT32_MAX);
+                hi.push_back(0);
+            }
+            lo[row] = std::min(lo[row], t.key_begin / kBlockSize);
+            hi[row] = std::max(hi[row], (t.key_end + kBlockSize - 1) / kBlockSize);
+        }
+        P->scratch_table.assign(reqs.size() * static_cast<size_t>(P->max_blocks), 0);
+        for (size_t row = 0; row < reqs.size(); ++row)
+            for (int32_t b = lo[row]; b < hi[row]; ++b) {
+                DequantItem di{};
+                di.req = reqs[row];
+                di.block = b;
+                di.dst = P->num_scratch_blocks++;
+                P->scratch_table[row * P->max_blocks + b] = di.dst;
+                P->dequant.push_back(di);
+            }
+        for (ExtendTile &t : P->tiles) t.req = row_of[t.req];
+    }
+
     // ------------------------------------------------------------- decode
     std::vector<int32_t> pieces;
     plan_decode(P, d, decode_rows, pieces);
@@ -351,12 +400,19 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d) {
     P->off_items = place(P->items.size() * sizeof(DecodeItem));
     P->off_tiles = place(P->tiles.size() * sizeof(ExtendTile));
     P->off_merges = place(P->merges.size() * sizeof(MergeRow));
+    P->off_scrtab = place(P->scratch_table.size() * sizeof(int32_t));
+    P->off_dequant = place(P->dequant.size() * sizeof(DequantItem));
     P->blob_bytes = off - kHeader;
     off = align_up(off, 256);
     P->off_opart = off;
     off = align_up(off + static_cast<size_t>(P->num_slots) * P->Hq * P->D * sizeof(float), 256);
     P->off_ml = off;
-    off = align_up(off + static_cast<size_t>(P->num_slots) * P->Hq * sizeof(float2), 256);
+    off = align_up(off + static_cast<size_t>(P->num_slots) * P->Hq * sizeof(float2), 1024);
+    const size_t scratch_bytes = static_cast<size_t>(P->num_scratch_blocks) * kBlockSize * P->Hkv * P->D * 2;
+    P->off_kscr = off;
+    off = align_up(off + scratch_bytes, 1024);
+    P->off_vscr = off;
+    off = align_up(off + scratch_bytes, 256);
     P->ws_bytes = off;
     P->blob.assign(P->blob_bytes, 0);
     auto put = [&](size_t at, const void *src, size_t n) {
@@ -367,6 +423,8 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d) {
     put(P->off_items, P->items.data(), P->items.size() * sizeof(DecodeItem));
     put(P->off_tiles, P->tiles.data(), P->tiles.size() * sizeof(ExtendTile));
     put(P->off_merges, P->merges.data(), P->merges.size() * sizeof(MergeRow));
+    put(P->off_scrtab, P->scratch_table.data(), P->scratch_table.size() * sizeof(int32_t));
+    put(P->off_dequant, P->dequant.data(), P->dequant.size() * sizeof(DequantItem));
 
     // ------------------------------------------------------------- info
     pa_plan_info &I = P->info;
@@ -378,8 +436,10 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d) {
     I.num_extend_tiles = static_cast<int32_t>(P->tiles.size());
     I.num_partial_slots = P->num_slots;
     I.num_merge_rows = static_cast<int32_t>(P->merges.size());
-    I.kernels_per_call = (P->items.empty() ? 0 : 1) + (P->tiles.empty() ? 0 : 1) + (P->merges.empty() ? 0 : 1);
-    const int64_t row_bytes = static_cast<int64_t>(P->Hkv) * P->D * 2 * 2;   // K and V, bf16
+    I.kernels_per_call = (P->items.empty() ? 0 : 1) + (P->tiles.empty() ? 0 : 1) + (P->merges.empty() ? 0 : 1) +
+                         (P->dequant.empty() ? 0 : 1);
+    I.num_dequant_blocks = P->num_scratch_blocks;
+    const int64_t row_bytes = static_cast<int64_t>(P->Hkv) * P->D * 2 * (P->kv8 ? 1 : 2);   // K and V
     for (int32_t r : decode_rows) I.decode_kv_bytes += (d->seq_lens[r] - kb_keys) * row_bytes;
     I.prefix_kv_bytes = cascade ? kb_keys * row_bytes : 0;
     double pairs = 0.0;
@@ -413,6 +473,115 @@ void clear_timing(pa_plan_s *P) {
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
+
+namespace pa {
+
+pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, const void *value_cache,
+                            const int32_t *block_table, void *out, uint8_t *ws, cudaStream_t stream, bool timed) {
+    auto rec = [&](int kind, bool start, cudaStream_t st) { return timed ? record(P, kind, start, st) : cudaSuccess; };
+    int32_t *err = reinterpret_cast<int32_t *>(ws);
+    const int32_t *part_offset = reinterpret_cast<const int32_t *>(ws + P->off_part);
+    float *o_part = reinterpret_cast<float *>(ws + P->off_opart);
+    float2 *ml_part = reinterpret_cast<float2 *>(ws + P->off_ml);
+    uint16_t *out16 = static_cast<uint16_t *>(out);
+
+    CUtensorMap tm_k, tm_v;
+    const uint64_t rows = static_cast<uint64_t>(P->num_blocks) * kBlockSize;
+    if (P->kv8 ? (!make_map_u8(&tm_k, key_cache, P->D, P->Hkv, rows, 1, kBlockSize) ||
+                  !make_map_u8(&tm_v, value_cache, P->D, P->Hkv, rows, 1, kBlockSize))
+               : (!make_map(&tm_k, key_cache, P->D, P->Hkv, rows, 1, kBlockSize) ||
+                  !make_map(&tm_v, value_cache, P->D, P->Hkv, rows, 1, kBlockSize)))
+        return PA_ERR_CUDA;
+
+    if (!P->tiles.empty()) {
+        // E4M3: the tiles read bf16 copies of their blocks, made here
+        CUtensorMap tm_tk = tm_k, tm_tv = tm_v;
+        const int32_t *tile_table = block_table;
+        int32_t tile_blocks = P->num_blocks;
+        if (P->kv8) {
+            DequantParams qp{};
+            qp.key_cache = static_cast<const uint8_t *>(key_cache);
+            qp.value_cache = static_cast<const uint8_t *>(value_cache);
+            qp.key_out = reinterpret_cast<uint16_t *>(ws + P->off_kscr);
+            qp.value_out = reinterpret_cast<uint16_t *>(ws + P->off_vscr);
+            qp.block_table = block_table;
+            qp.items = reinterpret_cast<const DequantItem *>(ws + P->off_dequant);
+            qp.err = err;
+            qp.num_items = static_cast<int32_t>(P->dequant.size());
+            qp.max_blocks = P->max_blocks;
+            qp.num_blocks = P->num_blocks;
+            qp.block_elems = kBlockSize * P->Hkv * P->D;
+            if (launch_dequant(qp, stream) != cudaSuccess) return PA_ERR_CUDA;
+            const uint64_t srows = static_cast<uint64_t>(P->num_scratch_blocks) * kBlockSize;
+            if (!make_map(&tm_tk, ws + P->off_kscr, P->D, P->Hkv, srows, 1, kBlockSize) ||
+                !make_map(&tm_tv, ws + P->off_vscr, P->D, P->Hkv, srows, 1, kBlockSize))
+                return PA_ERR_CUDA;
+            tile_table = reinterpret_cast<const int32_t *>(ws + P->off_scrtab);
+            tile_blocks = P->num_scratch_blocks;
+        }
+        CUtensorMap tm_q;
+        if (!make_map(&tm_q, q, P->D, P->Hq, P->T, P->G, kTileRows / P->G)) return PA_ERR_CUDA;
+        ExtendParams ep{};
+        ep.out = out16;
+        ep.block_table = tile_table;
+        ep.tiles = reinterpret_cast<const ExtendTile *>(ws + P->off_tiles);
+        ep.part_offset = part_offset;
+        ep.o_part = o_part;
+        ep.ml_part = ml_part;
+        ep.err = err;
+        ep.num_tiles = static_cast<int32_t>(P->tiles.size());
+        ep.max_blocks = P->max_blocks;
+        ep.num_blocks = tile_blocks;
+        ep.num_heads_q = P->Hq;
+        ep.group = P->G;
+        ep.n_groups = P->n_groups;
+        ep.heads_per_group = P->HG;
+        ep.scale_log2 = P->scale_log2;
+        ep.out_scale = P->out_scale;
+        if (rec(1, true, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_extend(P->D, tm_q, tm_tk, tm_tv, ep, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (rec(1, false, stream) != cudaSuccess) return PA_ERR_CUDA;
+    }
+    if (!P->items.empty()) {
+        DecodeParams dp{};
+        dp.q = static_cast<const uint16_t *>(q);
+        dp.out = out16;
+        dp.block_table = block_table;
+        dp.items = reinterpret_cast<const DecodeItem *>(ws + P->off_items);
+        dp.cta_begin = reinterpret_cast<const int32_t *>(ws + P->off_cta);
+        dp.part_offset = part_offset;
+        dp.o_part = o_part;
+        dp.ml_part = ml_part;
+        dp.err = err;
+        dp.max_blocks = P->max_blocks;
+        dp.num_blocks = P->num_blocks;
+        dp.num_heads_q = P->Hq;
+        dp.group = P->G;
+        dp.n_groups = P->n_groups;
+        dp.scale_log2 = P->scale_log2;
+        dp.out_scale = P->out_scale;
+        const int ncta = static_cast<int>(P->cta_begin.size()) - 1;
+        if (rec(0, true, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_decode(P->D, P->HG, P->kv8, ncta, tm_k, tm_v, dp, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (rec(0, false, stream) != cudaSuccess) return PA_ERR_CUDA;
+    }
+    if (!P->merges.empty()) {
+        MergeParams mp{};
+        mp.out = out16;
+        mp.rows = reinterpret_cast<const MergeRow *>(ws + P->off_merges);
+        mp.o_part = o_part;
+        mp.ml_part = ml_part;
+        mp.num_rows = static_cast<int32_t>(P->merges.size());
+        mp.num_heads_q = P->Hq;
+        mp.max_heads = P->HG * P->G;
+        if (rec(2, true, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_merge(P->D, mp, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (rec(2, false, stream) != cudaSuccess) return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+}  // namespace pa
 
 extern "C" {
 
@@ -485,6 +654,24 @@ pa_status pa_write_kv(const void *key, const void *value, const int64_t *slot_ma
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+pa_status pa_write_kv_fp8(const void *key, const void *value, const int64_t *slot_mapping, int32_t num_tokens,
+                          int32_t num_heads_kv, int32_t head_dim, void *key_cache, void *value_cache,
+                          int64_t num_slots, float k_scale, float v_scale, int32_t *device_error_word,
+                          void *stream) {
+    if (num_tokens < 0 || num_heads_kv <= 0 || head_dim <= 0 || num_slots < 0) return PA_ERR_INVALID_ARGUMENT;
+    if (!(k_scale > 0.f) || !std::isfinite(k_scale) || !(v_scale > 0.f) || !std::isfinite(v_scale))
+        return PA_ERR_INVALID_ARGUMENT;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !slot_mapping || !key_cache || !value_cache) return PA_ERR_INVALID_ARGUMENT;
+    if ((static_cast<int64_t>(num_heads_kv) * head_dim) % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16))
+        return PA_ERR_INVALID_ARGUMENT;
+    cudaError_t e = launch_write_kv_fp8(key, value, slot_mapping, num_tokens, num_heads_kv * head_dim, key_cache,
+                                        value_cache, num_slots, k_scale, v_scale, device_error_word,
+                                        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 pa_status pa_attention(const pa_plan_t *plan, const void *q, const void *key_cache, const void *value_cache,
                        const int32_t *block_table, void *out, void *workspace, size_t workspace_bytes,
                        void *stream_) {
@@ -512,77 +699,7 @@ pa_status pa_attention(const pa_plan_t *plan, const void *q, const void *key_cac
         if (record(P, 3, false, stream) != cudaSuccess) return PA_ERR_CUDA;
         if (cudaEventRecord(P->upload_evt, stream) != cudaSuccess) return PA_ERR_CUDA;
     }
-    int32_t *err = reinterpret_cast<int32_t *>(ws);
-    const int32_t *part_offset = reinterpret_cast<const int32_t *>(ws + P->off_part);
-    float *o_part = reinterpret_cast<float *>(ws + P->off_opart);
-    float2 *ml_part = reinterpret_cast<float2 *>(ws + P->off_ml);
-    uint16_t *out16 = static_cast<uint16_t *>(out);
-
-    CUtensorMap tm_k, tm_v;
-    const uint64_t rows = static_cast<uint64_t>(P->num_blocks) * kBlockSize;
-    if (!make_map(&tm_k, key_cache, P->D, P->Hkv, rows, 1, kBlockSize) ||
-        !make_map(&tm_v, value_cache, P->D, P->Hkv, rows, 1, kBlockSize))
-        return PA_ERR_CUDA;
-
-    if (!P->tiles.empty()) {
-        CUtensorMap tm_q;
-        if (!make_map(&tm_q, q, P->D, P->Hq, P->T, P->G, kTileRows / P->G)) return PA_ERR_CUDA;
-        ExtendParams ep{};
-        ep.out = out16;
-        ep.block_table = block_table;
-        ep.tiles = reinterpret_cast<const ExtendTile *>(ws + P->off_tiles);
-        ep.part_offset = part_offset;
-        ep.o_part = o_part;
-        ep.ml_part = ml_part;
-        ep.err = err;
-        ep.num_tiles = static_cast<int32_t>(P->tiles.size());
-        ep.max_blocks = P->max_blocks;
-        ep.num_blocks = P->num_blocks;
-        ep.num_heads_q = P->Hq;
-        ep.group = P->G;
-        ep.n_groups = P->n_groups;
-        ep.heads_per_group = P->HG;
-        ep.scale_log2 = P->scale_log2;
-        if (record(P, 1, true, stream) != cudaSuccess) return PA_ERR_CUDA;
-        if (launch_extend(P->D, tm_q, tm_k, tm_v, ep, stream) != cudaSuccess) return PA_ERR_CUDA;
-        if (record(P, 1, false, stream) != cudaSuccess) return PA_ERR_CUDA;
-    }
-    if (!P->items.empty()) {
-        DecodeParams dp{};
-        dp.q = static_cast<const uint16_t *>(q);
-        dp.out = out16;
-        dp.block_table = block_table;
-        dp.items = reinterpret_cast<const DecodeItem *>(ws + P->off_items);
-        dp.cta_begin = reinterpret_cast<const int32_t *>(ws + P->off_cta);
-        dp.part_offset = part_offset;
-        dp.o_part = o_part;
-        dp.ml_part = ml_part;
-        dp.err = err;
-        dp.max_blocks = P->max_blocks;
-        dp.num_blocks = P->num_blocks;
-        dp.num_heads_q = P->Hq;
-        dp.group = P->G;
-        dp.n_groups = P->n_groups;
-        dp.scale_log2 = P->scale_log2;
-        const int ncta = static_cast<int>(P->cta_begin.size()) - 1;
-        if (record(P, 0, true, stream) != cudaSuccess) return PA_ERR_CUDA;
-        if (launch_decode(P->D, P->HG, ncta, tm_k, tm_v, dp, stream) != cudaSuccess) return PA_ERR_CUDA;
-        if (record(P, 0, false, stream) != cudaSuccess) return PA_ERR_CUDA;
-    }
-    if (!P->merges.empty()) {
-        MergeParams mp{};
-        mp.out = out16;
-        mp.rows = reinterpret_cast<const MergeRow *>(ws + P->off_merges);
-        mp.o_part = o_part;
-        mp.ml_part = ml_part;
-        mp.num_rows = static_cast<int32_t>(P->merges.size());
-        mp.num_heads_q = P->Hq;
-        mp.max_heads = P->HG * P->G;
-        if (record(P, 2, true, stream) != cudaSuccess) return PA_ERR_CUDA;
-        if (launch_merge(P->D, mp, stream) != cudaSuccess) return PA_ERR_CUDA;
-        if (record(P, 2, false, stream) != cudaSuccess) return PA_ERR_CUDA;
-    }
-    return PA_OK;
+    return enqueue_attention(P, q, key_cache, value_cache, block_table, out, ws, stream, true);
 }
 
 pa_status pa_check_device_errors(int32_t *word, int32_t *bits, void *stream_) {

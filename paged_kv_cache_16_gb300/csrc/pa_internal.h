@@ -16,21 +16,27 @@ constexpr int kTileRows = 128;     // query rows per tensor-core sub-tile (two p
 constexpr int kMaxDecodeHeads = 8; // kv heads one decode CTA serves
 
 // Split-KV decode kernel resources, shared by the planner (which sizes the
-// persistent grid without touching a device) and the kernel.
-constexpr int decode_stage_bytes(int d, int hg) { return 2 * hg * (d / 64) * 16 * 128; }
-constexpr int decode_stages(int d, int hg) {
-    return decode_stage_bytes(d, hg) * 4 <= 200 * 1024   ? 4
-           : decode_stage_bytes(d, hg) * 3 <= 200 * 1024 ? 3
-                                                          : 2;
+// persistent grid without touching a device) and the kernel.  kv8: E4M3
+// caches (one byte per element, plus a per-warp f16 staging buffer of V).
+constexpr int decode_stage_bytes(int d, int hg, bool kv8) { return 2 * hg * 16 * d * (kv8 ? 1 : 2); }
+constexpr int decode_staging_bytes(int d, int hg, bool kv8) { return kv8 ? hg * 16 * d * 2 : 0; }
+constexpr int decode_stages(int d, int hg, bool kv8) {
+    return kv8 ? ((200 * 1024 - decode_staging_bytes(d, hg, kv8)) / decode_stage_bytes(d, hg, kv8) > 6
+                      ? 6
+                      : (200 * 1024 - decode_staging_bytes(d, hg, kv8)) / decode_stage_bytes(d, hg, kv8))
+               : (decode_stage_bytes(d, hg, kv8) * 4 <= 200 * 1024   ? 4
+                  : decode_stage_bytes(d, hg, kv8) * 3 <= 200 * 1024 ? 3
+                                                                       : 2);
 }
 constexpr int decode_threads(int hg) { return (hg + 1) * 32; }
-constexpr int decode_smem_bytes(int d, int hg) {
-    return decode_stages(d, hg) * decode_stage_bytes(d, hg) + 3 * decode_stages(d, hg) * 8 + 1024;
+constexpr int decode_smem_bytes(int d, int hg, bool kv8) {
+    return decode_stages(d, hg, kv8) * decode_stage_bytes(d, hg, kv8) + decode_staging_bytes(d, hg, kv8) +
+           3 * decode_stages(d, hg, kv8) * 8 + 1024;
 }
 constexpr int kSmemPerSm = 233472;  // 228 KiB of shared memory per SM
-constexpr int decode_ctas_per_sm_static(int d, int hg) {
-    return (kSmemPerSm / (decode_smem_bytes(d, hg) + 1024)) < (2048 / decode_threads(hg))
-               ? (kSmemPerSm / (decode_smem_bytes(d, hg) + 1024))
+constexpr int decode_ctas_per_sm_static(int d, int hg, bool kv8) {
+    return (kSmemPerSm / (decode_smem_bytes(d, hg, kv8) + 1024)) < (2048 / decode_threads(hg))
+               ? (kSmemPerSm / (decode_smem_bytes(d, hg, kv8) + 1024))
                : (2048 / decode_threads(hg));
 }
 
@@ -100,7 +106,8 @@ struct DecodeParams {
     int32_t num_heads_q;
     int32_t group;              // G = Hq / Hkv
     int32_t n_groups;           // kv-head groups (Hkv / heads per group)
-    float scale_log2;           // softmax_scale * log2(e)
+    float scale_log2;           // softmax_scale * k_scale * log2(e)
+    float out_scale;            // v_scale (1 for bf16 caches)
 };
 
 struct ExtendParams {
@@ -118,7 +125,30 @@ struct ExtendParams {
     int32_t group;
     int32_t n_groups;
     int32_t heads_per_group;    // kv heads per head group (indexes part_offset)
-    float scale_log2;
+    float scale_log2;           // softmax_scale * k_scale * log2(e)
+    float out_scale;            // v_scale (1 for bf16 caches)
+};
+
+// FP8 caches: one cache block the tensor-core tiles read, expanded to bf16.
+struct DequantItem {
+    int32_t req;                // block-table row of the source block
+    int32_t block;              // logical block index in that row
+    int32_t dst;                // block index in the bf16 scratch caches
+    int32_t pad;
+};
+
+struct DequantParams {
+    const uint8_t *key_cache;   // E4M3 caches
+    const uint8_t *value_cache;
+    uint16_t *key_out;          // bf16 scratch caches [n_dst][16][Hkv][D]
+    uint16_t *value_out;
+    const int32_t *block_table;
+    const DequantItem *items;
+    int32_t *err;
+    int32_t num_items;
+    int32_t max_blocks;
+    int32_t num_blocks;
+    int32_t block_elems;        // 16 * Hkv * D
 };
 
 struct MergeParams {
@@ -140,9 +170,13 @@ cudaError_t launch_write_kv(const void *key, const void *value, const int64_t *s
                             int32_t num_tokens, int32_t row_elems, void *key_cache,
                             void *value_cache, int64_t num_slots, int32_t *err,
                             cudaStream_t stream);
-// Decode kernel: head_dim D, heads per CTA hg.  Returns cudaErrorInvalidValue
-// for an unsupported (D, hg).
-cudaError_t launch_decode(int head_dim, int hg, int num_ctas, const CUtensorMap &tm_k,
+cudaError_t launch_write_kv_fp8(const void *key, const void *value, const int64_t *slots, int32_t num_tokens,
+                                int32_t row_elems, void *key_cache, void *value_cache, int64_t num_slots,
+                                float k_scale, float v_scale, int32_t *err, cudaStream_t stream);
+cudaError_t launch_dequant(const DequantParams &p, cudaStream_t stream);
+// Decode kernel: head_dim D, heads per CTA hg, E4M3 caches (kv8).  Returns
+// cudaErrorInvalidValue for an unsupported combination.
+cudaError_t launch_decode(int head_dim, int hg, bool kv8, int num_ctas, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_extend(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const ExtendParams &p, cudaStream_t stream);

@@ -76,69 +76,9 @@ extern "C" pa_status pa_attention_no_alloc(const pa_plan_t *plan, const void *q,
             cudaSuccess)
         return PA_ERR_CUDA;
 
-    int32_t *err = reinterpret_cast<int32_t *>(ws);
-    const int32_t *part_offset = reinterpret_cast<const int32_t *>(ws + P->off_part);
-    float *o_part = reinterpret_cast<float *>(ws + P->off_opart);
-    float2 *ml_part = reinterpret_cast<float2 *>(ws + P->off_ml);
-    uint16_t *out16 = static_cast<uint16_t *>(out);
-
-    CUtensorMap tm_k, tm_v;
-    const uint64_t rows = static_cast<uint64_t>(P->num_blocks) * kBlockSize;
-    if (!make_map(&tm_k, key_cache, P->D, P->Hkv, rows, 1, kBlockSize) ||
-        !make_map(&tm_v, value_cache, P->D, P->Hkv, rows, 1, kBlockSize))
-        return PA_ERR_CUDA;
-    if (!P->tiles.empty()) {
-        CUtensorMap tm_q;
-        if (!make_map(&tm_q, q, P->D, P->Hq, P->T, P->G, kTileRows / P->G)) return PA_ERR_CUDA;
-        ExtendParams ep{};
-        ep.out = out16;
-        ep.block_table = block_table;
-        ep.tiles = reinterpret_cast<const ExtendTile *>(ws + P->off_tiles);
-        ep.part_offset = part_offset;
-        ep.o_part = o_part;
-        ep.ml_part = ml_part;
-        ep.err = err;
-        ep.num_tiles = static_cast<int32_t>(P->tiles.size());
-        ep.max_blocks = P->max_blocks;
-        ep.num_blocks = P->num_blocks;
-        ep.num_heads_q = P->Hq;
-        ep.group = P->G;
-        ep.n_groups = P->n_groups;
-        ep.heads_per_group = P->HG;
-        ep.scale_log2 = P->scale_log2;
-        if (launch_extend(P->D, tm_q, tm_k, tm_v, ep, stream) != cudaSuccess) return PA_ERR_CUDA;
-    }
-    if (!P->items.empty()) {
-        DecodeParams dp{};
-        dp.q = static_cast<const uint16_t *>(q);
-        dp.out = out16;
-        dp.block_table = block_table;
-        dp.items = reinterpret_cast<const DecodeItem *>(ws + P->off_items);
-        dp.cta_begin = reinterpret_cast<const int32_t *>(ws + P->off_cta);
-        dp.part_offset = part_offset;
-        dp.o_part = o_part;
-        dp.ml_part = ml_part;
-        dp.err = err;
-        dp.max_blocks = P->max_blocks;
-        dp.num_blocks = P->num_blocks;
-        dp.num_heads_q = P->Hq;
-        dp.group = P->G;
-        dp.n_groups = P->n_groups;
-        dp.scale_log2 = P->scale_log2;
-        const int ncta = static_cast<int>(P->cta_begin.size()) - 1;
-        if (launch_decode(P->D, P->HG, ncta, tm_k, tm_v, dp, stream) != cudaSuccess) return PA_ERR_CUDA;
-    }
-    if (!P->merges.empty()) {
-        MergeParams mp{};
-        mp.out = out16;
-        mp.rows = reinterpret_cast<const MergeRow *>(ws + P->off_merges);
-        mp.o_part = o_part;
-        mp.ml_part = ml_part;
-        mp.num_rows = static_cast<int32_t>(P->merges.size());
-        mp.num_heads_q = P->Hq;
-        mp.max_heads = P->HG * P->G;
-        if (launch_merge(P->D, mp, stream) != cudaSuccess) return PA_ERR_CUDA;
-    }
+    const pa_status es = enqueue_attention(P, q, key_cache, value_cache, block_table, out, ws, stream, false);
+    if (es != PA_OK) return es;
+    const int32_t *err = reinterpret_cast<const int32_t *>(ws);
     if (device_error_word &&
         cudaMemcpyAsync(device_error_word, err, sizeof(int32_t), cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
         return PA_ERR_CUDA;

@@ -14,16 +14,22 @@ struct pa_plan_s {
     int32_t n_prefix = 0;         // num_common_prefix_blocks (cascade when > 0)
     int32_t prefix_req = -1;      // block-table row of the shared prefix
     int32_t prefix_splits = 0;
-    float scale_log2 = 0.f;
+    float scale_log2 = 0.f;     // softmax_scale * k_scale * log2(e)
+    bool kv8 = false;           // E4M3 caches
+    float out_scale = 1.f;      // v_scale for E4M3 caches
     // work lists
     std::vector<int32_t> part_offset;   // [T * n_groups]
     std::vector<int32_t> cta_begin;     // [ncta + 1]
     std::vector<pa::DecodeItem> items;
     std::vector<pa::ExtendTile> tiles;
     std::vector<pa::MergeRow> merges;
+    std::vector<int32_t> scratch_table;       // E4M3: [rows][max_blocks] bf16 scratch block ids
+    std::vector<pa::DequantItem> dequant;     // E4M3: blocks to expand each call
+    int32_t num_scratch_blocks = 0;
     int32_t num_slots = 0;
     // workspace layout
     size_t off_part = 0, off_cta = 0, off_items = 0, off_tiles = 0, off_merges = 0;
+    size_t off_scrtab = 0, off_dequant = 0, off_kscr = 0, off_vscr = 0;
     size_t blob_bytes = 0, off_opart = 0, off_ml = 0, ws_bytes = 0;
     std::vector<uint8_t> blob;          // host image of the metadata blob
     void *pinned = nullptr;             // pinned staging copy used for async uploads
@@ -45,5 +51,14 @@ constexpr size_t kWorkspaceHeader = 256;  // error word + reserved, then the met
 // the encoding is rejected).
 bool make_map(CUtensorMap *tm, const void *ptr, uint64_t d, uint64_t mid, uint64_t outer, uint32_t box_mid,
               uint32_t box_outer);
+// The same over one-byte elements (E4M3 caches): box [box_outer][box_mid][128].
+bool make_map_u8(CUtensorMap *tm, const void *ptr, uint64_t d, uint64_t mid, uint64_t outer, uint32_t box_mid,
+                 uint32_t box_outer);
+
+// Enqueue every kernel of one attention call on `stream`; the metadata blob
+// must already be (or be about to be, in stream order) at ws + header.
+// `timed` records the plan's per-kernel timing events when they are enabled.
+pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, const void *value_cache,
+                            const int32_t *block_table, void *out, uint8_t *ws, cudaStream_t stream, bool timed);
 
 }  // namespace pa

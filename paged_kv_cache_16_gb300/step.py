@@ -37,7 +37,9 @@ class DeviceStep:
                                block_table_host=b.block_table,
                                num_common_prefix_blocks=b.num_common_prefix_blocks,
                                softmax_scale=b.softmax_scale, num_sms=self.num_sms,
-                               block_size=b.block_size)
+                               block_size=b.block_size,
+                               kv_cache_dtype=binding.PA_KV_FP8_E4M3 if b.kv_cache_dtype == "fp8" else binding.PA_KV_BF16,
+                               k_scale=b.k_scale, v_scale=b.v_scale)
 
     @property
     def error_word(self) -> torch.Tensor:
@@ -50,7 +52,11 @@ class DeviceStep:
         return self.slots[:b.num_tokens]
 
     def write(self, key, value, key_cache, value_cache, stream=None):
-        binding.pa_write_kv(key, value, self.slots, key_cache, value_cache, self.error_word, stream)
+        if self.batch.kv_cache_dtype == "fp8":
+            binding.pa_write_kv_fp8(key, value, self.slots, key_cache, value_cache, self.batch.k_scale,
+                                    self.batch.v_scale, self.error_word, stream)
+        else:
+            binding.pa_write_kv(key, value, self.slots, key_cache, value_cache, self.error_word, stream)
 
     def attend(self, q, key_cache, value_cache, stream=None, plan=None):
         binding.pa_attention(plan or self.plan, q, key_cache, value_cache, self.block_table, self.out,

@@ -16,7 +16,10 @@ Recipe (all seeded):
     rounded to bfloat16 (round-to-nearest-even);
   * poison: slots past each request's ``seq_len`` inside its last block, the
     slots the step's new tokens will be written to, and the padding block are
-    overwritten with a large finite value (3.0e4, alternating sign) or NaN.
+    overwritten with a large finite value (3.0e4, alternating sign) or NaN;
+  * FP8 (E4M3) caches: the same N(0, 1) pool divided by the tensor's scale and
+    cast with torch's float8_e4m3fn conversion (clamped to +-448), so the codes
+    spread over the format's range; poison is the code 0x7E (448) or 0x7F (NaN).
 """
 from __future__ import annotations
 
@@ -51,6 +54,9 @@ class Batch:
     value_cache: torch.Tensor        # bf16 [num_blocks, block_size, Hkv, D]
     poison_block: int
     meta: dict = field(default_factory=dict)
+    kv_cache_dtype: str = "bf16"     # "bf16" or "fp8" (E4M3 codes, uint8 caches)
+    k_scale: float = 1.0
+    v_scale: float = 1.0
 
     @property
     def num_reqs(self) -> int:
@@ -92,6 +98,26 @@ def _randn_bf16(shape, gen: torch.Generator, device) -> torch.Tensor:
     return out.view(*shape)
 
 
+def _poison_codes(n: int, kind: str, device) -> torch.Tensor:
+    """E4M3 poison: the NaN code or the largest finite code, alternating sign."""
+    if kind == "nan":
+        return torch.full((n,), 0x7F, dtype=torch.uint8, device=device)
+    codes = torch.full((n,), 0x7E, dtype=torch.uint8, device=device)
+    codes[1::2] = 0xFE
+    return codes
+
+
+def _to_e4m3(pool: torch.Tensor, scale: float) -> torch.Tensor:
+    """bf16 pool -> E4M3 codes of pool / scale (torch's cast, clamped)."""
+    out = torch.empty(pool.shape, dtype=torch.uint8, device=pool.device)
+    flat_in, flat_out = pool.reshape(-1), out.reshape(-1)
+    chunk = 1 << 26
+    for start in range(0, flat_in.numel(), chunk):
+        x = flat_in[start:start + chunk].float() / scale
+        flat_out[start:start + chunk] = x.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    return out
+
+
 def _poison_values(n: int, kind: str, device) -> torch.Tensor:
     if kind == "nan":
         return torch.full((n,), float("nan"), dtype=torch.bfloat16, device=device)
@@ -105,7 +131,8 @@ def make_batch(*, name: str, num_heads_q: int, num_heads_kv: int, head_dim: int,
                shared_prefix: list[tuple[list[int], int]] | None = None,
                num_common_prefix_blocks: int = 0, max_blocks_per_req: int | None = None,
                poison: str = "finite", device="cpu", pool_device=None,
-               block_size: int = BLOCK_SIZE) -> Batch:
+               block_size: int = BLOCK_SIZE, kv_cache_dtype: str = "bf16", k_scale: float = 0.0125,
+               v_scale: float = 0.0125) -> Batch:
     """Build one batch.
 
     q_lens[r] new tokens are scheduled for request r whose total length after
@@ -163,12 +190,17 @@ def make_batch(*, name: str, num_heads_q: int, num_heads_kv: int, head_dim: int,
     kc = _randn_bf16((num_blocks, block_size, num_heads_kv, head_dim), gen_pool, pdev)
     vc = _randn_bf16((num_blocks, block_size, num_heads_kv, head_dim), gen_pool, pdev)
 
+    fp8 = kv_cache_dtype == "fp8"
+    if fp8:
+        kc, vc = _to_e4m3(kc, k_scale), _to_e4m3(vc, v_scale)
+    poison_fn = _poison_codes if fp8 else _poison_values
+
     # Poison: (a) the padding block, (b) every slot at or past num_computed in
     # a request's own (unshared) blocks -- the new tokens' destinations and
     # the unwritten tail of the last block.
     row = num_heads_kv * head_dim
-    kc[poison_block] = _poison_values(block_size * row, poison, pdev).view(block_size, num_heads_kv, head_dim)
-    vc[poison_block] = _poison_values(block_size * row, poison, pdev).view(block_size, num_heads_kv, head_dim)
+    kc[poison_block] = poison_fn(block_size * row, poison, pdev).view(block_size, num_heads_kv, head_dim)
+    vc[poison_block] = poison_fn(block_size * row, poison, pdev).view(block_size, num_heads_kv, head_dim)
     blocks, offsets = [], []
     for r in range(R):
         first = int(num_computed[r])
@@ -180,8 +212,8 @@ def make_batch(*, name: str, num_heads_q: int, num_heads_kv: int, head_dim: int,
         b = torch.as_tensor(np.asarray(blocks), device=pdev)
         o = torch.as_tensor(np.asarray(offsets), device=pdev)
         n = len(blocks)
-        kc[b, o] = _poison_values(n * row, poison, pdev).view(n, num_heads_kv, head_dim)
-        vc[b, o] = _poison_values(n * row, poison, pdev).view(n, num_heads_kv, head_dim)
+        kc[b, o] = poison_fn(n * row, poison, pdev).view(n, num_heads_kv, head_dim)
+        vc[b, o] = poison_fn(n * row, poison, pdev).view(n, num_heads_kv, head_dim)
 
     return Batch(name=name, num_heads_q=num_heads_q, num_heads_kv=num_heads_kv,
                  head_dim=head_dim, block_size=block_size, num_blocks=num_blocks,
@@ -190,7 +222,8 @@ def make_batch(*, name: str, num_heads_q: int, num_heads_kv: int, head_dim: int,
                  num_common_prefix_blocks=int(num_common_prefix_blocks),
                  softmax_scale=1.0 / math.sqrt(head_dim), q=q, key=key, value=value,
                  key_cache=kc, value_cache=vc, poison_block=poison_block,
-                 meta={"seed": seed, "poison": poison})
+                 meta={"seed": seed, "poison": poison}, kv_cache_dtype=kv_cache_dtype,
+                 k_scale=float(k_scale) if fp8 else 1.0, v_scale=float(v_scale) if fp8 else 1.0)
 
 
 # ---------------------------------------------------------------------------
@@ -220,7 +253,7 @@ def tiny(reading: str = "1A", seed: int = 0, poison: str = "finite", device="cpu
 
 
 def decode(seed: int = 0, batch: int = 64, lo: int = 512, hi: int = 4096, num_blocks: int = 20000,
-           poison: str = "finite", device="cpu", pool_device=None) -> Batch:
+           poison: str = "finite", device="cpu", pool_device=None, kv_cache_dtype: str = "bf16") -> Batch:
     """Decode-only Llama-3-8B-shaped layer: Hq=32, Hkv=8, D=128, 64 requests,
     seq_len ~ U[512, 4096] (including the new token), one query token each."""
     rng = np.random.default_rng(seed + 7)
@@ -228,12 +261,12 @@ def decode(seed: int = 0, batch: int = 64, lo: int = 512, hi: int = 4096, num_bl
     return make_batch(name="decode", num_heads_q=32, num_heads_kv=8, head_dim=128,
                       q_lens=np.ones(batch, dtype=np.int64), seq_lens=seq,
                       num_blocks=num_blocks, seed=seed, poison=poison, device=device,
-                      pool_device=pool_device)
+                      pool_device=pool_device, kv_cache_dtype=kv_cache_dtype)
 
 
 def mixed(seed: int = 0, n_decode: int = 256, lo: int = 1024, hi: int = 8192, n_shared: int = 32,
           shared_tokens: int = 1024, chunk: int = 2048, chunk_b_cached: int = 4096,
-          poison: str = "finite", device="cpu", pool_device=None) -> Batch:
+          poison: str = "finite", device="cpu", pool_device=None, kv_cache_dtype: str = "bf16") -> Batch:
     """Mixed continuous-batching step under an 8192-token budget: 256 decodes
     with seq_len ~ U[1024, 8192], 32 of which share a 1024-token prefix (the
     same 64 physical blocks; their lengths are drawn from [1025, 8192] so the
@@ -252,22 +285,24 @@ def mixed(seed: int = 0, n_decode: int = 256, lo: int = 1024, hi: int = 8192, n_
     sp = [(members, shared_tokens // BLOCK_SIZE)] if n_shared else None
     return make_batch(name="mixed", num_heads_q=32, num_heads_kv=8, head_dim=128,
                       q_lens=q_lens, seq_lens=seq_lens, num_blocks=num_blocks, seed=seed,
-                      shared_prefix=sp, poison=poison, device=device, pool_device=pool_device)
+                      shared_prefix=sp, poison=poison, device=device, pool_device=pool_device,
+                      kv_cache_dtype=kv_cache_dtype)
 
 
 def long_context(seed: int = 0, batch: int = 8, context: int = 131072, num_blocks: int = 70000,
-                 poison: str = "finite", device="cpu", pool_device=None) -> Batch:
+                 poison: str = "finite", device="cpu", pool_device=None, kv_cache_dtype: str = "bf16") -> Batch:
     """Long-context decode, 70B-shaped layer: Hq=64, Hkv=8, D=128, 8 requests
     of 131072 tokens each, one query token each, random block permutation."""
     return make_batch(name="long", num_heads_q=64, num_heads_kv=8, head_dim=128,
                       q_lens=np.ones(batch, dtype=np.int64),
                       seq_lens=np.full(batch, context, dtype=np.int64), num_blocks=num_blocks,
-                      seed=seed, poison=poison, device=device, pool_device=pool_device)
+                      seed=seed, poison=poison, device=device, pool_device=pool_device,
+                      kv_cache_dtype=kv_cache_dtype)
 
 
 def cascade(seed: int = 0, batch: int = 128, prefix_tokens: int = 4096, lo: int = 64,
             hi: int = 1024, use_cascade: bool = True, num_blocks: int = 8192,
-            poison: str = "finite", device="cpu", pool_device=None) -> Batch:
+            poison: str = "finite", device="cpu", pool_device=None, kv_cache_dtype: str = "bf16") -> Batch:
     """Cascade shared-prefix decode: 128 decodes over one 4096-token prefix
     (256 shared blocks) plus private suffixes ~ U[64, 1024] (including the new
     token).  ``use_cascade`` sets num_common_prefix_blocks to 256 or 0 on
@@ -280,7 +315,7 @@ def cascade(seed: int = 0, batch: int = 128, prefix_tokens: int = 4096, lo: int 
                       seq_lens=prefix_tokens + suffix, num_blocks=num_blocks, seed=seed,
                       shared_prefix=[(list(range(batch)), n_prefix)],
                       num_common_prefix_blocks=n_prefix if use_cascade else 0,
-                      poison=poison, device=device, pool_device=pool_device)
+                      poison=poison, device=device, pool_device=pool_device, kv_cache_dtype=kv_cache_dtype)
 
 
 CONFIGS = {

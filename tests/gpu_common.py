@@ -47,14 +47,22 @@ def run_gpu(batch: Batch, num_sms: int = 0, block_table=None) -> GpuRun:
     return GpuRun(out.clone(), kc, vc, st.slot_mapping().clone() if batch.num_tokens else None, bits, st)
 
 
+def cache_bits(t: torch.Tensor) -> np.ndarray:
+    """Host copy of a cache as its raw element patterns (uint16 bf16 / uint8 E4M3)."""
+    return t.detach().cpu().numpy() if t.dtype == torch.uint8 else bf16_bits(t)
+
+
 def run_oracle(batch: Batch, rows=None):
     """(key_cache, value_cache, slot_mapping, out) from the fp64 oracle."""
     orc = default_oracle()
-    return orc.step(query_start_loc=batch.query_start_loc, seq_lens=batch.seq_lens,
-                    num_computed=batch.num_computed, block_table=batch.block_table, q=bf16_bits(batch.q),
-                    key=bf16_bits(batch.key), value=bf16_bits(batch.value),
-                    key_cache=bf16_bits(batch.key_cache), value_cache=bf16_bits(batch.value_cache),
-                    softmax_scale=batch.softmax_scale, rows=rows)
+    common = dict(query_start_loc=batch.query_start_loc, seq_lens=batch.seq_lens,
+                  num_computed=batch.num_computed, block_table=batch.block_table, q=bf16_bits(batch.q),
+                  key=bf16_bits(batch.key), value=bf16_bits(batch.value),
+                  key_cache=cache_bits(batch.key_cache), value_cache=cache_bits(batch.value_cache),
+                  softmax_scale=batch.softmax_scale, rows=rows)
+    if batch.kv_cache_dtype == "fp8":
+        return orc.step_fp8(k_scale=batch.k_scale, v_scale=batch.v_scale, **common)
+    return orc.step(**common)
 
 
 def attention_error(gpu_out: torch.Tensor, oracle_out: np.ndarray, rows=None):

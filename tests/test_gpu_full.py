@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_common import assert_close, ensure_library, run_gpu
+from gpu_common import assert_close, cache_bits, ensure_library, run_gpu, run_oracle
 from oracle.oracle import default as default_oracle
 from paged_kv_cache_16_gb300 import workloads
 from paged_kv_cache_16_gb300.workloads import bf16_bits
@@ -43,15 +43,10 @@ def check_full(batch, n_decode=8):
     g = run_gpu(batch)
     assert g.bits == 0, f"device error bits {g.bits:#x}"
     rows = sample_rows(batch, n_decode=n_decode)
-    orc = default_oracle()
-    kc, vc, slots, out = orc.step(query_start_loc=batch.query_start_loc, seq_lens=batch.seq_lens,
-                                  num_computed=batch.num_computed, block_table=batch.block_table,
-                                  q=bf16_bits(batch.q), key=bf16_bits(batch.key), value=bf16_bits(batch.value),
-                                  key_cache=bf16_bits(batch.key_cache), value_cache=bf16_bits(batch.value_cache),
-                                  softmax_scale=batch.softmax_scale, rows=rows)
+    kc, vc, slots, out = run_oracle(batch, rows=rows)
     assert np.array_equal(g.slots.cpu().numpy(), slots)
-    assert np.array_equal(bf16_bits(g.key_cache), kc)
-    assert np.array_equal(bf16_bits(g.value_cache), vc)
+    assert np.array_equal(cache_bits(g.key_cache), kc)
+    assert np.array_equal(cache_bits(g.value_cache), vc)
     return assert_close(g.out, out, rows, batch.name)
 
 
@@ -75,3 +70,10 @@ def test_full_long():
 @pytest.mark.parametrize("use_cascade", [True, False])
 def test_full_cascade(use_cascade):
     check_full(workloads.cascade(device="cuda", pool_device="cuda", use_cascade=use_cascade))
+
+
+@pytest.mark.parametrize("maker", ["decode", "long", "mixed"])
+def test_full_fp8(maker):
+    """The decode, long-context and mixed workloads over E4M3 caches."""
+    fn = {"decode": workloads.decode, "long": workloads.long_context, "mixed": workloads.mixed}[maker]
+    check_full(fn(device="cuda", pool_device="cuda", kv_cache_dtype="fp8"), n_decode=2 if maker == "long" else 8)

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_common import assert_close, ensure_library, run_gpu, run_oracle
+from gpu_common import assert_close, cache_bits, ensure_library, run_gpu, run_oracle
 from oracle.oracle import default as default_oracle
 from paged_kv_cache_16_gb300 import binding, workloads
 from paged_kv_cache_16_gb300.workloads import bf16_bits, make_batch
@@ -30,8 +30,8 @@ def check_batch(batch, rows=None, num_sms=0, what=""):
     assert g.bits == 0, f"device error bits {g.bits:#x}"
     if batch.num_tokens:
         assert np.array_equal(g.slots.cpu().numpy(), slots), "slot mapping differs"
-    assert np.array_equal(bf16_bits(g.key_cache), kc), "key cache differs after the write"
-    assert np.array_equal(bf16_bits(g.value_cache), vc), "value cache differs after the write"
+    assert np.array_equal(cache_bits(g.key_cache), kc), "key cache differs after the write"
+    assert np.array_equal(cache_bits(g.value_cache), vc), "value cache differs after the write"
     if batch.num_tokens:
         assert_close(g.out, out, rows, what or batch.name)
     return g
