@@ -185,6 +185,13 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
     return r;
 }
 
+// byte permute of the pair {b:a} (bytes 0-3 from a, 4-7 from b)
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
 __device__ __forceinline__ float f16_lo(uint32_t v) {
     float f;
     asm("{\n\t.reg .f16 h;\n\tmov.b32 {h, _}, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(f) : "r"(v));

@@ -34,7 +34,6 @@ struct DecodeCfg {
     static constexpr int TSTAGE = HG * NH * BOX;           // K (or V) bytes per block
     static constexpr int STAGE = decode_stage_bytes(D, HG, KV8);
     static constexpr int NS = decode_stages(D, HG, KV8);
-    static constexpr int STAGING = decode_staging_bytes(D, HG, KV8);  // f16 V rows per warp (E4M3)
     static constexpr int THREADS = decode_threads(HG);
     static constexpr int SMEM = decode_smem_bytes(D, HG, KV8);
 };
@@ -51,8 +50,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     __shared__ int abort_flag;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;           // stages, 1024-aligned
-    const uint32_t staging = base + C::NS * C::STAGE;        // E4M3: per-warp f16 V rows
-    const uint32_t bar0 = staging + C::STAGING;              // full_k | full_v | empty
+    const uint32_t bar0 = base + C::NS * C::STAGE;           // full_k | full_v | empty
     auto full_k = [&](int s) { return bar0 + 8u * s; };
     auto full_v = [&](int s) { return bar0 + 8u * (C::NS + s); };
     auto empty = [&](int s) { return bar0 + 8u * (2 * C::NS + s); };
@@ -132,8 +130,204 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     atomicOr(p.err, kErrTimeout);
             }
         }
+    } else if constexpr (KV8) {
+        // ------------------------------------------- consumers (E4M3) --
+        // Two cache blocks (32 keys) per softmax round.  K codes feed the
+        // f16 MMAs as B fragments directly: the contraction index is permuted
+        // so that a lane's four k-values of a step are the four adjacent
+        // codes d = 16kk + 4t .. 16kk + 4t + 3 of one key (one 32-bit load).
+        // V codes are B fragments of O += P V the same way: n-tile 4a + i
+        // holds the dims 32a + 4n + i (n = 0..7 its column), so one 32-bit
+        // load of a key row feeds four n-tiles and a byte permute pairs the
+        // codes of keys 2t and 2t + 1 (and 2t + 8, 2t + 9).
+        const int g = lane >> 2;
+        const int t4 = lane & 3;
+        const int G = p.group;
+        const uint32_t k_lane = g * 128u + 4u * t4;                                      // key g, row g + 8 at +1024
+        const uint32_t va_lane = 256u * t4 + 16u * (g >> 2) + 4u * (g & 3);             // key 2t
+        const uint32_t vb_lane = 256u * t4 + 128u + 16u * ((g >> 2) ^ 1) + 4u * (g & 3);  // key 2t + 1
+        int consumed = 0;
+        bool ok = true;
+        for (int it = item_begin; it < item_end && ok; ++it) {
+            const DecodeItem item = p.items[it];
+            const int kvh = item.head_group * HG + warp;
+            const uint16_t *qrow = p.q + (static_cast<int64_t>(item.token) * p.num_heads_q + kvh * G) * D;
+            uint32_t qf[D / 16][4];
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int c = kk * 16 + 4 * t4;
+                auto ld = [&](int row, int col) {
+                    return bf16x2_to_f16x2(__ldg(reinterpret_cast<const uint32_t *>(qrow + row * D + col)));
+                };
+                qf[kk][0] = g < G ? ld(g, c) : 0u;
+                qf[kk][1] = g + 8 < G ? ld(g + 8, c) : 0u;
+                qf[kk][2] = g < G ? ld(g, c + 2) : 0u;
+                qf[kk][3] = g + 8 < G ? ld(g + 8, c + 2) : 0u;
+            }
+            float o[D / 8][4];
+#pragma unroll
+            for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+            float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+            for (int pg = item.page_begin; pg < item.page_end; pg += 2) {
+                const bool two = pg + 1 < item.page_end;
+                const int s0 = consumed % C::NS, s1 = (consumed + 1) % C::NS;
+                const uint32_t par0 = (consumed / C::NS) & 1, par1 = ((consumed + 1) / C::NS) & 1;
+                if (!warp_wait(full_k(s0), par0, &abort_flag) || (two && !warp_wait(full_k(s1), par1, &abort_flag))) {
+                    if (lane == 0) raise_abort(&abort_flag, p.err, kErrTimeout);
+                    ok = false;
+                    break;
+                }
+                // S = Q K^T over 32 keys: n-tiles 0,1 from block pg, 2,3 from pg + 1
+                float sc[4][4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+                auto qk = [&](uint32_t kb, float (&a)[4], float (&b)[4]) {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t x = kb + k_lane + ((static_cast<uint32_t>(kk ^ g)) << 4);
+                        const uint32_t w0 = lds_u32(x);
+                        const uint32_t w1 = lds_u32(x + 1024u);
+                        mma_f16_16816(a, qf[kk], e4m3x2_to_f16x2(w0 & 0xFFFFu), e4m3x2_to_f16x2(w0 >> 16));
+                        mma_f16_16816(b, qf[kk], e4m3x2_to_f16x2(w1 & 0xFFFFu), e4m3x2_to_f16x2(w1 >> 16));
+                    }
+                };
+                qk(stage(s0) + warp * C::BOX, sc[0], sc[1]);
+                if (two) qk(stage(s1) + warp * C::BOX, sc[2], sc[3]);
+                // mask keys past the context (their codes may be NaN) and, for a
+                // lone last block, the unloaded second half; log2 units
+                const int valid_keys = min(item.key_end - pg * kBlockSize, two ? 2 * kBlockSize : kBlockSize);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int key = j * 8 + 2 * t4 + (e & 1);
+                        sc[j][e] = key < valid_keys ? sc[j][e] * p.scale_log2 : -INFINITY;
+                    }
+                float mx0 = fmaxf(fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])),
+                                  fmaxf(fmaxf(sc[2][0], sc[2][1]), fmaxf(sc[3][0], sc[3][1])));
+                float mx1 = fmaxf(fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3])),
+                                  fmaxf(fmaxf(sc[2][2], sc[2][3]), fmaxf(sc[3][2], sc[3][3])));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                // rescale only when the running maximum grows by more than 2^8
+                const bool need0 = mx0 > m0 + 8.f;
+                const bool need1 = mx1 > m1 + 8.f;
+                float a0 = 1.f, a1 = 1.f;
+                if (need0) { a0 = ex2(m0 - mx0); m0 = mx0; l0 *= a0; }
+                if (need1) { a1 = ex2(m1 - mx1); m1 = mx1; l1 *= a1; }
+                if (__any_sync(0xffffffffu, need0 || need1)) {
+#pragma unroll
+                    for (int j = 0; j < D / 8; ++j) {
+                        o[j][0] *= a0; o[j][1] *= a0; o[j][2] *= a1; o[j][3] *= a1;
+                    }
+                }
+                const float r0 = m0 == -INFINITY ? 0.f : m0;
+                const float r1 = m1 == -INFINITY ? 0.f : m1;
+                uint32_t pa[2][4];
+#pragma unroll
+                for (int b = 0; b < 2; ++b) {
+                    pa[b][0] = pack_f16x2(ex2(sc[2 * b][0] - r0), ex2(sc[2 * b][1] - r0));
+                    pa[b][1] = pack_f16x2(ex2(sc[2 * b][2] - r1), ex2(sc[2 * b][3] - r1));
+                    pa[b][2] = pack_f16x2(ex2(sc[2 * b + 1][0] - r0), ex2(sc[2 * b + 1][1] - r0));
+                    pa[b][3] = pack_f16x2(ex2(sc[2 * b + 1][2] - r1), ex2(sc[2 * b + 1][3] - r1));
+                    l0 += f16_lo(pa[b][0]) + f16_hi(pa[b][0]) + f16_lo(pa[b][2]) + f16_hi(pa[b][2]);
+                    l1 += f16_lo(pa[b][1]) + f16_hi(pa[b][1]) + f16_lo(pa[b][3]) + f16_hi(pa[b][3]);
+                }
+
+                if (!warp_wait(full_v(s0), par0, &abort_flag) || (two && !warp_wait(full_v(s1), par1, &abort_flag))) {
+                    if (lane == 0) raise_abort(&abort_flag, p.err, kErrTimeout);
+                    ok = false;
+                    break;
+                }
+                // O += P V for one block; `valid` < 16 zeroes the codes of rows
+                // past the context (0-weight x NaN would poison the MMA)
+                auto pv = [&](uint32_t vb, const uint32_t (&pf)[4], int valid) {
+                    const uint32_t ra = vb + va_lane, rb = vb + vb_lane;
+                    const bool okA = 2 * t4 < valid, okB = 2 * t4 + 1 < valid;
+                    const bool okC = 2 * t4 + 8 < valid, okD = 2 * t4 + 9 < valid;
+#pragma unroll
+                    for (int a = 0; a < D / 32; ++a) {
+                        const uint32_t xa = static_cast<uint32_t>(a ^ t4) << 5;
+                        uint32_t wA = lds_u32(ra + xa), wB = lds_u32(rb + xa);
+                        uint32_t wC = lds_u32(ra + 1024u + xa), wD = lds_u32(rb + 1024u + xa);
+                        if (valid < kBlockSize) {
+                            wA = okA ? wA : 0u; wB = okB ? wB : 0u;
+                            wC = okC ? wC : 0u; wD = okD ? wD : 0u;
+                        }
+                        const uint32_t lo01 = prmt(wA, wB, 0x5140u), lo23 = prmt(wA, wB, 0x7362u);
+                        const uint32_t hi01 = prmt(wC, wD, 0x5140u), hi23 = prmt(wC, wD, 0x7362u);
+                        mma_f16_16816(o[4 * a + 0], pf, e4m3x2_to_f16x2(lo01 & 0xFFFFu), e4m3x2_to_f16x2(hi01 & 0xFFFFu));
+                        mma_f16_16816(o[4 * a + 1], pf, e4m3x2_to_f16x2(lo01 >> 16), e4m3x2_to_f16x2(hi01 >> 16));
+                        mma_f16_16816(o[4 * a + 2], pf, e4m3x2_to_f16x2(lo23 & 0xFFFFu), e4m3x2_to_f16x2(hi23 & 0xFFFFu));
+                        mma_f16_16816(o[4 * a + 3], pf, e4m3x2_to_f16x2(lo23 >> 16), e4m3x2_to_f16x2(hi23 >> 16));
+                    }
+                };
+                pv(stage(s0) + C::TSTAGE + warp * C::BOX, pa[0], valid_keys);
+                if (two) pv(stage(s1) + C::TSTAGE + warp * C::BOX, pa[1], valid_keys - kBlockSize);
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(empty(s0));
+                    if (two) mbar_arrive(empty(s1));
+                }
+                consumed += two ? 2 : 1;
+            }
+            if (!ok) break;
+            // ------------------------------------------------ finalize --
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+            const float inv0 = l0 > 0.f ? p.out_scale / l0 : 0.f;
+            const float inv1 = l1 > 0.f ? p.out_scale / l1 : 0.f;
+            const int h_row0 = kvh * G + g, h_row1 = kvh * G + g + 8;
+            // lane holds dims 32a + 8t .. 32a + 8t + 7 of heads g and g + 8:
+            // o[4a + i][0 / 2] -> dim 32a + 8t + i, o[4a + i][1 / 3] -> + 4
+            if (item.part < 0) {
+                uint16_t *orow = p.out + static_cast<int64_t>(item.token) * p.num_heads_q * D;
+#pragma unroll
+                for (int a = 0; a < D / 32; ++a) {
+                    const int d = 32 * a + 8 * t4;
+                    if (g < G)
+                        *reinterpret_cast<uint4 *>(orow + h_row0 * D + d) =
+                            make_uint4(pack_bf16x2(o[4 * a][0] * inv0, o[4 * a + 1][0] * inv0),
+                                       pack_bf16x2(o[4 * a + 2][0] * inv0, o[4 * a + 3][0] * inv0),
+                                       pack_bf16x2(o[4 * a][1] * inv0, o[4 * a + 1][1] * inv0),
+                                       pack_bf16x2(o[4 * a + 2][1] * inv0, o[4 * a + 3][1] * inv0));
+                    if (g + 8 < G)
+                        *reinterpret_cast<uint4 *>(orow + h_row1 * D + d) =
+                            make_uint4(pack_bf16x2(o[4 * a][2] * inv1, o[4 * a + 1][2] * inv1),
+                                       pack_bf16x2(o[4 * a + 2][2] * inv1, o[4 * a + 3][2] * inv1),
+                                       pack_bf16x2(o[4 * a][3] * inv1, o[4 * a + 1][3] * inv1),
+                                       pack_bf16x2(o[4 * a + 2][3] * inv1, o[4 * a + 3][3] * inv1));
+                }
+            } else {
+                const int64_t slot = static_cast<int64_t>(p.part_offset[item.token * p.n_groups + item.head_group]) + item.part;
+                float *op = p.o_part + slot * p.num_heads_q * D;
+#pragma unroll
+                for (int a = 0; a < D / 32; ++a) {
+                    const int d = 32 * a + 8 * t4;
+                    if (g < G) {
+                        float4 *dst = reinterpret_cast<float4 *>(op + h_row0 * D + d);
+                        dst[0] = make_float4(o[4 * a][0] * inv0, o[4 * a + 1][0] * inv0, o[4 * a + 2][0] * inv0, o[4 * a + 3][0] * inv0);
+                        dst[1] = make_float4(o[4 * a][1] * inv0, o[4 * a + 1][1] * inv0, o[4 * a + 2][1] * inv0, o[4 * a + 3][1] * inv0);
+                    }
+                    if (g + 8 < G) {
+                        float4 *dst = reinterpret_cast<float4 *>(op + h_row1 * D + d);
+                        dst[0] = make_float4(o[4 * a][2] * inv1, o[4 * a + 1][2] * inv1, o[4 * a + 2][2] * inv1, o[4 * a + 3][2] * inv1);
+                        dst[1] = make_float4(o[4 * a][3] * inv1, o[4 * a + 1][3] * inv1, o[4 * a + 2][3] * inv1, o[4 * a + 3][3] * inv1);
+                    }
+                }
+                if (t4 == 0) {
+                    if (g < G) p.ml_part[slot * p.num_heads_q + h_row0] = make_float2(m0, l0);
+                    if (g + 8 < G) p.ml_part[slot * p.num_heads_q + h_row1] = make_float2(m1, l1);
+                }
+            }
+        }
     } else {
-        // ------------------------------------------------------ consumers --
+        // ------------------------------------------------ consumers (bf16) --
         const int g = lane >> 2;   // MMA row group: query heads g and g + 8
         const int t4 = lane & 3;
         const int G = p.group;
@@ -144,30 +338,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const int kvh = item.head_group * HG + warp;
             const uint16_t *qrow = p.q + (static_cast<int64_t>(item.token) * p.num_heads_q + kvh * G) * D;
             uint32_t qf[D / 16][4];
-            if constexpr (!KV8) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const int c = kk * 16 + 2 * t4;
-                    qf[kk][0] = g < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + g * D + c)) : 0u;
-                    qf[kk][1] = g + 8 < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + (g + 8) * D + c)) : 0u;
-                    qf[kk][2] = g < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + g * D + c + 8)) : 0u;
-                    qf[kk][3] = g + 8 < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + (g + 8) * D + c + 8)) : 0u;
-                }
-            } else {
-                // f16 operands; the contraction index is permuted so that a
-                // lane's four k-values of a step are four adjacent key bytes:
-                // k = 2t,2t+1 <-> d = 16kk+4t+{0,1};  k = 2t+8,2t+9 <-> d = 16kk+4t+{2,3}
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const int c = kk * 16 + 4 * t4;
-                    auto ld = [&](int row, int col) {
-                        return bf16x2_to_f16x2(__ldg(reinterpret_cast<const uint32_t *>(qrow + row * D + col)));
-                    };
-                    qf[kk][0] = g < G ? ld(g, c) : 0u;
-                    qf[kk][1] = g + 8 < G ? ld(g + 8, c) : 0u;
-                    qf[kk][2] = g < G ? ld(g, c + 2) : 0u;
-                    qf[kk][3] = g + 8 < G ? ld(g + 8, c + 2) : 0u;
-                }
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int c = kk * 16 + 2 * t4;
+                qf[kk][0] = g < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + g * D + c)) : 0u;
+                qf[kk][1] = g + 8 < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + (g + 8) * D + c)) : 0u;
+                qf[kk][2] = g < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + g * D + c + 8)) : 0u;
+                qf[kk][3] = g + 8 < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + (g + 8) * D + c + 8)) : 0u;
             }
             float o[D / 8][4];
 #pragma unroll
@@ -186,27 +363,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 const uint32_t vb = kb + C::TSTAGE;
                 // S = Q K^T over this block's 16 keys (two n-tiles of 8 keys)
                 float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                if constexpr (!KV8) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const int mi = lane >> 3;
-                        const int key = (mi >> 1) * 8 + (lane & 7);
-                        const int chunk = (kk % 4) * 2 + (mi & 1);
-                        uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4(sw128(kb + (kk / 4) * C::BOX, key, chunk), b0, b1, b2, b3);
-                        mma_bf16_16816(sc[0], qf[kk], b0, b1);
-                        mma_bf16_16816(sc[1], qf[kk], b2, b3);
-                    }
-                } else {
-                    // keys g and g+8: the four codes d = 16kk+4t..+3 of each
-                    // (one 32-bit word, conflict-free across the warp)
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t w0 = lds_u32(sw128(kb, g, kk) + 4 * t4);
-                        const uint32_t w1 = lds_u32(sw128(kb, g + 8, kk) + 4 * t4);
-                        mma_f16_16816(sc[0], qf[kk], e4m3x2_to_f16x2(w0 & 0xFFFFu), e4m3x2_to_f16x2(w0 >> 16));
-                        mma_f16_16816(sc[1], qf[kk], e4m3x2_to_f16x2(w1 & 0xFFFFu), e4m3x2_to_f16x2(w1 >> 16));
-                    }
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int mi = lane >> 3;
+                    const int key = (mi >> 1) * 8 + (lane & 7);
+                    const int chunk = (kk % 4) * 2 + (mi & 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4(sw128(kb + (kk / 4) * C::BOX, key, chunk), b0, b1, b2, b3);
+                    mma_bf16_16816(sc[0], qf[kk], b0, b1);
+                    mma_bf16_16816(sc[1], qf[kk], b2, b3);
                 }
                 // mask keys past the context, scale to log2 units
                 const int key0 = pg * kBlockSize;
@@ -240,94 +405,45 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 const float r0 = m0 == -INFINITY ? 0.f : m0;
                 const float r1 = m1 == -INFINITY ? 0.f : m1;
                 uint32_t pa[4];
-                if constexpr (!KV8) {
-                    pa[0] = pack_bf16x2(ex2(sc[0][0] - r0), ex2(sc[0][1] - r0));
-                    pa[1] = pack_bf16x2(ex2(sc[0][2] - r1), ex2(sc[0][3] - r1));
-                    pa[2] = pack_bf16x2(ex2(sc[1][0] - r0), ex2(sc[1][1] - r0));
-                    pa[3] = pack_bf16x2(ex2(sc[1][2] - r1), ex2(sc[1][3] - r1));
-                    l0 += bf16_lo(pa[0]) + bf16_hi(pa[0]) + bf16_lo(pa[2]) + bf16_hi(pa[2]);
-                    l1 += bf16_lo(pa[1]) + bf16_hi(pa[1]) + bf16_lo(pa[3]) + bf16_hi(pa[3]);
-                } else {
-                    pa[0] = pack_f16x2(ex2(sc[0][0] - r0), ex2(sc[0][1] - r0));
-                    pa[1] = pack_f16x2(ex2(sc[0][2] - r1), ex2(sc[0][3] - r1));
-                    pa[2] = pack_f16x2(ex2(sc[1][0] - r0), ex2(sc[1][1] - r0));
-                    pa[3] = pack_f16x2(ex2(sc[1][2] - r1), ex2(sc[1][3] - r1));
-                    l0 += f16_lo(pa[0]) + f16_hi(pa[0]) + f16_lo(pa[2]) + f16_hi(pa[2]);
-                    l1 += f16_lo(pa[1]) + f16_hi(pa[1]) + f16_lo(pa[3]) + f16_hi(pa[3]);
-                }
+                pa[0] = pack_bf16x2(ex2(sc[0][0] - r0), ex2(sc[0][1] - r0));
+                pa[1] = pack_bf16x2(ex2(sc[0][2] - r1), ex2(sc[0][3] - r1));
+                pa[2] = pack_bf16x2(ex2(sc[1][0] - r0), ex2(sc[1][1] - r0));
+                pa[3] = pack_bf16x2(ex2(sc[1][2] - r1), ex2(sc[1][3] - r1));
+                l0 += bf16_lo(pa[0]) + bf16_hi(pa[0]) + bf16_lo(pa[2]) + bf16_hi(pa[2]);
+                l1 += bf16_lo(pa[1]) + bf16_hi(pa[1]) + bf16_lo(pa[3]) + bf16_hi(pa[3]);
 
                 if (!warp_wait(full_v(s), par, &abort_flag)) {
                     if (lane == 0) raise_abort(&abort_flag, p.err, kErrTimeout);
                     ok = false;
                     break;
                 }
-                if constexpr (!KV8) {
-                    if (valid_keys < kBlockSize) {
-                        // rows past the context may hold anything (even NaN); zero
-                        // them so that 0-weight * row stays 0 inside the MMA
-                        const int bad = kBlockSize - valid_keys;
-                        for (int i = lane; i < bad * C::NH * 8; i += 32) {
-                            const int row = valid_keys + i / (C::NH * 8);
-                            const int half = (i / 8) % C::NH;
-                            const int ch = i % 8;
-                            const uint32_t a = vb + half * C::BOX + row * 128 + ch * 16;
-                            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
+                if (valid_keys < kBlockSize) {
+                    // rows past the context may hold anything (even NaN); zero
+                    // them so that 0-weight * row stays 0 inside the MMA
+                    const int bad = kBlockSize - valid_keys;
+                    for (int i = lane; i < bad * C::NH * 8; i += 32) {
+                        const int row = valid_keys + i / (C::NH * 8);
+                        const int half = (i / 8) % C::NH;
+                        const int ch = i % 8;
+                        const uint32_t a = vb + half * C::BOX + row * 128 + ch * 16;
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
                     }
-                    // O += P V
-#pragma unroll
-                    for (int np = 0; np < D / 16; ++np) {
-                        const int mi = lane >> 3;
-                        const int key = (mi & 1) * 8 + (lane & 7);
-                        const int chunk = 2 * np + (mi >> 1);
-                        uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4_trans(sw128(vb + (chunk / 8) * C::BOX, key, chunk % 8), b0, b1, b2, b3);
-                        mma_bf16_16816(o[2 * np], pa, b0, b1);
-                        mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(empty(s));
-                } else {
-                    // this head's value rows, E4M3 -> f16 into the warp's staging
-                    // rows ([16][64] halves, same swizzle as a bf16 box); rows
-                    // past the context become 0 (their codes may be NaN)
-                    const uint32_t stg = staging + warp * (16 * D * 2);
-#pragma unroll
-                    for (int i = 0; i < (16 * D / 16) / 32; ++i) {
-                        const int ci = lane + 32 * i;
-                        const int row = ci / (D / 16);
-                        const int c = ci % (D / 16);          // 16 codes: d = 16c .. 16c+15
-                        uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-                        if (row < valid_keys) {
-                            const uint4 x = lds_v4(sw128(vb, row, c));
-                            const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                w[2 * q] = e4m3x2_to_f16x2(xs[q] & 0xFFFFu);
-                                w[2 * q + 1] = e4m3x2_to_f16x2(xs[q] >> 16);
-                            }
-                        }
-                        const uint32_t hb = stg + (c >> 2) * C::BOX;
-                        sts_v4(sw128(hb, row, (c & 3) * 2), w[0], w[1], w[2], w[3]);
-                        sts_v4(sw128(hb, row, (c & 3) * 2 + 1), w[4], w[5], w[6], w[7]);
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(empty(s));   // the E4M3 block is no longer read
-                    // O += P V (f16)
-#pragma unroll
-                    for (int np = 0; np < D / 16; ++np) {
-                        const int mi = lane >> 3;
-                        const int key = (mi & 1) * 8 + (lane & 7);
-                        const int chunk = 2 * np + (mi >> 1);
-                        uint32_t b0, b1, b2, b3;
-                        ldmatrix_x4_trans(sw128(stg + (chunk / 8) * C::BOX, key, chunk % 8), b0, b1, b2, b3);
-                        mma_f16_16816(o[2 * np], pa, b0, b1);
-                        mma_f16_16816(o[2 * np + 1], pa, b2, b3);
-                    }
+                    fence_proxy_async_smem();
                     __syncwarp();
                 }
+                // O += P V
+#pragma unroll
+                for (int np = 0; np < D / 16; ++np) {
+                    const int mi = lane >> 3;
+                    const int key = (mi & 1) * 8 + (lane & 7);
+                    const int chunk = 2 * np + (mi >> 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4_trans(sw128(vb + (chunk / 8) * C::BOX, key, chunk % 8), b0, b1, b2, b3);
+                    mma_bf16_16816(o[2 * np], pa, b0, b1);
+                    mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty(s));
             }
             if (!ok) break;
             // ------------------------------------------------ finalize --

@@ -17,21 +17,17 @@ constexpr int kMaxDecodeHeads = 8; // kv heads one decode CTA serves
 
 // Split-KV decode kernel resources, shared by the planner (which sizes the
 // persistent grid without touching a device) and the kernel.  kv8: E4M3
-// caches (one byte per element, plus a per-warp f16 staging buffer of V).
+// caches (one byte per element).
 constexpr int decode_stage_bytes(int d, int hg, bool kv8) { return 2 * hg * 16 * d * (kv8 ? 1 : 2); }
-constexpr int decode_staging_bytes(int d, int hg, bool kv8) { return kv8 ? hg * 16 * d * 2 : 0; }
 constexpr int decode_stages(int d, int hg, bool kv8) {
-    return kv8 ? ((200 * 1024 - decode_staging_bytes(d, hg, kv8)) / decode_stage_bytes(d, hg, kv8) > 6
-                      ? 6
-                      : (200 * 1024 - decode_staging_bytes(d, hg, kv8)) / decode_stage_bytes(d, hg, kv8))
+    return kv8 ? (200 * 1024 / decode_stage_bytes(d, hg, kv8) > 6 ? 6 : 200 * 1024 / decode_stage_bytes(d, hg, kv8))
                : (decode_stage_bytes(d, hg, kv8) * 4 <= 200 * 1024   ? 4
                   : decode_stage_bytes(d, hg, kv8) * 3 <= 200 * 1024 ? 3
                                                                        : 2);
 }
 constexpr int decode_threads(int hg) { return (hg + 1) * 32; }
 constexpr int decode_smem_bytes(int d, int hg, bool kv8) {
-    return decode_stages(d, hg, kv8) * decode_stage_bytes(d, hg, kv8) + decode_staging_bytes(d, hg, kv8) +
-           3 * decode_stages(d, hg, kv8) * 8 + 1024;
+    return decode_stages(d, hg, kv8) * decode_stage_bytes(d, hg, kv8) + 3 * decode_stages(d, hg, kv8) * 8 + 1024;
 }
 constexpr int kSmemPerSm = 233472;  // 228 KiB of shared memory per SM
 constexpr int decode_ctas_per_sm_static(int d, int hg, bool kv8) {

@@ -24,8 +24,8 @@ def _gpu():
     ensure_library()
 
 
-def check(batch, rows=None, what=""):
-    g = run_gpu(batch)
+def check(batch, rows=None, what="", num_sms=0):
+    g = run_gpu(batch, num_sms=num_sms)
     kc, vc, slots, out = run_oracle(batch, rows=rows)
     assert g.bits == 0, f"device error bits {g.bits:#x}"
     assert np.array_equal(g.slots.cpu().numpy(), slots)
@@ -68,6 +68,14 @@ def test_fp8_decode_small():
 
 def test_fp8_decode_nan_poison():
     check(workloads.decode(batch=12, lo=1, hi=300, num_blocks=400, seed=42, poison="nan", kv_cache_dtype="fp8"))
+
+
+@pytest.mark.parametrize("num_sms", [1, 7, 40, 152, 400])
+def test_fp8_partition_count(num_sms):
+    """Split-KV cuts at every granularity: page runs of odd and even length
+    that end inside a request, lone last blocks, single-block runs."""
+    check(workloads.decode(batch=12, lo=1, hi=300, num_blocks=400, seed=46, kv_cache_dtype="fp8"),
+          what=f"num_sms={num_sms}", num_sms=num_sms)
 
 
 def test_fp8_mixed_small():
