@@ -10,6 +10,7 @@
  * What it computes (the step traced on the page "vLLM 推理流程分析"):
  *   1. slot_mapping for every scheduled token                 (§5.1.2)
  *   2. the KV-cache scatter (reshape_and_cache_flash)          (§6.3)
+ *      and the zeroing of newly allocated blocks              (§4, §5.1.1)
  *   3. causal GQA attention of every scheduled query token over its
  *      request's context, read through block_table            (§6.2, §10.1-10.2)
  * and, for the partition pins, attention restricted to one key range with
@@ -115,6 +116,27 @@ int oracle_write_kv(int32_t num_tokens, int32_t num_heads_kv, int32_t head_dim,
             key_cache[slot * row + e] = key[(int64_t)t * row + e];
             value_cache[slot * row + e] = value[(int64_t)t * row + e];
         }
+    }
+    return status;
+}
+
+/*
+ * Zeroing of newly allocated cache blocks ("vLLM 推理流程分析" §4: the
+ * scheduler output lists new_block_ids_to_zero, blocks whose old contents must
+ * be cleared; §5.1.1: _update_states zeroes them so that cache positions not
+ * yet written are never read as stale KV).  Every byte of the K and V entries
+ * of each listed block becomes 0 (+0 in bf16, code 0x00 in E4M3); ids < 0 are
+ * skipped; an id past the cache is skipped and reported.
+ */
+int oracle_zero_blocks(int32_t num_ids, const int32_t *block_ids, int64_t num_blocks, int64_t block_bytes,
+                       uint8_t *key_cache, uint8_t *value_cache) {
+    int status = ORACLE_OK;
+    for (int32_t i = 0; i < num_ids; ++i) {
+        int64_t b = block_ids[i];
+        if (b < 0) continue;
+        if (b >= num_blocks) { status = ORACLE_BAD_BLOCK; continue; }
+        memset(key_cache + b * block_bytes, 0, (size_t)block_bytes);
+        memset(value_cache + b * block_bytes, 0, (size_t)block_bytes);
     }
     return status;
 }

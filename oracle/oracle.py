@@ -95,6 +95,9 @@ class Oracle:
         L.oracle_merge_partials.argtypes = [ctypes.c_int32, ctypes.c_int32, _f64p, _f64p, _f64p,
                                             _f64p, _f64p, _f64p]
         _u8p = ctypes.POINTER(ctypes.c_uint8)
+        L.oracle_zero_blocks.restype = ctypes.c_int
+        L.oracle_zero_blocks.argtypes = [ctypes.c_int32, _i32p, ctypes.c_int64, ctypes.c_int64,
+                                         ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(ctypes.c_uint8)]
         L.oracle_e4m3_value.restype = ctypes.c_double
         L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
         L.oracle_e4m3_encode.restype = ctypes.c_uint8
@@ -144,6 +147,18 @@ class Oracle:
         return int(self.lib.oracle_write_kv(T, hkv, d, _ptr(key, _u16p), _ptr(value, _u16p),
                                             _ptr(slots, _i64p), _ptr(key_cache, _u16p),
                                             _ptr(value_cache, _u16p), num_slots))
+
+    def zero_blocks(self, block_ids, key_cache, value_cache) -> int:
+        """Zero the K and V entries of the listed blocks in place (any cache
+        element type; ids < 0 skipped)."""
+        ids = np.ascontiguousarray(block_ids, dtype=np.int32)
+        assert key_cache.flags["C_CONTIGUOUS"] and value_cache.flags["C_CONTIGUOUS"]
+        assert key_cache.shape == value_cache.shape and key_cache.dtype == value_cache.dtype
+        nb = key_cache.shape[0]
+        block_bytes = key_cache.nbytes // nb
+        u8 = ctypes.POINTER(ctypes.c_uint8)
+        return int(self.lib.oracle_zero_blocks(len(ids), _ptr(ids, _i32p), nb, block_bytes,
+                                               key_cache.ctypes.data_as(u8), value_cache.ctypes.data_as(u8)))
 
     # -- step 3: attention -----------------------------------------------
     def attention_range(self, *, query_start_loc, seq_lens, num_computed, block_table, q,

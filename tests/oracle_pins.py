@@ -485,4 +485,52 @@ def pin_fp8_scale_roles(orc):
     assert not np.allclose(a, d)
 
 
+def pin_zero_blocks(orc):
+    """new_block_ids_to_zero ("vLLM 推理流程分析" §4, §5.1.1): every byte of
+    the K and V entries of each listed block becomes 0, nothing else changes,
+    negative ids are skipped, an id past the cache is reported and skipped;
+    the same holds for one-byte (E4M3) caches."""
+    rng = _rng(40)
+    for dtype, hi in ((np.uint16, 65536), (np.uint8, 256)):
+        nb, bs, hkv, d = 7, 16, 2, 64
+        kc = rng.integers(1, hi, size=(nb, bs, hkv, d), dtype=dtype)   # no zero byte pattern to hide in
+        vc = rng.integers(1, hi, size=(nb, bs, hkv, d), dtype=dtype)
+        gk, gv = kc.copy(), vc.copy()
+        assert orc.zero_blocks(np.array([5, -1, 2]), gk, gv) == 0
+        for b in range(nb):
+            if b in (2, 5):
+                assert not gk[b].any() and not gv[b].any(), b
+            else:
+                assert np.array_equal(gk[b], kc[b]) and np.array_equal(gv[b], vc[b]), b
+        # idempotent and independent of the order of the ids
+        hk, hv = kc.copy(), vc.copy()
+        assert orc.zero_blocks(np.array([2, 5, 2]), hk, hv) == 0
+        assert np.array_equal(hk, gk) and np.array_equal(hv, gv)
+        # an id past the cache: status 2, the valid ids are still zeroed
+        ik, iv = kc.copy(), vc.copy()
+        assert orc.zero_blocks(np.array([nb, 0]), ik, iv) == 2
+        assert not ik[0].any() and np.array_equal(ik[1:], kc[1:]) and np.array_equal(iv[1:], vc[1:])
+    # a zeroed element reads as +0 in both element types
+    assert orc.bf16_value(0) == 0.0 and math.copysign(1.0, orc.bf16_value(0)) == 1.0
+    assert orc.e4m3_value(0) == 0.0 and math.copysign(1.0, orc.e4m3_value(0)) == 1.0
+
+
+def pin_zeroed_tail_is_never_read(orc):
+    """The reason for zeroing (§5.1.1): slots of a new block not yet written
+    must not reach the result.  A decode whose last block was zeroed and then
+    written in part gives the dense result, and the same result when the
+    unwritten slots hold +inf / NaN instead of zeros."""
+    case = Case(_rng(41), hq=4, hkv=2, d=64, q_lens=[1], seq_lens=[21], num_blocks=4)
+    blk = int(case.block_table[0, 1])
+    a_k, a_v = case.kc.copy(), case.vc.copy()
+    assert orc.zero_blocks(np.array([blk]), a_k, a_v) == 0
+    a_k[blk, :5], a_v[blk, :5] = case.kc[blk, :5], case.vc[blk, :5]      # keys 16..20 written
+    b_k, b_v = a_k.copy(), a_v.copy()
+    b_k[blk, 5:], b_v[blk, 5:] = 0x7F80, 0x7FC0                           # +inf / NaN, never written
+    out_a = case.run(orc, key_cache=a_k, value_cache=a_v)
+    out_b = case.run(orc, key_cache=b_k, value_cache=b_v)
+    assert np.array_equal(out_a, out_b)
+    assert np.max(np.abs(out_a - case.dense_expected())) < 1e-12
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

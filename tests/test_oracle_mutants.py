@@ -48,6 +48,10 @@ MUTANTS = [
     ("fp8_key_scale_dropped", "softmax_scale * k_scale, scores, &m, &l, ov);", "softmax_scale, scores, &m, &l, ov);"),
     ("fp8_value_scale_dropped", "for (int32_t d = 0; d < head_dim; ++d) orow[d] = ov[d] * v_scale;",
      "for (int32_t d = 0; d < head_dim; ++d) orow[d] = ov[d];"),
+    ("zero_value_untouched", "memset(value_cache + b * block_bytes, 0, (size_t)block_bytes);", ";"),
+    ("zero_wrong_block", "memset(key_cache + b * block_bytes, 0, (size_t)block_bytes);",
+     "memset(key_cache + ((b + 1) % num_blocks) * block_bytes, 0, (size_t)block_bytes);"),
+    ("zero_negative_ids_wrap", "if (b < 0) continue;", "if (b < 0) b += num_blocks;"),
     ("query_head_transposed", "const uint16_t *qrow = q + ((int64_t)t * num_heads_q + h) * head_dim;",
      "const uint16_t *qrow = q + ((int64_t)t * num_heads_q + (num_heads_q - 1 - h)) * head_dim;"),
 ]
