@@ -32,7 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from paged_kv_cache_16_gb300 import binding, build, workloads  # noqa: E402
-from paged_kv_cache_16_gb300.step import DeviceStep  # noqa: E402
+from paged_kv_cache_16_gb300.step import DeviceStep, GraphStep  # noqa: E402
 from paged_kv_cache_16_gb300.workloads import bf16_bits  # noqa: E402
 
 METRIC = "paged-attn step tokens/s; decode KV GB/s & prefill TFLOPS as % GB300 roofline"
@@ -366,6 +366,54 @@ def run_ours(args, world, rank, local):
     if info["decode_kv_bytes"] and k_n[0]:
         kernels["decode"]["gbs"] = info["decode_kv_bytes"] / (k_ms[0] / k_n[0] / 1e3) / 1e9
 
+    # ---- the same step replayed from one CUDA graph (fixed-shape plan) ----
+    # Capacities are this workload's own sizes; the eager plan and the
+    # fixed-shape plan cut the work identically, so the kernels (timed per
+    # launch above) are the same ones the graph replays.
+    gs = GraphStep(num_heads_q=batch.num_heads_q, num_heads_kv=batch.num_heads_kv, head_dim=batch.head_dim,
+                   num_blocks=batch.num_blocks, max_blocks_per_req=batch.block_table.shape[1],
+                   softmax_scale=batch.softmax_scale, max_tokens=max(T, 1), max_reqs=max(batch.num_reqs, 1),
+                   max_extend_tiles=info["num_extend_tiles"], max_dequant_blocks=info["num_dequant_blocks"],
+                   max_partial_slots=max(info["num_partial_slots"], 1), kv_cache_dtype=batch.kv_cache_dtype,
+                   k_scale=batch.k_scale, v_scale=batch.v_scale, device=dev)
+    first = gs.make_plan(batch)
+    gs.load(batch, first, q, key, value)
+    gs.capture(first, kc, vc)
+
+    def graph_step(keep_plans):
+        plan = gs.make_plan(batch)
+        keep_plans.append(plan)
+        binding.pa_upload_metadata(plan, gs.workspace, stream)
+        gs.graph.replay()
+
+    for _ in range(args.warmup):
+        flush_l2()
+        graph_step(keep)
+    torch.cuda.synchronize(dev)
+    if gs.check_errors():
+        raise SystemExit("device error during graph warm-up")
+    keep.clear()
+    g_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    g_stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as g_clocks:
+        for i in range(args.steps):
+            flush_l2()
+            g_starts[i].record(stream)
+            graph_step(keep)
+            g_stops[i].record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    keep.clear()
+    g_ms_all = max_over_ranks(world, statistics.mean(s.elapsed_time(e) for s, e in zip(g_starts, g_stops)), dev)
+    bits |= gs.check_errors()
+    graph_mode = args.launch == "graph"
+    modes = {"eager": {"ms_per_step": ms_all, "value": tokens_all / (ms_all / 1e3)},
+             "graph": {"ms_per_step": g_ms_all, "value": tokens_all / (g_ms_all / 1e3)}}
+    if graph_mode:
+        ms_all, clocks = g_ms_all, g_clocks
+
     # ---- end to end through the C ABI with host buffers ----
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
     q_h, key_h, val_h = pin(batch.q), pin(batch.key), pin(batch.value)
@@ -380,16 +428,28 @@ def run_ours(args, world, rank, local):
         flush_l2()
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
-        q.copy_(q_h, non_blocking=True)
-        key.copy_(key_h, non_blocking=True)
-        value.copy_(val_h, non_blocking=True)
-        for d_, h_ in zip(meta_d, meta_h):
-            d_.copy_(h_, non_blocking=True)
-        plan = st.make_plan()
-        st.slot_mapping(stream)
-        st.write(key, value, kc, vc, stream)
-        st.attend(q, kc, vc, stream, plan=plan)
-        out_h[:T].copy_(st.out[:T], non_blocking=True)
+        if graph_mode:
+            gs.q[:T].copy_(q_h, non_blocking=True)
+            gs.key[:T].copy_(key_h, non_blocking=True)
+            gs.value[:T].copy_(val_h, non_blocking=True)
+            gs.qsl[:batch.num_reqs + 1].copy_(meta_h[0], non_blocking=True)
+            gs.num_computed[:batch.num_reqs].copy_(meta_h[1], non_blocking=True)
+            gs.block_table[:batch.num_reqs].copy_(meta_h[2], non_blocking=True)
+            plan = gs.make_plan(batch)
+            binding.pa_upload_metadata(plan, gs.workspace, stream)
+            gs.graph.replay()
+            out_h[:T].copy_(gs.out[:T], non_blocking=True)
+        else:
+            q.copy_(q_h, non_blocking=True)
+            key.copy_(key_h, non_blocking=True)
+            value.copy_(val_h, non_blocking=True)
+            for d_, h_ in zip(meta_d, meta_h):
+                d_.copy_(h_, non_blocking=True)
+            plan = st.make_plan()
+            st.slot_mapping(stream)
+            st.write(key, value, kc, vc, stream)
+            st.attend(q, kc, vc, stream, plan=plan)
+            out_h[:T].copy_(st.out[:T], non_blocking=True)
         torch.cuda.synchronize(dev)
         if i >= 2:
             e2e_times.append(time.perf_counter() - t0)
@@ -415,7 +475,11 @@ def run_ours(args, world, rank, local):
             "config": {"workload": desc, "name": args.workload, "tokens_per_step": T, "seed": args.seed,
                        "kv_cache_dtype": args.kv_dtype,
                        "l2": "flushed between timed steps (256 MiB write + read-back, outside the step events)",
-                       "step": "pa_plan (host) + pa_slot_mapping + pa_write_kv + pa_attention",
+                       "step": ("pa_plan_fixed (host) + pa_upload_metadata + CUDA-graph replay of pa_slot_mapping, "
+                                "pa_write_kv and pa_attention_launch") if graph_mode else
+                               "pa_plan (host) + pa_slot_mapping + pa_write_kv + pa_attention",
+                       "launch": args.launch, "modes": modes,
+                       "kernel_times": "eager pass, CUDA events around each launch (same kernels and work cut)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clocks.summary(), "kernels": kernels, "device_error_bits": bits,
@@ -437,6 +501,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--kv-dtype", choices=["bf16", "fp8"], default="bf16",
                     help="KV cache element type (fp8 = E4M3 codes with per-tensor scales)")
+    ap.add_argument("--launch", choices=["graph", "eager"], default="graph",
+                    help="time the step as a CUDA-graph replay (fixed-shape plan) or as eager launches")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

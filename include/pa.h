@@ -12,7 +12,13 @@
  *   pa_attention     device: causal GQA attention of every scheduled query
  *                    token over its request's context, read through the block
  *                    table; decode rows, chunked-prefill/extend rows, prefix
- *                    hits and the shared-prefix (cascade) route.
+ *                    hits and the shared-prefix (cascade) route;
+ *   pa_zero_blocks   device: clear newly allocated cache blocks (§4, §5.1.1).
+ *
+ * Fixed-shape plans (pa_plan_fixed) make the attention launches of a step a
+ * function of capacities only, so that they can be captured once in a CUDA
+ * graph and replayed for later steps: pa_upload_metadata then replay (or
+ * pa_attention_launch).
  *
  * Data types: every tensor element is IEEE bfloat16, passed as raw 16-bit
  * patterns; metadata is int32 except slot_mapping (int64).  All layouts are
@@ -54,12 +60,13 @@ typedef enum {
     PA_ERR_UNSUPPORTED = 2,        /* well-formed but outside the supported shapes    */
     PA_ERR_CUDA = 3,               /* a CUDA runtime call failed                      */
     PA_ERR_DEVICE_CHECK = 4,       /* a kernel recorded an error in the error word    */
-    PA_ERR_WORKSPACE_TOO_SMALL = 5 /* workspace smaller than pa_plan reported         */
+    PA_ERR_WORKSPACE_TOO_SMALL = 5,/* workspace smaller than pa_plan reported         */
+    PA_ERR_CAPACITY = 6            /* the step exceeds a fixed-shape plan's capacity  */
 } pa_status;
 
 /* Bits a kernel may set in the device error word (see pa_check_device_errors). */
 #define PA_DEVERR_SLOT_RANGE   0x1  /* pa_write_kv: slot >= number of cache slots      */
-#define PA_DEVERR_BLOCK_RANGE  0x2  /* pa_attention: block id outside [0, num_blocks)  */
+#define PA_DEVERR_BLOCK_RANGE  0x2  /* block id outside [0, num_blocks)                */
 #define PA_DEVERR_TIMEOUT      0x4  /* a bounded wait inside a kernel gave up          */
 
 typedef struct pa_plan_s pa_plan_t;
@@ -154,7 +161,10 @@ pa_status pa_plan_get_info(const pa_plan_t *plan, pa_plan_info *info);
  * and slot = block_table[r][p / block_size] * block_size + p % block_size.
  * All pointers are DEVICE memory: query_start_loc [R+1], num_computed [R],
  * block_table [R][max_blocks_per_req], slot_mapping [T] (written).  The
- * metadata must be the same that pa_plan accepted.
+ * metadata must be the same that pa_plan accepted.  num_tokens may exceed
+ * query_start_loc[num_reqs] (read on the device): tokens past it get slot -1,
+ * so a launch sized for a fixed token capacity skips the padding rows in
+ * pa_write_kv.
  */
 pa_status pa_slot_mapping(const int32_t *query_start_loc, const int32_t *num_computed,
                           const int32_t *block_table, int32_t num_reqs, int32_t num_tokens,
@@ -213,11 +223,92 @@ pa_status pa_write_kv_fp8(const void *key, const void *value, const int64_t *slo
  * block placement does not change a single bit of it.  Slots past seq_len in a
  * request's last block are never used (their contents may be anything,
  * including NaN).  Returns PA_ERR_WORKSPACE_TOO_SMALL, PA_ERR_INVALID_ARGUMENT
- * (NULL or misaligned pointer) or PA_ERR_CUDA (launch failure).
+ * (NULL or misaligned pointer) or PA_ERR_CUDA (launch failure).  Equivalent to
+ * pa_upload_metadata then pa_attention_launch, plus the optional timing events.
  */
 pa_status pa_attention(const pa_plan_t *plan, const void *q, const void *key_cache,
                        const void *value_cache, const int32_t *block_table, void *out,
                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Capacities of a fixed-shape plan.  Graph mode captures the execution of a
+ * stable shape once, then for each step copies the new data to fixed
+ * addresses and replays; request counts are rounded up to a capture size and
+ * the spare rows padded ("vLLM 源码完全拆解（十六）", fourth walk-through;
+ * "vLLM 推理流程分析" §4: total_num_scheduled_tokens selects the CUDA graph).
+ * A replay repeats the same launches with the same arguments, so a
+ * fixed-shape plan sizes its workspace
+ * layout, its grids and every kernel argument from these capacities, so every
+ * fixed-shape plan with equal capacities and equal model fields of
+ * pa_batch_desc (head counts, head_dim, block_size, num_blocks,
+ * max_blocks_per_req, softmax_scale, num_sms, kv_cache_dtype, k_scale,
+ * v_scale) launches identically; the step's own lengths reach the kernels
+ * only through the uploaded metadata.
+ */
+typedef struct {
+    int32_t max_tokens;          /* T <= max_tokens; q and out hold max_tokens rows */
+    int32_t max_reqs;            /* num_reqs <= max_reqs                            */
+    int32_t max_extend_tiles;    /* tensor-core tiles (extend rows and cascade
+                                    prefix); 0: steps made of decode rows only     */
+    int32_t max_dequant_blocks;  /* FP8 caches: blocks those tiles read; 0 if none  */
+    int32_t max_partial_slots;   /* partial results; 0 = room for every decode
+                                    split plus one slot per (token, head group)    */
+} pa_fixed_shape;
+
+/*
+ * pa_plan with a fixed shape (see pa_fixed_shape).  As pa_plan, plus
+ * PA_ERR_INVALID_ARGUMENT for a NULL shape or a capacity < 0 (max_tokens and
+ * max_reqs must be > 0), and PA_ERR_CAPACITY when this step needs more tokens,
+ * requests, tiles, FP8 blocks or partial slots than the shape allows.  The
+ * workspace size depends on the shape and model fields only.  The decode
+ * kernel always runs on num_sms x (CTAs per SM) CTAs.
+ */
+pa_status pa_plan_fixed(const pa_batch_desc *desc, const pa_fixed_shape *shape, pa_plan_t **out,
+                        size_t *workspace_bytes);
+
+/*
+ * Copy the plan's metadata into the workspace (stream ordered, from a pinned
+ * host buffer the plan owns) and prepare the kernels the plan launches.  Not
+ * for stream capture.  Arguments and errors as for pa_attention.
+ */
+pa_status pa_upload_metadata(const pa_plan_t *plan, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The kernels of pa_attention alone: they read the metadata that the last
+ * pa_upload_metadata put into this workspace, which must come from a plan of
+ * the same fixed shape (or, for a plan made by pa_plan, from this plan).
+ * Records no timing events and makes no host<->device copy, so it may be
+ * captured in a CUDA graph.  For a fixed-shape plan the enqueued work is
+ * identical for every plan of equal shape (see pa_fixed_shape): a graph
+ * captured once replays correctly after pa_upload_metadata of any later
+ * plan of that shape.  Call pa_upload_metadata (which prepares the kernels)
+ * at least once before the first capture.  Arguments and errors as for
+ * pa_attention; q and out must hold max_tokens rows for a fixed-shape plan.
+ */
+pa_status pa_attention_launch(const pa_plan_t *plan, const void *q, const void *key_cache,
+                              const void *value_cache, const int32_t *block_table, void *out,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Zero newly allocated cache blocks ("vLLM 推理流程分析" §4: the scheduler
+ * output lists new_block_ids_to_zero, blocks whose old contents must be
+ * cleared; §5.1.1: _update_states zeroes them so that cache positions not yet
+ * written are never read as stale KV).  Every byte of the K and V entries of
+ * each listed block becomes 0 (+0 in bf16, code 0x00 in E4M3).
+ *   block_ids        DEVICE int32 [num_ids]; ids < 0 are skipped (padding of a
+ *                    fixed-size launch); an id >= num_blocks is skipped and
+ *                    sets PA_DEVERR_BLOCK_RANGE in *device_error_word (if
+ *                    non-NULL)
+ *   key_cache,
+ *   value_cache      DEVICE, 16-byte aligned, [num_blocks][16][Hkv][D] of
+ *                    kv_cache_dtype (PA_KV_BF16 or PA_KV_FP8_E4M3)
+ * Returns PA_ERR_INVALID_ARGUMENT for a negative count or size, a NULL or
+ * misaligned pointer, or an unknown kv_cache_dtype; PA_ERR_CUDA on a launch
+ * failure.  Enqueue before the step's pa_write_kv.
+ */
+pa_status pa_zero_blocks(const int32_t *block_ids, int32_t num_ids, int32_t num_blocks, int32_t num_heads_kv,
+                         int32_t head_dim, int32_t kv_cache_dtype, void *key_cache, void *value_cache,
+                         int32_t *device_error_word, void *stream);
 
 /*
  * Read and clear the device error word (the first 4 bytes of a workspace, or

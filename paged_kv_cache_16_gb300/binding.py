@@ -21,6 +21,7 @@ PA_ERR_UNSUPPORTED = 2
 PA_ERR_CUDA = 3
 PA_ERR_DEVICE_CHECK = 4
 PA_ERR_WORKSPACE_TOO_SMALL = 5
+PA_ERR_CAPACITY = 6
 
 PA_KV_BF16 = 0
 PA_KV_FP8_E4M3 = 1
@@ -32,7 +33,8 @@ PA_DEVERR_TIMEOUT = 0x4
 # symbols include/pa.h declares (checked by the CPU tests)
 EXPORTED = ("pa_plan", "pa_plan_destroy", "pa_plan_get_info", "pa_slot_mapping", "pa_write_kv",
             "pa_attention", "pa_check_device_errors", "pa_plan_enable_timing",
-            "pa_plan_kernel_times", "pa_status_string", "pa_attention_no_alloc", "pa_write_kv_fp8")
+            "pa_plan_kernel_times", "pa_status_string", "pa_attention_no_alloc", "pa_write_kv_fp8",
+            "pa_plan_fixed", "pa_upload_metadata", "pa_attention_launch", "pa_zero_blocks")
 
 
 class PaError(RuntimeError):
@@ -89,6 +91,16 @@ class PlanInfo(ctypes.Structure):
 _LIB = None
 
 
+class FixedShape(ctypes.Structure):
+    _fields_ = [
+        ("max_tokens", ctypes.c_int32),
+        ("max_reqs", ctypes.c_int32),
+        ("max_extend_tiles", ctypes.c_int32),
+        ("max_dequant_blocks", ctypes.c_int32),
+        ("max_partial_slots", ctypes.c_int32),
+    ]
+
+
 def library_path() -> str:
     return _build.LIBRARY
 
@@ -111,6 +123,15 @@ def load(path: str | None = None, build_if_missing: bool = False) -> ctypes.CDLL
     lib.pa_status_string.argtypes = [ctypes.c_int]
     lib.pa_plan.restype = ctypes.c_int
     lib.pa_plan.argtypes = [ctypes.POINTER(BatchDesc), ctypes.POINTER(vp), ctypes.POINTER(sz)]
+    lib.pa_plan_fixed.restype = ctypes.c_int
+    lib.pa_plan_fixed.argtypes = [ctypes.POINTER(BatchDesc), ctypes.POINTER(FixedShape), ctypes.POINTER(vp),
+                                  ctypes.POINTER(sz)]
+    lib.pa_upload_metadata.restype = ctypes.c_int
+    lib.pa_upload_metadata.argtypes = [vp, vp, sz, vp]
+    lib.pa_attention_launch.restype = ctypes.c_int
+    lib.pa_attention_launch.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.pa_zero_blocks.restype = ctypes.c_int
+    lib.pa_zero_blocks.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]
     lib.pa_plan_destroy.restype = None
     lib.pa_plan_destroy.argtypes = [vp]
     lib.pa_plan_get_info.restype = ctypes.c_int
@@ -237,6 +258,39 @@ def pa_plan(**kw) -> Plan:
     return Plan(handle.value, ws.value, keep)
 
 
+def _fixed_shape(max_tokens, max_reqs, max_extend_tiles=0, max_dequant_blocks=0, max_partial_slots=0):
+    fs = FixedShape()
+    fs.max_tokens, fs.max_reqs = int(max_tokens), int(max_reqs)
+    fs.max_extend_tiles, fs.max_dequant_blocks = int(max_extend_tiles), int(max_dequant_blocks)
+    fs.max_partial_slots = int(max_partial_slots)
+    return fs
+
+
+def pa_plan_fixed(*, max_tokens, max_reqs, max_extend_tiles=0, max_dequant_blocks=0, max_partial_slots=0,
+                  **kw) -> Plan:
+    """A fixed-shape plan (graph-capturable launches, see pa.h)."""
+    d, keep = make_desc(**kw)
+    fs = _fixed_shape(max_tokens, max_reqs, max_extend_tiles, max_dequant_blocks, max_partial_slots)
+    handle = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    _check(load().pa_plan_fixed(ctypes.byref(d), ctypes.byref(fs), ctypes.byref(handle), ctypes.byref(ws)),
+           "pa_plan_fixed")
+    return Plan(handle.value, ws.value, keep)
+
+
+def pa_plan_fixed_status(*, max_tokens, max_reqs, max_extend_tiles=0, max_dequant_blocks=0, max_partial_slots=0,
+                         **kw) -> int:
+    """Status code pa_plan_fixed returns (plan discarded)."""
+    d, keep = make_desc(**kw)
+    fs = _fixed_shape(max_tokens, max_reqs, max_extend_tiles, max_dequant_blocks, max_partial_slots)
+    handle = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    st = load().pa_plan_fixed(ctypes.byref(d), ctypes.byref(fs), ctypes.byref(handle), ctypes.byref(ws))
+    if st == PA_OK:
+        load().pa_plan_destroy(handle.value)
+    return st
+
+
 def pa_plan_status(**kw) -> int:
     """Status code pa_plan returns for this descriptor (plan discarded)."""
     d, keep = make_desc(**kw)
@@ -277,6 +331,26 @@ def pa_attention(plan: Plan, q, key_cache, value_cache, block_table, out, worksp
     nbytes = workspace.numel() * workspace.element_size()
     _check(load().pa_attention(plan.handle, _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_table),
                                _ptr(out), _ptr(workspace), nbytes, _stream(stream)), "pa_attention")
+
+
+def pa_upload_metadata(plan: Plan, workspace, stream=None):
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().pa_upload_metadata(plan.handle, _ptr(workspace), nbytes, _stream(stream)), "pa_upload_metadata")
+
+
+def pa_attention_launch(plan: Plan, q, key_cache, value_cache, block_table, out, workspace, stream=None):
+    """The attention kernels alone (capturable in a CUDA graph; see pa.h)."""
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().pa_attention_launch(plan.handle, _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_table),
+                                      _ptr(out), _ptr(workspace), nbytes, _stream(stream)), "pa_attention_launch")
+
+
+def pa_zero_blocks(block_ids, key_cache, value_cache, device_error_word=None, stream=None):
+    """Zero the K and V entries of the listed blocks (ids < 0 skipped)."""
+    nb, bs, hkv, d = key_cache.shape
+    kv = PA_KV_FP8_E4M3 if key_cache.element_size() == 1 else PA_KV_BF16
+    _check(load().pa_zero_blocks(_ptr(block_ids), int(block_ids.numel()), nb, hkv, d, kv, _ptr(key_cache),
+                                 _ptr(value_cache), _ptr(device_error_word), _stream(stream)), "pa_zero_blocks")
 
 
 def pa_attention_no_alloc(plan: Plan, q, key_cache, value_cache, block_table, out, device_error_word=None,

@@ -18,6 +18,8 @@
 //    rows of a 16x16 bf16 MMA tile (G <= 16), so each K/V row loaded from HBM
 //    is used by all G heads; S = Q K^T and O += P V run on the tensor cores
 //    (mma.sync), the online softmax in fp32 registers with quad shuffles.
+#include <type_traits>
+
 #include "dev.cuh"
 
 namespace pa {
@@ -139,13 +141,22 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // V codes are B fragments of O += P V the same way: n-tile 4a + i
         // holds the dims 32a + 4n + i (n = 0..7 its column), so one 32-bit
         // load of a key row feeds four n-tiles and a byte permute pairs the
-        // codes of keys 2t and 2t + 1 (and 2t + 8, 2t + 9).
+        // codes of keys 2t and 2t + 1 (and 2t + 8, 2t + 9).  The row sums l
+        // come from one more MMA of P against a column of ones, so they add
+        // exactly the f16 weights the value MMAs use.
         const int g = lane >> 2;
         const int t4 = lane & 3;
         const int G = p.group;
-        const uint32_t k_lane = g * 128u + 4u * t4;                                      // key g, row g + 8 at +1024
+        constexpr uint32_t kOnes = 0x3C003C00u;  // f16x2 (1, 1)
+        uint32_t k_off[D / 16];                   // key g at +0, key g + 8 at +1024
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) k_off[kk] = g * 128u + 4u * t4 + (static_cast<uint32_t>(kk ^ g) << 4);
+        uint32_t v_off[D / 32];
+#pragma unroll
+        for (int a = 0; a < D / 32; ++a) v_off[a] = static_cast<uint32_t>(a ^ t4) << 5;
         const uint32_t va_lane = 256u * t4 + 16u * (g >> 2) + 4u * (g & 3);             // key 2t
         const uint32_t vb_lane = 256u * t4 + 128u + 16u * ((g >> 2) ^ 1) + 4u * (g & 3);  // key 2t + 1
+        const float sl2 = p.scale_log2;  // > 0: the maximum of raw scores scales
         int consumed = 0;
         bool ok = true;
         for (int it = item_begin; it < item_end && ok; ++it) {
@@ -167,119 +178,131 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             float o[D / 8][4];
 #pragma unroll
             for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-            float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+            float lacc[4] = {0.f, 0.f, 0.f, 0.f};
+            float m0 = -INFINITY, m1 = -INFINITY;
 
-            for (int pg = item.page_begin; pg < item.page_end; pg += 2) {
-                const bool two = pg + 1 < item.page_end;
+            auto qk = [&](uint32_t kb, float (&a)[4], float (&b)[4]) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t x = kb + k_off[kk];
+                    uint32_t k0, k1, k2, k3;
+                    e4m3x4_to_f16x2x2(lds_u32(x), k0, k1);
+                    e4m3x4_to_f16x2x2(lds_u32(x + 1024u), k2, k3);
+                    mma_f16_16816(a, qf[kk], k0, k1);
+                    mma_f16_16816(b, qf[kk], k2, k3);
+                }
+            };
+            // O += P V for one block; MASKED zeroes the codes of rows at or
+            // past `valid` (0-weight x NaN would poison the MMA)
+            auto pv = [&](auto masked, uint32_t vb, const uint32_t (&pf)[4], int valid) {
+                const uint32_t ra = vb + va_lane, rb = vb + vb_lane;
+                uint32_t mA = ~0u, mB = ~0u, mC = ~0u, mD = ~0u;
+                if constexpr (decltype(masked)::value) {
+                    mA = 2 * t4 < valid ? ~0u : 0u;
+                    mB = 2 * t4 + 1 < valid ? ~0u : 0u;
+                    mC = 2 * t4 + 8 < valid ? ~0u : 0u;
+                    mD = 2 * t4 + 9 < valid ? ~0u : 0u;
+                }
+#pragma unroll
+                for (int a = 0; a < D / 32; ++a) {
+                    uint32_t wA = lds_u32(ra + v_off[a]), wB = lds_u32(rb + v_off[a]);
+                    uint32_t wC = lds_u32(ra + 1024u + v_off[a]), wD = lds_u32(rb + 1024u + v_off[a]);
+                    if constexpr (decltype(masked)::value) {
+                        wA &= mA; wB &= mB; wC &= mC; wD &= mD;
+                    }
+                    uint32_t b0[4], b1[4];
+                    e4m3x4_to_f16x2x2(prmt(wA, wB, 0x5140u), b0[0], b0[1]);
+                    e4m3x4_to_f16x2x2(prmt(wA, wB, 0x7362u), b0[2], b0[3]);
+                    e4m3x4_to_f16x2x2(prmt(wC, wD, 0x5140u), b1[0], b1[1]);
+                    e4m3x4_to_f16x2x2(prmt(wC, wD, 0x7362u), b1[2], b1[3]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) mma_f16_16816(o[4 * a + i], pf, b0[i], b1[i]);
+                }
+                mma_f16_16816(lacc, pf, kOnes, kOnes);
+            };
+            // one softmax round over one (TWO = false) or two cache blocks
+            auto round = [&](auto two_c, int pg) -> bool {
+                constexpr bool TWO = decltype(two_c)::value;
                 const int s0 = consumed % C::NS, s1 = (consumed + 1) % C::NS;
                 const uint32_t par0 = (consumed / C::NS) & 1, par1 = ((consumed + 1) / C::NS) & 1;
-                if (!warp_wait(full_k(s0), par0, &abort_flag) || (two && !warp_wait(full_k(s1), par1, &abort_flag))) {
-                    if (lane == 0) raise_abort(&abort_flag, p.err, kErrTimeout);
-                    ok = false;
-                    break;
-                }
-                // S = Q K^T over 32 keys: n-tiles 0,1 from block pg, 2,3 from pg + 1
+                if (!warp_wait(full_k(s0), par0, &abort_flag) || (TWO && !warp_wait(full_k(s1), par1, &abort_flag)))
+                    return false;
                 float sc[4][4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-                auto qk = [&](uint32_t kb, float (&a)[4], float (&b)[4]) {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t x = kb + k_lane + ((static_cast<uint32_t>(kk ^ g)) << 4);
-                        const uint32_t w0 = lds_u32(x);
-                        const uint32_t w1 = lds_u32(x + 1024u);
-                        mma_f16_16816(a, qf[kk], e4m3x2_to_f16x2(w0 & 0xFFFFu), e4m3x2_to_f16x2(w0 >> 16));
-                        mma_f16_16816(b, qf[kk], e4m3x2_to_f16x2(w1 & 0xFFFFu), e4m3x2_to_f16x2(w1 >> 16));
-                    }
-                };
                 qk(stage(s0) + warp * C::BOX, sc[0], sc[1]);
-                if (two) qk(stage(s1) + warp * C::BOX, sc[2], sc[3]);
-                // mask keys past the context (their codes may be NaN) and, for a
-                // lone last block, the unloaded second half; log2 units
-                const int valid_keys = min(item.key_end - pg * kBlockSize, two ? 2 * kBlockSize : kBlockSize);
+                if constexpr (TWO) qk(stage(s1) + warp * C::BOX, sc[2], sc[3]);
+                // keys past the context (their codes may be NaN) or past the
+                // blocks loaded drop out; raw scores, scaled inside ex2
+                const int valid_keys = min(item.key_end - pg * kBlockSize, TWO ? 2 * kBlockSize : kBlockSize);
+                if (!TWO || valid_keys < 2 * kBlockSize) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
+                    for (int j = 0; j < 4; ++j)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int key = j * 8 + 2 * t4 + (e & 1);
-                        sc[j][e] = key < valid_keys ? sc[j][e] * p.scale_log2 : -INFINITY;
-                    }
-                float mx0 = fmaxf(fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])),
-                                  fmaxf(fmaxf(sc[2][0], sc[2][1]), fmaxf(sc[3][0], sc[3][1])));
-                float mx1 = fmaxf(fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3])),
-                                  fmaxf(fmaxf(sc[2][2], sc[2][3]), fmaxf(sc[3][2], sc[3][3])));
+                        for (int e = 0; e < 4; ++e)
+                            if (j * 8 + 2 * t4 + (e & 1) >= valid_keys) sc[j][e] = -INFINITY;
+                }
+                constexpr int NT = TWO ? 4 : 2;
+                float mx0 = fmaxf(sc[0][0], sc[0][1]), mx1 = fmaxf(sc[0][2], sc[0][3]);
+#pragma unroll
+                for (int j = 1; j < NT; ++j) {
+                    mx0 = fmaxf(mx0, fmaxf(sc[j][0], sc[j][1]));
+                    mx1 = fmaxf(mx1, fmaxf(sc[j][2], sc[j][3]));
+                }
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2)) * sl2;
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2)) * sl2;
                 // rescale only when the running maximum grows by more than 2^8
                 const bool need0 = mx0 > m0 + 8.f;
                 const bool need1 = mx1 > m1 + 8.f;
-                float a0 = 1.f, a1 = 1.f;
-                if (need0) { a0 = ex2(m0 - mx0); m0 = mx0; l0 *= a0; }
-                if (need1) { a1 = ex2(m1 - mx1); m1 = mx1; l1 *= a1; }
                 if (__any_sync(0xffffffffu, need0 || need1)) {
+                    float a0 = 1.f, a1 = 1.f;
+                    if (need0) { a0 = ex2(m0 - mx0); m0 = mx0; }
+                    if (need1) { a1 = ex2(m1 - mx1); m1 = mx1; }
 #pragma unroll
                     for (int j = 0; j < D / 8; ++j) {
                         o[j][0] *= a0; o[j][1] *= a0; o[j][2] *= a1; o[j][3] *= a1;
                     }
+                    lacc[0] *= a0; lacc[1] *= a0; lacc[2] *= a1; lacc[3] *= a1;
                 }
                 const float r0 = m0 == -INFINITY ? 0.f : m0;
                 const float r1 = m1 == -INFINITY ? 0.f : m1;
                 uint32_t pa[2][4];
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    pa[b][0] = pack_f16x2(ex2(sc[2 * b][0] - r0), ex2(sc[2 * b][1] - r0));
-                    pa[b][1] = pack_f16x2(ex2(sc[2 * b][2] - r1), ex2(sc[2 * b][3] - r1));
-                    pa[b][2] = pack_f16x2(ex2(sc[2 * b + 1][0] - r0), ex2(sc[2 * b + 1][1] - r0));
-                    pa[b][3] = pack_f16x2(ex2(sc[2 * b + 1][2] - r1), ex2(sc[2 * b + 1][3] - r1));
-                    l0 += f16_lo(pa[b][0]) + f16_hi(pa[b][0]) + f16_lo(pa[b][2]) + f16_hi(pa[b][2]);
-                    l1 += f16_lo(pa[b][1]) + f16_hi(pa[b][1]) + f16_lo(pa[b][3]) + f16_hi(pa[b][3]);
+                for (int b = 0; b < NT / 2; ++b) {
+                    pa[b][0] = pack_f16x2(ex2(fmaf(sc[2 * b][0], sl2, -r0)), ex2(fmaf(sc[2 * b][1], sl2, -r0)));
+                    pa[b][1] = pack_f16x2(ex2(fmaf(sc[2 * b][2], sl2, -r1)), ex2(fmaf(sc[2 * b][3], sl2, -r1)));
+                    pa[b][2] = pack_f16x2(ex2(fmaf(sc[2 * b + 1][0], sl2, -r0)), ex2(fmaf(sc[2 * b + 1][1], sl2, -r0)));
+                    pa[b][3] = pack_f16x2(ex2(fmaf(sc[2 * b + 1][2], sl2, -r1)), ex2(fmaf(sc[2 * b + 1][3], sl2, -r1)));
                 }
-
-                if (!warp_wait(full_v(s0), par0, &abort_flag) || (two && !warp_wait(full_v(s1), par1, &abort_flag))) {
-                    if (lane == 0) raise_abort(&abort_flag, p.err, kErrTimeout);
-                    ok = false;
-                    break;
+                if (!warp_wait(full_v(s0), par0, &abort_flag) || (TWO && !warp_wait(full_v(s1), par1, &abort_flag)))
+                    return false;
+                const uint32_t vb0 = stage(s0) + C::TSTAGE + warp * C::BOX;
+                if (valid_keys < kBlockSize) pv(std::true_type{}, vb0, pa[0], valid_keys);
+                else pv(std::false_type{}, vb0, pa[0], kBlockSize);
+                if constexpr (TWO) {
+                    const uint32_t vb1 = stage(s1) + C::TSTAGE + warp * C::BOX;
+                    if (valid_keys < 2 * kBlockSize) pv(std::true_type{}, vb1, pa[1], valid_keys - kBlockSize);
+                    else pv(std::false_type{}, vb1, pa[1], kBlockSize);
                 }
-                // O += P V for one block; `valid` < 16 zeroes the codes of rows
-                // past the context (0-weight x NaN would poison the MMA)
-                auto pv = [&](uint32_t vb, const uint32_t (&pf)[4], int valid) {
-                    const uint32_t ra = vb + va_lane, rb = vb + vb_lane;
-                    const bool okA = 2 * t4 < valid, okB = 2 * t4 + 1 < valid;
-                    const bool okC = 2 * t4 + 8 < valid, okD = 2 * t4 + 9 < valid;
-#pragma unroll
-                    for (int a = 0; a < D / 32; ++a) {
-                        const uint32_t xa = static_cast<uint32_t>(a ^ t4) << 5;
-                        uint32_t wA = lds_u32(ra + xa), wB = lds_u32(rb + xa);
-                        uint32_t wC = lds_u32(ra + 1024u + xa), wD = lds_u32(rb + 1024u + xa);
-                        if (valid < kBlockSize) {
-                            wA = okA ? wA : 0u; wB = okB ? wB : 0u;
-                            wC = okC ? wC : 0u; wD = okD ? wD : 0u;
-                        }
-                        const uint32_t lo01 = prmt(wA, wB, 0x5140u), lo23 = prmt(wA, wB, 0x7362u);
-                        const uint32_t hi01 = prmt(wC, wD, 0x5140u), hi23 = prmt(wC, wD, 0x7362u);
-                        mma_f16_16816(o[4 * a + 0], pf, e4m3x2_to_f16x2(lo01 & 0xFFFFu), e4m3x2_to_f16x2(hi01 & 0xFFFFu));
-                        mma_f16_16816(o[4 * a + 1], pf, e4m3x2_to_f16x2(lo01 >> 16), e4m3x2_to_f16x2(hi01 >> 16));
-                        mma_f16_16816(o[4 * a + 2], pf, e4m3x2_to_f16x2(lo23 & 0xFFFFu), e4m3x2_to_f16x2(hi23 & 0xFFFFu));
-                        mma_f16_16816(o[4 * a + 3], pf, e4m3x2_to_f16x2(lo23 >> 16), e4m3x2_to_f16x2(hi23 >> 16));
-                    }
-                };
-                pv(stage(s0) + C::TSTAGE + warp * C::BOX, pa[0], valid_keys);
-                if (two) pv(stage(s1) + C::TSTAGE + warp * C::BOX, pa[1], valid_keys - kBlockSize);
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(empty(s0));
-                    if (two) mbar_arrive(empty(s1));
+                    if constexpr (TWO) mbar_arrive(empty(s1));
                 }
-                consumed += two ? 2 : 1;
+                consumed += TWO ? 2 : 1;
+                return true;
+            };
+            int pg = item.page_begin;
+            for (; ok && pg + 1 < item.page_end; pg += 2) ok = round(std::true_type{}, pg);
+            if (ok && pg < item.page_end) ok = round(std::false_type{}, pg);
+            if (!ok) {
+                if (lane == 0) raise_abort(&abort_flag, p.err, kErrTimeout);
+                break;
             }
-            if (!ok) break;
             // ------------------------------------------------ finalize --
-            l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-            l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+            const float l0 = lacc[0], l1 = lacc[2];
             const float inv0 = l0 > 0.f ? p.out_scale / l0 : 0.f;
             const float inv1 = l1 > 0.f ? p.out_scale / l1 : 0.f;
             const int h_row0 = kvh * G + g, h_row1 = kvh * G + g + 8;
@@ -486,16 +509,23 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 }
 
 template <int D, int HG, bool KV8>
-cudaError_t launch_t(int num_ctas, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                     const DecodeParams &p, cudaStream_t stream) {
-    using C = DecodeCfg<D, HG, KV8>;
+cudaError_t configure() {
     static bool configured = false;  // attribute is per function, set once per process
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, HG, KV8>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, HG, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             DecodeCfg<D, HG, KV8>::SMEM);
         if (e != cudaSuccess) return e;
         configured = true;
     }
+    return cudaSuccess;
+}
+
+template <int D, int HG, bool KV8>
+cudaError_t launch_t(int num_ctas, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                     const DecodeParams &p, cudaStream_t stream) {
+    using C = DecodeCfg<D, HG, KV8>;
+    cudaError_t e = configure<D, HG, KV8>();
+    if (e != cudaSuccess) return e;
     decode_kernel<D, HG, KV8><<<num_ctas, C::THREADS, C::SMEM, stream>>>(tm_k, tm_v, p);
     return cudaGetLastError();
 }
@@ -505,6 +535,14 @@ cudaError_t launch_t(int num_ctas, const CUtensorMap &tm_k, const CUtensorMap &t
 #define PA_DECODE_CASES(X)                                                                                  \
     X(64, 1, false) X(64, 2, false) X(64, 4, false) X(64, 8, false) X(128, 1, false) X(128, 2, false)      \
     X(128, 4, false) X(128, 8, false) X(128, 1, true) X(128, 2, true) X(128, 4, true) X(128, 8, true)
+
+cudaError_t prepare_decode(int head_dim, int hg, bool kv8) {
+#define X(d, h, f) \
+    if (head_dim == d && hg == h && kv8 == f) return configure<d, h, f>();
+    PA_DECODE_CASES(X)
+#undef X
+    return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_decode(int head_dim, int hg, bool kv8, int num_ctas, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const DecodeParams &p, cudaStream_t stream) {

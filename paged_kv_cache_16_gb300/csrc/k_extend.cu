@@ -93,6 +93,7 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     auto v_s = [&](int s) { return k_s(s) + C::KVB; };
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
+    if (static_cast<int>(blockIdx.x) >= p.counts[kCountTiles]) return;   // grid sized for a capacity
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const ExtendTile tile = p.tiles[blockIdx.x];
@@ -423,27 +424,40 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 }
 
 template <int D>
-cudaError_t launch_t(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                     const ExtendParams &p, cudaStream_t stream) {
-    using C = ExtCfg<D>;
-    static bool configured = false;
+cudaError_t configure() {
+    static bool configured = false;  // attribute is per function, set once per process
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(extend_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM);
+                                             ExtCfg<D>::SMEM);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    extend_kernel<D><<<p.num_tiles, C::THREADS, C::SMEM, stream>>>(tm_q, tm_k, tm_v, p);
+    return cudaSuccess;
+}
+
+template <int D>
+cudaError_t launch_t(int grid, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                     const ExtendParams &p, cudaStream_t stream) {
+    using C = ExtCfg<D>;
+    cudaError_t e = configure<D>();
+    if (e != cudaSuccess) return e;
+    extend_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tm_q, tm_k, tm_v, p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_extend(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+cudaError_t prepare_extend(int head_dim) {
+    if (head_dim == 128) return configure<128>();
+    if (head_dim == 64) return configure<64>();
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_extend(int head_dim, int grid, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const ExtendParams &p, cudaStream_t stream) {
-    if (p.num_tiles <= 0) return cudaSuccess;
-    if (head_dim == 128) return launch_t<128>(tm_q, tm_k, tm_v, p, stream);
-    if (head_dim == 64) return launch_t<64>(tm_q, tm_k, tm_v, p, stream);
+    if (grid <= 0) return cudaSuccess;
+    if (head_dim == 128) return launch_t<128>(grid, tm_q, tm_k, tm_v, p, stream);
+    if (head_dim == 64) return launch_t<64>(grid, tm_q, tm_k, tm_v, p, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -1,5 +1,5 @@
-// Bandwidth-trivial kernels of the step: slot mapping, the KV-cache scatter
-// and the merge of partition partials.
+// Bandwidth-trivial kernels of the step: slot mapping, the KV-cache scatter,
+// block zeroing, the FP8 block expansion and the merge of partition partials.
 #include "dev.cuh"
 
 namespace pa {
@@ -14,6 +14,10 @@ __global__ void slot_mapping_kernel(const int32_t *__restrict__ qsl,
                                     int64_t *__restrict__ slots) {
     const int32_t t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= num_tokens) return;
+    if (t >= qsl[num_reqs]) {            // padding of a launch sized for a token capacity
+        slots[t] = -1;
+        return;
+    }
     int32_t lo = 0, hi = num_reqs - 1;  // last r with qsl[r] <= t
     while (lo < hi) {
         const int32_t mid = (lo + hi + 1) >> 1;
@@ -107,21 +111,42 @@ __device__ __forceinline__ void expand16(const uint4 codes, uint4 *dst) {
 }
 
 __global__ void dequant_kernel(DequantParams p) {
-    const DequantItem it = p.items[blockIdx.x];
-    const int32_t src = p.block_table[static_cast<int64_t>(it.req) * p.max_blocks + it.block];
+    const int32_t n = p.counts[kCountDequant];
     const int32_t chunks = p.block_elems / 16;
-    uint4 *kd = reinterpret_cast<uint4 *>(p.key_out + static_cast<int64_t>(it.dst) * p.block_elems);
-    uint4 *vd = reinterpret_cast<uint4 *>(p.value_out + static_cast<int64_t>(it.dst) * p.block_elems);
-    if (src < 0 || src >= p.num_blocks) {
-        if (threadIdx.x == 0) atomicOr(p.err, kErrBlockRange);
-        for (int32_t c = threadIdx.x; c < 2 * chunks; c += blockDim.x) kd[c] = vd[c] = make_uint4(0, 0, 0, 0);
+    for (int32_t i = blockIdx.x; i < n; i += gridDim.x) {
+        const DequantItem it = p.items[i];
+        const int32_t src = p.block_table[static_cast<int64_t>(it.req) * p.max_blocks + it.block];
+        uint4 *kd = reinterpret_cast<uint4 *>(p.key_out + static_cast<int64_t>(it.dst) * p.block_elems);
+        uint4 *vd = reinterpret_cast<uint4 *>(p.value_out + static_cast<int64_t>(it.dst) * p.block_elems);
+        if (src < 0 || src >= p.num_blocks) {
+            if (threadIdx.x == 0) atomicOr(p.err, kErrBlockRange);
+            for (int32_t c = threadIdx.x; c < 2 * chunks; c += blockDim.x) kd[c] = vd[c] = make_uint4(0, 0, 0, 0);
+            continue;
+        }
+        const uint4 *ks = reinterpret_cast<const uint4 *>(p.key_cache + static_cast<int64_t>(src) * p.block_elems);
+        const uint4 *vs = reinterpret_cast<const uint4 *>(p.value_cache + static_cast<int64_t>(src) * p.block_elems);
+        for (int32_t c = threadIdx.x; c < chunks; c += blockDim.x) {
+            expand16(__ldg(ks + c), kd + 2 * c);
+            expand16(__ldg(vs + c), vd + 2 * c);
+        }
+    }
+}
+
+// Zeroing of newly allocated blocks ("vLLM 推理流程分析" §4 new_block_ids_to_zero,
+// §5.1.1 _zero_block_ids): one CTA per listed id, 16-byte stores over the
+// block's K and V bytes.
+__global__ void zero_blocks_kernel(const int32_t *__restrict__ ids, int32_t num_blocks, int64_t chunks,
+                                   uint4 *__restrict__ key_cache, uint4 *__restrict__ value_cache, int32_t *err) {
+    const int32_t b = ids[blockIdx.x];
+    if (b < 0) return;
+    if (b >= num_blocks) {
+        if (err != nullptr && threadIdx.x == 0) atomicOr(err, kErrBlockRange);
         return;
     }
-    const uint4 *ks = reinterpret_cast<const uint4 *>(p.key_cache + static_cast<int64_t>(src) * p.block_elems);
-    const uint4 *vs = reinterpret_cast<const uint4 *>(p.value_cache + static_cast<int64_t>(src) * p.block_elems);
-    for (int32_t c = threadIdx.x; c < chunks; c += blockDim.x) {
-        expand16(__ldg(ks + c), kd + 2 * c);
-        expand16(__ldg(vs + c), vd + 2 * c);
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int64_t c = threadIdx.x; c < chunks; c += blockDim.x) {
+        key_cache[b * chunks + c] = z;
+        value_cache[b * chunks + c] = z;
     }
 }
 
@@ -130,14 +155,16 @@ __global__ void dequant_kernel(DequantParams p) {
 // rescaling).  One warp per (token, query head); m is in log2 units.
 template <int D>
 __global__ void merge_kernel(MergeParams p) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (warp >= p.num_rows * p.max_heads) return;
-    const MergeRow row = p.rows[warp / p.max_heads];
-    const int hi = warp % p.max_heads;
-    if (hi >= row.hq_count) return;
-    dev::merge_head<D>(p.out + static_cast<int64_t>(row.token) * p.num_heads_q * D, p.o_part, p.ml_part,
-                       row.slot0, row.count, p.num_heads_q, row.hq_begin + hi, lane);
+    const int64_t total = static_cast<int64_t>(p.counts[kCountMerges]) * p.max_heads;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x / 32;
+    for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < total; w += stride) {
+        const MergeRow row = p.rows[w / p.max_heads];
+        const int hi = static_cast<int>(w % p.max_heads);
+        if (hi >= row.hq_count) continue;
+        dev::merge_head<D>(p.out + static_cast<int64_t>(row.token) * p.num_heads_q * D, p.o_part, p.ml_part,
+                           row.slot0, row.count, p.num_heads_q, row.hq_begin + hi, lane);
+    }
 }
 
 }  // namespace
@@ -186,20 +213,26 @@ cudaError_t launch_write_kv_fp8(const void *key, const void *value, const int64_
     return cudaGetLastError();
 }
 
-cudaError_t launch_dequant(const DequantParams &p, cudaStream_t stream) {
-    if (p.num_items <= 0) return cudaSuccess;
-    dequant_kernel<<<p.num_items, 256, 0, stream>>>(p);
+cudaError_t launch_dequant(int grid, const DequantParams &p, cudaStream_t stream) {
+    if (grid <= 0) return cudaSuccess;
+    dequant_kernel<<<grid, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_merge(int head_dim, const MergeParams &p, cudaStream_t stream) {
-    if (p.num_rows <= 0) return cudaSuccess;
-    const int64_t warps = static_cast<int64_t>(p.num_rows) * p.max_heads;
-    const int threads = 256;
-    const unsigned blocks = static_cast<unsigned>((warps * 32 + threads - 1) / threads);
-    if (head_dim == 128) merge_kernel<128><<<blocks, threads, 0, stream>>>(p);
-    else if (head_dim == 64) merge_kernel<64><<<blocks, threads, 0, stream>>>(p);
+cudaError_t launch_merge(int head_dim, int grid, const MergeParams &p, cudaStream_t stream) {
+    if (grid <= 0) return cudaSuccess;
+    if (head_dim == 128) merge_kernel<128><<<grid, 256, 0, stream>>>(p);
+    else if (head_dim == 64) merge_kernel<64><<<grid, 256, 0, stream>>>(p);
     else return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_zero_blocks(const int32_t *ids, int32_t num_ids, int32_t num_blocks, int64_t block_bytes,
+                               void *key_cache, void *value_cache, int32_t *err, cudaStream_t stream) {
+    if (num_ids <= 0) return cudaSuccess;
+    zero_blocks_kernel<<<num_ids, 256, 0, stream>>>(ids, num_blocks, block_bytes / 16,
+                                                    static_cast<uint4 *>(key_cache),
+                                                    static_cast<uint4 *>(value_cache), err);
     return cudaGetLastError();
 }
 

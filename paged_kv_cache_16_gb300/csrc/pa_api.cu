@@ -193,8 +193,10 @@ pa_status validate(const pa_batch_desc *d) {
 }
 
 // Cut the concatenated decode runs into ncta equal contiguous shares.
+// fixed_ncta > 0: the grid has exactly that many CTAs; the shares past the
+// ones the work needs are empty.
 void plan_decode(pa_plan_s *P, const pa_batch_desc *d, const std::vector<int32_t> &decode_rows,
-                 std::vector<int32_t> &pieces) {
+                 std::vector<int32_t> &pieces, int64_t fixed_ncta) {
     struct Run { int32_t r, grp, pb, pe; };
     std::vector<Run> runs;
     const int32_t kb = P->n_prefix;  // first block of the suffix work
@@ -208,11 +210,15 @@ void plan_decode(pa_plan_s *P, const pa_batch_desc *d, const std::vector<int32_t
         }
     pieces.assign(static_cast<size_t>(d->num_reqs) * P->n_groups, 0);
     P->cta_begin.assign(1, 0);
-    if (total == 0) return;
+    if (total == 0) {
+        if (fixed_ncta > 0) P->cta_begin.assign(static_cast<size_t>(fixed_ncta) + 1, 0);
+        return;
+    }
     const int cps = std::max(1, decode_ctas_per_sm_static(P->D, P->HG, P->kv8));
     const int64_t min_pages = 4;
     int64_t ncta = std::min<int64_t>(static_cast<int64_t>(P->num_sms) * cps, (total + min_pages - 1) / min_pages);
     ncta = std::max<int64_t>(ncta, 1);
+    if (fixed_ncta > 0) ncta = std::min(ncta, fixed_ncta);
     size_t run = 0;
     int32_t cursor = runs.empty() ? 0 : runs[0].pb;
     for (int64_t c = 0; c < ncta; ++c) {
@@ -238,9 +244,12 @@ void plan_decode(pa_plan_s *P, const pa_batch_desc *d, const std::vector<int32_t
         }
         P->cta_begin.push_back(static_cast<int32_t>(P->items.size()));
     }
+    while (static_cast<int64_t>(P->cta_begin.size()) < fixed_ncta + 1)
+        P->cta_begin.push_back(static_cast<int32_t>(P->items.size()));
 }
 
-pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d) {
+pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape *shape) {
+    P->fixed = shape != nullptr;
     P->R = d->num_reqs;
     P->Hq = d->num_heads_q;
     P->Hkv = d->num_heads_kv;
@@ -261,6 +270,7 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d) {
             cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return PA_ERR_CUDA;
     }
+    if (P->fixed && (P->T > shape->max_tokens || P->R > shape->max_reqs)) return PA_ERR_CAPACITY;
     const int32_t *qsl = d->query_start_loc;
     std::vector<int32_t> decode_rows, extend_rows;
     for (int32_t r = 0; r < P->R; ++r) {
@@ -354,7 +364,8 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d) {
 
     // ------------------------------------------------------------- decode
     std::vector<int32_t> pieces;
-    plan_decode(P, d, decode_rows, pieces);
+    const int cps = std::max(1, decode_ctas_per_sm_static(P->D, P->HG, P->kv8));
+    plan_decode(P, d, decode_rows, pieces, P->fixed ? static_cast<int64_t>(P->num_sms) * cps : 0);
 
     // ----------------------------------------------------- partial slots
     std::vector<int32_t> count(static_cast<size_t>(P->T) * P->n_groups, 0);
@@ -392,23 +403,56 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d) {
     if (slots > INT32_MAX) return PA_ERR_UNSUPPORTED;
     P->num_slots = static_cast<int32_t>(slots);
 
+    // ------------------------------------------------- launch shape
+    P->ncta = static_cast<int32_t>(P->cta_begin.size()) - 1;
+    const int32_t scr_rows = P->max_blocks > 0 ? static_cast<int32_t>(P->scratch_table.size() / P->max_blocks) : 0;
+    if (P->fixed) {
+        const int64_t items_cap = static_cast<int64_t>(P->ncta) + static_cast<int64_t>(shape->max_reqs) * P->n_groups;
+        const int64_t merges_cap = static_cast<int64_t>(shape->max_tokens) * P->n_groups;
+        const int64_t slots_cap = shape->max_partial_slots > 0 ? shape->max_partial_slots : items_cap + merges_cap;
+        if (items_cap > INT32_MAX || merges_cap > INT32_MAX || slots_cap > INT32_MAX) return PA_ERR_UNSUPPORTED;
+        P->cap_tokens = shape->max_tokens;
+        P->cap_items = static_cast<int32_t>(items_cap);
+        P->cap_tiles = shape->max_extend_tiles;
+        P->cap_merges = static_cast<int32_t>(merges_cap);
+        P->cap_dequant = P->kv8 && P->cap_tiles > 0 ? shape->max_dequant_blocks : 0;
+        P->cap_slots = static_cast<int32_t>(slots_cap);
+        P->cap_scr_rows = P->kv8 && P->cap_tiles > 0 ? shape->max_reqs : 0;
+        if (static_cast<int64_t>(P->items.size()) > P->cap_items ||
+            static_cast<int64_t>(P->tiles.size()) > P->cap_tiles ||
+            static_cast<int64_t>(P->merges.size()) > P->cap_merges || P->num_scratch_blocks > P->cap_dequant ||
+            P->num_slots > P->cap_slots || scr_rows > P->cap_scr_rows)
+            return PA_ERR_CAPACITY;
+    } else {
+        P->cap_tokens = P->T;
+        P->cap_items = static_cast<int32_t>(P->items.size());
+        P->cap_tiles = static_cast<int32_t>(P->tiles.size());
+        P->cap_merges = static_cast<int32_t>(P->merges.size());
+        P->cap_dequant = P->num_scratch_blocks;
+        P->cap_slots = P->num_slots;
+        P->cap_scr_rows = scr_rows;
+    }
+
     // ------------------------------------------------- workspace layout
+    // (every size below is a capacity: for a fixed-shape plan the layout
+    // depends on the shape only)
     size_t off = kHeader;
     auto place = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes, 16); return o; };
-    P->off_part = place(P->part_offset.size() * sizeof(int32_t));
+    const size_t off_counts = place(kNumCounts * sizeof(int32_t));
+    P->off_part = place(static_cast<size_t>(P->cap_tokens) * P->n_groups * sizeof(int32_t));
     P->off_cta = place(P->cta_begin.size() * sizeof(int32_t));
-    P->off_items = place(P->items.size() * sizeof(DecodeItem));
-    P->off_tiles = place(P->tiles.size() * sizeof(ExtendTile));
-    P->off_merges = place(P->merges.size() * sizeof(MergeRow));
-    P->off_scrtab = place(P->scratch_table.size() * sizeof(int32_t));
-    P->off_dequant = place(P->dequant.size() * sizeof(DequantItem));
+    P->off_items = place(static_cast<size_t>(P->cap_items) * sizeof(DecodeItem));
+    P->off_tiles = place(static_cast<size_t>(P->cap_tiles) * sizeof(ExtendTile));
+    P->off_merges = place(static_cast<size_t>(P->cap_merges) * sizeof(MergeRow));
+    P->off_scrtab = place(static_cast<size_t>(P->cap_scr_rows) * P->max_blocks * sizeof(int32_t));
+    P->off_dequant = place(static_cast<size_t>(P->cap_dequant) * sizeof(DequantItem));
     P->blob_bytes = off - kHeader;
     off = align_up(off, 256);
     P->off_opart = off;
-    off = align_up(off + static_cast<size_t>(P->num_slots) * P->Hq * P->D * sizeof(float), 256);
+    off = align_up(off + static_cast<size_t>(P->cap_slots) * P->Hq * P->D * sizeof(float), 256);
     P->off_ml = off;
-    off = align_up(off + static_cast<size_t>(P->num_slots) * P->Hq * sizeof(float2), 1024);
-    const size_t scratch_bytes = static_cast<size_t>(P->num_scratch_blocks) * kBlockSize * P->Hkv * P->D * 2;
+    off = align_up(off + static_cast<size_t>(P->cap_slots) * P->Hq * sizeof(float2), 1024);
+    const size_t scratch_bytes = static_cast<size_t>(P->cap_dequant) * kBlockSize * P->Hkv * P->D * 2;
     P->off_kscr = off;
     off = align_up(off + scratch_bytes, 1024);
     P->off_vscr = off;
@@ -418,6 +462,9 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d) {
     auto put = [&](size_t at, const void *src, size_t n) {
         if (n) std::memcpy(P->blob.data() + (at - kHeader), src, n);
     };
+    const int32_t counts[kNumCounts] = {static_cast<int32_t>(P->tiles.size()), static_cast<int32_t>(P->merges.size()),
+                                        static_cast<int32_t>(P->dequant.size()), P->T};
+    put(off_counts, counts, sizeof counts);
     put(P->off_part, P->part_offset.data(), P->part_offset.size() * sizeof(int32_t));
     put(P->off_cta, P->cta_begin.data(), P->cta_begin.size() * sizeof(int32_t));
     put(P->off_items, P->items.data(), P->items.size() * sizeof(DecodeItem));
@@ -431,13 +478,13 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d) {
     I.num_tokens = P->T;
     I.num_decode_rows = static_cast<int32_t>(decode_rows.size());
     I.num_extend_rows = static_cast<int32_t>(extend_rows.size());
-    I.num_decode_ctas = static_cast<int32_t>(P->cta_begin.size()) - 1;
+    I.num_decode_ctas = P->ncta;
     I.num_decode_items = static_cast<int32_t>(P->items.size());
     I.num_extend_tiles = static_cast<int32_t>(P->tiles.size());
     I.num_partial_slots = P->num_slots;
     I.num_merge_rows = static_cast<int32_t>(P->merges.size());
-    I.kernels_per_call = (P->items.empty() ? 0 : 1) + (P->tiles.empty() ? 0 : 1) + (P->merges.empty() ? 0 : 1) +
-                         (P->dequant.empty() ? 0 : 1);
+    I.kernels_per_call = (P->ncta > 0 ? 1 : 0) + (P->cap_tiles > 0 ? 1 : 0) + (P->cap_merges > 0 ? 1 : 0) +
+                         (P->cap_dequant > 0 ? 1 : 0);
     I.num_dequant_blocks = P->num_scratch_blocks;
     const int64_t row_bytes = static_cast<int64_t>(P->Hkv) * P->D * 2 * (P->kv8 ? 1 : 2);   // K and V
     for (int32_t r : decode_rows) I.decode_kv_bytes += (d->seq_lens[r] - kb_keys) * row_bytes;
@@ -476,14 +523,24 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 namespace pa {
 
+pa_status prepare_plan(pa_plan_s *P) {
+    if (P->prepared) return PA_OK;
+    if (P->ncta > 0 && prepare_decode(P->D, P->HG, P->kv8) != cudaSuccess) return PA_ERR_CUDA;
+    if (P->cap_tiles > 0 && prepare_extend(P->D) != cudaSuccess) return PA_ERR_CUDA;
+    P->prepared = true;
+    return PA_OK;
+}
+
 pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, const void *value_cache,
                             const int32_t *block_table, void *out, uint8_t *ws, cudaStream_t stream, bool timed) {
     auto rec = [&](int kind, bool start, cudaStream_t st) { return timed ? record(P, kind, start, st) : cudaSuccess; };
     int32_t *err = reinterpret_cast<int32_t *>(ws);
+    const int32_t *counts = reinterpret_cast<const int32_t *>(ws + kHeader);
     const int32_t *part_offset = reinterpret_cast<const int32_t *>(ws + P->off_part);
     float *o_part = reinterpret_cast<float *>(ws + P->off_opart);
     float2 *ml_part = reinterpret_cast<float2 *>(ws + P->off_ml);
     uint16_t *out16 = static_cast<uint16_t *>(out);
+    const int sms = std::max(1, P->num_sms);
 
     CUtensorMap tm_k, tm_v;
     const uint64_t rows = static_cast<uint64_t>(P->num_blocks) * kBlockSize;
@@ -493,7 +550,7 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
                   !make_map(&tm_v, value_cache, P->D, P->Hkv, rows, 1, kBlockSize)))
         return PA_ERR_CUDA;
 
-    if (!P->tiles.empty()) {
+    if (P->cap_tiles > 0) {
         // E4M3: the tiles read bf16 copies of their blocks, made here
         CUtensorMap tm_tk = tm_k, tm_tv = tm_v;
         const int32_t *tile_table = block_table;
@@ -507,20 +564,20 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
             qp.block_table = block_table;
             qp.items = reinterpret_cast<const DequantItem *>(ws + P->off_dequant);
             qp.err = err;
-            qp.num_items = static_cast<int32_t>(P->dequant.size());
+            qp.counts = counts;
             qp.max_blocks = P->max_blocks;
             qp.num_blocks = P->num_blocks;
             qp.block_elems = kBlockSize * P->Hkv * P->D;
-            if (launch_dequant(qp, stream) != cudaSuccess) return PA_ERR_CUDA;
-            const uint64_t srows = static_cast<uint64_t>(P->num_scratch_blocks) * kBlockSize;
+            if (launch_dequant(std::min(P->cap_dequant, 8 * sms), qp, stream) != cudaSuccess) return PA_ERR_CUDA;
+            const uint64_t srows = static_cast<uint64_t>(std::max(1, P->cap_dequant)) * kBlockSize;
             if (!make_map(&tm_tk, ws + P->off_kscr, P->D, P->Hkv, srows, 1, kBlockSize) ||
                 !make_map(&tm_tv, ws + P->off_vscr, P->D, P->Hkv, srows, 1, kBlockSize))
                 return PA_ERR_CUDA;
             tile_table = reinterpret_cast<const int32_t *>(ws + P->off_scrtab);
-            tile_blocks = P->num_scratch_blocks;
+            tile_blocks = P->cap_dequant;
         }
         CUtensorMap tm_q;
-        if (!make_map(&tm_q, q, P->D, P->Hq, P->T, P->G, kTileRows / P->G)) return PA_ERR_CUDA;
+        if (!make_map(&tm_q, q, P->D, P->Hq, std::max(1, P->cap_tokens), P->G, kTileRows / P->G)) return PA_ERR_CUDA;
         ExtendParams ep{};
         ep.out = out16;
         ep.block_table = tile_table;
@@ -529,7 +586,7 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
         ep.o_part = o_part;
         ep.ml_part = ml_part;
         ep.err = err;
-        ep.num_tiles = static_cast<int32_t>(P->tiles.size());
+        ep.counts = counts;
         ep.max_blocks = P->max_blocks;
         ep.num_blocks = tile_blocks;
         ep.num_heads_q = P->Hq;
@@ -539,10 +596,10 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
         ep.scale_log2 = P->scale_log2;
         ep.out_scale = P->out_scale;
         if (rec(1, true, stream) != cudaSuccess) return PA_ERR_CUDA;
-        if (launch_extend(P->D, tm_q, tm_tk, tm_tv, ep, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_extend(P->D, P->cap_tiles, tm_q, tm_tk, tm_tv, ep, stream) != cudaSuccess) return PA_ERR_CUDA;
         if (rec(1, false, stream) != cudaSuccess) return PA_ERR_CUDA;
     }
-    if (!P->items.empty()) {
+    if (P->ncta > 0) {
         DecodeParams dp{};
         dp.q = static_cast<const uint16_t *>(q);
         dp.out = out16;
@@ -560,22 +617,23 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
         dp.n_groups = P->n_groups;
         dp.scale_log2 = P->scale_log2;
         dp.out_scale = P->out_scale;
-        const int ncta = static_cast<int>(P->cta_begin.size()) - 1;
         if (rec(0, true, stream) != cudaSuccess) return PA_ERR_CUDA;
-        if (launch_decode(P->D, P->HG, P->kv8, ncta, tm_k, tm_v, dp, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_decode(P->D, P->HG, P->kv8, P->ncta, tm_k, tm_v, dp, stream) != cudaSuccess) return PA_ERR_CUDA;
         if (rec(0, false, stream) != cudaSuccess) return PA_ERR_CUDA;
     }
-    if (!P->merges.empty()) {
+    if (P->cap_merges > 0) {
         MergeParams mp{};
         mp.out = out16;
         mp.rows = reinterpret_cast<const MergeRow *>(ws + P->off_merges);
         mp.o_part = o_part;
         mp.ml_part = ml_part;
-        mp.num_rows = static_cast<int32_t>(P->merges.size());
+        mp.counts = counts;
         mp.num_heads_q = P->Hq;
         mp.max_heads = P->HG * P->G;
+        const int64_t warps = static_cast<int64_t>(P->cap_merges) * mp.max_heads;   // 8 warps per CTA
+        const int grid = static_cast<int>(std::min<int64_t>((warps + 7) / 8, 16 * sms));
         if (rec(2, true, stream) != cudaSuccess) return PA_ERR_CUDA;
-        if (launch_merge(P->D, mp, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_merge(P->D, grid, mp, stream) != cudaSuccess) return PA_ERR_CUDA;
         if (rec(2, false, stream) != cudaSuccess) return PA_ERR_CUDA;
     }
     return PA_OK;
@@ -593,6 +651,7 @@ const char *pa_status_string(pa_status s) {
         case PA_ERR_CUDA: return "CUDA runtime error";
         case PA_ERR_DEVICE_CHECK: return "device-side check failed";
         case PA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case PA_ERR_CAPACITY: return "step exceeds the plan's fixed capacity";
     }
     return "unknown status";
 }
@@ -604,7 +663,31 @@ pa_status pa_plan(const pa_batch_desc *desc, pa_plan_t **out, size_t *workspace_
     if (st != PA_OK) return st;
     pa_plan_s *P = new (std::nothrow) pa_plan_s();
     if (!P) return PA_ERR_INVALID_ARGUMENT;
-    st = build_plan(P, desc);
+    st = build_plan(P, desc, nullptr);
+    if (st != PA_OK) {
+        delete P;
+        return st;
+    }
+    *out = P;
+    *workspace_bytes = P->ws_bytes;
+    return PA_OK;
+}
+
+pa_status pa_plan_fixed(const pa_batch_desc *desc, const pa_fixed_shape *shape, pa_plan_t **out,
+                        size_t *workspace_bytes) {
+    if (out) *out = nullptr;
+    if (desc == nullptr || shape == nullptr || out == nullptr || workspace_bytes == nullptr)
+        return PA_ERR_INVALID_ARGUMENT;
+    if (shape->max_tokens <= 0 || shape->max_reqs <= 0 || shape->max_extend_tiles < 0 ||
+        shape->max_dequant_blocks < 0 || shape->max_partial_slots < 0)
+        return PA_ERR_INVALID_ARGUMENT;
+    pa_status st = validate(desc);
+    if (st != PA_OK) return st;
+    if (desc->kv_cache_dtype == PA_KV_FP8_E4M3 && shape->max_extend_tiles > 0 && shape->max_dequant_blocks == 0)
+        return PA_ERR_INVALID_ARGUMENT;   // FP8 tiles read bf16 copies: they need room
+    pa_plan_s *P = new (std::nothrow) pa_plan_s();
+    if (!P) return PA_ERR_INVALID_ARGUMENT;
+    st = build_plan(P, desc, shape);
     if (st != PA_OK) {
         delete P;
         return st;
@@ -672,34 +755,92 @@ pa_status pa_write_kv_fp8(const void *key, const void *value, const int64_t *slo
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-pa_status pa_attention(const pa_plan_t *plan, const void *q, const void *key_cache, const void *value_cache,
-                       const int32_t *block_table, void *out, void *workspace, size_t workspace_bytes,
-                       void *stream_) {
-    if (!plan) return PA_ERR_INVALID_ARGUMENT;
-    pa_plan_s *P = const_cast<pa_plan_s *>(plan);
-    if (P->T == 0) return PA_OK;
+namespace {
+
+pa_status check_launch_args(const pa_plan_s *P, const void *q, const void *key_cache, const void *value_cache,
+                            const int32_t *block_table, const void *out, const void *workspace,
+                            size_t workspace_bytes) {
     if (!q || !key_cache || !value_cache || !block_table || !out || !workspace) return PA_ERR_INVALID_ARGUMENT;
     if (!aligned(workspace, 256) || !aligned(q, 16) || !aligned(out, 16) || !aligned(key_cache, 16) ||
         !aligned(value_cache, 16) || !aligned(block_table, 4))
         return PA_ERR_INVALID_ARGUMENT;
     if (workspace_bytes < P->ws_bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
+    return PA_OK;
+}
+
+// metadata upload (pinned, stream ordered); the caller holds P->mu
+pa_status upload(pa_plan_s *P, uint8_t *ws, cudaStream_t stream, bool timed) {
+    if (!P->blob_bytes) return PA_OK;
+    if (!P->pinned) {
+        if (!staging().acquire(P->blob_bytes, &P->pinned, &P->pinned_cap, &P->upload_evt)) return PA_ERR_CUDA;
+        std::memcpy(P->pinned, P->blob.data(), P->blob_bytes);
+    }
+    if (timed && record(P, 3, true, stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaMemcpyAsync(ws + kHeader, P->pinned, P->blob_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (timed && record(P, 3, false, stream) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaEventRecord(P->upload_evt, stream) != cudaSuccess) return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+}  // namespace
+
+pa_status pa_attention(const pa_plan_t *plan, const void *q, const void *key_cache, const void *value_cache,
+                       const int32_t *block_table, void *out, void *workspace, size_t workspace_bytes,
+                       void *stream_) {
+    if (!plan) return PA_ERR_INVALID_ARGUMENT;
+    pa_plan_s *P = const_cast<pa_plan_s *>(plan);
+    if (P->T == 0 && !P->fixed) return PA_OK;
+    pa_status st = check_launch_args(P, q, key_cache, value_cache, block_table, out, workspace, workspace_bytes);
+    if (st != PA_OK) return st;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     std::lock_guard<std::mutex> lock(P->mu);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-
-    // metadata upload (pinned, stream ordered)
-    if (P->blob_bytes) {
-        if (!P->pinned) {
-            if (!staging().acquire(P->blob_bytes, &P->pinned, &P->pinned_cap, &P->upload_evt)) return PA_ERR_CUDA;
-            std::memcpy(P->pinned, P->blob.data(), P->blob_bytes);
-        }
-        if (record(P, 3, true, stream) != cudaSuccess) return PA_ERR_CUDA;
-        if (cudaMemcpyAsync(ws + kHeader, P->pinned, P->blob_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-            return PA_ERR_CUDA;
-        if (record(P, 3, false, stream) != cudaSuccess) return PA_ERR_CUDA;
-        if (cudaEventRecord(P->upload_evt, stream) != cudaSuccess) return PA_ERR_CUDA;
-    }
+    if ((st = prepare_plan(P)) != PA_OK) return st;
+    if ((st = upload(P, ws, stream, true)) != PA_OK) return st;
     return enqueue_attention(P, q, key_cache, value_cache, block_table, out, ws, stream, true);
+}
+
+pa_status pa_upload_metadata(const pa_plan_t *plan, void *workspace, size_t workspace_bytes, void *stream_) {
+    if (!plan || !workspace) return PA_ERR_INVALID_ARGUMENT;
+    pa_plan_s *P = const_cast<pa_plan_s *>(plan);
+    if (!aligned(workspace, 256)) return PA_ERR_INVALID_ARGUMENT;
+    if (workspace_bytes < P->ws_bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
+    std::lock_guard<std::mutex> lock(P->mu);
+    pa_status st = prepare_plan(P);
+    if (st != PA_OK) return st;
+    return upload(P, static_cast<uint8_t *>(workspace), static_cast<cudaStream_t>(stream_), false);
+}
+
+pa_status pa_attention_launch(const pa_plan_t *plan, const void *q, const void *key_cache, const void *value_cache,
+                              const int32_t *block_table, void *out, void *workspace, size_t workspace_bytes,
+                              void *stream_) {
+    if (!plan) return PA_ERR_INVALID_ARGUMENT;
+    pa_plan_s *P = const_cast<pa_plan_s *>(plan);
+    if (P->T == 0 && !P->fixed) return PA_OK;
+    pa_status st = check_launch_args(P, q, key_cache, value_cache, block_table, out, workspace, workspace_bytes);
+    if (st != PA_OK) return st;
+    std::lock_guard<std::mutex> lock(P->mu);
+    if ((st = prepare_plan(P)) != PA_OK) return st;
+    return enqueue_attention(P, q, key_cache, value_cache, block_table, out, static_cast<uint8_t *>(workspace),
+                             static_cast<cudaStream_t>(stream_), false);
+}
+
+pa_status pa_zero_blocks(const int32_t *block_ids, int32_t num_ids, int32_t num_blocks, int32_t num_heads_kv,
+                         int32_t head_dim, int32_t kv_cache_dtype, void *key_cache, void *value_cache,
+                         int32_t *device_error_word, void *stream) {
+    if (num_ids < 0 || num_blocks < 0 || num_heads_kv <= 0 || head_dim <= 0) return PA_ERR_INVALID_ARGUMENT;
+    if (kv_cache_dtype != PA_KV_BF16 && kv_cache_dtype != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARGUMENT;
+    if (num_ids == 0) return PA_OK;
+    if (!block_ids || !key_cache || !value_cache || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
+        !aligned(block_ids, 4))
+        return PA_ERR_INVALID_ARGUMENT;
+    const int64_t block_bytes =
+        static_cast<int64_t>(kBlockSize) * num_heads_kv * head_dim * (kv_cache_dtype == PA_KV_FP8_E4M3 ? 1 : 2);
+    if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    cudaError_t e = launch_zero_blocks(block_ids, num_ids, num_blocks, block_bytes, key_cache, value_cache,
+                                       device_error_word, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 pa_status pa_check_device_errors(int32_t *word, int32_t *bits, void *stream_) {

@@ -114,7 +114,7 @@ struct ExtendParams {
     float *o_part;
     float2 *ml_part;
     int32_t *err;
-    int32_t num_tiles;
+    const int32_t *counts;      // device work counts (MetaCounts); CTAs past the tile count exit
     int32_t max_blocks;
     int32_t num_blocks;
     int32_t num_heads_q;
@@ -141,7 +141,7 @@ struct DequantParams {
     const int32_t *block_table;
     const DequantItem *items;
     int32_t *err;
-    int32_t num_items;
+    const int32_t *counts;      // device work counts (MetaCounts)
     int32_t max_blocks;
     int32_t num_blocks;
     int32_t block_elems;        // 16 * Hkv * D
@@ -152,10 +152,14 @@ struct MergeParams {
     const MergeRow *rows;
     const float *o_part;
     const float2 *ml_part;
-    int32_t num_rows;
+    const int32_t *counts;      // device work counts (MetaCounts)
     int32_t num_heads_q;
     int32_t max_heads;          // largest hq_count of any row
 };
+
+// Work counts at the head of the uploaded metadata: kernels launched on a
+// grid sized for a capacity read their real counts here.
+enum MetaCount : int { kCountTiles = 0, kCountMerges = 1, kCountDequant = 2, kCountTokens = 3, kNumCounts = 4 };
 
 // Launchers (each returns the launch's cudaError_t).
 cudaError_t launch_slot_mapping(const int32_t *qsl, const int32_t *num_computed,
@@ -169,13 +173,23 @@ cudaError_t launch_write_kv(const void *key, const void *value, const int64_t *s
 cudaError_t launch_write_kv_fp8(const void *key, const void *value, const int64_t *slots, int32_t num_tokens,
                                 int32_t row_elems, void *key_cache, void *value_cache, int64_t num_slots,
                                 float k_scale, float v_scale, int32_t *err, cudaStream_t stream);
-cudaError_t launch_dequant(const DequantParams &p, cudaStream_t stream);
+// The grid-sized launchers take the CTA count to launch; kernels read their
+// real work counts from the device (MetaCount), so a grid sized for a
+// capacity is as correct as an exact one.
+cudaError_t launch_dequant(int grid, const DequantParams &p, cudaStream_t stream);
 // Decode kernel: head_dim D, heads per CTA hg, E4M3 caches (kv8).  Returns
 // cudaErrorInvalidValue for an unsupported combination.
 cudaError_t launch_decode(int head_dim, int hg, bool kv8, int num_ctas, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const DecodeParams &p, cudaStream_t stream);
-cudaError_t launch_extend(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+cudaError_t launch_extend(int head_dim, int grid, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const ExtendParams &p, cudaStream_t stream);
-cudaError_t launch_merge(int head_dim, const MergeParams &p, cudaStream_t stream);
+cudaError_t launch_merge(int head_dim, int grid, const MergeParams &p, cudaStream_t stream);
+// Zero the K and V entries of the listed blocks (ids < 0 skipped).
+cudaError_t launch_zero_blocks(const int32_t *ids, int32_t num_ids, int32_t num_blocks, int64_t block_bytes,
+                               void *key_cache, void *value_cache, int32_t *err, cudaStream_t stream);
+// One-time per-process kernel attributes (dynamic shared memory sizes) of the
+// kernels a plan launches, so that later launches can be captured.
+cudaError_t prepare_decode(int head_dim, int hg, bool kv8);
+cudaError_t prepare_extend(int head_dim);
 
 }  // namespace pa

@@ -31,6 +31,12 @@ struct pa_plan_s {
     size_t off_part = 0, off_cta = 0, off_items = 0, off_tiles = 0, off_merges = 0;
     size_t off_scrtab = 0, off_dequant = 0, off_kscr = 0, off_vscr = 0;
     size_t blob_bytes = 0, off_opart = 0, off_ml = 0, ws_bytes = 0;
+    // launch shape: exact sizes for pa_plan, capacities for pa_plan_fixed
+    bool fixed = false;
+    int32_t ncta = 0;                   // decode CTAs
+    int32_t cap_tokens = 0, cap_items = 0, cap_tiles = 0, cap_merges = 0, cap_dequant = 0;
+    int32_t cap_slots = 0, cap_scr_rows = 0;
+    bool prepared = false;              // kernel attributes set (pa_upload_metadata)
     std::vector<uint8_t> blob;          // host image of the metadata blob
     void *pinned = nullptr;             // pinned staging copy used for async uploads
     size_t pinned_cap = 0;
@@ -58,7 +64,12 @@ bool make_map_u8(CUtensorMap *tm, const void *ptr, uint64_t d, uint64_t mid, uin
 // Enqueue every kernel of one attention call on `stream`; the metadata blob
 // must already be (or be about to be, in stream order) at ws + header.
 // `timed` records the plan's per-kernel timing events when they are enabled.
+// For a fixed-shape plan every launch and argument depends on the plan's
+// capacities only.
 pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, const void *value_cache,
                             const int32_t *block_table, void *out, uint8_t *ws, cudaStream_t stream, bool timed);
+
+// Set the kernel attributes the plan's launches need (once per plan).
+pa_status prepare_plan(pa_plan_s *P);
 
 }  // namespace pa

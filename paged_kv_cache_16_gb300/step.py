@@ -4,6 +4,7 @@ Thin glue over the C ABI; torch only allocates memory and supplies streams.
 """
 from __future__ import annotations
 
+import numpy as np
 import torch
 
 from . import binding
@@ -68,6 +69,117 @@ class DeviceStep:
         self.slot_mapping(stream)
         self.write(key, value, key_cache, value_cache, stream)
         return self.attend(q, key_cache, value_cache, stream)
+
+    def check_errors(self, stream=None) -> int:
+        return binding.pa_check_device_errors(self.error_word, stream)
+
+
+class GraphStep:
+    """Engine steps replayed from one CUDA graph (fixed-shape plans).
+
+    Graph mode as the page "vLLM 源码完全拆解（十六）" (fourth walk-through)
+    describes it: the execution of a stable shape is captured once; for every
+    step the new data is copied to the same addresses and the graph replayed,
+    with request counts rounded up to a capture size and spare rows padded.
+    Static buffers hold max_tokens rows of q / key / value / out and max_reqs
+    rows of metadata; padding requests have no tokens, so padding tokens get
+    slot -1 and are neither written nor attended.  The graph holds slot
+    mapping, cache write and the attention kernels of pa_attention_launch;
+    the per-step metadata upload (pa_upload_metadata) precedes each replay.
+    """
+
+    def __init__(self, *, num_heads_q, num_heads_kv, head_dim, num_blocks, max_blocks_per_req, softmax_scale,
+                 max_tokens, max_reqs, max_extend_tiles=0, max_dequant_blocks=0, max_partial_slots=0,
+                 kv_cache_dtype="bf16", k_scale=1.0, v_scale=1.0, num_sms=0, device="cuda"):
+        dev = torch.device(device)
+        self.device = dev
+        self.model = dict(num_heads_q=num_heads_q, num_heads_kv=num_heads_kv, head_dim=head_dim,
+                          num_blocks=num_blocks, max_blocks_per_req=max_blocks_per_req,
+                          softmax_scale=softmax_scale, num_sms=num_sms,
+                          kv_cache_dtype=binding.PA_KV_FP8_E4M3 if kv_cache_dtype == "fp8" else binding.PA_KV_BF16,
+                          k_scale=k_scale, v_scale=v_scale)
+        self.shape = dict(max_tokens=max_tokens, max_reqs=max_reqs, max_extend_tiles=max_extend_tiles,
+                          max_dequant_blocks=max_dequant_blocks, max_partial_slots=max_partial_slots)
+        self.fp8 = kv_cache_dtype == "fp8"
+        self.k_scale, self.v_scale = k_scale, v_scale
+        self.q = torch.zeros(max_tokens, num_heads_q, head_dim, dtype=torch.bfloat16, device=dev)
+        self.key = torch.zeros(max_tokens, num_heads_kv, head_dim, dtype=torch.bfloat16, device=dev)
+        self.value = torch.zeros_like(self.key)
+        self.out = torch.zeros_like(self.q)
+        self.qsl = torch.zeros(max_reqs + 1, dtype=torch.int32, device=dev)
+        self.num_computed = torch.zeros(max_reqs, dtype=torch.int32, device=dev)
+        self.block_table = torch.zeros(max_reqs, max_blocks_per_req, dtype=torch.int32, device=dev)
+        self.slots = torch.zeros(max_tokens, dtype=torch.int64, device=dev)
+        self.workspace = None
+        self.graph = None
+        self.caches = None
+
+    def make_plan(self, batch: Batch) -> binding.Plan:
+        bt = batch.block_table
+        mb = self.model["max_blocks_per_req"]
+        if bt.shape[1] != mb:                      # host copy with the static row stride
+            padded = np.zeros((bt.shape[0], mb), dtype=np.int32)
+            padded[:, :bt.shape[1]] = bt
+            bt = padded
+        return binding.pa_plan_fixed(**self.shape, query_start_loc=batch.query_start_loc, seq_lens=batch.seq_lens,
+                                     num_computed_tokens=batch.num_computed, block_table_host=bt,
+                                     num_common_prefix_blocks=batch.num_common_prefix_blocks, **self.model)
+
+    @property
+    def error_word(self) -> torch.Tensor:
+        return self.workspace[:4].view(torch.int32)
+
+    def load(self, batch: Batch, plan: binding.Plan, q=None, key=None, value=None, stream=None):
+        """Copy a step's metadata (and, if given, its new q / key / value rows)
+        into the static buffers and upload the plan's metadata (not captured)."""
+        R, T = batch.num_reqs, batch.num_tokens
+        mr, mb = self.num_computed.numel(), self.block_table.shape[1]
+        qsl = np.full(mr + 1, T, dtype=np.int32)
+        qsl[:R + 1] = batch.query_start_loc
+        nc = np.zeros(mr, dtype=np.int32)
+        nc[:R] = batch.num_computed
+        bt = np.zeros((mr, mb), dtype=np.int32)
+        bt[:R, :batch.block_table.shape[1]] = batch.block_table
+        self.qsl.copy_(torch.from_numpy(qsl))
+        self.num_computed.copy_(torch.from_numpy(nc))
+        self.block_table.copy_(torch.from_numpy(bt))
+        for dst, src in ((self.q, q), (self.key, key), (self.value, value)):
+            if src is not None:
+                dst[:T].copy_(src)
+        if self.workspace is None:
+            self.workspace = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device=self.device)
+        binding.pa_upload_metadata(plan, self.workspace, stream)
+
+    def enqueue(self, plan: binding.Plan, key_cache, value_cache, stream=None):
+        """Slot mapping, cache write and attention over the static buffers
+        (every launch sized by the capacities; capturable)."""
+        binding.pa_slot_mapping(self.qsl, self.num_computed, self.block_table, self.slots.numel(), self.slots,
+                                stream=stream)
+        if self.fp8:
+            binding.pa_write_kv_fp8(self.key, self.value, self.slots, key_cache, value_cache, self.k_scale,
+                                    self.v_scale, self.error_word, stream)
+        else:
+            binding.pa_write_kv(self.key, self.value, self.slots, key_cache, value_cache, self.error_word, stream)
+        binding.pa_attention_launch(plan, self.q, key_cache, value_cache, self.block_table, self.out,
+                                    self.workspace, stream)
+
+    def capture(self, plan: binding.Plan, key_cache, value_cache):
+        """Capture enqueue() once; the caches are part of the graph."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.enqueue(plan, key_cache, value_cache)
+        self.graph, self.caches = g, (key_cache.data_ptr(), value_cache.data_ptr())
+
+    def run(self, batch: Batch, q, key, value, key_cache, value_cache) -> torch.Tensor:
+        """One step: plan, copy in, replay (capturing on first use)."""
+        plan = self.make_plan(batch)
+        self.load(batch, plan, q, key, value)
+        if self.graph is None:
+            self.capture(plan, key_cache, value_cache)
+        elif self.caches != (key_cache.data_ptr(), value_cache.data_ptr()):
+            raise ValueError("a captured step replays on the caches it was captured with")
+        self.graph.replay()
+        return self.out[:batch.num_tokens]
 
     def check_errors(self, stream=None) -> int:
         return binding.pa_check_device_errors(self.error_word, stream)

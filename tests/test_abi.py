@@ -34,8 +34,8 @@ def test_header_symbols_exported(lib):
 
 
 def test_status_strings(lib):
-    for s in range(6):
-        assert binding.status_string(s)
+    for s in range(7):
+        assert binding.status_string(s) != "unknown status"
     assert binding.status_string(99) == "unknown status"
 
 
@@ -201,3 +201,74 @@ def test_idle_requests_and_zero_lengths(lib):
               softmax_scale=0.125, num_sms=152)
     info = binding.pa_plan(**kw).info()
     assert info["num_decode_rows"] == 1 and info["num_extend_rows"] == 0 and info["num_tokens"] == 1
+
+
+# ------------------------------------------------------ fixed-shape plans --
+def fixed(batch, **shape):
+    return binding.pa_plan_fixed(**shape, **desc(batch))
+
+
+def test_fixed_plan_layout_depends_on_shape_only(lib):
+    """Plans of one fixed shape have the same workspace size and launches
+    whatever the step's lengths and request count; the decode cut itself is
+    the eager plan's."""
+    shape = dict(max_tokens=96, max_reqs=96)
+    plans = [fixed(workloads.decode(batch=n, lo=lo, hi=hi, num_blocks=4000, seed=n), **shape)
+             for n, lo, hi in ((8, 20, 300), (64, 100, 700), (96, 1, 100), (1, 1, 1))]
+    sizes = {p.workspace_bytes for p in plans}
+    assert len(sizes) == 1
+    for p in plans:
+        i = p.info()
+        assert i["num_decode_ctas"] == 152 and i["kernels_per_call"] == 2
+    b = workloads.decode(batch=64, lo=100, hi=700, num_blocks=4000, seed=64)
+    e, f = binding.pa_plan(**desc(b)).info(), fixed(b, **shape).info()
+    for k in ("num_decode_items", "num_partial_slots", "num_merge_rows", "decode_kv_bytes"):
+        assert e[k] == f[k], k
+
+
+def test_fixed_plan_mixed_shape(lib):
+    """With tile room, extend rows and cascade prefixes fit; the tile and
+    merge launches are always made."""
+    b = workloads.mixed(n_decode=24, n_shared=4, chunk=300, chunk_b_cached=500, lo=100, hi=900)
+    eager = binding.pa_plan(**desc(b)).info()
+    p = fixed(b, max_tokens=1024, max_reqs=64, max_extend_tiles=128)
+    i = p.info()
+    assert i["num_extend_tiles"] == eager["num_extend_tiles"] and i["kernels_per_call"] == 3
+    d = workloads.decode(batch=8, lo=100, hi=700, num_blocks=4000)
+    j = fixed(d, max_tokens=1024, max_reqs=64, max_extend_tiles=128)
+    assert j.info()["kernels_per_call"] == 3 and j.workspace_bytes == p.workspace_bytes
+
+
+@pytest.mark.parametrize("shape,status", [
+    (dict(max_tokens=8, max_reqs=64), binding.PA_ERR_CAPACITY),            # too many tokens
+    (dict(max_tokens=64, max_reqs=4), binding.PA_ERR_CAPACITY),            # too many requests
+    (dict(max_tokens=0, max_reqs=64), binding.PA_ERR_INVALID_ARGUMENT),
+    (dict(max_tokens=64, max_reqs=64, max_extend_tiles=-1), binding.PA_ERR_INVALID_ARGUMENT),
+    (dict(max_tokens=64, max_reqs=64, max_partial_slots=3), binding.PA_ERR_CAPACITY),
+])
+def test_fixed_plan_capacity_errors(lib, shape, status):
+    b = workloads.decode(batch=16, lo=300, hi=900, num_blocks=4000)
+    assert binding.pa_plan_fixed_status(**shape, **desc(b)) == status
+
+
+def test_fixed_plan_tile_capacity(lib):
+    b = workloads.mixed(n_decode=8, n_shared=0, chunk=300, chunk_b_cached=500, lo=100, hi=900)
+    kw = desc(b)
+    assert binding.pa_plan_fixed_status(max_tokens=1024, max_reqs=64, **kw) == binding.PA_ERR_CAPACITY
+    fp8 = dict(kw, kv_cache_dtype=binding.PA_KV_FP8_E4M3, k_scale=0.1, v_scale=0.1)
+    # FP8 tiles read bf16 copies: tile room without block room is malformed
+    assert binding.pa_plan_fixed_status(max_tokens=1024, max_reqs=64, max_extend_tiles=128,
+                                        **fp8) == binding.PA_ERR_INVALID_ARGUMENT
+    assert binding.pa_plan_fixed_status(max_tokens=1024, max_reqs=64, max_extend_tiles=128,
+                                        max_dequant_blocks=4, **fp8) == binding.PA_ERR_CAPACITY
+    assert binding.pa_plan_fixed_status(max_tokens=1024, max_reqs=64, max_extend_tiles=128,
+                                        max_dequant_blocks=4096, **fp8) == binding.PA_OK
+
+
+def test_zero_blocks_argument_checks(lib):
+    """Host-side validation of pa_zero_blocks (no kernel is enqueued)."""
+    L = binding.load()
+    assert L.pa_zero_blocks(None, 0, 10, 8, 128, binding.PA_KV_BF16, None, None, None, None) == binding.PA_OK
+    assert L.pa_zero_blocks(None, -1, 10, 8, 128, 0, None, None, None, None) == binding.PA_ERR_INVALID_ARGUMENT
+    assert L.pa_zero_blocks(None, 1, 10, 8, 128, 0, None, None, None, None) == binding.PA_ERR_INVALID_ARGUMENT
+    assert L.pa_zero_blocks(None, 0, 10, 8, 128, 7, None, None, None, None) == binding.PA_ERR_INVALID_ARGUMENT

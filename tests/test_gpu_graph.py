@@ -1,0 +1,153 @@
+"""Fixed-shape plans and CUDA-graph replays (needs a GB300).
+
+One graph is captured per shape (slot mapping, cache write and the attention
+kernels); every later step of a different size only uploads its metadata and
+replays.  Each replayed step is checked against the oracle (caches bit for
+bit, attention within tolerance) on the cache state it started from, and
+against the eager path (pa_plan + pa_attention) on the same inputs, bit for
+bit: a fixed-shape plan cuts the work exactly as the eager plan does.
+Also here: block zeroing against the oracle.
+"""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_common import assert_close, cache_bits, ensure_library, run_gpu, run_oracle
+from oracle.oracle import default as default_oracle
+from paged_kv_cache_16_gb300 import binding, workloads
+from paged_kv_cache_16_gb300.step import GraphStep
+from paged_kv_cache_16_gb300.workloads import make_batch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_library()
+
+
+def graph_for(b, max_blocks, **shape):
+    return GraphStep(num_heads_q=b.num_heads_q, num_heads_kv=b.num_heads_kv, head_dim=b.head_dim,
+                     num_blocks=b.num_blocks, max_blocks_per_req=max_blocks, softmax_scale=b.softmax_scale,
+                     kv_cache_dtype=b.kv_cache_dtype, k_scale=b.k_scale, v_scale=b.v_scale, **shape)
+
+
+def replay_steps(batches, **shape):
+    """Run every batch through one captured graph on one shared cache pool."""
+    dev = torch.device("cuda")
+    mb = max(b.block_table.shape[1] for b in batches)
+    gs = graph_for(batches[0], mb, **shape)
+    kc = batches[0].key_cache.to(dev, copy=True)
+    vc = batches[0].value_cache.to(dev, copy=True)
+    for b in batches:
+        before = replace(b, key_cache=kc.cpu(), value_cache=vc.cpu())
+        out = gs.run(b, b.q.to(dev), b.key.to(dev), b.value.to(dev), kc, vc).clone()
+        torch.cuda.synchronize()
+        assert gs.check_errors() == 0, b.name
+        okc, ovc, _, oout = run_oracle(before)
+        assert np.array_equal(cache_bits(kc), okc) and np.array_equal(cache_bits(vc), ovc), b.name
+        if b.num_tokens:
+            assert_close(out, oout, what=b.name)
+            eager = run_gpu(before)
+            assert eager.bits == 0
+            assert torch.equal(eager.out, out), f"{b.name}: graph replay differs from the eager path"
+    return gs
+
+
+def decode_steps(kv="bf16"):
+    """Three decode steps on one 3000-block pool: 40, 17 and 48 requests."""
+    out = []
+    for i, (n, lo, hi) in enumerate(((40, 1, 700), (17, 300, 2000), (48, 1, 64))):
+        b = workloads.decode(batch=n, lo=lo, hi=hi, num_blocks=3000, seed=60 + i, kv_cache_dtype=kv)
+        out.append(replace(b, name=f"decode-step{i}"))
+    return out
+
+
+def test_graph_replay_decode_steps():
+    replay_steps(decode_steps(), max_tokens=48, max_reqs=48)
+
+
+def test_graph_replay_decode_steps_fp8():
+    replay_steps(decode_steps("fp8"), max_tokens=48, max_reqs=48)
+
+
+def mixed_steps(kv="bf16"):
+    """Decodes with chunked prefills of changing size (and a step of decodes
+    only) on one 600-block pool, one shape."""
+    specs = [([1, 1, 37, 1, 129, 1], [300, 77, 37, 512, 400, 19]),
+             ([200, 1, 1, 3], [1000, 64, 1, 500]),
+             ([1, 1, 1], [90, 1, 700]),
+             ([64, 1, 300, 1, 2], [64, 33, 700, 16, 17])]
+    out = []
+    for i, (ql, sl) in enumerate(specs):
+        out.append(make_batch(name=f"mixed-step{i}", num_heads_q=32, num_heads_kv=8, head_dim=128, q_lens=ql,
+                              seq_lens=sl, num_blocks=600, seed=70 + i, max_blocks_per_req=64,
+                              kv_cache_dtype=kv))
+    return out
+
+
+def test_graph_replay_mixed_steps():
+    replay_steps(mixed_steps(), max_tokens=512, max_reqs=8, max_extend_tiles=64)
+
+
+def test_graph_replay_mixed_steps_fp8():
+    replay_steps(mixed_steps("fp8"), max_tokens=512, max_reqs=8, max_extend_tiles=64, max_dequant_blocks=256)
+
+
+def test_graph_replay_cascade_steps():
+    """Cascade steps (shared prefix, batch-wide n) of two sizes in one shape;
+    prefix splits need explicit partial-slot room."""
+    steps = []
+    for i, (n, nb) in enumerate(((24, 16), (9, 8))):
+        steps.append(replace(workloads.cascade(batch=n, prefix_tokens=16 * nb, lo=1, hi=200, num_blocks=700,
+                                               seed=80 + i), name=f"cascade-step{i}"))
+    replay_steps(steps, max_tokens=24, max_reqs=24, max_extend_tiles=256, max_partial_slots=24 * 160)
+
+
+def test_fixed_plan_eager_equals_plain_plan():
+    """pa_attention with a fixed-shape plan (no graph) is the eager result bit for bit."""
+    dev = torch.device("cuda")
+    b = workloads.mixed(n_decode=20, n_shared=4, shared_tokens=64, lo=65, hi=700, chunk=200, chunk_b_cached=300,
+                        seed=90)
+    ref = run_gpu(b)
+    gs = graph_for(b, b.block_table.shape[1], max_tokens=1024, max_reqs=64, max_extend_tiles=256)
+    plan = gs.make_plan(b)
+    kc, vc = b.key_cache.to(dev, copy=True), b.value_cache.to(dev, copy=True)
+    gs.load(b, plan, b.q.to(dev), b.key.to(dev), b.value.to(dev))
+    gs.enqueue(plan, kc, vc)
+    torch.cuda.synchronize()
+    assert gs.check_errors() == 0
+    assert torch.equal(gs.out[:b.num_tokens], ref.out)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_zero_blocks(kv):
+    """pa_zero_blocks against the oracle: listed blocks zero, the rest
+    untouched, -1 skipped, an id past the cache reported."""
+    dev = torch.device("cuda")
+    nb, hkv, d = 40, 8, 128
+    g = torch.Generator().manual_seed(5)
+    if kv == "fp8":
+        kc = torch.randint(1, 256, (nb, 16, hkv, d), generator=g, dtype=torch.uint8)
+        vc = torch.randint(1, 256, (nb, 16, hkv, d), generator=g, dtype=torch.uint8)
+        okc, ovc = kc.numpy().copy(), vc.numpy().copy()
+    else:
+        kc = torch.randn(nb, 16, hkv, d, generator=g).to(torch.bfloat16)
+        vc = torch.randn(nb, 16, hkv, d, generator=g).to(torch.bfloat16)
+        okc, ovc = workloads.bf16_bits(kc).copy(), workloads.bf16_bits(vc).copy()
+    ids = np.array([7, -1, 0, 39, 7, 12], dtype=np.int32)
+    assert default_oracle().zero_blocks(ids, okc, ovc) == 0
+    gkc, gvc = kc.to(dev), vc.to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    binding.pa_zero_blocks(torch.as_tensor(ids, device=dev), gkc, gvc, err)
+    torch.cuda.synchronize()
+    assert binding.pa_check_device_errors(err) == 0
+    assert np.array_equal(cache_bits(gkc), okc) and np.array_equal(cache_bits(gvc), ovc)
+    bad = torch.tensor([3, nb], dtype=torch.int32, device=dev)
+    binding.pa_zero_blocks(bad, gkc, gvc, err)
+    assert binding.pa_check_device_errors(err) & binding.PA_DEVERR_BLOCK_RANGE
+    assert not gkc[3].any() and not gvc[3].any()
