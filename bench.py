@@ -256,6 +256,15 @@ def run_reference(args, world, rank):
 
 # --------------------------------------------------------------------- ours --
 
+def step_desc(graph_mode: bool, fused: bool) -> str:
+    body = "pa_attention_with_kv_update" if fused else "pa_slot_mapping + pa_write_kv + pa_attention"
+    if graph_mode:
+        body = ("pa_attention_with_kv_update_launch" if fused else
+                "pa_slot_mapping + pa_write_kv + pa_attention_launch")
+        return f"pa_plan_fixed (host) + pa_upload_metadata + CUDA-graph replay of {body}"
+    return f"pa_plan (host) + {body}"
+
+
 def run_ours(args, world, rank, local):
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device (the CUDA library has no CPU path)")
@@ -280,14 +289,19 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     info = st.plan.info()
 
+    fused = args.write == "fused"
+
     def one_step(plans, timing):
         plan = st.make_plan()
         if timing:
             plan.enable_timing(True)
         plans.append(plan)
-        st.slot_mapping(stream)
-        st.write(key, value, kc, vc, stream)
-        st.attend(q, kc, vc, stream, plan=plan)
+        if fused:
+            st.run_fused(q, key, value, kc, vc, stream, plan=plan)
+        else:
+            st.slot_mapping(stream)
+            st.write(key, value, kc, vc, stream)
+            st.attend(q, kc, vc, stream, plan=plan)
 
     keep = []
     for _ in range(args.warmup):
@@ -327,7 +341,11 @@ def run_ours(args, world, rank, local):
         for k in range(4):
             k_ms[k] += t[k]
             k_n[k] += n[k]
-    launches = args.steps * (2 + info["kernels_per_call"])
+    # our kernels per step: the attention call's, the upload kernel, and the
+    # separate slot-mapping + write launches (fused: one extend write kernel
+    # when the step has extend rows)
+    per_step = info["kernels_per_call"] + 1 + ((1 if info["num_extend_rows"] else 0) if fused else 2)
+    launches = args.steps * per_step
     plans.clear()
 
     hbm, bf16, bf16_sus, peak_src = measured_peaks()
@@ -375,7 +393,7 @@ def run_ours(args, world, rank, local):
                    softmax_scale=batch.softmax_scale, max_tokens=max(T, 1), max_reqs=max(batch.num_reqs, 1),
                    max_extend_tiles=info["num_extend_tiles"], max_dequant_blocks=info["num_dequant_blocks"],
                    max_partial_slots=max(info["num_partial_slots"], 1), kv_cache_dtype=batch.kv_cache_dtype,
-                   k_scale=batch.k_scale, v_scale=batch.v_scale, device=dev)
+                   k_scale=batch.k_scale, v_scale=batch.v_scale, device=dev, fused=fused)
     first = gs.make_plan(batch)
     gs.load(batch, first, q, key, value)
     gs.capture(first, kc, vc)
@@ -446,9 +464,12 @@ def run_ours(args, world, rank, local):
             for d_, h_ in zip(meta_d, meta_h):
                 d_.copy_(h_, non_blocking=True)
             plan = st.make_plan()
-            st.slot_mapping(stream)
-            st.write(key, value, kc, vc, stream)
-            st.attend(q, kc, vc, stream, plan=plan)
+            if fused:
+                st.run_fused(q, key, value, kc, vc, stream, plan=plan)
+            else:
+                st.slot_mapping(stream)
+                st.write(key, value, kc, vc, stream)
+                st.attend(q, kc, vc, stream, plan=plan)
             out_h[:T].copy_(st.out[:T], non_blocking=True)
         torch.cuda.synchronize(dev)
         if i >= 2:
@@ -475,9 +496,7 @@ def run_ours(args, world, rank, local):
             "config": {"workload": desc, "name": args.workload, "tokens_per_step": T, "seed": args.seed,
                        "kv_cache_dtype": args.kv_dtype,
                        "l2": "flushed between timed steps (256 MiB write + read-back, outside the step events)",
-                       "step": ("pa_plan_fixed (host) + pa_upload_metadata + CUDA-graph replay of pa_slot_mapping, "
-                                "pa_write_kv and pa_attention_launch") if graph_mode else
-                               "pa_plan (host) + pa_slot_mapping + pa_write_kv + pa_attention",
+                       "step": step_desc(graph_mode, fused), "write": args.write,
                        "launch": args.launch, "modes": modes,
                        "kernel_times": "eager pass, CUDA events around each launch (same kernels and work cut)",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -503,6 +522,8 @@ def main():
                     help="KV cache element type (fp8 = E4M3 codes with per-tensor scales)")
     ap.add_argument("--launch", choices=["graph", "eager"], default="graph",
                     help="time the step as a CUDA-graph replay (fixed-shape plan) or as eager launches")
+    ap.add_argument("--write", choices=["fused", "separate"], default="fused",
+                    help="cache write inside the attention call (pa_attention_with_kv_update) or as its own launches")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -13,7 +13,10 @@
  *                    token over its request's context, read through the block
  *                    table; decode rows, chunked-prefill/extend rows, prefix
  *                    hits and the shared-prefix (cascade) route;
- *   pa_zero_blocks   device: clear newly allocated cache blocks (§4, §5.1.1).
+ *   pa_zero_blocks   device: clear newly allocated cache blocks (§4, §5.1.1);
+ *   pa_attention_with_kv_update
+ *                    device: the cache write and attention as one call (§6.1,
+ *                    fused dispatch).
  *
  * Fixed-shape plans (pa_plan_fixed) make the attention launches of a step a
  * function of capacities only, so that they can be captured once in a CUDA
@@ -288,6 +291,35 @@ pa_status pa_upload_metadata(const pa_plan_t *plan, void *workspace, size_t work
 pa_status pa_attention_launch(const pa_plan_t *plan, const void *q, const void *key_cache,
                               const void *value_cache, const int32_t *block_table, void *out,
                               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The step's cache write and attention in one call: the fused dispatch of
+ * "vLLM 推理流程分析" §6.1 (the attention layer's forward includes the KV-cache
+ * update instead of a separate unified_kv_cache_update).  The caches end up
+ * exactly as pa_slot_mapping + pa_write_kv (bf16) or pa_write_kv_fp8 (E4M3,
+ * with the plan's k_scale / v_scale) would leave them, and out is the result
+ * pa_attention computes over those caches.  A decode row's new K/V row is
+ * stored by the decode kernel itself (and used from on-chip memory); the new
+ * rows of extend rows are stored by one kernel before the tensor-core tiles
+ * read them.  No separate slot-mapping or write launch is needed.
+ *   key, value     DEVICE bf16 [T][Hkv][D] (16-byte aligned): the new rows
+ *   key_cache,
+ *   value_cache    written (the new slots) and read
+ *   slot_mapping   optional DEVICE int64 [T]: receives every token's slot
+ * Other arguments, errors and ordering as for pa_attention (a block id out of
+ * range sets PA_DEVERR_BLOCK_RANGE and that row is not stored).
+ */
+pa_status pa_attention_with_kv_update(const pa_plan_t *plan, const void *q, const void *key, const void *value,
+                                      void *key_cache, void *value_cache, const int32_t *block_table,
+                                      int64_t *slot_mapping, void *out, void *workspace, size_t workspace_bytes,
+                                      void *stream);
+
+/* Its kernels alone, after pa_upload_metadata: as pa_attention_launch is to
+ * pa_attention (capturable; identical launches for plans of one fixed shape). */
+pa_status pa_attention_with_kv_update_launch(const pa_plan_t *plan, const void *q, const void *key,
+                                             const void *value, void *key_cache, void *value_cache,
+                                             const int32_t *block_table, int64_t *slot_mapping, void *out,
+                                             void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Zero newly allocated cache blocks ("vLLM 推理流程分析" §4: the scheduler

@@ -34,7 +34,8 @@ PA_DEVERR_TIMEOUT = 0x4
 EXPORTED = ("pa_plan", "pa_plan_destroy", "pa_plan_get_info", "pa_slot_mapping", "pa_write_kv",
             "pa_attention", "pa_check_device_errors", "pa_plan_enable_timing",
             "pa_plan_kernel_times", "pa_status_string", "pa_attention_no_alloc", "pa_write_kv_fp8",
-            "pa_plan_fixed", "pa_upload_metadata", "pa_attention_launch", "pa_zero_blocks")
+            "pa_plan_fixed", "pa_upload_metadata", "pa_attention_launch", "pa_zero_blocks",
+            "pa_attention_with_kv_update", "pa_attention_with_kv_update_launch")
 
 
 class PaError(RuntimeError):
@@ -130,6 +131,10 @@ def load(path: str | None = None, build_if_missing: bool = False) -> ctypes.CDLL
     lib.pa_upload_metadata.argtypes = [vp, vp, sz, vp]
     lib.pa_attention_launch.restype = ctypes.c_int
     lib.pa_attention_launch.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.pa_attention_with_kv_update.restype = ctypes.c_int
+    lib.pa_attention_with_kv_update.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.pa_attention_with_kv_update_launch.restype = ctypes.c_int
+    lib.pa_attention_with_kv_update_launch.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.pa_zero_blocks.restype = ctypes.c_int
     lib.pa_zero_blocks.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]
     lib.pa_plan_destroy.restype = None
@@ -343,6 +348,25 @@ def pa_attention_launch(plan: Plan, q, key_cache, value_cache, block_table, out,
     nbytes = workspace.numel() * workspace.element_size()
     _check(load().pa_attention_launch(plan.handle, _ptr(q), _ptr(key_cache), _ptr(value_cache), _ptr(block_table),
                                       _ptr(out), _ptr(workspace), nbytes, _stream(stream)), "pa_attention_launch")
+
+
+def pa_attention_with_kv_update(plan: Plan, q, key, value, key_cache, value_cache, block_table, out, workspace,
+                                slot_mapping=None, stream=None):
+    """Cache write + attention in one call (see pa.h)."""
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().pa_attention_with_kv_update(plan.handle, _ptr(q), _ptr(key), _ptr(value), _ptr(key_cache),
+                                              _ptr(value_cache), _ptr(block_table), _ptr(slot_mapping), _ptr(out),
+                                              _ptr(workspace), nbytes, _stream(stream)),
+           "pa_attention_with_kv_update")
+
+
+def pa_attention_with_kv_update_launch(plan: Plan, q, key, value, key_cache, value_cache, block_table, out,
+                                       workspace, slot_mapping=None, stream=None):
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().pa_attention_with_kv_update_launch(plan.handle, _ptr(q), _ptr(key), _ptr(value), _ptr(key_cache),
+                                                     _ptr(value_cache), _ptr(block_table), _ptr(slot_mapping),
+                                                     _ptr(out), _ptr(workspace), nbytes, _stream(stream)),
+           "pa_attention_with_kv_update_launch")
 
 
 def pa_zero_blocks(block_ids, key_cache, value_cache, device_error_word=None, stream=None):

@@ -178,6 +178,21 @@ __device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
     return r;
 }
 
+// The E4M3 cache write of two bf16 elements (low half first): the codes of
+// x / scale, the quotient rounded once in IEEE binary32 (low byte first).
+__device__ __forceinline__ uint16_t e4m3_quantize2(uint32_t bf16x2, float scale) {
+    return pack_e4m3x2(__fdiv_rn(__uint_as_float(bf16x2 << 16), scale),
+                       __fdiv_rn(__uint_as_float(bf16x2 & 0xFFFF0000u), scale));
+}
+
+// Eight bf16 elements (16 bytes) -> their eight E4M3 codes (8 bytes).
+__device__ __forceinline__ uint2 e4m3_quantize8(uint4 v, float scale) {
+    return make_uint2(static_cast<uint32_t>(e4m3_quantize2(v.x, scale)) |
+                          (static_cast<uint32_t>(e4m3_quantize2(v.y, scale)) << 16),
+                      static_cast<uint32_t>(e4m3_quantize2(v.z, scale)) |
+                          (static_cast<uint32_t>(e4m3_quantize2(v.w, scale)) << 16));
+}
+
 // two E4M3 codes (low byte first) -> f16x2; every E4M3 value is exact in f16
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
     uint32_t r;
@@ -285,6 +300,14 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
 __device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
+
+// 16-byte global -> shared copy that completes asynchronously (no register
+// staging); cp_async_wait_all waits for the calling thread's copies.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Address of the 16-byte chunk `chunk` (0..7) of row `row` inside a tile of
 // 128-byte rows written by TMA with 128-byte swizzling (tile base 1024-aligned).

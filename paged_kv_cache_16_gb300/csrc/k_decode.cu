@@ -35,6 +35,7 @@ struct DecodeCfg {
     static constexpr int BOX = 16 * 128;                   // one [16 rows][128 B] box
     static constexpr int TSTAGE = HG * NH * BOX;           // K (or V) bytes per block
     static constexpr int STAGE = decode_stage_bytes(D, HG, KV8);
+    static constexpr int NEWROW = decode_newrow_bytes(D, HG);       // fused update buffers
     static constexpr int NS = decode_stages(D, HG, KV8);
     static constexpr int THREADS = decode_threads(HG);
     static constexpr int SMEM = decode_smem_bytes(D, HG, KV8);
@@ -43,7 +44,60 @@ struct DecodeCfg {
 // bf16 pair -> f16 pair (saturating at the largest finite f16)
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) { return pack_f16x2_sat(bf16_lo(w), bf16_hi(w)); }
 
-template <int D, int HG, bool KV8>
+// Fused cache update of one decode row (pa_attention_with_kv_update; the
+// fused dispatch of "vLLM 推理流程分析" §6.1, the write of §6.3): the warp of kv
+// head kvh in the CTA whose run holds the row's last page loads the row's new
+// K and V (16 bytes of each per lane) when the item starts, and stores them
+// into the stage it computes on (over whatever the TMA brought for that slot)
+// and into the caches (E4M3: quantised exactly as pa_write_kv_fp8 does).
+// Every other slot a decode row reads was written by an earlier step.
+template <int D, bool KV8>
+struct RowUpdate {
+    int last_page = -1;  // the row's last page if this item holds it, else -1
+    int64_t off = -1;    // element offset of (slot, kv head) in a cache; -1: bad block id, no store
+
+    // buf: this warp's shared buffer, the new K row then the new V row (bf16)
+    __device__ __forceinline__ void begin(const DecodeParams &p, const DecodeItem &item, int kvh, int lane,
+                                          uint32_t buf) {
+        const int lp = (item.key_end - 1) / kBlockSize;
+        last_page = p.new_k != nullptr && item.key_end > 0 && item.page_begin <= lp && lp < item.page_end ? lp : -1;
+        if (last_page < 0) return;
+        const int32_t blk = __ldg(p.block_table + static_cast<int64_t>(item.req) * p.max_blocks + lp);
+        const int64_t slot = static_cast<int64_t>(blk) * kBlockSize + (item.key_end - 1) % kBlockSize;
+        off = blk >= 0 && blk < p.num_blocks ? (slot * p.num_heads_kv + kvh) * D : -1;
+        if (lane < D / 8) {
+            const int64_t src = (static_cast<int64_t>(item.token) * p.num_heads_kv + kvh) * D;
+            cp_async16(buf + 16u * lane, reinterpret_cast<const uint4 *>(p.new_k + src) + lane);
+            cp_async16(buf + 2u * D + 16u * lane, reinterpret_cast<const uint4 *>(p.new_v + src) + lane);
+            cp_async_commit();
+        }
+        if (kvh == 0 && lane == 0 && p.slots_out != nullptr && off >= 0) p.slots_out[item.token] = slot;
+    }
+
+    // the new row (which = 0: K, 1: V) into the stage box(es) starting at box0
+    // (bf16: D / 64 boxes of [16][64], E4M3: one [16][128]) and into the cache
+    __device__ __forceinline__ void put(uint32_t box0, int row, uint32_t buf, int which, void *cache, float scale,
+                                        int lane) const {
+        if (lane < D / 8) {
+            cp_async_wait_all();
+            const uint4 x = lds_v4(buf + which * 2u * D + 16u * lane);
+            if constexpr (KV8) {
+                const uint2 c = e4m3_quantize8(x, scale);
+                asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(sw128(box0, row, lane >> 1) + 8u * (lane & 1)),
+                             "r"(c.x), "r"(c.y)
+                             : "memory");
+                if (off >= 0) reinterpret_cast<uint2 *>(static_cast<uint8_t *>(cache) + off)[lane] = c;
+            } else {
+                sts_v4(sw128(box0 + (lane / 8) * (16 * 128), row, lane % 8), x.x, x.y, x.z, x.w);
+                if (off >= 0) reinterpret_cast<uint4 *>(static_cast<uint16_t *>(cache) + off)[lane] = x;
+            }
+        }
+        fence_proxy_async_smem();   // generic writes before later TMA writes of the stage
+        __syncwarp();
+    }
+};
+
+template <int D, int HG, bool KV8, bool FUSED>
 __global__ void __launch_bounds__((HG + 1) * 32, 1)
 decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const DecodeParams p) {
@@ -52,7 +106,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     __shared__ int abort_flag;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;           // stages, 1024-aligned
-    const uint32_t bar0 = base + C::NS * C::STAGE;           // full_k | full_v | empty
+    const uint32_t newrow = base + C::NS * C::STAGE;         // per-warp new K/V rows (fused update)
+    const uint32_t bar0 = newrow + C::NEWROW;   // full_k | full_v | empty
     auto full_k = [&](int s) { return bar0 + 8u * s; };
     auto full_v = [&](int s) { return bar0 + 8u * (C::NS + s); };
     auto empty = [&](int s) { return bar0 + 8u * (2 * C::NS + s); };
@@ -148,12 +203,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         const int t4 = lane & 3;
         const int G = p.group;
         constexpr uint32_t kOnes = 0x3C003C00u;  // f16x2 (1, 1)
-        uint32_t k_off[D / 16];                   // key g at +0, key g + 8 at +1024
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) k_off[kk] = g * 128u + 4u * t4 + (static_cast<uint32_t>(kk ^ g) << 4);
-        uint32_t v_off[D / 32];
-#pragma unroll
-        for (int a = 0; a < D / 32; ++a) v_off[a] = static_cast<uint32_t>(a ^ t4) << 5;
+        const uint32_t k_lane = g * 128u + 4u * t4;   // key g at +0, key g + 8 at +1024
         const uint32_t va_lane = 256u * t4 + 16u * (g >> 2) + 4u * (g & 3);             // key 2t
         const uint32_t vb_lane = 256u * t4 + 128u + 16u * ((g >> 2) ^ 1) + 4u * (g & 3);  // key 2t + 1
         const float sl2 = p.scale_log2;  // > 0: the maximum of raw scores scales
@@ -180,11 +230,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
             float lacc[4] = {0.f, 0.f, 0.f, 0.f};
             float m0 = -INFINITY, m1 = -INFINITY;
+            RowUpdate<D, true> upd;
+            if constexpr (FUSED) upd.begin(p, item, kvh, lane, newrow + warp * 4u * D);
 
             auto qk = [&](uint32_t kb, float (&a)[4], float (&b)[4]) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t x = kb + k_off[kk];
+                    const uint32_t x = kb + k_lane + (static_cast<uint32_t>(kk ^ g) << 4);
                     uint32_t k0, k1, k2, k3;
                     e4m3x4_to_f16x2x2(lds_u32(x), k0, k1);
                     e4m3x4_to_f16x2x2(lds_u32(x + 1024u), k2, k3);
@@ -205,8 +257,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 }
 #pragma unroll
                 for (int a = 0; a < D / 32; ++a) {
-                    uint32_t wA = lds_u32(ra + v_off[a]), wB = lds_u32(rb + v_off[a]);
-                    uint32_t wC = lds_u32(ra + 1024u + v_off[a]), wD = lds_u32(rb + 1024u + v_off[a]);
+                    const uint32_t xa = static_cast<uint32_t>(a ^ t4) << 5;
+                    uint32_t wA = lds_u32(ra + xa), wB = lds_u32(rb + xa);
+                    uint32_t wC = lds_u32(ra + 1024u + xa), wD = lds_u32(rb + 1024u + xa);
                     if constexpr (decltype(masked)::value) {
                         wA &= mA; wB &= mB; wC &= mC; wD &= mD;
                     }
@@ -227,6 +280,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 const uint32_t par0 = (consumed / C::NS) & 1, par1 = ((consumed + 1) / C::NS) & 1;
                 if (!warp_wait(full_k(s0), par0, &abort_flag) || (TWO && !warp_wait(full_k(s1), par1, &abort_flag)))
                     return false;
+                const bool new0 = FUSED && pg == upd.last_page;
+                const bool new1 = FUSED && TWO && pg + 1 == upd.last_page;
+                const int nrow = (item.key_end - 1) % kBlockSize;
+                const uint32_t nbuf = newrow + warp * 4u * D;
+                if (new0) upd.put(stage(s0) + warp * C::BOX, nrow, nbuf, 0, p.cache_k, p.k_scale, lane);
+                if (new1) upd.put(stage(s1) + warp * C::BOX, nrow, nbuf, 0, p.cache_k, p.k_scale, lane);
                 float sc[4][4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
@@ -278,6 +337,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 }
                 if (!warp_wait(full_v(s0), par0, &abort_flag) || (TWO && !warp_wait(full_v(s1), par1, &abort_flag)))
                     return false;
+                if (new0) upd.put(stage(s0) + C::TSTAGE + warp * C::BOX, nrow, nbuf, 1, p.cache_v, p.v_scale, lane);
+                if (new1) upd.put(stage(s1) + C::TSTAGE + warp * C::BOX, nrow, nbuf, 1, p.cache_v, p.v_scale, lane);
                 const uint32_t vb0 = stage(s0) + C::TSTAGE + warp * C::BOX;
                 if (valid_keys < kBlockSize) pv(std::true_type{}, vb0, pa[0], valid_keys);
                 else pv(std::false_type{}, vb0, pa[0], kBlockSize);
@@ -373,6 +434,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #pragma unroll
             for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
             float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+            RowUpdate<D, false> upd;
+            if constexpr (FUSED) upd.begin(p, item, kvh, lane, newrow + warp * 4u * D);
 
             for (int pg = item.page_begin; pg < item.page_end; ++pg, ++consumed) {
                 const int s = consumed % C::NS;
@@ -384,6 +447,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 }
                 const uint32_t kb = stage(s) + warp * C::NH * C::BOX;
                 const uint32_t vb = kb + C::TSTAGE;
+                const bool new_row = FUSED && pg == upd.last_page;
+                if (new_row) upd.put(kb, (item.key_end - 1) % kBlockSize, newrow + warp * 4u * D, 0, p.cache_k, p.k_scale, lane);
                 // S = Q K^T over this block's 16 keys (two n-tiles of 8 keys)
                 float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
@@ -440,6 +505,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     ok = false;
                     break;
                 }
+                if (new_row) upd.put(vb, (item.key_end - 1) % kBlockSize, newrow + warp * 4u * D, 1, p.cache_v, p.v_scale, lane);
                 if (valid_keys < kBlockSize) {
                     // rows past the context may hold anything (even NaN); zero
                     // them so that 0-weight * row stays 0 inside the MMA
@@ -508,12 +574,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     __syncthreads();
 }
 
-template <int D, int HG, bool KV8>
+template <int D, int HG, bool KV8, bool FUSED>
 cudaError_t configure() {
     static bool configured = false;  // attribute is per function, set once per process
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, HG, KV8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             DecodeCfg<D, HG, KV8>::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, HG, KV8, FUSED>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, DecodeCfg<D, HG, KV8>::SMEM);
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -521,12 +587,21 @@ cudaError_t configure() {
 }
 
 template <int D, int HG, bool KV8>
+cudaError_t configure_both() {
+    cudaError_t e = configure<D, HG, KV8, false>();
+    return e == cudaSuccess ? configure<D, HG, KV8, true>() : e;
+}
+
+template <int D, int HG, bool KV8>
 cudaError_t launch_t(int num_ctas, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                      const DecodeParams &p, cudaStream_t stream) {
     using C = DecodeCfg<D, HG, KV8>;
-    cudaError_t e = configure<D, HG, KV8>();
+    cudaError_t e = configure_both<D, HG, KV8>();
     if (e != cudaSuccess) return e;
-    decode_kernel<D, HG, KV8><<<num_ctas, C::THREADS, C::SMEM, stream>>>(tm_k, tm_v, p);
+    if (p.new_k != nullptr)
+        decode_kernel<D, HG, KV8, true><<<num_ctas, C::THREADS, C::SMEM, stream>>>(tm_k, tm_v, p);
+    else
+        decode_kernel<D, HG, KV8, false><<<num_ctas, C::THREADS, C::SMEM, stream>>>(tm_k, tm_v, p);
     return cudaGetLastError();
 }
 
@@ -538,7 +613,7 @@ cudaError_t launch_t(int num_ctas, const CUtensorMap &tm_k, const CUtensorMap &t
 
 cudaError_t prepare_decode(int head_dim, int hg, bool kv8) {
 #define X(d, h, f) \
-    if (head_dim == d && hg == h && kv8 == f) return configure<d, h, f>();
+    if (head_dim == d && hg == h && kv8 == f) return configure_both<d, h, f>();
     PA_DECODE_CASES(X)
 #undef X
     return cudaErrorInvalidValue;

@@ -59,17 +59,8 @@ __global__ void write_kv_kernel(const uint4 *__restrict__ key, const uint4 *__re
 // row (and of its value row) into 16 codes, code = E4M3(bf16 / scale) with the
 // quotient rounded once in IEEE binary32.
 __device__ __forceinline__ uint4 quantize16(uint4 a, uint4 b, float scale) {
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint16_t lo = dev::pack_e4m3x2(__fdiv_rn(dev::bf16_lo(w[2 * i]), scale),
-                                             __fdiv_rn(dev::bf16_hi(w[2 * i]), scale));
-        const uint16_t hi = dev::pack_e4m3x2(__fdiv_rn(dev::bf16_lo(w[2 * i + 1]), scale),
-                                             __fdiv_rn(dev::bf16_hi(w[2 * i + 1]), scale));
-        o[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
+    const uint2 lo = dev::e4m3_quantize8(a, scale), hi = dev::e4m3_quantize8(b, scale);
+    return make_uint4(lo.x, lo.y, hi.x, hi.y);
 }
 
 __global__ void write_kv_fp8_kernel(const uint4 *__restrict__ key, const uint4 *__restrict__ value,
@@ -129,6 +120,64 @@ __global__ void dequant_kernel(DequantParams p) {
             expand16(__ldg(ks + c), kd + 2 * c);
             expand16(__ldg(vs + c), vd + 2 * c);
         }
+    }
+}
+
+// Fused cache update, extend rows (pa_attention_with_kv_update): token e of
+// the runs' concatenation lies in the last run with wbegin <= e; its slot
+// comes from the block table as in slot mapping ("vLLM 推理流程分析" §5.1.2),
+// and its row is stored as pa_write_kv / pa_write_kv_fp8 store it (§6.3).
+// One thread per 16-byte output chunk.
+__global__ void write_runs_kernel(WriteParams p) {
+    const int32_t nruns = p.counts[kCountWriteRuns];
+    const int64_t ntok = p.counts[kCountWriteTokens];
+    const int32_t cpr = p.kv8 ? p.row_elems / 16 : p.row_elems / 8;   // output chunks per row
+    const int64_t total = ntok * cpr;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int32_t e = static_cast<int32_t>(i / cpr);
+        const int32_t c = static_cast<int32_t>(i - static_cast<int64_t>(e) * cpr);
+        int32_t lo = 0, hi = nruns - 1;
+        while (lo < hi) {
+            const int32_t mid = (lo + hi + 1) >> 1;
+            if (p.runs[mid].wbegin <= e) lo = mid; else hi = mid - 1;
+        }
+        const WriteRun run = p.runs[lo];
+        const int32_t t = run.t0 + (e - run.wbegin);
+        const int32_t pos = run.pos0 + (e - run.wbegin);
+        const int32_t blk = p.block_table[static_cast<int64_t>(run.req) * p.max_blocks + pos / kBlockSize];
+        if (blk < 0 || blk >= p.num_blocks) {
+            if (c == 0) atomicOr(p.err, kErrBlockRange);
+            continue;
+        }
+        const int64_t slot = static_cast<int64_t>(blk) * kBlockSize + pos % kBlockSize;
+        if (c == 0 && p.slots_out != nullptr) p.slots_out[t] = slot;
+        const uint4 *k = reinterpret_cast<const uint4 *>(p.key) + static_cast<int64_t>(t) * (p.row_elems / 8);
+        const uint4 *v = reinterpret_cast<const uint4 *>(p.value) + static_cast<int64_t>(t) * (p.row_elems / 8);
+        uint4 *kd = static_cast<uint4 *>(p.key_cache) + slot * cpr + c;
+        uint4 *vd = static_cast<uint4 *>(p.value_cache) + slot * cpr + c;
+        if (p.kv8) {
+            *kd = quantize16(__ldcs(k + 2 * c), __ldcs(k + 2 * c + 1), p.k_scale);
+            *vd = quantize16(__ldcs(v + 2 * c), __ldcs(v + 2 * c + 1), p.v_scale);
+        } else {
+            *kd = __ldcs(k + c);
+            *vd = __ldcs(v + c);
+        }
+    }
+}
+
+// Metadata upload: the plan's pinned host image, read across the host link
+// by the SMs themselves (no copy-engine round trip), into the workspace.
+// Uncached loads: a recycled host buffer must never be served from a line
+// cached for an earlier plan.
+__global__ void upload_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst, int64_t n16) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride) {
+        uint4 v;
+        asm volatile("ld.global.cv.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "l"(src + i));
+        dst[i] = v;
     }
 }
 
@@ -224,6 +273,24 @@ cudaError_t launch_merge(int head_dim, int grid, const MergeParams &p, cudaStrea
     if (head_dim == 128) merge_kernel<128><<<grid, 256, 0, stream>>>(p);
     else if (head_dim == 64) merge_kernel<64><<<grid, 256, 0, stream>>>(p);
     else return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_upload(const void *src, void *dst, size_t bytes, cudaStream_t stream) {
+    if (bytes == 0) return cudaSuccess;
+    if (bytes % 16 != 0) return cudaErrorInvalidValue;
+    const int64_t n16 = static_cast<int64_t>(bytes / 16);
+    const int threads = 256;
+    int64_t blocks = (n16 + threads - 1) / threads;
+    if (blocks > 64) blocks = 64;
+    upload_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(static_cast<const uint4 *>(src),
+                                                                        static_cast<uint4 *>(dst), n16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_write_runs(int grid, const WriteParams &p, cudaStream_t stream) {
+    if (grid <= 0) return cudaSuccess;
+    write_runs_kernel<<<grid, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -263,6 +263,8 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     P->kv8 = d->kv_cache_dtype == PA_KV_FP8_E4M3;
     P->scale_log2 = d->softmax_scale * (P->kv8 ? d->k_scale : 1.f) * 1.4426950408889634f;
     P->out_scale = P->kv8 ? d->v_scale : 1.f;
+    P->k_scale = P->kv8 ? d->k_scale : 1.f;
+    P->v_scale = P->kv8 ? d->v_scale : 1.f;
     P->num_sms = d->num_sms;
     if (P->num_sms == 0) {
         int dev = 0;
@@ -367,6 +369,18 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     const int cps = std::max(1, decode_ctas_per_sm_static(P->D, P->HG, P->kv8));
     plan_decode(P, d, decode_rows, pieces, P->fixed ? static_cast<int64_t>(P->num_sms) * cps : 0);
 
+    // ------------------------------- fused cache update of extend rows
+    for (int32_t r : extend_rows) {
+        WriteRun w{};
+        w.t0 = qsl[r];
+        w.n_tok = qsl[r + 1] - qsl[r];
+        w.req = r;
+        w.pos0 = d->num_computed_tokens[r];
+        w.wbegin = P->write_tokens;
+        P->write_tokens += w.n_tok;
+        P->write_runs.push_back(w);
+    }
+
     // ----------------------------------------------------- partial slots
     std::vector<int32_t> count(static_cast<size_t>(P->T) * P->n_groups, 0);
     for (int32_t r : decode_rows)
@@ -418,10 +432,12 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
         P->cap_dequant = P->kv8 && P->cap_tiles > 0 ? shape->max_dequant_blocks : 0;
         P->cap_slots = static_cast<int32_t>(slots_cap);
         P->cap_scr_rows = P->kv8 && P->cap_tiles > 0 ? shape->max_reqs : 0;
+        P->cap_runs = P->cap_tiles > 0 ? shape->max_reqs : 0;
         if (static_cast<int64_t>(P->items.size()) > P->cap_items ||
             static_cast<int64_t>(P->tiles.size()) > P->cap_tiles ||
             static_cast<int64_t>(P->merges.size()) > P->cap_merges || P->num_scratch_blocks > P->cap_dequant ||
-            P->num_slots > P->cap_slots || scr_rows > P->cap_scr_rows)
+            P->num_slots > P->cap_slots || scr_rows > P->cap_scr_rows ||
+            static_cast<int64_t>(P->write_runs.size()) > P->cap_runs)
             return PA_ERR_CAPACITY;
     } else {
         P->cap_tokens = P->T;
@@ -431,6 +447,7 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
         P->cap_dequant = P->num_scratch_blocks;
         P->cap_slots = P->num_slots;
         P->cap_scr_rows = scr_rows;
+        P->cap_runs = static_cast<int32_t>(P->write_runs.size());
     }
 
     // ------------------------------------------------- workspace layout
@@ -446,6 +463,7 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     P->off_merges = place(static_cast<size_t>(P->cap_merges) * sizeof(MergeRow));
     P->off_scrtab = place(static_cast<size_t>(P->cap_scr_rows) * P->max_blocks * sizeof(int32_t));
     P->off_dequant = place(static_cast<size_t>(P->cap_dequant) * sizeof(DequantItem));
+    P->off_runs = place(static_cast<size_t>(P->cap_runs) * sizeof(WriteRun));
     P->blob_bytes = off - kHeader;
     off = align_up(off, 256);
     P->off_opart = off;
@@ -462,8 +480,13 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     auto put = [&](size_t at, const void *src, size_t n) {
         if (n) std::memcpy(P->blob.data() + (at - kHeader), src, n);
     };
-    const int32_t counts[kNumCounts] = {static_cast<int32_t>(P->tiles.size()), static_cast<int32_t>(P->merges.size()),
-                                        static_cast<int32_t>(P->dequant.size()), P->T};
+    int32_t counts[kNumCounts] = {};
+    counts[kCountTiles] = static_cast<int32_t>(P->tiles.size());
+    counts[kCountMerges] = static_cast<int32_t>(P->merges.size());
+    counts[kCountDequant] = static_cast<int32_t>(P->dequant.size());
+    counts[kCountTokens] = P->T;
+    counts[kCountWriteRuns] = static_cast<int32_t>(P->write_runs.size());
+    counts[kCountWriteTokens] = P->write_tokens;
     put(off_counts, counts, sizeof counts);
     put(P->off_part, P->part_offset.data(), P->part_offset.size() * sizeof(int32_t));
     put(P->off_cta, P->cta_begin.data(), P->cta_begin.size() * sizeof(int32_t));
@@ -472,6 +495,7 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     put(P->off_merges, P->merges.data(), P->merges.size() * sizeof(MergeRow));
     put(P->off_scrtab, P->scratch_table.data(), P->scratch_table.size() * sizeof(int32_t));
     put(P->off_dequant, P->dequant.data(), P->dequant.size() * sizeof(DequantItem));
+    put(P->off_runs, P->write_runs.data(), P->write_runs.size() * sizeof(WriteRun));
 
     // ------------------------------------------------------------- info
     pa_plan_info &I = P->info;
@@ -532,7 +556,8 @@ pa_status prepare_plan(pa_plan_s *P) {
 }
 
 pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, const void *value_cache,
-                            const int32_t *block_table, void *out, uint8_t *ws, cudaStream_t stream, bool timed) {
+                            const int32_t *block_table, void *out, uint8_t *ws, cudaStream_t stream, bool timed,
+                            const KvUpdate &update) {
     auto rec = [&](int kind, bool start, cudaStream_t st) { return timed ? record(P, kind, start, st) : cudaSuccess; };
     int32_t *err = reinterpret_cast<int32_t *>(ws);
     const int32_t *counts = reinterpret_cast<const int32_t *>(ws + kHeader);
@@ -550,6 +575,30 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
                   !make_map(&tm_v, value_cache, P->D, P->Hkv, rows, 1, kBlockSize)))
         return PA_ERR_CUDA;
 
+    if (update.key != nullptr && P->cap_runs > 0) {
+        // fused cache update: extend rows' new tokens first (the tiles read
+        // them); decode rows' are stored by the decode kernel itself
+        WriteParams wp{};
+        wp.key = static_cast<const uint16_t *>(update.key);
+        wp.value = static_cast<const uint16_t *>(update.value);
+        wp.key_cache = const_cast<void *>(key_cache);
+        wp.value_cache = const_cast<void *>(value_cache);
+        wp.block_table = block_table;
+        wp.runs = reinterpret_cast<const WriteRun *>(ws + P->off_runs);
+        wp.counts = counts;
+        wp.slots_out = update.slots_out;
+        wp.err = err;
+        wp.row_elems = P->Hkv * P->D;
+        wp.max_blocks = P->max_blocks;
+        wp.num_blocks = P->num_blocks;
+        wp.kv8 = P->kv8 ? 1 : 0;
+        wp.k_scale = P->k_scale;
+        wp.v_scale = P->v_scale;
+        const int64_t chunks = static_cast<int64_t>(std::max(1, P->fixed ? P->cap_tokens : P->write_tokens)) *
+                               (P->kv8 ? wp.row_elems / 16 : wp.row_elems / 8);
+        const int grid = static_cast<int>(std::min<int64_t>((chunks + 255) / 256, 16 * sms));
+        if (launch_write_runs(grid, wp, stream) != cudaSuccess) return PA_ERR_CUDA;
+    }
     if (P->cap_tiles > 0) {
         // E4M3: the tiles read bf16 copies of their blocks, made here
         CUtensorMap tm_tk = tm_k, tm_tv = tm_v;
@@ -617,6 +666,14 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
         dp.n_groups = P->n_groups;
         dp.scale_log2 = P->scale_log2;
         dp.out_scale = P->out_scale;
+        dp.new_k = static_cast<const uint16_t *>(update.key);
+        dp.new_v = static_cast<const uint16_t *>(update.value);
+        dp.cache_k = const_cast<void *>(key_cache);
+        dp.cache_v = const_cast<void *>(value_cache);
+        dp.slots_out = update.slots_out;
+        dp.num_heads_kv = P->Hkv;
+        dp.k_scale = P->k_scale;
+        dp.v_scale = P->v_scale;
         if (rec(0, true, stream) != cudaSuccess) return PA_ERR_CUDA;
         if (launch_decode(P->D, P->HG, P->kv8, P->ncta, tm_k, tm_v, dp, stream) != cudaSuccess) return PA_ERR_CUDA;
         if (rec(0, false, stream) != cudaSuccess) return PA_ERR_CUDA;
@@ -775,9 +832,9 @@ pa_status upload(pa_plan_s *P, uint8_t *ws, cudaStream_t stream, bool timed) {
         if (!staging().acquire(P->blob_bytes, &P->pinned, &P->pinned_cap, &P->upload_evt)) return PA_ERR_CUDA;
         std::memcpy(P->pinned, P->blob.data(), P->blob_bytes);
     }
+    if (!P->pinned_dev && cudaHostGetDevicePointer(&P->pinned_dev, P->pinned, 0) != cudaSuccess) return PA_ERR_CUDA;
     if (timed && record(P, 3, true, stream) != cudaSuccess) return PA_ERR_CUDA;
-    if (cudaMemcpyAsync(ws + kHeader, P->pinned, P->blob_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-        return PA_ERR_CUDA;
+    if (launch_upload(P->pinned_dev, ws + kHeader, P->blob_bytes, stream) != cudaSuccess) return PA_ERR_CUDA;
     if (timed && record(P, 3, false, stream) != cudaSuccess) return PA_ERR_CUDA;
     if (cudaEventRecord(P->upload_evt, stream) != cudaSuccess) return PA_ERR_CUDA;
     return PA_OK;
@@ -824,6 +881,50 @@ pa_status pa_attention_launch(const pa_plan_t *plan, const void *q, const void *
     if ((st = prepare_plan(P)) != PA_OK) return st;
     return enqueue_attention(P, q, key_cache, value_cache, block_table, out, static_cast<uint8_t *>(workspace),
                              static_cast<cudaStream_t>(stream_), false);
+}
+
+pa_status pa_attention_with_kv_update(const pa_plan_t *plan, const void *q, const void *key, const void *value,
+                                      void *key_cache, void *value_cache, const int32_t *block_table,
+                                      int64_t *slot_mapping, void *out, void *workspace, size_t workspace_bytes,
+                                      void *stream_) {
+    if (!plan) return PA_ERR_INVALID_ARGUMENT;
+    pa_plan_s *P = const_cast<pa_plan_s *>(plan);
+    if (P->T == 0 && !P->fixed) return PA_OK;
+    pa_status st = check_launch_args(P, q, key_cache, value_cache, block_table, out, workspace, workspace_bytes);
+    if (st != PA_OK) return st;
+    if (!key || !value || !aligned(key, 16) || !aligned(value, 16) || (slot_mapping && !aligned(slot_mapping, 8)))
+        return PA_ERR_INVALID_ARGUMENT;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    std::lock_guard<std::mutex> lock(P->mu);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    if ((st = prepare_plan(P)) != PA_OK) return st;
+    if ((st = upload(P, ws, stream, true)) != PA_OK) return st;
+    KvUpdate u;
+    u.key = key;
+    u.value = value;
+    u.slots_out = slot_mapping;
+    return enqueue_attention(P, q, key_cache, value_cache, block_table, out, ws, stream, true, u);
+}
+
+pa_status pa_attention_with_kv_update_launch(const pa_plan_t *plan, const void *q, const void *key,
+                                             const void *value, void *key_cache, void *value_cache,
+                                             const int32_t *block_table, int64_t *slot_mapping, void *out,
+                                             void *workspace, size_t workspace_bytes, void *stream_) {
+    if (!plan) return PA_ERR_INVALID_ARGUMENT;
+    pa_plan_s *P = const_cast<pa_plan_s *>(plan);
+    if (P->T == 0 && !P->fixed) return PA_OK;
+    pa_status st = check_launch_args(P, q, key_cache, value_cache, block_table, out, workspace, workspace_bytes);
+    if (st != PA_OK) return st;
+    if (!key || !value || !aligned(key, 16) || !aligned(value, 16) || (slot_mapping && !aligned(slot_mapping, 8)))
+        return PA_ERR_INVALID_ARGUMENT;
+    std::lock_guard<std::mutex> lock(P->mu);
+    if ((st = prepare_plan(P)) != PA_OK) return st;
+    KvUpdate u;
+    u.key = key;
+    u.value = value;
+    u.slots_out = slot_mapping;
+    return enqueue_attention(P, q, key_cache, value_cache, block_table, out, static_cast<uint8_t *>(workspace),
+                             static_cast<cudaStream_t>(stream_), false, u);
 }
 
 pa_status pa_zero_blocks(const int32_t *block_ids, int32_t num_ids, int32_t num_blocks, int32_t num_heads_kv,

@@ -26,8 +26,11 @@ constexpr int decode_stages(int d, int hg, bool kv8) {
                                                                        : 2);
 }
 constexpr int decode_threads(int hg) { return (hg + 1) * 32; }
+// per-warp buffer of a decode row's new K and V rows (bf16) for the fused update
+constexpr int decode_newrow_bytes(int d, int hg) { return hg * 4 * d; }
 constexpr int decode_smem_bytes(int d, int hg, bool kv8) {
-    return decode_stages(d, hg, kv8) * decode_stage_bytes(d, hg, kv8) + 3 * decode_stages(d, hg, kv8) * 8 + 1024;
+    return decode_stages(d, hg, kv8) * decode_stage_bytes(d, hg, kv8) + decode_newrow_bytes(d, hg) +
+           3 * decode_stages(d, hg, kv8) * 8 + 1024;
 }
 constexpr int kSmemPerSm = 233472;  // 228 KiB of shared memory per SM
 constexpr int decode_ctas_per_sm_static(int d, int hg, bool kv8) {
@@ -104,6 +107,15 @@ struct DecodeParams {
     int32_t n_groups;           // kv-head groups (Hkv / heads per group)
     float scale_log2;           // softmax_scale * k_scale * log2(e)
     float out_scale;            // v_scale (1 for bf16 caches)
+    // fused cache update (new_k != null): the CTA holding a decode row's last
+    // page stores the row's new K/V into the caches and into its stage
+    const uint16_t *new_k;      // [T][Hkv][D] bf16
+    const uint16_t *new_v;
+    void *cache_k;
+    void *cache_v;
+    int64_t *slots_out;         // optional [T]
+    int32_t num_heads_kv;
+    float k_scale, v_scale;     // E4M3 quantisation scales of the write
 };
 
 struct ExtendParams {
@@ -159,7 +171,45 @@ struct MergeParams {
 
 // Work counts at the head of the uploaded metadata: kernels launched on a
 // grid sized for a capacity read their real counts here.
-enum MetaCount : int { kCountTiles = 0, kCountMerges = 1, kCountDequant = 2, kCountTokens = 3, kNumCounts = 4 };
+enum MetaCount : int {
+    kCountTiles = 0,
+    kCountMerges = 1,
+    kCountDequant = 2,
+    kCountTokens = 3,
+    kCountWriteRuns = 4,     // extend rows whose new K/V the fused write kernel stores
+    kCountWriteTokens = 5,   // their tokens in total
+    kNumCounts = 8
+};
+
+// Fused cache update: the new tokens of one extend row, stored by the write
+// kernel before the tensor-core tiles read them (decode rows are stored by
+// the decode kernel itself).
+struct WriteRun {
+    int32_t t0;          // first token row
+    int32_t n_tok;       // tokens
+    int32_t req;         // block-table row
+    int32_t pos0;        // position of the first token (num_computed)
+    int32_t wbegin;      // tokens of the runs before this one
+    int32_t pad[3];
+};
+
+// The fused write of extend-row tokens (pa_attention_with_kv_update).
+struct WriteParams {
+    const uint16_t *key;        // [T][Hkv][D] bf16
+    const uint16_t *value;
+    void *key_cache;            // bf16 or E4M3 caches
+    void *value_cache;
+    const int32_t *block_table;
+    const WriteRun *runs;
+    const int32_t *counts;
+    int64_t *slots_out;         // optional [T]
+    int32_t *err;
+    int32_t row_elems;          // Hkv * D
+    int32_t max_blocks;
+    int32_t num_blocks;
+    int32_t kv8;
+    float k_scale, v_scale;     // E4M3 quantisation (code of x / scale)
+};
 
 // Launchers (each returns the launch's cudaError_t).
 cudaError_t launch_slot_mapping(const int32_t *qsl, const int32_t *num_computed,
@@ -184,6 +234,11 @@ cudaError_t launch_decode(int head_dim, int hg, bool kv8, int num_ctas, const CU
 cudaError_t launch_extend(int head_dim, int grid, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const ExtendParams &p, cudaStream_t stream);
 cudaError_t launch_merge(int head_dim, int grid, const MergeParams &p, cudaStream_t stream);
+// Copy `bytes` (a multiple of 16) from device-accessible pinned host memory
+// to device memory with a kernel.
+cudaError_t launch_upload(const void *src, void *dst, size_t bytes, cudaStream_t stream);
+// Fused write of extend-row tokens: grid-stride over their 16-element chunks.
+cudaError_t launch_write_runs(int grid, const WriteParams &p, cudaStream_t stream);
 // Zero the K and V entries of the listed blocks (ids < 0 skipped).
 cudaError_t launch_zero_blocks(const int32_t *ids, int32_t num_ids, int32_t num_blocks, int64_t block_bytes,
                                void *key_cache, void *value_cache, int32_t *err, cudaStream_t stream);

@@ -17,28 +17,32 @@ struct pa_plan_s {
     float scale_log2 = 0.f;     // softmax_scale * k_scale * log2(e)
     bool kv8 = false;           // E4M3 caches
     float out_scale = 1.f;      // v_scale for E4M3 caches
+    float k_scale = 1.f, v_scale = 1.f;   // E4M3 quantisation scales of the fused write
     // work lists
     std::vector<int32_t> part_offset;   // [T * n_groups]
     std::vector<int32_t> cta_begin;     // [ncta + 1]
     std::vector<pa::DecodeItem> items;
     std::vector<pa::ExtendTile> tiles;
     std::vector<pa::MergeRow> merges;
+    std::vector<pa::WriteRun> write_runs;     // extend rows (fused cache update)
+    int32_t write_tokens = 0;
     std::vector<int32_t> scratch_table;       // E4M3: [rows][max_blocks] bf16 scratch block ids
     std::vector<pa::DequantItem> dequant;     // E4M3: blocks to expand each call
     int32_t num_scratch_blocks = 0;
     int32_t num_slots = 0;
     // workspace layout
     size_t off_part = 0, off_cta = 0, off_items = 0, off_tiles = 0, off_merges = 0;
-    size_t off_scrtab = 0, off_dequant = 0, off_kscr = 0, off_vscr = 0;
+    size_t off_scrtab = 0, off_dequant = 0, off_kscr = 0, off_vscr = 0, off_runs = 0;
     size_t blob_bytes = 0, off_opart = 0, off_ml = 0, ws_bytes = 0;
     // launch shape: exact sizes for pa_plan, capacities for pa_plan_fixed
     bool fixed = false;
     int32_t ncta = 0;                   // decode CTAs
     int32_t cap_tokens = 0, cap_items = 0, cap_tiles = 0, cap_merges = 0, cap_dequant = 0;
-    int32_t cap_slots = 0, cap_scr_rows = 0;
+    int32_t cap_slots = 0, cap_scr_rows = 0, cap_runs = 0;
     bool prepared = false;              // kernel attributes set (pa_upload_metadata)
     std::vector<uint8_t> blob;          // host image of the metadata blob
     void *pinned = nullptr;             // pinned staging copy used for async uploads
+    void *pinned_dev = nullptr;         // its device-side address (read by the upload kernel)
     size_t pinned_cap = 0;
     cudaEvent_t upload_evt = nullptr;   // recorded after each upload from `pinned`
     pa_plan_info info{};
@@ -66,8 +70,16 @@ bool make_map_u8(CUtensorMap *tm, const void *ptr, uint64_t d, uint64_t mid, uin
 // `timed` records the plan's per-kernel timing events when they are enabled.
 // For a fixed-shape plan every launch and argument depends on the plan's
 // capacities only.
+// Fused cache update (pa_attention_with_kv_update): the step's new rows.
+struct KvUpdate {
+    const void *key = nullptr;      // [T][Hkv][D] bf16; null = no update
+    const void *value = nullptr;
+    int64_t *slots_out = nullptr;   // optional [T]
+};
+
 pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, const void *value_cache,
-                            const int32_t *block_table, void *out, uint8_t *ws, cudaStream_t stream, bool timed);
+                            const int32_t *block_table, void *out, uint8_t *ws, cudaStream_t stream, bool timed,
+                            const KvUpdate &update = KvUpdate{});
 
 // Set the kernel attributes the plan's launches need (once per plan).
 pa_status prepare_plan(pa_plan_s *P);

@@ -70,6 +70,12 @@ class DeviceStep:
         self.write(key, value, key_cache, value_cache, stream)
         return self.attend(q, key_cache, value_cache, stream)
 
+    def run_fused(self, q, key, value, key_cache, value_cache, stream=None, plan=None):
+        """Cache write and attention as one call (slots land in self.slots)."""
+        binding.pa_attention_with_kv_update(plan or self.plan, q, key, value, key_cache, value_cache,
+                                            self.block_table, self.out, self.workspace, self.slots, stream)
+        return self.out[:self.batch.num_tokens]
+
     def check_errors(self, stream=None) -> int:
         return binding.pa_check_device_errors(self.error_word, stream)
 
@@ -83,16 +89,18 @@ class GraphStep:
     with request counts rounded up to a capture size and spare rows padded.
     Static buffers hold max_tokens rows of q / key / value / out and max_reqs
     rows of metadata; padding requests have no tokens, so padding tokens get
-    slot -1 and are neither written nor attended.  The graph holds slot
-    mapping, cache write and the attention kernels of pa_attention_launch;
-    the per-step metadata upload (pa_upload_metadata) precedes each replay.
+    slot -1 and are neither written nor attended.  The graph holds the cache
+    write and the attention kernels (fused: pa_attention_with_kv_update_launch;
+    else slot mapping, pa_write_kv and pa_attention_launch); the per-step
+    metadata upload (pa_upload_metadata) precedes each replay.
     """
 
     def __init__(self, *, num_heads_q, num_heads_kv, head_dim, num_blocks, max_blocks_per_req, softmax_scale,
                  max_tokens, max_reqs, max_extend_tiles=0, max_dequant_blocks=0, max_partial_slots=0,
-                 kv_cache_dtype="bf16", k_scale=1.0, v_scale=1.0, num_sms=0, device="cuda"):
+                 kv_cache_dtype="bf16", k_scale=1.0, v_scale=1.0, num_sms=0, device="cuda", fused=True):
         dev = torch.device(device)
         self.device = dev
+        self.fused = fused
         self.model = dict(num_heads_q=num_heads_q, num_heads_kv=num_heads_kv, head_dim=head_dim,
                           num_blocks=num_blocks, max_blocks_per_req=max_blocks_per_req,
                           softmax_scale=softmax_scale, num_sms=num_sms,
@@ -152,7 +160,12 @@ class GraphStep:
 
     def enqueue(self, plan: binding.Plan, key_cache, value_cache, stream=None):
         """Slot mapping, cache write and attention over the static buffers
-        (every launch sized by the capacities; capturable)."""
+        (every launch sized by the capacities; capturable).  Fused: one
+        pa_attention_with_kv_update_launch does all three."""
+        if self.fused:
+            binding.pa_attention_with_kv_update_launch(plan, self.q, self.key, self.value, key_cache, value_cache,
+                                                       self.block_table, self.out, self.workspace, self.slots, stream)
+            return
         binding.pa_slot_mapping(self.qsl, self.num_computed, self.block_table, self.slots.numel(), self.slots,
                                 stream=stream)
         if self.fp8:

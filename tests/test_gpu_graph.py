@@ -1,7 +1,7 @@
 """Fixed-shape plans and CUDA-graph replays (needs a GB300).
 
 One graph is captured per shape (slot mapping, cache write and the attention
-kernels); every later step of a different size only uploads its metadata and
+kernels, or the fused write + attention call); every later step of a different size only uploads its metadata and
 replays.  Each replayed step is checked against the oracle (caches bit for
 bit, attention within tolerance) on the cache state it started from, and
 against the eager path (pa_plan + pa_attention) on the same inputs, bit for
@@ -30,17 +30,18 @@ def _gpu():
     ensure_library()
 
 
-def graph_for(b, max_blocks, **shape):
-    return GraphStep(num_heads_q=b.num_heads_q, num_heads_kv=b.num_heads_kv, head_dim=b.head_dim,
+def graph_for(b, max_blocks, fused=False, **shape):
+    return GraphStep(fused=fused, num_heads_q=b.num_heads_q, num_heads_kv=b.num_heads_kv, head_dim=b.head_dim,
                      num_blocks=b.num_blocks, max_blocks_per_req=max_blocks, softmax_scale=b.softmax_scale,
                      kv_cache_dtype=b.kv_cache_dtype, k_scale=b.k_scale, v_scale=b.v_scale, **shape)
 
 
-def replay_steps(batches, **shape):
-    """Run every batch through one captured graph on one shared cache pool."""
+def replay_steps(batches, fused=False, **shape):
+    """Run every batch through one captured graph on one shared cache pool
+    (fused: the graph holds pa_attention_with_kv_update_launch)."""
     dev = torch.device("cuda")
     mb = max(b.block_table.shape[1] for b in batches)
-    gs = graph_for(batches[0], mb, **shape)
+    gs = graph_for(batches[0], mb, fused, **shape)
     kc = batches[0].key_cache.to(dev, copy=True)
     vc = batches[0].value_cache.to(dev, copy=True)
     for b in batches:
@@ -48,9 +49,10 @@ def replay_steps(batches, **shape):
         out = gs.run(b, b.q.to(dev), b.key.to(dev), b.value.to(dev), kc, vc).clone()
         torch.cuda.synchronize()
         assert gs.check_errors() == 0, b.name
-        okc, ovc, _, oout = run_oracle(before)
+        okc, ovc, oslots, oout = run_oracle(before)
         assert np.array_equal(cache_bits(kc), okc) and np.array_equal(cache_bits(vc), ovc), b.name
         if b.num_tokens:
+            assert np.array_equal(gs.slots[:b.num_tokens].cpu().numpy(), oslots), b.name
             assert_close(out, oout, what=b.name)
             eager = run_gpu(before)
             assert eager.bits == 0
@@ -67,12 +69,14 @@ def decode_steps(kv="bf16"):
     return out
 
 
-def test_graph_replay_decode_steps():
-    replay_steps(decode_steps(), max_tokens=48, max_reqs=48)
+@pytest.mark.parametrize("fused", [False, True])
+def test_graph_replay_decode_steps(fused):
+    replay_steps(decode_steps(), fused, max_tokens=48, max_reqs=48)
 
 
-def test_graph_replay_decode_steps_fp8():
-    replay_steps(decode_steps("fp8"), max_tokens=48, max_reqs=48)
+@pytest.mark.parametrize("fused", [False, True])
+def test_graph_replay_decode_steps_fp8(fused):
+    replay_steps(decode_steps("fp8"), fused, max_tokens=48, max_reqs=48)
 
 
 def mixed_steps(kv="bf16"):
@@ -90,22 +94,26 @@ def mixed_steps(kv="bf16"):
     return out
 
 
-def test_graph_replay_mixed_steps():
-    replay_steps(mixed_steps(), max_tokens=512, max_reqs=8, max_extend_tiles=64)
+@pytest.mark.parametrize("fused", [False, True])
+def test_graph_replay_mixed_steps(fused):
+    replay_steps(mixed_steps(), fused, max_tokens=512, max_reqs=8, max_extend_tiles=64)
 
 
-def test_graph_replay_mixed_steps_fp8():
-    replay_steps(mixed_steps("fp8"), max_tokens=512, max_reqs=8, max_extend_tiles=64, max_dequant_blocks=256)
+@pytest.mark.parametrize("fused", [False, True])
+def test_graph_replay_mixed_steps_fp8(fused):
+    replay_steps(mixed_steps("fp8"), fused, max_tokens=512, max_reqs=8, max_extend_tiles=64,
+                 max_dequant_blocks=256)
 
 
-def test_graph_replay_cascade_steps():
+@pytest.mark.parametrize("fused", [False, True])
+def test_graph_replay_cascade_steps(fused):
     """Cascade steps (shared prefix, batch-wide n) of two sizes in one shape;
     prefix splits need explicit partial-slot room."""
     steps = []
     for i, (n, nb) in enumerate(((24, 16), (9, 8))):
         steps.append(replace(workloads.cascade(batch=n, prefix_tokens=16 * nb, lo=1, hi=200, num_blocks=700,
                                                seed=80 + i), name=f"cascade-step{i}"))
-    replay_steps(steps, max_tokens=24, max_reqs=24, max_extend_tiles=256, max_partial_slots=24 * 160)
+    replay_steps(steps, fused, max_tokens=24, max_reqs=24, max_extend_tiles=256, max_partial_slots=24 * 160)
 
 
 def test_fixed_plan_eager_equals_plain_plan():
