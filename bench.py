@@ -57,6 +57,9 @@ WORKLOADS = {
     "cascade": ("cascade shared-prefix decode: 128 decodes over a 4096-token common prefix "
                 "(num_common_prefix_blocks=256) + private suffixes U[64,1024]; Hq=32 Hkv=8 D=128",
                 lambda seed, dev, kv: workloads.cascade(seed=seed, device=dev, pool_device=dev, kv_cache_dtype=kv)),
+    "verify": ("speculative-decoding verify step: 64 requests x 4 query tokens (1 + 3 drafts), seq_len "
+               "U[512,4096], Hq=32 Hkv=8 D=128 (rows of 2..8 tokens run on the split-KV decode kernel)",
+               lambda seed, dev, kv: workloads.verify(seed=seed, device=dev, pool_device=dev, kv_cache_dtype=kv)),
     "cascade-off": ("the cascade workload on the plain route (num_common_prefix_blocks=0)",
                     lambda seed, dev, kv: workloads.cascade(seed=seed, device=dev, pool_device=dev,
                                                             use_cascade=False, kv_cache_dtype=kv)),

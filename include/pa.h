@@ -117,7 +117,7 @@ typedef struct {
 typedef struct {
     int32_t num_tokens;            /* T                                               */
     int32_t num_decode_rows;       /* requests with exactly one query token           */
-    int32_t num_extend_rows;       /* requests with more than one query token         */
+    int32_t num_extend_rows;       /* requests on the tensor-core tiles (> 1 token)   */
     int32_t num_decode_ctas;       /* persistent CTAs of the split-KV decode kernel   */
     int32_t num_decode_items;      /* (request, key range, head group) segments       */
     int32_t num_extend_tiles;      /* CTA tiles (<= 256 rows) of the tensor-core kernel */
@@ -127,10 +127,16 @@ typedef struct {
     int32_t kernels_per_call;      /* kernel launches one pa_attention call makes     */
     int32_t num_dequant_blocks;    /* FP8: cache blocks the tensor-core tiles read,
                                       expanded to bf16 in the workspace each call   */
-    int64_t decode_kv_bytes;       /* K+V bytes the decode rows must read             */
+    int64_t decode_kv_bytes;       /* K+V bytes the decode kernel's rows must read    */
     int64_t prefix_kv_bytes;       /* K+V bytes of the shared prefix (read once)      */
     double  extend_flops;          /* 4*D*Hq * visible (query, key) pairs, extend     */
     double  prefix_flops;          /* the same for the shared-prefix tiles            */
+    int32_t num_small_q_rows;      /* rows of 2..8 query tokens (speculative verify)
+                                      on the split-KV decode kernel, in units of
+                                      16 / G tokens: every row of at most 16 / G
+                                      tokens, longer ones only while their tiles
+                                      (Hkv per row) would not fill the GPU
+                                      (decode_kv_bytes counts each unit's keys)   */
 } pa_plan_info;
 
 /*

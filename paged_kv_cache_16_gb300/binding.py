@@ -83,6 +83,7 @@ class PlanInfo(ctypes.Structure):
         ("prefix_kv_bytes", ctypes.c_int64),
         ("extend_flops", ctypes.c_double),
         ("prefix_flops", ctypes.c_double),
+        ("num_small_q_rows", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

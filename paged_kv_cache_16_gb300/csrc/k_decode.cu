@@ -60,7 +60,10 @@ struct RowUpdate {
     __device__ __forceinline__ void begin(const DecodeParams &p, const DecodeItem &item, int kvh, int lane,
                                           uint32_t buf) {
         const int lp = (item.key_end - 1) / kBlockSize;
-        last_page = p.new_k != nullptr && item.key_end > 0 && item.page_begin <= lp && lp < item.page_end ? lp : -1;
+        last_page = p.new_k != nullptr && item.n_tok == 1 && item.key_end > 0 && item.page_begin <= lp &&
+                            lp < item.page_end
+                        ? lp
+                        : -1;
         if (last_page < 0) return;
         const int32_t blk = __ldg(p.block_table + static_cast<int64_t>(item.req) * p.max_blocks + lp);
         const int64_t slot = static_cast<int64_t>(blk) * kBlockSize + (item.key_end - 1) % kBlockSize;
@@ -202,6 +205,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         const int g = lane >> 2;
         const int t4 = lane & 3;
         const int G = p.group;
+        const int gsh = __ffs(G) - 1;   // G is a power of two; MMA row r = (token r / G, head r % G)
         constexpr uint32_t kOnes = 0x3C003C00u;  // f16x2 (1, 1)
         const uint32_t k_lane = g * 128u + 4u * t4;   // key g at +0, key g + 8 at +1024
         const uint32_t va_lane = 256u * t4 + 16u * (g >> 2) + 4u * (g & 3);             // key 2t
@@ -212,18 +216,26 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         for (int it = item_begin; it < item_end && ok; ++it) {
             const DecodeItem item = p.items[it];
             const int kvh = item.head_group * HG + warp;
-            const uint16_t *qrow = p.q + (static_cast<int64_t>(item.token) * p.num_heads_q + kvh * G) * D;
+            const int nrow = item.n_tok * G;
+            const int tok0 = g >> gsh, tok1 = (g + 8) >> gsh;
+            const int head0 = kvh * G + (g & (G - 1)), head1 = kvh * G + ((g + 8) & (G - 1));
+            const uint16_t *q0 = p.q + (static_cast<int64_t>(item.token + tok0) * p.num_heads_q + head0) * D;
+            const uint16_t *q1 = p.q + (static_cast<int64_t>(item.token + tok1) * p.num_heads_q + head1) * D;
+            // causal limit of each row: token i sees keys < key_end - (n_tok - 1 - i)
+            const int lim0 = min(item.key_end, item.key_end - (item.n_tok - 1 - tok0));
+            const int lim1 = min(item.key_end, item.key_end - (item.n_tok - 1 - tok1));
+            const int lim_min = item.key_end - (item.n_tok - 1);
             uint32_t qf[D / 16][4];
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const int c = kk * 16 + 4 * t4;
-                auto ld = [&](int row, int col) {
-                    return bf16x2_to_f16x2(__ldg(reinterpret_cast<const uint32_t *>(qrow + row * D + col)));
+                auto ld = [&](const uint16_t *row, int col) {
+                    return bf16x2_to_f16x2(__ldg(reinterpret_cast<const uint32_t *>(row + col)));
                 };
-                qf[kk][0] = g < G ? ld(g, c) : 0u;
-                qf[kk][1] = g + 8 < G ? ld(g + 8, c) : 0u;
-                qf[kk][2] = g < G ? ld(g, c + 2) : 0u;
-                qf[kk][3] = g + 8 < G ? ld(g + 8, c + 2) : 0u;
+                qf[kk][0] = g < nrow ? ld(q0, c) : 0u;
+                qf[kk][1] = g + 8 < nrow ? ld(q1, c) : 0u;
+                qf[kk][2] = g < nrow ? ld(q0, c + 2) : 0u;
+                qf[kk][3] = g + 8 < nrow ? ld(q1, c + 2) : 0u;
             }
             float o[D / 8][4];
 #pragma unroll
@@ -293,13 +305,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 if constexpr (TWO) qk(stage(s1) + warp * C::BOX, sc[2], sc[3]);
                 // keys past the context (their codes may be NaN) or past the
                 // blocks loaded drop out; raw scores, scaled inside ex2
-                const int valid_keys = min(item.key_end - pg * kBlockSize, TWO ? 2 * kBlockSize : kBlockSize);
-                if (!TWO || valid_keys < 2 * kBlockSize) {
+                const int loaded = TWO ? 2 * kBlockSize : kBlockSize;
+                const int valid_keys = min(item.key_end - pg * kBlockSize, loaded);   // V rows past it may be anything
+                if (!TWO || lim_min - pg * kBlockSize < 2 * kBlockSize) {
+                    const int valid0 = min(lim0 - pg * kBlockSize, loaded), valid1 = min(lim1 - pg * kBlockSize, loaded);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            if (j * 8 + 2 * t4 + (e & 1) >= valid_keys) sc[j][e] = -INFINITY;
+                            if (j * 8 + 2 * t4 + (e & 1) >= (e < 2 ? valid0 : valid1)) sc[j][e] = -INFINITY;
                 }
                 constexpr int NT = TWO ? 4 : 2;
                 float mx0 = fmaxf(sc[0][0], sc[0][1]), mx1 = fmaxf(sc[0][2], sc[0][3]);
@@ -366,69 +380,82 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const float l0 = lacc[0], l1 = lacc[2];
             const float inv0 = l0 > 0.f ? p.out_scale / l0 : 0.f;
             const float inv1 = l1 > 0.f ? p.out_scale / l1 : 0.f;
-            const int h_row0 = kvh * G + g, h_row1 = kvh * G + g + 8;
-            // lane holds dims 32a + 8t .. 32a + 8t + 7 of heads g and g + 8:
+            const bool has0 = g < nrow, has1 = g + 8 < nrow;
+            // lane holds dims 32a + 8t .. 32a + 8t + 7 of rows g and g + 8:
             // o[4a + i][0 / 2] -> dim 32a + 8t + i, o[4a + i][1 / 3] -> + 4
             if (item.part < 0) {
-                uint16_t *orow = p.out + static_cast<int64_t>(item.token) * p.num_heads_q * D;
+                uint16_t *orow0 = p.out + (static_cast<int64_t>(item.token + tok0) * p.num_heads_q + head0) * D;
+                uint16_t *orow1 = p.out + (static_cast<int64_t>(item.token + tok1) * p.num_heads_q + head1) * D;
 #pragma unroll
                 for (int a = 0; a < D / 32; ++a) {
                     const int d = 32 * a + 8 * t4;
-                    if (g < G)
-                        *reinterpret_cast<uint4 *>(orow + h_row0 * D + d) =
+                    if (has0)
+                        *reinterpret_cast<uint4 *>(orow0 + d) =
                             make_uint4(pack_bf16x2(o[4 * a][0] * inv0, o[4 * a + 1][0] * inv0),
                                        pack_bf16x2(o[4 * a + 2][0] * inv0, o[4 * a + 3][0] * inv0),
                                        pack_bf16x2(o[4 * a][1] * inv0, o[4 * a + 1][1] * inv0),
                                        pack_bf16x2(o[4 * a + 2][1] * inv0, o[4 * a + 3][1] * inv0));
-                    if (g + 8 < G)
-                        *reinterpret_cast<uint4 *>(orow + h_row1 * D + d) =
+                    if (has1)
+                        *reinterpret_cast<uint4 *>(orow1 + d) =
                             make_uint4(pack_bf16x2(o[4 * a][2] * inv1, o[4 * a + 1][2] * inv1),
                                        pack_bf16x2(o[4 * a + 2][2] * inv1, o[4 * a + 3][2] * inv1),
                                        pack_bf16x2(o[4 * a][3] * inv1, o[4 * a + 1][3] * inv1),
                                        pack_bf16x2(o[4 * a + 2][3] * inv1, o[4 * a + 3][3] * inv1));
                 }
             } else {
-                const int64_t slot = static_cast<int64_t>(p.part_offset[item.token * p.n_groups + item.head_group]) + item.part;
-                float *op = p.o_part + slot * p.num_heads_q * D;
+                const int64_t slot0 = has0 ? static_cast<int64_t>(p.part_offset[(item.token + tok0) * p.n_groups + item.head_group]) + item.part : 0;
+                const int64_t slot1 = has1 ? static_cast<int64_t>(p.part_offset[(item.token + tok1) * p.n_groups + item.head_group]) + item.part : 0;
+                float *op0 = p.o_part + (slot0 * p.num_heads_q + head0) * D;
+                float *op1 = p.o_part + (slot1 * p.num_heads_q + head1) * D;
 #pragma unroll
                 for (int a = 0; a < D / 32; ++a) {
                     const int d = 32 * a + 8 * t4;
-                    if (g < G) {
-                        float4 *dst = reinterpret_cast<float4 *>(op + h_row0 * D + d);
+                    if (has0) {
+                        float4 *dst = reinterpret_cast<float4 *>(op0 + d);
                         dst[0] = make_float4(o[4 * a][0] * inv0, o[4 * a + 1][0] * inv0, o[4 * a + 2][0] * inv0, o[4 * a + 3][0] * inv0);
                         dst[1] = make_float4(o[4 * a][1] * inv0, o[4 * a + 1][1] * inv0, o[4 * a + 2][1] * inv0, o[4 * a + 3][1] * inv0);
                     }
-                    if (g + 8 < G) {
-                        float4 *dst = reinterpret_cast<float4 *>(op + h_row1 * D + d);
+                    if (has1) {
+                        float4 *dst = reinterpret_cast<float4 *>(op1 + d);
                         dst[0] = make_float4(o[4 * a][2] * inv1, o[4 * a + 1][2] * inv1, o[4 * a + 2][2] * inv1, o[4 * a + 3][2] * inv1);
                         dst[1] = make_float4(o[4 * a][3] * inv1, o[4 * a + 1][3] * inv1, o[4 * a + 2][3] * inv1, o[4 * a + 3][3] * inv1);
                     }
                 }
                 if (t4 == 0) {
-                    if (g < G) p.ml_part[slot * p.num_heads_q + h_row0] = make_float2(m0, l0);
-                    if (g + 8 < G) p.ml_part[slot * p.num_heads_q + h_row1] = make_float2(m1, l1);
+                    if (has0) p.ml_part[slot0 * p.num_heads_q + head0] = make_float2(m0, l0);
+                    if (has1) p.ml_part[slot1 * p.num_heads_q + head1] = make_float2(m1, l1);
                 }
             }
         }
     } else {
         // ------------------------------------------------ consumers (bf16) --
-        const int g = lane >> 2;   // MMA row group: query heads g and g + 8
+        // MMA rows g and g + 8 are (query token, head) pairs: row r is token
+        // r / G of the item and head r % G of the kv head's group
+        const int g = lane >> 2;
         const int t4 = lane & 3;
         const int G = p.group;
+        const int gsh = __ffs(G) - 1;   // G is a power of two
         int consumed = 0;
         bool ok = true;
         for (int it = item_begin; it < item_end && ok; ++it) {
             const DecodeItem item = p.items[it];
             const int kvh = item.head_group * HG + warp;
-            const uint16_t *qrow = p.q + (static_cast<int64_t>(item.token) * p.num_heads_q + kvh * G) * D;
+            const int nrow = item.n_tok * G;
+            const int tok0 = g >> gsh, tok1 = (g + 8) >> gsh;
+            const int head0 = kvh * G + (g & (G - 1)), head1 = kvh * G + ((g + 8) & (G - 1));
+            const uint16_t *q0 = p.q + (static_cast<int64_t>(item.token + tok0) * p.num_heads_q + head0) * D;
+            const uint16_t *q1 = p.q + (static_cast<int64_t>(item.token + tok1) * p.num_heads_q + head1) * D;
+            // causal limit of each row: token i sees keys < key_end - (n_tok - 1 - i)
+            const int lim0 = min(item.key_end, item.key_end - (item.n_tok - 1 - tok0));
+            const int lim1 = min(item.key_end, item.key_end - (item.n_tok - 1 - tok1));
             uint32_t qf[D / 16][4];
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const int c = kk * 16 + 2 * t4;
-                qf[kk][0] = g < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + g * D + c)) : 0u;
-                qf[kk][1] = g + 8 < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + (g + 8) * D + c)) : 0u;
-                qf[kk][2] = g < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + g * D + c + 8)) : 0u;
-                qf[kk][3] = g + 8 < G ? __ldg(reinterpret_cast<const uint32_t *>(qrow + (g + 8) * D + c + 8)) : 0u;
+                qf[kk][0] = g < nrow ? __ldg(reinterpret_cast<const uint32_t *>(q0 + c)) : 0u;
+                qf[kk][1] = g + 8 < nrow ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c)) : 0u;
+                qf[kk][2] = g < nrow ? __ldg(reinterpret_cast<const uint32_t *>(q0 + c + 8)) : 0u;
+                qf[kk][3] = g + 8 < nrow ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c + 8)) : 0u;
             }
             float o[D / 8][4];
 #pragma unroll
@@ -461,15 +488,16 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     mma_bf16_16816(sc[0], qf[kk], b0, b1);
                     mma_bf16_16816(sc[1], qf[kk], b2, b3);
                 }
-                // mask keys past the context, scale to log2 units
+                // mask keys past each row's limit, scale to log2 units
                 const int key0 = pg * kBlockSize;
-                const int valid_keys = item.key_end - key0;  // >= 1
+                const int valid_keys = item.key_end - key0;  // >= 1: rows past it may hold anything
+                const int valid0 = lim0 - key0, valid1 = lim1 - key0;
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int key = j * 8 + 2 * t4 + (e & 1);
-                        sc[j][e] = key < valid_keys ? sc[j][e] * p.scale_log2 : -INFINITY;
+                        sc[j][e] = key < (e < 2 ? valid0 : valid1) ? sc[j][e] * p.scale_log2 : -INFINITY;
                     }
                 float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
                 float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
@@ -542,31 +570,30 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
             const float inv0 = l0 > 0.f ? p.out_scale / l0 : 0.f;
             const float inv1 = l1 > 0.f ? p.out_scale / l1 : 0.f;
-            const int h_row0 = kvh * G + g, h_row1 = kvh * G + g + 8;
+            const bool has0 = g < nrow, has1 = g + 8 < nrow;
             if (item.part < 0) {
-                uint16_t *orow = p.out + static_cast<int64_t>(item.token) * p.num_heads_q * D;
+                uint16_t *orow0 = p.out + (static_cast<int64_t>(item.token + tok0) * p.num_heads_q + head0) * D;
+                uint16_t *orow1 = p.out + (static_cast<int64_t>(item.token + tok1) * p.num_heads_q + head1) * D;
 #pragma unroll
                 for (int j = 0; j < D / 8; ++j) {
                     const int d = j * 8 + 2 * t4;
-                    if (g < G)
-                        *reinterpret_cast<uint32_t *>(orow + h_row0 * D + d) = pack_bf16x2(o[j][0] * inv0, o[j][1] * inv0);
-                    if (g + 8 < G)
-                        *reinterpret_cast<uint32_t *>(orow + h_row1 * D + d) = pack_bf16x2(o[j][2] * inv1, o[j][3] * inv1);
+                    if (has0) *reinterpret_cast<uint32_t *>(orow0 + d) = pack_bf16x2(o[j][0] * inv0, o[j][1] * inv0);
+                    if (has1) *reinterpret_cast<uint32_t *>(orow1 + d) = pack_bf16x2(o[j][2] * inv1, o[j][3] * inv1);
                 }
             } else {
-                const int64_t slot = static_cast<int64_t>(p.part_offset[item.token * p.n_groups + item.head_group]) + item.part;
-                float *op = p.o_part + slot * p.num_heads_q * D;
+                const int64_t slot0 = has0 ? static_cast<int64_t>(p.part_offset[(item.token + tok0) * p.n_groups + item.head_group]) + item.part : 0;
+                const int64_t slot1 = has1 ? static_cast<int64_t>(p.part_offset[(item.token + tok1) * p.n_groups + item.head_group]) + item.part : 0;
+                float *op0 = p.o_part + (slot0 * p.num_heads_q + head0) * D;
+                float *op1 = p.o_part + (slot1 * p.num_heads_q + head1) * D;
 #pragma unroll
                 for (int j = 0; j < D / 8; ++j) {
                     const int d = j * 8 + 2 * t4;
-                    if (g < G)
-                        *reinterpret_cast<float2 *>(op + h_row0 * D + d) = make_float2(o[j][0] * inv0, o[j][1] * inv0);
-                    if (g + 8 < G)
-                        *reinterpret_cast<float2 *>(op + h_row1 * D + d) = make_float2(o[j][2] * inv1, o[j][3] * inv1);
+                    if (has0) *reinterpret_cast<float2 *>(op0 + d) = make_float2(o[j][0] * inv0, o[j][1] * inv0);
+                    if (has1) *reinterpret_cast<float2 *>(op1 + d) = make_float2(o[j][2] * inv1, o[j][3] * inv1);
                 }
                 if (t4 == 0) {
-                    if (g < G) p.ml_part[slot * p.num_heads_q + h_row0] = make_float2(m0, l0);
-                    if (g + 8 < G) p.ml_part[slot * p.num_heads_q + h_row1] = make_float2(m1, l1);
+                    if (has0) p.ml_part[slot0 * p.num_heads_q + head0] = make_float2(m0, l0);
+                    if (has1) p.ml_part[slot1 * p.num_heads_q + head1] = make_float2(m1, l1);
                 }
             }
         }

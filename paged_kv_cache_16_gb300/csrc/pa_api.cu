@@ -192,23 +192,33 @@ pa_status validate(const pa_batch_desc *d) {
     return PA_OK;
 }
 
+// A unit of the split-KV decode kernel: n_tok <= 16 / G consecutive query
+// tokens of one request whose G heads fill the 16 rows of one MMA tile; the
+// unit reads keys [0, key_end), key_end = one past its last token's position.
+struct DecodeUnit {
+    int32_t r, t0, n_tok, key_end;
+};
+
 // Cut the concatenated decode runs into ncta equal contiguous shares.
+// pieces[u * n_groups + grp] receives the number of runs unit u was cut into;
+// item_unit[i] the unit of item i.
 // fixed_ncta > 0: the grid has exactly that many CTAs; the shares past the
 // ones the work needs are empty.
-void plan_decode(pa_plan_s *P, const pa_batch_desc *d, const std::vector<int32_t> &decode_rows,
-                 std::vector<int32_t> &pieces, int64_t fixed_ncta) {
-    struct Run { int32_t r, grp, pb, pe; };
+void plan_decode(pa_plan_s *P, const std::vector<DecodeUnit> &units, std::vector<int32_t> &pieces,
+                 std::vector<int32_t> &item_unit, int64_t fixed_ncta) {
+    struct Run { int32_t u, grp, pb, pe; };
     std::vector<Run> runs;
     const int32_t kb = P->n_prefix;  // first block of the suffix work
     int64_t total = 0;
     for (int grp = 0; grp < P->n_groups; ++grp)
-        for (int32_t r : decode_rows) {
-            const int32_t pe = (d->seq_lens[r] + kBlockSize - 1) / kBlockSize;
+        for (size_t u = 0; u < units.size(); ++u) {
+            const int32_t pe = (units[u].key_end + kBlockSize - 1) / kBlockSize;
             if (pe <= kb) continue;
-            runs.push_back({r, grp, kb, pe});
+            runs.push_back({static_cast<int32_t>(u), grp, kb, pe});
             total += pe - kb;
         }
-    pieces.assign(static_cast<size_t>(d->num_reqs) * P->n_groups, 0);
+    pieces.assign(units.size() * P->n_groups, 0);
+    item_unit.clear();
     P->cta_begin.assign(1, 0);
     if (total == 0) {
         if (fixed_ncta > 0) P->cta_begin.assign(static_cast<size_t>(fixed_ncta) + 1, 0);
@@ -225,16 +235,19 @@ void plan_decode(pa_plan_s *P, const pa_batch_desc *d, const std::vector<int32_t
         int64_t quota = total / ncta + (c < total % ncta ? 1 : 0);
         while (quota > 0 && run < runs.size()) {
             const Run &R = runs[run];
+            const DecodeUnit &U = units[R.u];
             const int32_t take = static_cast<int32_t>(std::min<int64_t>(quota, R.pe - cursor));
             DecodeItem it{};
-            it.token = d->query_start_loc[R.r];
-            it.req = R.r;
+            it.token = U.t0;
+            it.req = U.r;
             it.page_begin = cursor;
             it.page_end = cursor + take;
-            it.key_end = d->seq_lens[R.r];
+            it.key_end = U.key_end;
             it.head_group = R.grp;
-            it.part = pieces[static_cast<size_t>(R.r) * P->n_groups + R.grp]++;
+            it.part = pieces[static_cast<size_t>(R.u) * P->n_groups + R.grp]++;
+            it.n_tok = U.n_tok;
             P->items.push_back(it);
+            item_unit.push_back(R.u);
             cursor += take;
             quota -= take;
             if (cursor >= R.pe) {
@@ -274,12 +287,27 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     }
     if (P->fixed && (P->T > shape->max_tokens || P->R > shape->max_reqs)) return PA_ERR_CAPACITY;
     const int32_t *qsl = d->query_start_loc;
-    std::vector<int32_t> decode_rows, extend_rows;
+    // q_len 1: decode rows.  2..kMaxSmallQ (speculative verify): on the
+    // split-KV decode kernel when the row fits one 16-row unit, or when it
+    // needs several units (each re-reads the row's keys) but the tensor-core
+    // tiles of all such rows would not fill the GPU; else, and for longer
+    // rows, tensor-core tiles.
+    const int32_t tg = std::max(1, kMmaRows / P->G);   // tokens per decode unit
+    std::vector<int32_t> decode_rows, small_rows, extend_rows, multi_unit;
     for (int32_t r = 0; r < P->R; ++r) {
         const int32_t q_len = qsl[r + 1] - qsl[r];
         if (q_len == 1) decode_rows.push_back(r);
+        else if (q_len > 1 && q_len <= tg) small_rows.push_back(r);
+        else if (q_len > 1 && q_len <= kMaxSmallQ) multi_unit.push_back(r);
         else if (q_len > 1) extend_rows.push_back(r);
     }
+    const bool multi_on_decode = static_cast<int64_t>(multi_unit.size()) * P->Hkv < P->num_sms;
+    for (int32_t r : multi_unit) (multi_on_decode ? small_rows : extend_rows).push_back(r);
+    std::sort(small_rows.begin(), small_rows.end());
+    std::sort(extend_rows.begin(), extend_rows.end());
+    std::vector<char> on_decode(static_cast<size_t>(P->R), 0);
+    for (int32_t r : decode_rows) on_decode[r] = 1;
+    for (int32_t r : small_rows) on_decode[r] = 1;
     const bool cascade = d->num_common_prefix_blocks > 0 && P->T > 0;
     P->n_prefix = cascade ? d->num_common_prefix_blocks : 0;
     const int32_t kb_keys = P->n_prefix * kBlockSize;
@@ -365,12 +393,24 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     }
 
     // ------------------------------------------------------------- decode
-    std::vector<int32_t> pieces;
+    std::vector<DecodeUnit> units;
+    for (int32_t r = 0; r < P->R; ++r) {
+        const int32_t q_len = qsl[r + 1] - qsl[r];
+        if (!on_decode[r]) continue;
+        for (int32_t j = 0; j < q_len; j += tg) {
+            const int32_t n = std::min(tg, q_len - j);
+            units.push_back({r, qsl[r] + j, n, d->num_computed_tokens[r] + j + n});
+        }
+    }
+    std::vector<int32_t> pieces, item_unit;
     const int cps = std::max(1, decode_ctas_per_sm_static(P->D, P->HG, P->kv8));
-    plan_decode(P, d, decode_rows, pieces, P->fixed ? static_cast<int64_t>(P->num_sms) * cps : 0);
+    plan_decode(P, units, pieces, item_unit, P->fixed ? static_cast<int64_t>(P->num_sms) * cps : 0);
 
     // ------------------------------- fused cache update of extend rows
-    for (int32_t r : extend_rows) {
+    std::vector<int32_t> multi_rows(small_rows);
+    multi_rows.insert(multi_rows.end(), extend_rows.begin(), extend_rows.end());
+    std::sort(multi_rows.begin(), multi_rows.end());
+    for (int32_t r : multi_rows) {
         WriteRun w{};
         w.t0 = qsl[r];
         w.n_tok = qsl[r + 1] - qsl[r];
@@ -383,19 +423,20 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
 
     // ----------------------------------------------------- partial slots
     std::vector<int32_t> count(static_cast<size_t>(P->T) * P->n_groups, 0);
-    for (int32_t r : decode_rows)
+    for (size_t u = 0; u < units.size(); ++u)
         for (int grp = 0; grp < P->n_groups; ++grp) {
-            const int32_t k = pieces[static_cast<size_t>(r) * P->n_groups + grp];
-            count[static_cast<size_t>(qsl[r]) * P->n_groups + grp] =
-                cascade ? P->prefix_splits + k : (k > 1 ? k : 0);
+            const int32_t k = pieces[u * P->n_groups + grp];
+            for (int32_t t = units[u].t0; t < units[u].t0 + units[u].n_tok; ++t)
+                count[static_cast<size_t>(t) * P->n_groups + grp] = cascade ? P->prefix_splits + k : (k > 1 ? k : 0);
         }
     if (cascade)
         for (int32_t r : extend_rows)
             for (int32_t t = qsl[r]; t < qsl[r + 1]; ++t)
                 for (int grp = 0; grp < P->n_groups; ++grp)
                     count[static_cast<size_t>(t) * P->n_groups + grp] = P->prefix_splits + 1;
-    for (DecodeItem &it : P->items) {
-        const int32_t k = pieces[static_cast<size_t>(it.req) * P->n_groups + it.head_group];
+    for (size_t i = 0; i < P->items.size(); ++i) {
+        DecodeItem &it = P->items[i];
+        const int32_t k = pieces[static_cast<size_t>(item_unit[i]) * P->n_groups + it.head_group];
         if (cascade) it.part += P->prefix_splits;
         else if (k == 1) it.part = -1;
     }
@@ -421,7 +462,8 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     P->ncta = static_cast<int32_t>(P->cta_begin.size()) - 1;
     const int32_t scr_rows = P->max_blocks > 0 ? static_cast<int32_t>(P->scratch_table.size() / P->max_blocks) : 0;
     if (P->fixed) {
-        const int64_t items_cap = static_cast<int64_t>(P->ncta) + static_cast<int64_t>(shape->max_reqs) * P->n_groups;
+        // every decode unit holds at least one token
+        const int64_t items_cap = static_cast<int64_t>(P->ncta) + static_cast<int64_t>(shape->max_tokens) * P->n_groups;
         const int64_t merges_cap = static_cast<int64_t>(shape->max_tokens) * P->n_groups;
         const int64_t slots_cap = shape->max_partial_slots > 0 ? shape->max_partial_slots : items_cap + merges_cap;
         if (items_cap > INT32_MAX || merges_cap > INT32_MAX || slots_cap > INT32_MAX) return PA_ERR_UNSUPPORTED;
@@ -432,7 +474,8 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
         P->cap_dequant = P->kv8 && P->cap_tiles > 0 ? shape->max_dequant_blocks : 0;
         P->cap_slots = static_cast<int32_t>(slots_cap);
         P->cap_scr_rows = P->kv8 && P->cap_tiles > 0 ? shape->max_reqs : 0;
-        P->cap_runs = P->cap_tiles > 0 ? shape->max_reqs : 0;
+        // a row of several query tokens makes T exceed the request count
+        P->cap_runs = shape->max_tokens > shape->max_reqs ? shape->max_reqs : 0;
         if (static_cast<int64_t>(P->items.size()) > P->cap_items ||
             static_cast<int64_t>(P->tiles.size()) > P->cap_tiles ||
             static_cast<int64_t>(P->merges.size()) > P->cap_merges || P->num_scratch_blocks > P->cap_dequant ||
@@ -502,6 +545,7 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     I.num_tokens = P->T;
     I.num_decode_rows = static_cast<int32_t>(decode_rows.size());
     I.num_extend_rows = static_cast<int32_t>(extend_rows.size());
+    I.num_small_q_rows = static_cast<int32_t>(small_rows.size());
     I.num_decode_ctas = P->ncta;
     I.num_decode_items = static_cast<int32_t>(P->items.size());
     I.num_extend_tiles = static_cast<int32_t>(P->tiles.size());
@@ -511,7 +555,7 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
                          (P->cap_dequant > 0 ? 1 : 0);
     I.num_dequant_blocks = P->num_scratch_blocks;
     const int64_t row_bytes = static_cast<int64_t>(P->Hkv) * P->D * 2 * (P->kv8 ? 1 : 2);   // K and V
-    for (int32_t r : decode_rows) I.decode_kv_bytes += (d->seq_lens[r] - kb_keys) * row_bytes;
+    for (const DecodeUnit &u : units) I.decode_kv_bytes += std::max(0, u.key_end - kb_keys) * row_bytes;
     I.prefix_kv_bytes = cascade ? kb_keys * row_bytes : 0;
     double pairs = 0.0;
     for (int32_t r : extend_rows) {

@@ -14,6 +14,8 @@ constexpr int kBlockSize = 16;     // tokens per cache block
 constexpr int kTileKeys = 128;     // keys per tensor-core tile (8 blocks)
 constexpr int kTileRows = 128;     // query rows per tensor-core sub-tile (two per CTA)
 constexpr int kMaxDecodeHeads = 8; // kv heads one decode CTA serves
+constexpr int kMmaRows = 16;       // rows of one decode MMA tile: (query token, head) pairs
+constexpr int kMaxSmallQ = 8;      // longest row (query tokens) the decode kernel takes
 
 // Split-KV decode kernel resources, shared by the planner (which sizes the
 // persistent grid without touching a device) and the kernel.  kv8: E4M3
@@ -51,10 +53,11 @@ struct DecodeItem {
     int32_t req;         // block-table row
     int32_t page_begin;  // first logical block of the run
     int32_t page_end;    // one past the last logical block of the run
-    int32_t key_end;     // keys >= key_end are masked (= seq_len)
+    int32_t key_end;     // keys >= key_end are masked (one past the last token's position)
     int32_t head_group;  // kv heads [head_group*HG, head_group*HG + HG)
     int32_t part;        // partial index of this run (-1: write bf16 output)
-    int32_t pad;
+    int32_t n_tok;       // query tokens token .. token + n_tok - 1 (n_tok * G <= 16); token i
+                         // sees keys < key_end - (n_tok - 1 - i)
 };
 
 // One CTA tile of up to 256 query rows (2 x 128/G consecutive tokens x the

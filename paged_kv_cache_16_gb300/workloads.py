@@ -264,6 +264,19 @@ def decode(seed: int = 0, batch: int = 64, lo: int = 512, hi: int = 4096, num_bl
                       pool_device=pool_device, kv_cache_dtype=kv_cache_dtype)
 
 
+def verify(seed: int = 0, batch: int = 64, q_len: int = 4, lo: int = 512, hi: int = 4096, num_blocks: int = 20000,
+           poison: str = "finite", device="cpu", pool_device=None, kv_cache_dtype: str = "bf16") -> Batch:
+    """Speculative-decoding verify step on the decode workload's shape: 64
+    requests each scoring q_len tokens (the last accepted token + q_len - 1
+    drafts) over seq_len ~ U[512, 4096] (including the q_len new tokens)."""
+    rng = np.random.default_rng(seed + 11)
+    seq = rng.integers(lo, hi + 1, size=batch)
+    return make_batch(name="verify", num_heads_q=32, num_heads_kv=8, head_dim=128,
+                      q_lens=np.full(batch, q_len, dtype=np.int64), seq_lens=seq,
+                      num_blocks=num_blocks, seed=seed, poison=poison, device=device,
+                      pool_device=pool_device, kv_cache_dtype=kv_cache_dtype)
+
+
 def mixed(seed: int = 0, n_decode: int = 256, lo: int = 1024, hi: int = 8192, n_shared: int = 32,
           shared_tokens: int = 1024, chunk: int = 2048, chunk_b_cached: int = 4096,
           poison: str = "finite", device="cpu", pool_device=None, kv_cache_dtype: str = "bf16") -> Batch:

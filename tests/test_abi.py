@@ -125,9 +125,13 @@ def test_mixed_batch_example_metadata(lib):
               num_computed_tokens=nc, max_blocks_per_req=65, softmax_scale=0.1, num_sms=152)
     plan = binding.pa_plan(**kw)
     info = plan.info()
-    assert info["num_decode_rows"] == 1 and info["num_extend_rows"] == 2
-    # 256 + 3 query tokens, G = 4 -> 64 tokens per CTA tile: 4 + 1 tiles per kv head
-    assert info["num_extend_tiles"] == 2 * (4 + 1)
+    # R0 decode; R1's 256-token chunk on the tiles; R2's 3-token verify row on
+    # the decode kernel (3 tokens x G = 4 heads fill one 16-row MMA tile)
+    assert info["num_decode_rows"] == 1 and info["num_extend_rows"] == 1 and info["num_small_q_rows"] == 1
+    # 256 query tokens, G = 4 -> 64 tokens per CTA tile: 4 tiles per kv head
+    assert info["num_extend_tiles"] == 2 * 4
+    row_bytes = 2 * 128 * 4
+    assert info["decode_kv_bytes"] == (1025 + 603) * row_bytes
     bad = nc.copy()
     bad[1] = 511
     assert binding.pa_plan_status(**{**kw, "num_computed_tokens": bad}) == binding.PA_ERR_INVALID_ARGUMENT
@@ -272,3 +276,40 @@ def test_zero_blocks_argument_checks(lib):
     assert L.pa_zero_blocks(None, -1, 10, 8, 128, 0, None, None, None, None) == binding.PA_ERR_INVALID_ARGUMENT
     assert L.pa_zero_blocks(None, 1, 10, 8, 128, 0, None, None, None, None) == binding.PA_ERR_INVALID_ARGUMENT
     assert L.pa_zero_blocks(None, 0, 10, 8, 128, 7, None, None, None, None) == binding.PA_ERR_INVALID_ARGUMENT
+
+
+@pytest.mark.parametrize("g,q_len,units", [(4, 3, 1), (4, 4, 1), (4, 5, 2), (8, 3, 2), (8, 8, 4), (1, 8, 1),
+                                           (16, 2, 2), (4, 9, 0)])
+def test_small_q_units(lib, g, q_len, units):
+    """Rows of 2..8 query tokens run on the decode kernel in units of 16 / G
+    tokens (each unit reads its keys once); longer rows go to the tiles."""
+    hkv = 2
+    qsl = np.array([0, q_len], np.int32)
+    seq = np.array([500], np.int32)
+    kw = dict(num_heads_q=g * hkv, num_heads_kv=hkv, head_dim=128, num_blocks=64, query_start_loc=qsl,
+              seq_lens=seq, num_computed_tokens=seq - q_len, max_blocks_per_req=32, softmax_scale=0.1,
+              num_sms=152)
+    info = binding.pa_plan(**kw).info()
+    if units == 0:
+        assert info["num_small_q_rows"] == 0 and info["num_extend_rows"] == 1
+        return
+    assert info["num_small_q_rows"] == 1 and info["num_extend_tiles"] == 0
+    tg = max(1, 16 // g)
+    ends = [500 - q_len + min(q_len, j + tg) for j in range(0, q_len, tg)]
+    assert len(ends) == units
+    assert info["decode_kv_bytes"] == sum(ends) * hkv * 128 * 4
+
+
+def test_small_q_routing_by_parallelism(lib):
+    """Rows needing several units go to the decode kernel only while their
+    tiles would not fill the GPU; one-unit rows always do."""
+    def plan(n, q_len, g=4):
+        qsl = np.arange(n + 1, dtype=np.int32) * q_len
+        seq = np.full(n, 1000, np.int32)
+        return binding.pa_plan(num_heads_q=8 * g, num_heads_kv=8, head_dim=128, num_blocks=64 * n + 64,
+                               query_start_loc=qsl, seq_lens=seq, num_computed_tokens=seq - q_len,
+                               max_blocks_per_req=64, softmax_scale=0.1, num_sms=152).info()
+    assert plan(64, 4)["num_small_q_rows"] == 64                      # one unit each
+    assert plan(18, 8)["num_small_q_rows"] == 18                      # 18 x 8 tiles < 152 SMs
+    i = plan(64, 8)                                                   # 512 tile CTAs: tiles read keys once
+    assert i["num_small_q_rows"] == 0 and i["num_extend_rows"] == 64
