@@ -69,10 +69,12 @@ WORKLOADS = {
 # dominant kernel from one ncu capture, valid only while the kernel source is
 # unchanged (sha256 of the file).  Filled in from profiles/.
 TRAFFIC = {
-    # (kernel, workload, source sha) -> bytes per launch; profiles/decode_kernel_decode-workload.md
-    ("decode", "decode", "556c55355d272fd6"): 644_464_640,
-    # profiles/extend_kernel_prefill-workload.md
-    ("extend", "prefill", "ac26b38d115f117e"): 73_388_800,
+    # (kernel, workload, kv dtype, source sha) -> bytes per launch (fused-write variant, the one the
+    # default step runs); profiles/decode_kernel_decode-workload.md, profiles/extend_kernel_prefill-workload.md,
+    # profiles/decode_kernel_e4m3_decode-workload.md
+    ("decode", "decode", "bf16", "79d3029d410f26bd"): 645_937_152,
+    ("decode", "decode", "fp8", "79d3029d410f26bd"): 327_966_208,
+    ("extend", "prefill", "bf16", "444f2a654d3f3c75"): 76_144_128,
 }
 KERNEL_SOURCES = {"decode": "paged_kv_cache_16_gb300/csrc/k_decode.cu",
                   "extend": "paged_kv_cache_16_gb300/csrc/k_extend.cu"}
@@ -359,7 +361,7 @@ def run_ours(args, world, rank, local):
         algo = info["decode_kv_bytes"] + q_out_bytes
         achieved = algo / t_launch / 1e9
         sha = source_sha("decode")
-        traffic = TRAFFIC.get(("decode", args.workload, sha))
+        traffic = TRAFFIC.get(("decode", args.workload, args.kv_dtype, sha))
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                     "traffic": traffic, "kernel": "decode_kernel", "peak_source": f"{peak_src} hbm_gbs",
                     "algorithmic_bytes_per_launch": algo, "launch_ms": t_launch * 1e3}
@@ -369,7 +371,7 @@ def run_ours(args, world, rank, local):
         flops = info["extend_flops"] + info["prefix_flops"]
         achieved = flops / t_launch / 1e12
         sha = source_sha("extend")
-        traffic = TRAFFIC.get(("extend", args.workload, sha))
+        traffic = TRAFFIC.get(("extend", args.workload, args.kv_dtype, sha))
         roofline = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
                     "frac": achieved / bf16, "traffic": traffic, "kernel": "extend_kernel",
                     "peak_source": f"{peak_src} bf16_tflops (burst)", "algorithmic_flops_per_launch": flops,

@@ -229,28 +229,36 @@ __device__ __forceinline__ float f16_hi(uint32_t v) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// Packed fp32 pairs (one 64-bit register pair, low element first) and the
+// paired FMA / add of the sm_100 family; 3-input max.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-// 2^x on the FMA pipe, for x <= 2^22 (inputs below -120 give ~2^-120):
-// x = n + f with n = round(x) and f in [-1/2, 1/2]; 2^f from a degree-3
-// polynomial fitted for minimum relative error (coefficients printed by
-// csrc/gen_exp2_poly.py, max relative error 7.5e-5); n is added to the
-// exponent field of the polynomial's value as an integer.
-__device__ __forceinline__ float ex2_fma(float x) {
-    constexpr float kRound = 12582912.f;          // 1.5 * 2^23
-    x = fmaxf(x, -120.f);
-    const float y = x + kRound;                   // integer part in the low mantissa bits
-    const float f = x - (y - kRound);
-    float p = 0.05517132207751274f;
-    p = fmaf(p, f, 0.24261054396629333f);
-    p = fmaf(p, f, 0.6932609677314758f);
-    p = fmaf(p, f, 0.9999281167984009f);
-    // (bits of y) << 23 == n << 23: the low 9 bits of kRound's pattern are 0
-    return __int_as_float(__float_as_int(p) + (__float_as_int(y) << 23));
 }
 
 // ---------------------------------------------- legacy warp MMA (mma.sync) --

@@ -17,7 +17,8 @@
 //   P_t = exp2(S_t*scale*log2e - m)   softmax warpgroup t, one row per thread,
 //                        written back to tensor memory over S_t as bf16 pairs
 //   O_t += P_t V         tcgen05.mma M=128 N=D K=128, A from tensor memory
-// Warp roles: warp 0 TMA producer (Q once, K and V blocks into 2-stage rings),
+// Warp roles: warp 0 TMA producer (Q once, K and V blocks into 2- and 3-stage
+// rings; a V stage is released as soon as both PVs reading it are done),
 // warp 1 MMA issuer (one thread) and tensor-memory owner, warps 2-5 softmax
 // of sub-tile 0, warps 6-9 softmax of sub-tile 1.  The MMA thread alternates
 // between the sub-tiles, so the tensor core works on one while the other's
@@ -41,9 +42,10 @@ struct ExtCfg {
     static constexpr int HALF = 128 * 128;            // [128 rows][64] bf16 half tile
     static constexpr int QB = NH * HALF;              // one Q sub-tile
     static constexpr int KVB = NH * HALF;             // K (or V) tile bytes per stage
-    static constexpr int NS = 2;
+    static constexpr int NSK = 2;                     // K stages
+    static constexpr int NSV = 3;                     // V stages (V waits longest for its stage)
     static constexpr int THREADS = 320;
-    static constexpr int TILE_SMEM = 2 * QB + NS * 2 * KVB;
+    static constexpr int TILE_SMEM = 2 * QB + (NSK + NSV) * KVB;
     // one CTA per SM: it owns all 512 tensor-memory columns
     static constexpr int SMEM = (TILE_SMEM + 2048 < 120 * 1024) ? 120 * 1024 : TILE_SMEM + 2048;
     static constexpr uint32_t TMEM_COLS = 512;
@@ -51,12 +53,6 @@ struct ExtCfg {
     static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
 };
 
-// Every kFmaExpEvery-th exponential of the softmax is evaluated on the FMA
-// pipe (ex2_fma) instead of the special-function unit (0 = never).
-#ifndef PA_FMA_EXP_EVERY
-#define PA_FMA_EXP_EVERY 0
-#endif
-constexpr int kFmaExpEvery = PA_FMA_EXP_EVERY;
 
 __device__ __forceinline__ uint32_t col_s(int t) { return static_cast<uint32_t>(t) * 128u; }
 __device__ __forceinline__ uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(t) * 128u; }
@@ -66,15 +62,15 @@ __device__ __forceinline__ uint32_t col_o(int t) { return 256u + static_cast<uin
 // next K tile is loaded while the current tile's softmax and PV still run.
 enum : int {
     B_Q = 0,
-    B_KFULL = 1,   // +stage
-    B_VFULL = 3,   // +stage
-    B_KEMPTY = 5,  // +stage
-    B_VEMPTY = 7,  // +stage
-    B_SFULL = 9,   // +sub-tile
-    B_PFULL = 11,  // +sub-tile
-    B_ODONE = 13,  // +sub-tile
-    B_DRAIN = 15,
-    NUM_BARS = 16
+    B_KFULL = 1,    // +stage (2)
+    B_VFULL = 3,    // +stage (3)
+    B_KEMPTY = 6,   // +stage (2)
+    B_VEMPTY = 8,   // +stage (3)
+    B_SFULL = 11,   // +sub-tile
+    B_PFULL = 13,   // +sub-tile
+    B_ODONE = 15,   // +sub-tile
+    B_DRAIN = 17,
+    NUM_BARS = 18
 };
 
 template <int D>
@@ -89,8 +85,8 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     auto q_s = [&](int t) { return base + static_cast<uint32_t>(t) * C::QB; };
-    auto k_s = [&](int s) { return base + 2 * C::QB + static_cast<uint32_t>(s) * 2 * C::KVB; };
-    auto v_s = [&](int s) { return k_s(s) + C::KVB; };
+    auto k_s = [&](int s) { return base + 2 * C::QB + static_cast<uint32_t>(s) * C::KVB; };
+    auto v_s = [&](int s) { return base + 2 * C::QB + static_cast<uint32_t>(C::NSK + s) * C::KVB; };
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
     if (static_cast<int>(blockIdx.x) >= p.counts[kCountTiles]) return;   // grid sized for a capacity
@@ -117,10 +113,12 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     if (threadIdx.x == 0) {
         abort_flag = 0;
         mbar_init(bar(B_Q), 1);
-        for (int s = 0; s < C::NS; ++s) {
+        for (int s = 0; s < C::NSK; ++s) {
             mbar_init(bar(B_KFULL + s), 1);
-            mbar_init(bar(B_VFULL + s), 1);
             mbar_init(bar(B_KEMPTY + s), 1);
+        }
+        for (int s = 0; s < C::NSV; ++s) {
+            mbar_init(bar(B_VFULL + s), 1);
             mbar_init(bar(B_VEMPTY + s), 1);
         }
         for (int t = 0; t < 2; ++t) {
@@ -157,8 +155,6 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int32_t *bt = p.block_table + static_cast<int64_t>(tile.req) * p.max_blocks;
         int issued[2] = {0, 0};   // K and V tiles whose loads were issued
         for (int j = 0; j < n_tiles; ++j) {
-            const int s = j % C::NS;
-            const int n = j / C::NS;
             const int kt0 = tile.key_begin + j * kTileKeys;
             const int pages = min(8, (tile.key_end - kt0 + kBlockSize - 1) / kBlockSize);
             int32_t blk = 0;
@@ -178,6 +174,8 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             bool ok = true;
 #pragma unroll
             for (int tensor = 0; tensor < 2; ++tensor) {
+                const int ns = tensor ? C::NSV : C::NSK;
+                const int s = j % ns, n = j / ns;
                 const int empty = tensor ? B_VEMPTY : B_KEMPTY;
                 const int full = tensor ? B_VFULL : B_KFULL;
                 if (n > 0 && !warp_wait(bar(empty + s), (n & 1) ^ 1, &abort_flag)) {
@@ -198,8 +196,9 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // no TMA write may outlive the CTA
             if (!mbar_wait(bar(B_Q), 0, nullptr)) atomicOr(p.err, kErrTimeout);
             for (int tensor = 0; tensor < 2; ++tensor)
-                for (int k = issued[tensor] - 1; k >= 0 && k >= issued[tensor] - C::NS; --k) {
-                    const int s = k % C::NS, n = k / C::NS;
+                for (int k = issued[tensor] - 1; k >= 0 && k >= issued[tensor] - (tensor ? C::NSV : C::NSK); --k) {
+                    const int ns = tensor ? C::NSV : C::NSK;
+                    const int s = k % ns, n = k / ns;
                     if (!mbar_wait(bar((tensor ? B_VFULL : B_KFULL) + s), n & 1, nullptr))
                         atomicOr(p.err, kErrTimeout);
                 }
@@ -209,7 +208,7 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (lane == 0) {
             bool ok = mbar_wait_spin(bar(B_Q), 0, &abort_flag);
             auto qk = [&](int t, int j) {
-                const int s = j % C::NS;
+                const int s = j % C::NSK;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t a = sdesc_sw128(q_s(t) + (kk / 4) * C::HALF + (kk % 4) * 32, 16, 1024);
@@ -221,7 +220,7 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             auto pv = [&](int t, int j) -> bool {
                 if (!mbar_wait_spin(bar(B_PFULL + t), j & 1, &abort_flag)) return false;
                 tc_fence_after();
-                const int s = j % C::NS;
+                const int s = j % C::NSV;
 #pragma unroll
                 for (int kk = 0; kk < kTileKeys / 16; ++kk) {
                     const uint64_t b = sdesc_sw128(v_s(s) + kk * 2048, C::HALF, 1024);
@@ -238,16 +237,18 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 if (ok) tc_commit(bar(B_KEMPTY));          // K tile 0 read by both QK^T
             }
             for (int j = 0; j < n_tiles && ok; ++j) {
-                const int s = j % C::NS;
-                const int s1 = (j + 1) % C::NS;
-                const uint32_t par1 = ((j + 1) / C::NS) & 1;
+                const int sv = j % C::NSV;
+                const int s1 = (j + 1) % C::NSK;
+                const uint32_t par1 = ((j + 1) / C::NSK) & 1;
+                const int t_last = j < n_sub[1] ? 1 : 0;   // last sub-tile that reads V tile j
                 bool k_next_ready = false;
-                ok = mbar_wait_spin(bar(B_VFULL + s), (j / C::NS) & 1, &abort_flag);
+                ok = mbar_wait_spin(bar(B_VFULL + sv), (j / C::NSV) & 1, &abort_flag);
 #pragma unroll
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (j >= n_sub[t]) continue;
                     ok = pv(t, j);
                     if (!ok) break;
+                    if (t == t_last) tc_commit(bar(B_VEMPTY + sv));   // V tile j read by both PV
                     if (j + 1 < n_sub[t]) {
                         if (!k_next_ready) {
                             ok = mbar_wait_spin(bar(B_KFULL + s1), par1, &abort_flag);
@@ -260,10 +261,7 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         tc_commit(bar(B_ODONE + t));
                     }
                 }
-                if (ok) {
-                    tc_commit(bar(B_VEMPTY + s));                      // V tile j read by both PV
-                    if (j + 1 < n_tiles) tc_commit(bar(B_KEMPTY + s1));  // K tile j+1 read by both QK^T
-                }
+                if (ok && j + 1 < n_tiles) tc_commit(bar(B_KEMPTY + s1));  // K tile j+1 read by both QK^T
             }
             if (!ok) raise_abort(&abort_flag, p.err, kErrTimeout);
             // every MMA of this CTA must finish before tensor memory is released
@@ -303,13 +301,14 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 for (int c = 0; c < 128; ++c)
                     if (c >= lim) sr[c] = __float_as_uint(-INFINITY);
             }
+            // row max: 3-input max, four chains
             float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 128; c += 4) {
-                mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
-                mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
-                mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
-                mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+            for (int c = 0; c < 128; c += 8) {
+                mx0 = max3(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+                mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+                mx2 = max3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+                mx3 = max3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
             }
             const float mxs = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
             const bool need = mxs > m + 8.f;
@@ -322,22 +321,24 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const float nref = m == -INFINITY ? 0.f : -m;
             // P = exp2(s*scale - m) as bf16 pairs, packed in place (entry e
             // takes columns 2e and 2e+1, which are read before entry e is
-            // written), then stored over the first 64 columns of S
-            float l0 = 0.f, l1 = 0.f;
+            // written), then stored over the first 64 columns of S; the
+            // scale-and-shift and the row sum run on packed fp32 pairs
+            const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2), shift2 = f32x2(nref, nref);
+            uint64_t la = f32x2(0.f, 0.f), lb = la;
 #pragma unroll
             for (int e = 0; e < 64; ++e) {
-                // one exponential in kFmaExpEvery goes to the FMA pipe, the
-                // rest to the special-function unit, to balance the two
-                const float x0 = fmaf(__uint_as_float(sr[2 * e]), p.scale_log2, nref);
-                const float x1 = fmaf(__uint_as_float(sr[2 * e + 1]), p.scale_log2, nref);
-                const float p0 = ex2(x0);
-                const float p1 = (kFmaExpEvery > 0 && (2 * e + 1) % kFmaExpEvery == kFmaExpEvery - 1)
-                                     ? ex2_fma(x1) : ex2(x1);
-                l0 += p0;
-                l1 += p1;
+                float x0, x1;
+                f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1])), scale2, shift2),
+                            x0, x1);
+                const float p0 = ex2(x0), p1 = ex2(x1);
+                if (e & 1) lb = add_f32x2(lb, f32x2(p0, p1));
+                else la = add_f32x2(la, f32x2(p0, p1));
                 sr[e] = pack_bf16x2(p0, p1);
             }
-            l += l0 + l1;
+            float a0, a1, b0, b1;
+            f32x2_split(la, a0, a1);
+            f32x2_split(lb, b0, b1);
+            l += (a0 + b0) + (a1 + b1);
             tmem_st32(t_row + col_s(t) + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
             tmem_st32(t_row + col_s(t) + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
             if (j >= 1 && __any_sync(0xffffffffu, need)) {
@@ -358,8 +359,8 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // 0 * row stays 0 inside the MMA
             const int valid_keys = tile.key_end - kt0;
             if (valid_keys < kTileKeys && j == n_tiles - 1 && t == zero_owner_last) {
-                const int s = j % C::NS;
-                if (!warp_wait(bar(B_VFULL + s), (j / C::NS) & 1, &abort_flag)) { ok = false; break; }
+                const int s = j % C::NSV;
+                if (!warp_wait(bar(B_VFULL + s), (j / C::NSV) & 1, &abort_flag)) { ok = false; break; }
                 if (row >= valid_keys) {
 #pragma unroll
                     for (int h = 0; h < C::NH; ++h)
