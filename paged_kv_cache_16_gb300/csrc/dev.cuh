@@ -386,6 +386,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// A shared-memory descriptor moved by `bytes` (a multiple of 16 that keeps
+// the start address inside the 18-bit window): only the low word changes,
+// one add instead of rebuilding the descriptor.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t d, uint32_t bytes) {
+    uint64_t r;
+    asm("{\n\t.reg .b32 lo, hi;\n\tmov.b64 {lo, hi}, %1;\n\tadd.u32 lo, lo, %2;\n\tmov.b64 %0, {lo, hi};\n\t}"
+        : "=l"(r)
+        : "l"(d), "r"(bytes >> 4));
+    return r;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 D.
 // Bits: [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B
 // format, 15 A major (1 = MN), 16 B major, [17,23) N>>3, [24,29) M>>4.

@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <queue>
 #include <new>
 #include <vector>
 
@@ -392,6 +393,51 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
         for (ExtendTile &t : P->tiles) t.req = row_of[t.req];
     }
 
+    // ------------------------------- persistent tensor-core CTAs (LPT)
+    // cost of a tile: its 128-key steps (as the kernel counts them) plus one
+    // for the Q load and epilogue; each tile goes to the least loaded CTA,
+    // longest tiles first
+    {
+        const int64_t max_ctas = P->fixed ? std::min<int64_t>(shape->max_extend_tiles, P->num_sms)
+                                          : std::min<int64_t>(static_cast<int64_t>(P->tiles.size()), P->num_sms);
+        P->ext_ctas = static_cast<int32_t>(std::max<int64_t>(max_ctas, 0));
+        std::vector<std::vector<int32_t>> lists(static_cast<size_t>(P->ext_ctas));
+        if (P->ext_ctas > 0) {
+            const int tpt_rows = kTileRows / P->G;
+            std::vector<std::pair<int64_t, int32_t>> cost;
+            for (size_t i = 0; i < P->tiles.size(); ++i) {
+                const ExtendTile &t = P->tiles[i];
+                int n_tiles = 0;
+                for (int sub = 0; sub < 2; ++sub) {
+                    const int first = sub * tpt_rows;
+                    if (first >= t.n_tok) continue;
+                    const int last = std::min(t.n_tok, first + tpt_rows);
+                    const int kend = t.causal ? std::min(t.key_end, t.pos0 + last) : t.key_end;
+                    n_tiles = std::max(n_tiles, (kend - t.key_begin + kTileKeys - 1) / kTileKeys);
+                }
+                cost.push_back({n_tiles + 1, static_cast<int32_t>(i)});
+            }
+            std::stable_sort(cost.begin(), cost.end(),
+                             [](const std::pair<int64_t, int32_t> &a, const std::pair<int64_t, int32_t> &b) {
+                                 return a.first > b.first;
+                             });
+            using Load = std::pair<int64_t, int32_t>;   // (work so far, CTA)
+            std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+            for (int32_t c = 0; c < P->ext_ctas; ++c) heap.push({0, c});
+            for (const auto &ct : cost) {
+                Load ld = heap.top();
+                heap.pop();
+                lists[ld.second].push_back(ct.second);
+                heap.push({ld.first + ct.first, ld.second});
+            }
+        }
+        P->cta_tile_begin.assign(1, 0);
+        for (const auto &l : lists) {
+            P->cta_tiles.insert(P->cta_tiles.end(), l.begin(), l.end());
+            P->cta_tile_begin.push_back(static_cast<int32_t>(P->cta_tiles.size()));
+        }
+    }
+
     // ------------------------------------------------------------- decode
     std::vector<DecodeUnit> units;
     for (int32_t r = 0; r < P->R; ++r) {
@@ -507,6 +553,8 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     P->off_scrtab = place(static_cast<size_t>(P->cap_scr_rows) * P->max_blocks * sizeof(int32_t));
     P->off_dequant = place(static_cast<size_t>(P->cap_dequant) * sizeof(DequantItem));
     P->off_runs = place(static_cast<size_t>(P->cap_runs) * sizeof(WriteRun));
+    P->off_ctb = place(P->cta_tile_begin.size() * sizeof(int32_t));
+    P->off_ctiles = place(static_cast<size_t>(P->cap_tiles) * sizeof(int32_t));
     P->blob_bytes = off - kHeader;
     off = align_up(off, 256);
     P->off_opart = off;
@@ -539,6 +587,8 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     put(P->off_scrtab, P->scratch_table.data(), P->scratch_table.size() * sizeof(int32_t));
     put(P->off_dequant, P->dequant.data(), P->dequant.size() * sizeof(DequantItem));
     put(P->off_runs, P->write_runs.data(), P->write_runs.size() * sizeof(WriteRun));
+    put(P->off_ctb, P->cta_tile_begin.data(), P->cta_tile_begin.size() * sizeof(int32_t));
+    put(P->off_ctiles, P->cta_tiles.data(), P->cta_tiles.size() * sizeof(int32_t));
 
     // ------------------------------------------------------------- info
     pa_plan_info &I = P->info;
@@ -679,7 +729,8 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
         ep.o_part = o_part;
         ep.ml_part = ml_part;
         ep.err = err;
-        ep.counts = counts;
+        ep.cta_tile_begin = reinterpret_cast<const int32_t *>(ws + P->off_ctb);
+        ep.cta_tiles = reinterpret_cast<const int32_t *>(ws + P->off_ctiles);
         ep.max_blocks = P->max_blocks;
         ep.num_blocks = tile_blocks;
         ep.num_heads_q = P->Hq;
@@ -689,7 +740,7 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
         ep.scale_log2 = P->scale_log2;
         ep.out_scale = P->out_scale;
         if (rec(1, true, stream) != cudaSuccess) return PA_ERR_CUDA;
-        if (launch_extend(P->D, P->cap_tiles, tm_q, tm_tk, tm_tv, ep, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_extend(P->D, P->ext_ctas, tm_q, tm_tk, tm_tv, ep, stream) != cudaSuccess) return PA_ERR_CUDA;
         if (rec(1, false, stream) != cudaSuccess) return PA_ERR_CUDA;
     }
     if (P->ncta > 0) {

@@ -129,7 +129,8 @@ struct ExtendParams {
     float *o_part;
     float2 *ml_part;
     int32_t *err;
-    const int32_t *counts;      // device work counts (MetaCounts); CTAs past the tile count exit
+    const int32_t *cta_tile_begin;  // [grid + 1]: CTA c runs tiles cta_tiles[begin[c] .. begin[c+1])
+    const int32_t *cta_tiles;       // tile indices, each CTA's longest first
     int32_t max_blocks;
     int32_t num_blocks;
     int32_t num_heads_q;

@@ -24,6 +24,9 @@ struct pa_plan_s {
     std::vector<pa::DecodeItem> items;
     std::vector<pa::ExtendTile> tiles;
     std::vector<pa::MergeRow> merges;
+    std::vector<int32_t> cta_tile_begin;      // persistent tensor-core CTAs: [ext_ctas + 1]
+    std::vector<int32_t> cta_tiles;           // their tile lists
+    int32_t ext_ctas = 0;
     std::vector<pa::WriteRun> write_runs;     // extend rows (fused cache update)
     int32_t write_tokens = 0;
     std::vector<int32_t> scratch_table;       // E4M3: [rows][max_blocks] bf16 scratch block ids
@@ -33,6 +36,7 @@ struct pa_plan_s {
     // workspace layout
     size_t off_part = 0, off_cta = 0, off_items = 0, off_tiles = 0, off_merges = 0;
     size_t off_scrtab = 0, off_dequant = 0, off_kscr = 0, off_vscr = 0, off_runs = 0;
+    size_t off_ctb = 0, off_ctiles = 0;
     size_t blob_bytes = 0, off_opart = 0, off_ml = 0, ws_bytes = 0;
     // launch shape: exact sizes for pa_plan, capacities for pa_plan_fixed
     bool fixed = false;
