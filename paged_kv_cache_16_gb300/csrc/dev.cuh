@@ -112,6 +112,16 @@ __device__ __forceinline__ void raise_abort(volatile int *abort_flag, int32_t *e
     atomicOr(err, bits);
 }
 
+// ------------------------------------------- programmatic dependent launch --
+// launch_dependents: the next kernel in the stream (launched with the
+// programmatic-serialisation attribute) may start its prologue now.
+// dep_wait: block until the previous kernel in the stream has completed and
+// its memory is visible; every kernel launched with the attribute calls it
+// before it reads or writes anything an earlier kernel touches (a no-op when
+// launched without the attribute).
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // --------------------------------------------------------------------- TMA --
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *tm) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
@@ -334,32 +344,48 @@ template <int D>
 __device__ __forceinline__ void merge_head(uint16_t *out_row, const float *o_part, const float2 *ml_part,
                                            int64_t slot0, int count, int num_heads_q, int h, int lane) {
     constexpr int V = D / 32;
+    // lane s holds (m, l) of partial s of each group of 32: the loads are
+    // independent, so the merge costs a few round trips whatever the count
+    // (L2 loads: partials written by other SMs in this same launch must not
+    // be served from a stale L1 line)
     float m = -INFINITY;
-    for (int s = 0; s < count; ++s) {
-        const float2 ml = __ldcg(ml_part + (slot0 + s) * num_heads_q + h);
-        if (ml.y > 0.f) m = fmaxf(m, ml.x);
+    for (int s0 = 0; s0 < count; s0 += 32) {
+        if (s0 + lane < count) {
+            const float2 ml = __ldcg(ml_part + (slot0 + s0 + lane) * num_heads_q + h);
+            if (ml.y > 0.f) m = fmaxf(m, ml.x);
+        }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float acc[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[v] = 0.f;
-    float total = 0.f;
-    for (int s = 0; s < count; ++s) {
-        const int64_t slot = slot0 + s;
-        const float2 ml = __ldcg(ml_part + slot * num_heads_q + h);
-        if (!(ml.y > 0.f)) continue;
-        const float w = ex2(ml.x - m) * ml.y;
-        total += w;
-        const float *o = o_part + (slot * num_heads_q + h) * D + lane * V;
-        // L2 loads: partials written by other SMs in this same launch must
-        // not be served from a stale L1 line
-        if constexpr (V == 4) {
-            const float4 x = __ldcg(reinterpret_cast<const float4 *>(o));
-            acc[0] += w * x.x; acc[1] += w * x.y; acc[2] += w * x.z; acc[3] += w * x.w;
-        } else {
-            const float2 x = __ldcg(reinterpret_cast<const float2 *>(o));
-            acc[0] += w * x.x; acc[1] += w * x.y;
+    float wsum = 0.f;   // this lane's partials' weights
+    for (int s0 = 0; s0 < count; s0 += 32) {
+        float w = 0.f;
+        if (s0 + lane < count) {
+            const float2 ml = __ldcg(ml_part + (slot0 + s0 + lane) * num_heads_q + h);
+            if (ml.y > 0.f) w = ex2(ml.x - m) * ml.y;
+        }
+        wsum += w;
+        const int n = min(32, count - s0);
+#pragma unroll 4
+        for (int j = 0; j < n; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, w, j);
+            if (wj == 0.f) continue;   // empty partial: its o was never written
+            const float *o = o_part + ((slot0 + s0 + j) * num_heads_q + h) * D + lane * V;
+            if constexpr (V == 4) {
+                const float4 x = __ldcg(reinterpret_cast<const float4 *>(o));
+                acc[0] += wj * x.x; acc[1] += wj * x.y; acc[2] += wj * x.z; acc[3] += wj * x.w;
+            } else {
+                const float2 x = __ldcg(reinterpret_cast<const float2 *>(o));
+                acc[0] += wj * x.x; acc[1] += wj * x.y;
+            }
         }
     }
+    float total = wsum;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
     const float inv = total > 0.f ? 1.f / total : 0.f;
     uint16_t *dst = out_row + static_cast<int64_t>(h) * D + lane * V;
     if constexpr (V == 4) {

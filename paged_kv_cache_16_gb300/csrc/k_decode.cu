@@ -118,6 +118,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    grid_launch_dependents();
     if (threadIdx.x == 0) {
         abort_flag = 0;
         for (int s = 0; s < C::NS; ++s) {
@@ -126,7 +127,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             mbar_init(empty(s), HG);
         }
         fence_barrier_init();
+    } else if (threadIdx.x == 32 * HG) {
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
     }
+    // everything below reads or writes what earlier kernels of the stream
+    // produce or consume (work list, caches, partials)
+    grid_dep_wait();
     __syncthreads();
 
     const int item_begin = p.cta_begin[blockIdx.x];
@@ -134,10 +141,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
     if (warp == HG) {
         // ------------------------------------------------------ producer --
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-        }
         int issued = 0;
         bool ok = true;
         for (int it = item_begin; it < item_end && ok; ++it) {
@@ -626,10 +629,10 @@ cudaError_t launch_t(int num_ctas, const CUtensorMap &tm_k, const CUtensorMap &t
     cudaError_t e = configure_both<D, HG, KV8>();
     if (e != cudaSuccess) return e;
     if (p.new_k != nullptr)
-        decode_kernel<D, HG, KV8, true><<<num_ctas, C::THREADS, C::SMEM, stream>>>(tm_k, tm_v, p);
-    else
-        decode_kernel<D, HG, KV8, false><<<num_ctas, C::THREADS, C::SMEM, stream>>>(tm_k, tm_v, p);
-    return cudaGetLastError();
+        return launch_pdl(decode_kernel<D, HG, KV8, true>, dim3(num_ctas), dim3(C::THREADS), C::SMEM, stream, tm_k,
+                          tm_v, p);
+    return launch_pdl(decode_kernel<D, HG, KV8, false>, dim3(num_ctas), dim3(C::THREADS), C::SMEM, stream, tm_k, tm_v,
+                      p);
 }
 
 }  // namespace

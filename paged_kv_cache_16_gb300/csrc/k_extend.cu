@@ -123,6 +123,8 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     auto v_s = [&](int s) { return base + 2 * C::QB + static_cast<uint32_t>(C::NSK + s) * C::KVB; };
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
+    grid_launch_dependents();
+    grid_dep_wait();    // the work list and caches come from earlier kernels of the stream
     // this CTA's tiles, longest first (the planner's greedy assignment)
     const int tile_begin = p.cta_tile_begin[blockIdx.x];
     const int tile_end = p.cta_tile_begin[blockIdx.x + 1];
@@ -521,8 +523,7 @@ cudaError_t launch_t(int grid, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
     using C = ExtCfg<D>;
     cudaError_t e = configure<D>();
     if (e != cudaSuccess) return e;
-    extend_kernel<D><<<grid, C::THREADS, C::SMEM, stream>>>(tm_q, tm_k, tm_v, p);
-    return cudaGetLastError();
+    return launch_pdl(extend_kernel<D>, dim3(grid), dim3(C::THREADS), C::SMEM, stream, tm_q, tm_k, tm_v, p);
 }
 
 }  // namespace

@@ -102,6 +102,8 @@ __device__ __forceinline__ void expand16(const uint4 codes, uint4 *dst) {
 }
 
 __global__ void dequant_kernel(DequantParams p) {
+    dev::grid_launch_dependents();
+    dev::grid_dep_wait();
     const int32_t n = p.counts[kCountDequant];
     const int32_t chunks = p.block_elems / 16;
     for (int32_t i = blockIdx.x; i < n; i += gridDim.x) {
@@ -129,6 +131,8 @@ __global__ void dequant_kernel(DequantParams p) {
 // and its row is stored as pa_write_kv / pa_write_kv_fp8 store it (§6.3).
 // One thread per 16-byte output chunk.
 __global__ void write_runs_kernel(WriteParams p) {
+    dev::grid_launch_dependents();
+    dev::grid_dep_wait();
     const int32_t nruns = p.counts[kCountWriteRuns];
     const int64_t ntok = p.counts[kCountWriteTokens];
     const int32_t cpr = p.kv8 ? p.row_elems / 16 : p.row_elems / 8;   // output chunks per row
@@ -171,6 +175,7 @@ __global__ void write_runs_kernel(WriteParams p) {
 // Uncached loads: a recycled host buffer must never be served from a line
 // cached for an earlier plan.
 __global__ void upload_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst, int64_t n16) {
+    dev::grid_launch_dependents();   // the next kernel may start its prologue (it waits for this one)
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride) {
         uint4 v;
@@ -204,6 +209,8 @@ __global__ void zero_blocks_kernel(const int32_t *__restrict__ ids, int32_t num_
 // rescaling).  One warp per (token, query head); m is in log2 units.
 template <int D>
 __global__ void merge_kernel(MergeParams p) {
+    dev::grid_launch_dependents();
+    dev::grid_dep_wait();
     const int lane = threadIdx.x & 31;
     const int64_t total = static_cast<int64_t>(p.counts[kCountMerges]) * p.max_heads;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x / 32;
@@ -264,16 +271,14 @@ cudaError_t launch_write_kv_fp8(const void *key, const void *value, const int64_
 
 cudaError_t launch_dequant(int grid, const DequantParams &p, cudaStream_t stream) {
     if (grid <= 0) return cudaSuccess;
-    dequant_kernel<<<grid, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(dequant_kernel, dim3(grid), dim3(256), 0, stream, p);
 }
 
 cudaError_t launch_merge(int head_dim, int grid, const MergeParams &p, cudaStream_t stream) {
     if (grid <= 0) return cudaSuccess;
-    if (head_dim == 128) merge_kernel<128><<<grid, 256, 0, stream>>>(p);
-    else if (head_dim == 64) merge_kernel<64><<<grid, 256, 0, stream>>>(p);
-    else return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    if (head_dim == 128) return launch_pdl(merge_kernel<128>, dim3(grid), dim3(256), 0, stream, p);
+    if (head_dim == 64) return launch_pdl(merge_kernel<64>, dim3(grid), dim3(256), 0, stream, p);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_upload(const void *src, void *dst, size_t bytes, cudaStream_t stream) {
@@ -290,8 +295,7 @@ cudaError_t launch_upload(const void *src, void *dst, size_t bytes, cudaStream_t
 
 cudaError_t launch_write_runs(int grid, const WriteParams &p, cudaStream_t stream) {
     if (grid <= 0) return cudaSuccess;
-    write_runs_kernel<<<grid, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(write_runs_kernel, dim3(grid), dim3(256), 0, stream, p);
 }
 
 cudaError_t launch_zero_blocks(const int32_t *ids, int32_t num_ids, int32_t num_blocks, int64_t block_bytes,

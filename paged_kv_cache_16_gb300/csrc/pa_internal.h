@@ -2,6 +2,7 @@
 // Everything here is plain old data: the planner fills host arrays of these,
 // pa_attention copies them into the workspace, the kernels read them there.
 #pragma once
+#include <utility>
 #include <cstddef>
 #include <cstdint>
 
@@ -214,6 +215,24 @@ struct WriteParams {
     int32_t kv8;
     float k_scale, v_scale;     // E4M3 quantisation (code of x / scale)
 };
+
+// Launch with programmatic stream serialisation (the kernel calls
+// grid_dep_wait before touching data of earlier kernels).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Launchers (each returns the launch's cudaError_t).
 cudaError_t launch_slot_mapping(const int32_t *qsl, const int32_t *num_computed,
