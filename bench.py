@@ -266,7 +266,8 @@ def step_desc(graph_mode: bool, fused: bool) -> str:
     if graph_mode:
         body = ("pa_attention_with_kv_update_launch" if fused else
                 "pa_slot_mapping + pa_write_kv + pa_attention_launch")
-        return f"pa_plan_fixed (host) + pa_upload_metadata + CUDA-graph replay of {body}"
+        return (f"pa_plan_fixed + pa_plan_copy_metadata (host) + CUDA-graph replay of pa_upload_metadata_from "
+                f"+ {body}")
     return f"pa_plan (host) + {body}"
 
 
@@ -406,8 +407,7 @@ def run_ours(args, world, rank, local):
     def graph_step(keep_plans):
         plan = gs.make_plan(batch)
         keep_plans.append(plan)
-        binding.pa_upload_metadata(plan, gs.workspace, stream)
-        gs.graph.replay()
+        gs.replay(plan)
 
     for _ in range(args.warmup):
         flush_l2()
@@ -459,8 +459,7 @@ def run_ours(args, world, rank, local):
             gs.num_computed[:batch.num_reqs].copy_(meta_h[1], non_blocking=True)
             gs.block_table[:batch.num_reqs].copy_(meta_h[2], non_blocking=True)
             plan = gs.make_plan(batch)
-            binding.pa_upload_metadata(plan, gs.workspace, stream)
-            gs.graph.replay()
+            gs.replay(plan)
             out_h[:T].copy_(gs.out[:T], non_blocking=True)
         else:
             q.copy_(q_h, non_blocking=True)

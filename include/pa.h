@@ -283,6 +283,36 @@ pa_status pa_plan_fixed(const pa_batch_desc *desc, const pa_fixed_shape *shape, 
 pa_status pa_upload_metadata(const pa_plan_t *plan, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Capturable metadata upload (graph mode with the upload inside the graph).
+ * pa_plan_metadata_bytes: size of the plan's metadata image (equal for every
+ * fixed-shape plan of one shape; 0 for a NULL plan).
+ * pa_plan_copy_metadata: copy that image into caller memory, e.g. the
+ * page-locked buffer a captured pa_upload_metadata_from reads (host work
+ * only; PA_ERR_INVALID_ARGUMENT for a NULL or too small buffer).
+ *   host_dst   HOST, bytes >= pa_plan_metadata_bytes(plan)
+ * pa_upload_metadata_from: enqueue the copy of an image from page-locked host
+ * memory into a workspace, read by the GPU when the copy runs.  Its
+ * arguments are plain addresses, so it may be captured in a CUDA graph: the
+ * caller refreshes the image (pa_plan_copy_metadata) before each replay and
+ * must not overwrite it while an enqueued copy of it has not run yet (use
+ * two images and two graphs, or wait for the previous replay).  As for
+ * pa_attention_launch, call pa_upload_metadata (which prepares the kernels)
+ * at least once before the first capture.
+ *   host_src   HOST, page-locked and device-mapped (cudaHostAlloc /
+ *              cudaHostRegister), 16-byte aligned
+ *   bytes      the image size (a multiple of 16)
+ *   workspace  DEVICE, as for pa_attention; workspace_bytes must cover the
+ *              plan the image came from
+ * Errors: PA_ERR_INVALID_ARGUMENT (NULL, misaligned, bytes not a multiple of
+ * 16 or host_src not page-locked), PA_ERR_WORKSPACE_TOO_SMALL,
+ * PA_ERR_CUDA.
+ */
+size_t pa_plan_metadata_bytes(const pa_plan_t *plan);
+pa_status pa_plan_copy_metadata(const pa_plan_t *plan, void *host_dst, size_t bytes);
+pa_status pa_upload_metadata_from(const void *host_src, size_t bytes, void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
+/*
  * The kernels of pa_attention alone: they read the metadata that the last
  * pa_upload_metadata put into this workspace, which must come from a plan of
  * the same fixed shape (or, for a plan made by pa_plan, from this plan).

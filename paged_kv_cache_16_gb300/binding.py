@@ -35,7 +35,8 @@ EXPORTED = ("pa_plan", "pa_plan_destroy", "pa_plan_get_info", "pa_slot_mapping",
             "pa_attention", "pa_check_device_errors", "pa_plan_enable_timing",
             "pa_plan_kernel_times", "pa_status_string", "pa_attention_no_alloc", "pa_write_kv_fp8",
             "pa_plan_fixed", "pa_upload_metadata", "pa_attention_launch", "pa_zero_blocks",
-            "pa_attention_with_kv_update", "pa_attention_with_kv_update_launch")
+            "pa_attention_with_kv_update", "pa_attention_with_kv_update_launch", "pa_plan_metadata_bytes",
+            "pa_plan_copy_metadata", "pa_upload_metadata_from")
 
 
 class PaError(RuntimeError):
@@ -130,6 +131,12 @@ def load(path: str | None = None, build_if_missing: bool = False) -> ctypes.CDLL
                                   ctypes.POINTER(sz)]
     lib.pa_upload_metadata.restype = ctypes.c_int
     lib.pa_upload_metadata.argtypes = [vp, vp, sz, vp]
+    lib.pa_plan_metadata_bytes.restype = sz
+    lib.pa_plan_metadata_bytes.argtypes = [vp]
+    lib.pa_plan_copy_metadata.restype = ctypes.c_int
+    lib.pa_plan_copy_metadata.argtypes = [vp, vp, sz]
+    lib.pa_upload_metadata_from.restype = ctypes.c_int
+    lib.pa_upload_metadata_from.argtypes = [vp, sz, vp, sz, vp]
     lib.pa_attention_launch.restype = ctypes.c_int
     lib.pa_attention_launch.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.pa_attention_with_kv_update.restype = ctypes.c_int
@@ -342,6 +349,30 @@ def pa_attention(plan: Plan, q, key_cache, value_cache, block_table, out, worksp
 def pa_upload_metadata(plan: Plan, workspace, stream=None):
     nbytes = workspace.numel() * workspace.element_size()
     _check(load().pa_upload_metadata(plan.handle, _ptr(workspace), nbytes, _stream(stream)), "pa_upload_metadata")
+
+
+def pa_plan_metadata_bytes(plan: Plan) -> int:
+    return int(load().pa_plan_metadata_bytes(plan.handle))
+
+
+def pa_plan_copy_metadata_status(plan: Plan, host_dst, nbytes: int) -> int:
+    """Raw status of pa_plan_copy_metadata into host memory at address host_dst."""
+    return load().pa_plan_copy_metadata(plan.handle, host_dst, nbytes)
+
+
+def pa_plan_copy_metadata(plan: Plan, host_dst):
+    """Copy the plan's metadata image into a host tensor (uint8, at least
+    pa_plan_metadata_bytes long)."""
+    nbytes = host_dst.numel() * host_dst.element_size()
+    _check(pa_plan_copy_metadata_status(plan, _ptr(host_dst), nbytes), "pa_plan_copy_metadata")
+
+
+def pa_upload_metadata_from(host_src, nbytes: int, workspace, stream=None):
+    """Enqueue the upload of a metadata image from page-locked host memory
+    (capturable; see pa.h)."""
+    wbytes = workspace.numel() * workspace.element_size()
+    _check(load().pa_upload_metadata_from(_ptr(host_src), nbytes, _ptr(workspace), wbytes, _stream(stream)),
+           "pa_upload_metadata_from")
 
 
 def pa_attention_launch(plan: Plan, q, key_cache, value_cache, block_table, out, workspace, stream=None):

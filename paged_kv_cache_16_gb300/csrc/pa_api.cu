@@ -964,6 +964,35 @@ pa_status pa_upload_metadata(const pa_plan_t *plan, void *workspace, size_t work
     return upload(P, static_cast<uint8_t *>(workspace), static_cast<cudaStream_t>(stream_), false);
 }
 
+size_t pa_plan_metadata_bytes(const pa_plan_t *plan) { return plan ? plan->blob_bytes : 0; }
+
+pa_status pa_plan_copy_metadata(const pa_plan_t *plan, void *host_dst, size_t bytes) {
+    if (!plan || (!host_dst && plan->blob_bytes)) return PA_ERR_INVALID_ARGUMENT;
+    pa_plan_s *P = const_cast<pa_plan_s *>(plan);
+    if (bytes < P->blob_bytes) return PA_ERR_INVALID_ARGUMENT;
+    if (P->blob_bytes) std::memcpy(host_dst, P->blob.data(), P->blob_bytes);
+    return PA_OK;
+}
+
+pa_status pa_upload_metadata_from(const void *host_src, size_t bytes, void *workspace, size_t workspace_bytes,
+                                  void *stream_) {
+    if (!workspace || !aligned(workspace, 256) || bytes % 16 != 0 || (bytes && (!host_src || !aligned(host_src, 16))))
+        return PA_ERR_INVALID_ARGUMENT;
+    if (workspace_bytes < kHeader + bytes) return PA_ERR_WORKSPACE_TOO_SMALL;
+    if (!bytes) return PA_OK;
+    cudaPointerAttributes attr{};
+    if (cudaPointerGetAttributes(&attr, host_src) != cudaSuccess || attr.type != cudaMemoryTypeHost) {
+        cudaGetLastError();   // clear the error of an unregistered pointer
+        return PA_ERR_INVALID_ARGUMENT;
+    }
+    void *dev_src = nullptr;
+    if (cudaHostGetDevicePointer(&dev_src, const_cast<void *>(host_src), 0) != cudaSuccess) return PA_ERR_CUDA;
+    return launch_upload(dev_src, static_cast<uint8_t *>(workspace) + kHeader, bytes,
+                         static_cast<cudaStream_t>(stream_)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
 pa_status pa_attention_launch(const pa_plan_t *plan, const void *q, const void *key_cache, const void *value_cache,
                               const int32_t *block_table, void *out, void *workspace, size_t workspace_bytes,
                               void *stream_) {

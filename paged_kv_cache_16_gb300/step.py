@@ -89,10 +89,12 @@ class GraphStep:
     with request counts rounded up to a capture size and spare rows padded.
     Static buffers hold max_tokens rows of q / key / value / out and max_reqs
     rows of metadata; padding requests have no tokens, so padding tokens get
-    slot -1 and are neither written nor attended.  The graph holds the cache
-    write and the attention kernels (fused: pa_attention_with_kv_update_launch;
-    else slot mapping, pa_write_kv and pa_attention_launch); the per-step
-    metadata upload (pa_upload_metadata) precedes each replay.
+    slot -1 and are neither written nor attended.  A graph holds the metadata
+    upload from a page-locked image (pa_upload_metadata_from), the cache write
+    and the attention kernels (fused: pa_attention_with_kv_update_launch; else
+    slot mapping, pa_write_kv and pa_attention_launch).  Two images and two
+    graphs alternate, so the host writes one step's image while the previous
+    step's graph may still be reading the other.
     """
 
     def __init__(self, *, num_heads_q, num_heads_kv, head_dim, num_blocks, max_blocks_per_req, softmax_scale,
@@ -119,7 +121,10 @@ class GraphStep:
         self.block_table = torch.zeros(max_reqs, max_blocks_per_req, dtype=torch.int32, device=dev)
         self.slots = torch.zeros(max_tokens, dtype=torch.int64, device=dev)
         self.workspace = None
-        self.graph = None
+        self.graphs = None       # two captures, one per metadata image
+        self.images = None       # page-locked metadata images
+        self.done = None         # events: the last replay of graph i has run
+        self.turn = 0
         self.caches = None
 
     def make_plan(self, batch: Batch) -> binding.Plan:
@@ -140,6 +145,13 @@ class GraphStep:
     def load(self, batch: Batch, plan: binding.Plan, q=None, key=None, value=None, stream=None):
         """Copy a step's metadata (and, if given, its new q / key / value rows)
         into the static buffers and upload the plan's metadata (not captured)."""
+        self.stage(batch, q, key, value)
+        if self.workspace is None:
+            self.workspace = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device=self.device)
+        binding.pa_upload_metadata(plan, self.workspace, stream)
+
+    def stage(self, batch: Batch, q=None, key=None, value=None):
+        """Copy a step's request metadata and new rows into the static buffers."""
         R, T = batch.num_reqs, batch.num_tokens
         mr, mb = self.num_computed.numel(), self.block_table.shape[1]
         qsl = np.full(mr + 1, T, dtype=np.int32)
@@ -154,9 +166,6 @@ class GraphStep:
         for dst, src in ((self.q, q), (self.key, key), (self.value, value)):
             if src is not None:
                 dst[:T].copy_(src)
-        if self.workspace is None:
-            self.workspace = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device=self.device)
-        binding.pa_upload_metadata(plan, self.workspace, stream)
 
     def enqueue(self, plan: binding.Plan, key_cache, value_cache, stream=None):
         """Slot mapping, cache write and attention over the static buffers
@@ -177,21 +186,44 @@ class GraphStep:
                                     self.workspace, stream)
 
     def capture(self, plan: binding.Plan, key_cache, value_cache):
-        """Capture enqueue() once; the caches are part of the graph."""
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            self.enqueue(plan, key_cache, value_cache)
-        self.graph, self.caches = g, (key_cache.data_ptr(), value_cache.data_ptr())
+        """Capture the upload of each metadata image followed by enqueue();
+        the caches are part of the graphs."""
+        if self.workspace is None:
+            self.workspace = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device=self.device)
+        binding.pa_upload_metadata(plan, self.workspace)   # prepares the kernels (not capturable)
+        nbytes = binding.pa_plan_metadata_bytes(plan)
+        self.images = [torch.zeros(max(nbytes, 16), dtype=torch.uint8).pin_memory() for _ in range(2)]
+        for img in self.images:
+            binding.pa_plan_copy_metadata(plan, img)
+        self.graphs = []
+        for img in self.images:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                binding.pa_upload_metadata_from(img, nbytes, self.workspace)
+                self.enqueue(plan, key_cache, value_cache)
+            self.graphs.append(g)
+        self.done = [torch.cuda.Event(), torch.cuda.Event()]
+        self.turn = 0
+        self.caches = (key_cache.data_ptr(), value_cache.data_ptr())
+
+    def replay(self, plan: binding.Plan):
+        """Write the plan's metadata image and replay the graph that uploads it."""
+        i = self.turn
+        self.done[i].synchronize()   # the replay that last read image i has run
+        binding.pa_plan_copy_metadata(plan, self.images[i])
+        self.graphs[i].replay()
+        self.done[i].record()
+        self.turn = 1 - i
 
     def run(self, batch: Batch, q, key, value, key_cache, value_cache) -> torch.Tensor:
         """One step: plan, copy in, replay (capturing on first use)."""
         plan = self.make_plan(batch)
-        self.load(batch, plan, q, key, value)
-        if self.graph is None:
+        self.stage(batch, q, key, value)
+        if self.graphs is None:
             self.capture(plan, key_cache, value_cache)
         elif self.caches != (key_cache.data_ptr(), value_cache.data_ptr()):
             raise ValueError("a captured step replays on the caches it was captured with")
-        self.graph.replay()
+        self.replay(plan)
         return self.out[:batch.num_tokens]
 
     def check_errors(self, stream=None) -> int:

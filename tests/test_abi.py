@@ -243,6 +243,34 @@ def test_fixed_plan_mixed_shape(lib):
     assert j.info()["kernels_per_call"] == 3 and j.workspace_bytes == p.workspace_bytes
 
 
+def test_metadata_image_for_captured_uploads(lib):
+    """pa_plan_metadata_bytes / pa_plan_copy_metadata: one image size per
+    fixed shape, an image per step, too small a buffer refused;
+    pa_upload_metadata_from checks its arguments before any CUDA call."""
+    import torch
+    shape = dict(max_tokens=96, max_reqs=96)
+    a = fixed(workloads.decode(batch=8, lo=20, hi=300, num_blocks=4000, seed=1), **shape)
+    b = fixed(workloads.decode(batch=64, lo=100, hi=700, num_blocks=4000, seed=2), **shape)
+    n = binding.pa_plan_metadata_bytes(a)
+    assert n > 0 and n % 16 == 0 and n == binding.pa_plan_metadata_bytes(b)
+    ia, ib = torch.zeros(n, dtype=torch.uint8), torch.zeros(n, dtype=torch.uint8)
+    binding.pa_plan_copy_metadata(a, ia)
+    binding.pa_plan_copy_metadata(b, ib)
+    assert ia.any() and not torch.equal(ia, ib)
+    again = torch.zeros(n, dtype=torch.uint8)
+    binding.pa_plan_copy_metadata(a, again)
+    assert torch.equal(ia, again)
+    small = torch.zeros(n - 16, dtype=torch.uint8)
+    assert binding.pa_plan_copy_metadata_status(a, small.data_ptr(), n - 16) == binding.PA_ERR_INVALID_ARGUMENT
+    up = lib.pa_upload_metadata_from
+    ws = 1 << 20   # a fake, 256-aligned address: never dereferenced on these paths
+    assert up(None, 16, ws, 1 << 20, None) == binding.PA_ERR_INVALID_ARGUMENT
+    assert up(ia.data_ptr(), 16, None, 1 << 20, None) == binding.PA_ERR_INVALID_ARGUMENT
+    assert up(ia.data_ptr(), 24, ws, 1 << 20, None) == binding.PA_ERR_INVALID_ARGUMENT
+    assert up(ia.data_ptr(), n, ws, 256 + n - 16, None) == binding.PA_ERR_WORKSPACE_TOO_SMALL
+    assert up(None, 0, ws, 1 << 20, None) == binding.PA_OK
+
+
 @pytest.mark.parametrize("shape,status", [
     (dict(max_tokens=8, max_reqs=64), binding.PA_ERR_CAPACITY),            # too many tokens
     (dict(max_tokens=64, max_reqs=4), binding.PA_ERR_CAPACITY),            # too many requests

@@ -132,6 +132,28 @@ def test_fixed_plan_eager_equals_plain_plan():
     assert torch.equal(gs.out[:b.num_tokens], ref.out)
 
 
+def test_upload_from_pageable_memory_refused():
+    """The captured upload reads page-locked memory only."""
+    dev = torch.device("cuda")
+    ws = torch.zeros(1 << 16, dtype=torch.uint8, device=dev)
+    pageable = torch.zeros(1024, dtype=torch.uint8)
+    st = binding.load().pa_upload_metadata_from(pageable.data_ptr(), 1024, ws.data_ptr(), ws.numel(), None)
+    assert st == binding.PA_ERR_INVALID_ARGUMENT
+    pinned = torch.zeros(1024, dtype=torch.uint8).pin_memory()
+    pinned[:] = torch.arange(1024) % 251
+    binding.pa_upload_metadata_from(pinned, 1024, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(ws[256:256 + 1024].cpu(), pinned)
+
+
+def test_graph_images_alternate():
+    """Consecutive steps replay the two captures in turn; a step whose image
+    the host rewrote while the other graph ran still sees its own metadata."""
+    steps = decode_steps() + decode_steps()
+    gs = replay_steps(steps, max_tokens=48, max_reqs=48)
+    assert len(gs.graphs) == 2 and gs.turn == len(steps) % 2
+
+
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
 def test_zero_blocks(kv):
     """pa_zero_blocks against the oracle: listed blocks zero, the rest
