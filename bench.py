@@ -72,9 +72,9 @@ TRAFFIC = {
     # (kernel, workload, kv dtype, source sha) -> bytes per launch (fused-write variant, the one the
     # default step runs); profiles/decode_kernel_decode-workload.md, profiles/extend_kernel_prefill-workload.md,
     # profiles/decode_kernel_e4m3_decode-workload.md
-    ("decode", "decode", "bf16", "79d3029d410f26bd"): 645_937_152,
-    ("decode", "decode", "fp8", "79d3029d410f26bd"): 327_966_208,
-    ("extend", "prefill", "bf16", "444f2a654d3f3c75"): 76_144_128,
+    ("decode", "decode", "bf16", "ec94cc0252b8909f"): 645_365_760,
+    ("decode", "decode", "fp8", "ec94cc0252b8909f"): 327_622_656,
+    ("extend", "prefill", "bf16", "059d9582423e486a"): 73_212_672,
 }
 KERNEL_SOURCES = {"decode": "paged_kv_cache_16_gb300/csrc/k_decode.cu",
                   "extend": "paged_kv_cache_16_gb300/csrc/k_extend.cu"}
