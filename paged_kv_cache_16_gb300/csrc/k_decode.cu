@@ -22,6 +22,18 @@
 
 #include "dev.cuh"
 
+// This file is compiled twice: as itself (kernels for any item) and, through
+// k_decode_rows8.cu, with PA_DECODE_ROWS8 = 1 (kernels for launches whose
+// items all have at most 8 MMA rows), so the two sets compile in parallel.
+#ifndef PA_DECODE_ROWS8
+#define PA_DECODE_ROWS8 0
+#endif
+#if PA_DECODE_ROWS8
+#define PA_DECODE_NAME(n) n##_rows8
+#else
+#define PA_DECODE_NAME(n) n
+#endif
+
 namespace pa {
 namespace {
 
@@ -100,7 +112,10 @@ struct RowUpdate {
     }
 };
 
-template <int D, int HG, bool KV8, bool FUSED>
+// ROWS8: every item of the launch has at most 8 (query token, head) rows, so
+// MMA rows 8..15 are padding: their q fragments are zero and their results
+// are never accumulated (half the accumulator registers).
+template <int D, int HG, bool KV8, bool FUSED, bool ROWS8>
 __global__ void __launch_bounds__((HG + 1) * 32, 1)
 decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const DecodeParams p) {
@@ -236,9 +251,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     return bf16x2_to_f16x2(__ldg(reinterpret_cast<const uint32_t *>(row + col)));
                 };
                 qf[kk][0] = g < nrow ? ld(q0, c) : 0u;
-                qf[kk][1] = g + 8 < nrow ? ld(q1, c) : 0u;
+                qf[kk][1] = !ROWS8 && g + 8 < nrow ? ld(q1, c) : 0u;
                 qf[kk][2] = g < nrow ? ld(q0, c + 2) : 0u;
-                qf[kk][3] = g + 8 < nrow ? ld(q1, c + 2) : 0u;
+                qf[kk][3] = !ROWS8 && g + 8 < nrow ? ld(q1, c + 2) : 0u;
             }
             float o[D / 8][4];
 #pragma unroll
@@ -255,8 +270,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     uint32_t k0, k1, k2, k3;
                     e4m3x4_to_f16x2x2(lds_u32(x), k0, k1);
                     e4m3x4_to_f16x2x2(lds_u32(x + 1024u), k2, k3);
-                    mma_f16_16816(a, qf[kk], k0, k1);
-                    mma_f16_16816(b, qf[kk], k2, k3);
+                    mma_f16<ROWS8>(a, qf[kk], k0, k1);
+                    mma_f16<ROWS8>(b, qf[kk], k2, k3);
                 }
             };
             // O += P V for one block; MASKED zeroes the codes of rows at or
@@ -284,9 +299,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     e4m3x4_to_f16x2x2(prmt(wC, wD, 0x5140u), b1[0], b1[1]);
                     e4m3x4_to_f16x2x2(prmt(wC, wD, 0x7362u), b1[2], b1[3]);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) mma_f16_16816(o[4 * a + i], pf, b0[i], b1[i]);
+                    for (int i = 0; i < 4; ++i) mma_f16<ROWS8>(o[4 * a + i], pf, b0[i], b1[i]);
                 }
-                mma_f16_16816(lacc, pf, kOnes, kOnes);
+                mma_f16<ROWS8>(lacc, pf, kOnes, kOnes);
             };
             // one softmax round over one (TWO = false) or two cache blocks
             auto round = [&](auto two_c, int pg) -> bool {
@@ -331,16 +346,18 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2)) * sl2;
                 // rescale only when the running maximum grows by more than 2^8
                 const bool need0 = mx0 > m0 + 8.f;
-                const bool need1 = mx1 > m1 + 8.f;
+                const bool need1 = !ROWS8 && mx1 > m1 + 8.f;
                 if (__any_sync(0xffffffffu, need0 || need1)) {
                     float a0 = 1.f, a1 = 1.f;
                     if (need0) { a0 = ex2(m0 - mx0); m0 = mx0; }
                     if (need1) { a1 = ex2(m1 - mx1); m1 = mx1; }
 #pragma unroll
                     for (int j = 0; j < D / 8; ++j) {
-                        o[j][0] *= a0; o[j][1] *= a0; o[j][2] *= a1; o[j][3] *= a1;
+                        o[j][0] *= a0; o[j][1] *= a0;
+                        if constexpr (!ROWS8) { o[j][2] *= a1; o[j][3] *= a1; }
                     }
-                    lacc[0] *= a0; lacc[1] *= a0; lacc[2] *= a1; lacc[3] *= a1;
+                    lacc[0] *= a0; lacc[1] *= a0;
+                    if constexpr (!ROWS8) { lacc[2] *= a1; lacc[3] *= a1; }
                 }
                 const float r0 = m0 == -INFINITY ? 0.f : m0;
                 const float r1 = m1 == -INFINITY ? 0.f : m1;
@@ -348,9 +365,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #pragma unroll
                 for (int b = 0; b < NT / 2; ++b) {
                     pa[b][0] = pack_f16x2(ex2(fmaf(sc[2 * b][0], sl2, -r0)), ex2(fmaf(sc[2 * b][1], sl2, -r0)));
-                    pa[b][1] = pack_f16x2(ex2(fmaf(sc[2 * b][2], sl2, -r1)), ex2(fmaf(sc[2 * b][3], sl2, -r1)));
                     pa[b][2] = pack_f16x2(ex2(fmaf(sc[2 * b + 1][0], sl2, -r0)), ex2(fmaf(sc[2 * b + 1][1], sl2, -r0)));
-                    pa[b][3] = pack_f16x2(ex2(fmaf(sc[2 * b + 1][2], sl2, -r1)), ex2(fmaf(sc[2 * b + 1][3], sl2, -r1)));
+                    if constexpr (ROWS8) {
+                        pa[b][1] = pa[b][3] = 0u;
+                    } else {
+                        pa[b][1] = pack_f16x2(ex2(fmaf(sc[2 * b][2], sl2, -r1)), ex2(fmaf(sc[2 * b][3], sl2, -r1)));
+                        pa[b][3] = pack_f16x2(ex2(fmaf(sc[2 * b + 1][2], sl2, -r1)), ex2(fmaf(sc[2 * b + 1][3], sl2, -r1)));
+                    }
                 }
                 if (!warp_wait(full_v(s0), par0, &abort_flag) || (TWO && !warp_wait(full_v(s1), par1, &abort_flag)))
                     return false;
@@ -380,10 +401,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 break;
             }
             // ------------------------------------------------ finalize --
-            const float l0 = lacc[0], l1 = lacc[2];
+            const float l0 = lacc[0], l1 = ROWS8 ? 0.f : lacc[2];
             const float inv0 = l0 > 0.f ? p.out_scale / l0 : 0.f;
             const float inv1 = l1 > 0.f ? p.out_scale / l1 : 0.f;
-            const bool has0 = g < nrow, has1 = g + 8 < nrow;
+            const bool has0 = g < nrow, has1 = !ROWS8 && g + 8 < nrow;
             // lane holds dims 32a + 8t .. 32a + 8t + 7 of rows g and g + 8:
             // o[4a + i][0 / 2] -> dim 32a + 8t + i, o[4a + i][1 / 3] -> + 4
             if (item.part < 0) {
@@ -456,9 +477,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             for (int kk = 0; kk < D / 16; ++kk) {
                 const int c = kk * 16 + 2 * t4;
                 qf[kk][0] = g < nrow ? __ldg(reinterpret_cast<const uint32_t *>(q0 + c)) : 0u;
-                qf[kk][1] = g + 8 < nrow ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c)) : 0u;
+                qf[kk][1] = !ROWS8 && g + 8 < nrow ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c)) : 0u;
                 qf[kk][2] = g < nrow ? __ldg(reinterpret_cast<const uint32_t *>(q0 + c + 8)) : 0u;
-                qf[kk][3] = g + 8 < nrow ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c + 8)) : 0u;
+                qf[kk][3] = !ROWS8 && g + 8 < nrow ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c + 8)) : 0u;
             }
             float o[D / 8][4];
 #pragma unroll
@@ -488,8 +509,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     const int chunk = (kk % 4) * 2 + (mi & 1);
                     uint32_t b0, b1, b2, b3;
                     ldmatrix_x4(sw128(kb + (kk / 4) * C::BOX, key, chunk), b0, b1, b2, b3);
-                    mma_bf16_16816(sc[0], qf[kk], b0, b1);
-                    mma_bf16_16816(sc[1], qf[kk], b2, b3);
+                    mma_bf16<ROWS8>(sc[0], qf[kk], b0, b1);
+                    mma_bf16<ROWS8>(sc[1], qf[kk], b2, b3);
                 }
                 // mask keys past each row's limit, scale to log2 units
                 const int key0 = pg * kBlockSize;
@@ -511,25 +532,30 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 // Rescale only when the running maximum grows by more than 2^8;
                 // otherwise keep the stale reference (weights stay <= 256).
                 const bool need0 = mx0 > m0 + 8.f;
-                const bool need1 = mx1 > m1 + 8.f;
+                const bool need1 = !ROWS8 && mx1 > m1 + 8.f;
                 float a0 = 1.f, a1 = 1.f;
                 if (need0) { a0 = ex2(m0 - mx0); m0 = mx0; l0 *= a0; }
                 if (need1) { a1 = ex2(m1 - mx1); m1 = mx1; l1 *= a1; }
                 if (__any_sync(0xffffffffu, need0 || need1)) {
 #pragma unroll
                     for (int j = 0; j < D / 8; ++j) {
-                        o[j][0] *= a0; o[j][1] *= a0; o[j][2] *= a1; o[j][3] *= a1;
+                        o[j][0] *= a0; o[j][1] *= a0;
+                        if constexpr (!ROWS8) { o[j][2] *= a1; o[j][3] *= a1; }
                     }
                 }
                 const float r0 = m0 == -INFINITY ? 0.f : m0;
                 const float r1 = m1 == -INFINITY ? 0.f : m1;
                 uint32_t pa[4];
                 pa[0] = pack_bf16x2(ex2(sc[0][0] - r0), ex2(sc[0][1] - r0));
-                pa[1] = pack_bf16x2(ex2(sc[0][2] - r1), ex2(sc[0][3] - r1));
                 pa[2] = pack_bf16x2(ex2(sc[1][0] - r0), ex2(sc[1][1] - r0));
-                pa[3] = pack_bf16x2(ex2(sc[1][2] - r1), ex2(sc[1][3] - r1));
                 l0 += bf16_lo(pa[0]) + bf16_hi(pa[0]) + bf16_lo(pa[2]) + bf16_hi(pa[2]);
-                l1 += bf16_lo(pa[1]) + bf16_hi(pa[1]) + bf16_lo(pa[3]) + bf16_hi(pa[3]);
+                if constexpr (ROWS8) {
+                    pa[1] = pa[3] = 0u;
+                } else {
+                    pa[1] = pack_bf16x2(ex2(sc[0][2] - r1), ex2(sc[0][3] - r1));
+                    pa[3] = pack_bf16x2(ex2(sc[1][2] - r1), ex2(sc[1][3] - r1));
+                    l1 += bf16_lo(pa[1]) + bf16_hi(pa[1]) + bf16_lo(pa[3]) + bf16_hi(pa[3]);
+                }
 
                 if (!warp_wait(full_v(s), par, &abort_flag)) {
                     if (lane == 0) raise_abort(&abort_flag, p.err, kErrTimeout);
@@ -559,8 +585,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     const int chunk = 2 * np + (mi >> 1);
                     uint32_t b0, b1, b2, b3;
                     ldmatrix_x4_trans(sw128(vb + (chunk / 8) * C::BOX, key, chunk % 8), b0, b1, b2, b3);
-                    mma_bf16_16816(o[2 * np], pa, b0, b1);
-                    mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
+                    mma_bf16<ROWS8>(o[2 * np], pa, b0, b1);
+                    mma_bf16<ROWS8>(o[2 * np + 1], pa, b2, b3);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty(s));
@@ -573,7 +599,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
             const float inv0 = l0 > 0.f ? p.out_scale / l0 : 0.f;
             const float inv1 = l1 > 0.f ? p.out_scale / l1 : 0.f;
-            const bool has0 = g < nrow, has1 = g + 8 < nrow;
+            const bool has0 = g < nrow, has1 = !ROWS8 && g + 8 < nrow;
             if (item.part < 0) {
                 uint16_t *orow0 = p.out + (static_cast<int64_t>(item.token + tok0) * p.num_heads_q + head0) * D;
                 uint16_t *orow1 = p.out + (static_cast<int64_t>(item.token + tok1) * p.num_heads_q + head1) * D;
@@ -608,7 +634,7 @@ template <int D, int HG, bool KV8, bool FUSED>
 cudaError_t configure() {
     static bool configured = false;  // attribute is per function, set once per process
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, HG, KV8, FUSED>,
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, HG, KV8, FUSED, PA_DECODE_ROWS8 != 0>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, DecodeCfg<D, HG, KV8>::SMEM);
         if (e != cudaSuccess) return e;
         configured = true;
@@ -629,10 +655,10 @@ cudaError_t launch_t(int num_ctas, const CUtensorMap &tm_k, const CUtensorMap &t
     cudaError_t e = configure_both<D, HG, KV8>();
     if (e != cudaSuccess) return e;
     if (p.new_k != nullptr)
-        return launch_pdl(decode_kernel<D, HG, KV8, true>, dim3(num_ctas), dim3(C::THREADS), C::SMEM, stream, tm_k,
-                          tm_v, p);
-    return launch_pdl(decode_kernel<D, HG, KV8, false>, dim3(num_ctas), dim3(C::THREADS), C::SMEM, stream, tm_k, tm_v,
-                      p);
+        return launch_pdl(decode_kernel<D, HG, KV8, true, PA_DECODE_ROWS8 != 0>, dim3(num_ctas), dim3(C::THREADS),
+                          C::SMEM, stream, tm_k, tm_v, p);
+    return launch_pdl(decode_kernel<D, HG, KV8, false, PA_DECODE_ROWS8 != 0>, dim3(num_ctas), dim3(C::THREADS),
+                      C::SMEM, stream, tm_k, tm_v, p);
 }
 
 }  // namespace
@@ -641,7 +667,7 @@ cudaError_t launch_t(int num_ctas, const CUtensorMap &tm_k, const CUtensorMap &t
     X(64, 1, false) X(64, 2, false) X(64, 4, false) X(64, 8, false) X(128, 1, false) X(128, 2, false)      \
     X(128, 4, false) X(128, 8, false) X(128, 1, true) X(128, 2, true) X(128, 4, true) X(128, 8, true)
 
-cudaError_t prepare_decode(int head_dim, int hg, bool kv8) {
+cudaError_t PA_DECODE_NAME(prepare_decode)(int head_dim, int hg, bool kv8) {
 #define X(d, h, f) \
     if (head_dim == d && hg == h && kv8 == f) return configure_both<d, h, f>();
     PA_DECODE_CASES(X)
@@ -649,8 +675,8 @@ cudaError_t prepare_decode(int head_dim, int hg, bool kv8) {
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_decode(int head_dim, int hg, bool kv8, int num_ctas, const CUtensorMap &tm_k,
-                          const CUtensorMap &tm_v, const DecodeParams &p, cudaStream_t stream) {
+cudaError_t PA_DECODE_NAME(launch_decode)(int head_dim, int hg, bool kv8, int num_ctas, const CUtensorMap &tm_k,
+                                          const CUtensorMap &tm_v, const DecodeParams &p, cudaStream_t stream) {
     if (num_ctas <= 0) return cudaSuccess;
 #define X(d, h, f) \
     if (head_dim == d && hg == h && kv8 == f) return launch_t<d, h, f>(num_ctas, tm_k, tm_v, p, stream);

@@ -254,6 +254,9 @@ cudaError_t launch_dequant(int grid, const DequantParams &p, cudaStream_t stream
 // cudaErrorInvalidValue for an unsupported combination.
 cudaError_t launch_decode(int head_dim, int hg, bool kv8, int num_ctas, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const DecodeParams &p, cudaStream_t stream);
+// The same kernels for launches whose items all have at most 8 MMA rows.
+cudaError_t launch_decode_rows8(int head_dim, int hg, bool kv8, int num_ctas, const CUtensorMap &tm_k,
+                                const CUtensorMap &tm_v, const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_extend(int head_dim, int grid, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const ExtendParams &p, cudaStream_t stream);
 cudaError_t launch_merge(int head_dim, int grid, const MergeParams &p, cudaStream_t stream);
@@ -268,6 +271,7 @@ cudaError_t launch_zero_blocks(const int32_t *ids, int32_t num_ids, int32_t num_
 // One-time per-process kernel attributes (dynamic shared memory sizes) of the
 // kernels a plan launches, so that later launches can be captured.
 cudaError_t prepare_decode(int head_dim, int hg, bool kv8);
+cudaError_t prepare_decode_rows8(int head_dim, int hg, bool kv8);
 cudaError_t prepare_extend(int head_dim);
 
 }  // namespace pa
