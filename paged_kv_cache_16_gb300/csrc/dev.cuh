@@ -160,6 +160,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// generic-proxy global stores of this thread before later async-proxy (TMA)
+// reads of the same addresses
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ------------------------------------------------------------ conversions --
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
@@ -303,40 +309,6 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
         "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// The same two MMAs when rows 8..15 of A are zero and their results unused
-// (every MMA row past the item's query rows): only d[0], d[1] (rows 0..7)
-// are accumulated, so d[2], d[3] need no registers.
-__device__ __forceinline__ void mma_bf16_16816_top(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                                   uint32_t b1) {
-    float u2, u3;
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %10, %10};"
-        : "+f"(d[0]), "+f"(d[1]), "=f"(u2), "=f"(u3)
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
-}
-
-__device__ __forceinline__ void mma_f16_16816_top(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    float u2, u3;
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
-        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %10, %10};"
-        : "+f"(d[0]), "+f"(d[1]), "=f"(u2), "=f"(u3)
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
-}
-
-// TOP: rows 8..15 are padding (see the _top variants)
-template <bool TOP>
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    if constexpr (TOP) mma_bf16_16816_top(d, a, b0, b1);
-    else mma_bf16_16816(d, a, b0, b1);
-}
-template <bool TOP>
-__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    if constexpr (TOP) mma_f16_16816_top(d, a, b0, b1);
-    else mma_f16_16816(d, a, b0, b1);
 }
 
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {

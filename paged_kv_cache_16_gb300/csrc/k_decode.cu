@@ -22,18 +22,6 @@
 
 #include "dev.cuh"
 
-// This file is compiled twice: as itself (kernels for any item) and, through
-// k_decode_rows8.cu, with PA_DECODE_ROWS8 = 1 (kernels for launches whose
-// items all have at most 8 MMA rows), so the two sets compile in parallel.
-#ifndef PA_DECODE_ROWS8
-#define PA_DECODE_ROWS8 0
-#endif
-#if PA_DECODE_ROWS8
-#define PA_DECODE_NAME(n) n##_rows8
-#else
-#define PA_DECODE_NAME(n) n
-#endif
-
 namespace pa {
 namespace {
 
@@ -47,7 +35,6 @@ struct DecodeCfg {
     static constexpr int BOX = 16 * 128;                   // one [16 rows][128 B] box
     static constexpr int TSTAGE = HG * NH * BOX;           // K (or V) bytes per block
     static constexpr int STAGE = decode_stage_bytes(D, HG, KV8);
-    static constexpr int NEWROW = decode_newrow_bytes(D, HG);       // fused update buffers
     static constexpr int NS = decode_stages(D, HG, KV8);
     static constexpr int THREADS = decode_threads(HG);
     static constexpr int SMEM = decode_smem_bytes(D, HG, KV8);
@@ -57,65 +44,41 @@ struct DecodeCfg {
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) { return pack_f16x2_sat(bf16_lo(w), bf16_hi(w)); }
 
 // Fused cache update of one decode row (pa_attention_with_kv_update; the
-// fused dispatch of "vLLM 推理流程分析" §6.1, the write of §6.3): the warp of kv
-// head kvh in the CTA whose run holds the row's last page loads the row's new
-// K and V (16 bytes of each per lane) when the item starts, and stores them
-// into the stage it computes on (over whatever the TMA brought for that slot)
-// and into the caches (E4M3: quantised exactly as pa_write_kv_fp8 does).
-// Every other slot a decode row reads was written by an earlier step.
+// fused dispatch of "vLLM 推理流程分析" §6.1, the write of §6.3): the item
+// whose run holds a decode row's last page stores the row's new K and V
+// (E4M3: quantised exactly as pa_write_kv_fp8 does) when it starts, one warp
+// per kv head, before the producer loads that page, which then reads the new
+// row from the cache like every other row.  Every other slot a decode row
+// reads was written by an earlier step.
+__device__ __forceinline__ int new_row_page(const DecodeItem &item) {
+    const int lp = (item.key_end - 1) / kBlockSize;
+    return item.n_tok == 1 && item.key_end > 0 && item.page_begin <= lp && lp < item.page_end ? lp : -1;
+}
+
 template <int D, bool KV8>
-struct RowUpdate {
-    int last_page = -1;  // the row's last page if this item holds it, else -1
-    int64_t off = -1;    // element offset of (slot, kv head) in a cache; -1: bad block id, no store
-
-    // buf: this warp's shared buffer, the new K row then the new V row (bf16)
-    __device__ __forceinline__ void begin(const DecodeParams &p, const DecodeItem &item, int kvh, int lane,
-                                          uint32_t buf) {
-        const int lp = (item.key_end - 1) / kBlockSize;
-        last_page = p.new_k != nullptr && item.n_tok == 1 && item.key_end > 0 && item.page_begin <= lp &&
-                            lp < item.page_end
-                        ? lp
-                        : -1;
-        if (last_page < 0) return;
-        const int32_t blk = __ldg(p.block_table + static_cast<int64_t>(item.req) * p.max_blocks + lp);
-        const int64_t slot = static_cast<int64_t>(blk) * kBlockSize + (item.key_end - 1) % kBlockSize;
-        off = blk >= 0 && blk < p.num_blocks ? (slot * p.num_heads_kv + kvh) * D : -1;
-        if (lane < D / 8) {
-            const int64_t src = (static_cast<int64_t>(item.token) * p.num_heads_kv + kvh) * D;
-            cp_async16(buf + 16u * lane, reinterpret_cast<const uint4 *>(p.new_k + src) + lane);
-            cp_async16(buf + 2u * D + 16u * lane, reinterpret_cast<const uint4 *>(p.new_v + src) + lane);
-            cp_async_commit();
+__device__ __forceinline__ void store_new_row(const DecodeParams &p, const DecodeItem &item, int lp, int kvh,
+                                              int lane) {
+    const int32_t blk = __ldg(p.block_table + static_cast<int64_t>(item.req) * p.max_blocks + lp);
+    const int64_t slot = static_cast<int64_t>(blk) * kBlockSize + (item.key_end - 1) % kBlockSize;
+    const bool ok = blk >= 0 && blk < p.num_blocks;   // else: not stored (the page load reports it)
+    if (ok && lane < D / 8) {
+        const int64_t src = (static_cast<int64_t>(item.token) * p.num_heads_kv + kvh) * D;
+        const int64_t dst = (slot * p.num_heads_kv + kvh) * D;
+        const uint4 k = __ldg(reinterpret_cast<const uint4 *>(p.new_k + src) + lane);
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p.new_v + src) + lane);
+        if constexpr (KV8) {
+            reinterpret_cast<uint2 *>(static_cast<uint8_t *>(p.cache_k) + dst)[lane] = e4m3_quantize8(k, p.k_scale);
+            reinterpret_cast<uint2 *>(static_cast<uint8_t *>(p.cache_v) + dst)[lane] = e4m3_quantize8(v, p.v_scale);
+        } else {
+            reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.cache_k) + dst)[lane] = k;
+            reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.cache_v) + dst)[lane] = v;
         }
-        if (kvh == 0 && lane == 0 && p.slots_out != nullptr && off >= 0) p.slots_out[item.token] = slot;
     }
+    if (kvh == 0 && lane == 0 && p.slots_out != nullptr && ok) p.slots_out[item.token] = slot;
+    fence_proxy_async_global();   // the stores before the async-proxy (TMA) load of the page
+}
 
-    // the new row (which = 0: K, 1: V) into the stage box(es) starting at box0
-    // (bf16: D / 64 boxes of [16][64], E4M3: one [16][128]) and into the cache
-    __device__ __forceinline__ void put(uint32_t box0, int row, uint32_t buf, int which, void *cache, float scale,
-                                        int lane) const {
-        if (lane < D / 8) {
-            cp_async_wait_all();
-            const uint4 x = lds_v4(buf + which * 2u * D + 16u * lane);
-            if constexpr (KV8) {
-                const uint2 c = e4m3_quantize8(x, scale);
-                asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(sw128(box0, row, lane >> 1) + 8u * (lane & 1)),
-                             "r"(c.x), "r"(c.y)
-                             : "memory");
-                if (off >= 0) reinterpret_cast<uint2 *>(static_cast<uint8_t *>(cache) + off)[lane] = c;
-            } else {
-                sts_v4(sw128(box0 + (lane / 8) * (16 * 128), row, lane % 8), x.x, x.y, x.z, x.w);
-                if (off >= 0) reinterpret_cast<uint4 *>(static_cast<uint16_t *>(cache) + off)[lane] = x;
-            }
-        }
-        fence_proxy_async_smem();   // generic writes before later TMA writes of the stage
-        __syncwarp();
-    }
-};
-
-// ROWS8: every item of the launch has at most 8 (query token, head) rows, so
-// MMA rows 8..15 are padding: their q fragments are zero and their results
-// are never accumulated (half the accumulator registers).
-template <int D, int HG, bool KV8, bool FUSED, bool ROWS8>
+template <int D, int HG, bool KV8, bool FUSED>
 __global__ void __launch_bounds__((HG + 1) * 32, 1)
 decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const DecodeParams p) {
@@ -124,11 +87,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     __shared__ int abort_flag;
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;           // stages, 1024-aligned
-    const uint32_t newrow = base + C::NS * C::STAGE;         // per-warp new K/V rows (fused update)
-    const uint32_t bar0 = newrow + C::NEWROW;   // full_k | full_v | empty
+    const uint32_t bar0 = base + C::NS * C::STAGE;   // full_k | full_v | empty | row_ready
     auto full_k = [&](int s) { return bar0 + 8u * s; };
     auto full_v = [&](int s) { return bar0 + 8u * (C::NS + s); };
     auto empty = [&](int s) { return bar0 + 8u * (2 * C::NS + s); };
+    const uint32_t row_ready = bar0 + 8u * (3 * C::NS);   // fused update: new rows stored (HG arrivals)
     auto stage = [&](int s) { return base + static_cast<uint32_t>(s) * C::STAGE; };
 
     const int warp = threadIdx.x >> 5;
@@ -141,6 +104,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             mbar_init(full_v(s), 1);
             mbar_init(empty(s), HG);
         }
+        mbar_init(row_ready, HG);
         fence_barrier_init();
     } else if (threadIdx.x == 32 * HG) {
         tma_prefetch_desc(&tm_k);
@@ -157,11 +121,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     if (warp == HG) {
         // ------------------------------------------------------ producer --
         int issued = 0;
+        int rows_waited = 0;            // fused update: row_ready phases consumed
         bool ok = true;
         for (int it = item_begin; it < item_end && ok; ++it) {
             const DecodeItem item = p.items[it];
             const int32_t *bt = p.block_table + static_cast<int64_t>(item.req) * p.max_blocks;
             const int h0 = item.head_group * HG;
+            const int new_page = FUSED ? new_row_page(item) : -1;   // load only after its new rows are stored
             int32_t blk_lane = 0;       // block id of page (window + lane), 32 pages at a time
             int window = item.page_begin - 32;
             for (int pg = item.page_begin; pg < item.page_end; ++pg) {
@@ -178,6 +144,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 }
                 const int32_t blk = __shfl_sync(0xffffffffu, blk_lane, pg - window);
                 const bool valid = blk >= 0 && blk < p.num_blocks;
+                if (pg == new_page) {
+                    if (!warp_wait(row_ready, rows_waited & 1, &abort_flag)) {
+                        if (lane == 0) raise_abort(&abort_flag, p.err, kErrTimeout);
+                        ok = false;
+                        break;
+                    }
+                    ++rows_waited;
+                }
                 if (lane == 0) {
                     if (valid) {
                         mbar_arrive_expect_tx(full_k(s), C::TSTAGE);
@@ -251,17 +225,23 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     return bf16x2_to_f16x2(__ldg(reinterpret_cast<const uint32_t *>(row + col)));
                 };
                 qf[kk][0] = g < nrow ? ld(q0, c) : 0u;
-                qf[kk][1] = !ROWS8 && g + 8 < nrow ? ld(q1, c) : 0u;
+                qf[kk][1] = g + 8 < nrow ? ld(q1, c) : 0u;
                 qf[kk][2] = g < nrow ? ld(q0, c + 2) : 0u;
-                qf[kk][3] = !ROWS8 && g + 8 < nrow ? ld(q1, c + 2) : 0u;
+                qf[kk][3] = g + 8 < nrow ? ld(q1, c + 2) : 0u;
             }
             float o[D / 8][4];
 #pragma unroll
             for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
             float lacc[4] = {0.f, 0.f, 0.f, 0.f};
             float m0 = -INFINITY, m1 = -INFINITY;
-            RowUpdate<D, true> upd;
-            if constexpr (FUSED) upd.begin(p, item, kvh, lane, newrow + warp * 4u * D);
+            if constexpr (FUSED) {
+                const int lp = new_row_page(item);
+                if (lp >= 0) {
+                    store_new_row<D, true>(p, item, lp, kvh, lane);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(row_ready);
+                }
+            }
 
             auto qk = [&](uint32_t kb, float (&a)[4], float (&b)[4]) {
 #pragma unroll
@@ -270,8 +250,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     uint32_t k0, k1, k2, k3;
                     e4m3x4_to_f16x2x2(lds_u32(x), k0, k1);
                     e4m3x4_to_f16x2x2(lds_u32(x + 1024u), k2, k3);
-                    mma_f16<ROWS8>(a, qf[kk], k0, k1);
-                    mma_f16<ROWS8>(b, qf[kk], k2, k3);
+                    mma_f16_16816(a, qf[kk], k0, k1);
+                    mma_f16_16816(b, qf[kk], k2, k3);
                 }
             };
             // O += P V for one block; MASKED zeroes the codes of rows at or
@@ -299,9 +279,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     e4m3x4_to_f16x2x2(prmt(wC, wD, 0x5140u), b1[0], b1[1]);
                     e4m3x4_to_f16x2x2(prmt(wC, wD, 0x7362u), b1[2], b1[3]);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) mma_f16<ROWS8>(o[4 * a + i], pf, b0[i], b1[i]);
+                    for (int i = 0; i < 4; ++i) mma_f16_16816(o[4 * a + i], pf, b0[i], b1[i]);
                 }
-                mma_f16<ROWS8>(lacc, pf, kOnes, kOnes);
+                mma_f16_16816(lacc, pf, kOnes, kOnes);
             };
             // one softmax round over one (TWO = false) or two cache blocks
             auto round = [&](auto two_c, int pg) -> bool {
@@ -310,12 +290,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 const uint32_t par0 = (consumed / C::NS) & 1, par1 = ((consumed + 1) / C::NS) & 1;
                 if (!warp_wait(full_k(s0), par0, &abort_flag) || (TWO && !warp_wait(full_k(s1), par1, &abort_flag)))
                     return false;
-                const bool new0 = FUSED && pg == upd.last_page;
-                const bool new1 = FUSED && TWO && pg + 1 == upd.last_page;
-                const int nrow = (item.key_end - 1) % kBlockSize;
-                const uint32_t nbuf = newrow + warp * 4u * D;
-                if (new0) upd.put(stage(s0) + warp * C::BOX, nrow, nbuf, 0, p.cache_k, p.k_scale, lane);
-                if (new1) upd.put(stage(s1) + warp * C::BOX, nrow, nbuf, 0, p.cache_k, p.k_scale, lane);
                 float sc[4][4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
@@ -346,18 +320,16 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2)) * sl2;
                 // rescale only when the running maximum grows by more than 2^8
                 const bool need0 = mx0 > m0 + 8.f;
-                const bool need1 = !ROWS8 && mx1 > m1 + 8.f;
+                const bool need1 = mx1 > m1 + 8.f;
                 if (__any_sync(0xffffffffu, need0 || need1)) {
                     float a0 = 1.f, a1 = 1.f;
                     if (need0) { a0 = ex2(m0 - mx0); m0 = mx0; }
                     if (need1) { a1 = ex2(m1 - mx1); m1 = mx1; }
 #pragma unroll
                     for (int j = 0; j < D / 8; ++j) {
-                        o[j][0] *= a0; o[j][1] *= a0;
-                        if constexpr (!ROWS8) { o[j][2] *= a1; o[j][3] *= a1; }
+                        o[j][0] *= a0; o[j][1] *= a0; o[j][2] *= a1; o[j][3] *= a1;
                     }
-                    lacc[0] *= a0; lacc[1] *= a0;
-                    if constexpr (!ROWS8) { lacc[2] *= a1; lacc[3] *= a1; }
+                    lacc[0] *= a0; lacc[1] *= a0; lacc[2] *= a1; lacc[3] *= a1;
                 }
                 const float r0 = m0 == -INFINITY ? 0.f : m0;
                 const float r1 = m1 == -INFINITY ? 0.f : m1;
@@ -365,18 +337,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #pragma unroll
                 for (int b = 0; b < NT / 2; ++b) {
                     pa[b][0] = pack_f16x2(ex2(fmaf(sc[2 * b][0], sl2, -r0)), ex2(fmaf(sc[2 * b][1], sl2, -r0)));
+                    pa[b][1] = pack_f16x2(ex2(fmaf(sc[2 * b][2], sl2, -r1)), ex2(fmaf(sc[2 * b][3], sl2, -r1)));
                     pa[b][2] = pack_f16x2(ex2(fmaf(sc[2 * b + 1][0], sl2, -r0)), ex2(fmaf(sc[2 * b + 1][1], sl2, -r0)));
-                    if constexpr (ROWS8) {
-                        pa[b][1] = pa[b][3] = 0u;
-                    } else {
-                        pa[b][1] = pack_f16x2(ex2(fmaf(sc[2 * b][2], sl2, -r1)), ex2(fmaf(sc[2 * b][3], sl2, -r1)));
-                        pa[b][3] = pack_f16x2(ex2(fmaf(sc[2 * b + 1][2], sl2, -r1)), ex2(fmaf(sc[2 * b + 1][3], sl2, -r1)));
-                    }
+                    pa[b][3] = pack_f16x2(ex2(fmaf(sc[2 * b + 1][2], sl2, -r1)), ex2(fmaf(sc[2 * b + 1][3], sl2, -r1)));
                 }
                 if (!warp_wait(full_v(s0), par0, &abort_flag) || (TWO && !warp_wait(full_v(s1), par1, &abort_flag)))
                     return false;
-                if (new0) upd.put(stage(s0) + C::TSTAGE + warp * C::BOX, nrow, nbuf, 1, p.cache_v, p.v_scale, lane);
-                if (new1) upd.put(stage(s1) + C::TSTAGE + warp * C::BOX, nrow, nbuf, 1, p.cache_v, p.v_scale, lane);
                 const uint32_t vb0 = stage(s0) + C::TSTAGE + warp * C::BOX;
                 if (valid_keys < kBlockSize) pv(std::true_type{}, vb0, pa[0], valid_keys);
                 else pv(std::false_type{}, vb0, pa[0], kBlockSize);
@@ -401,10 +367,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 break;
             }
             // ------------------------------------------------ finalize --
-            const float l0 = lacc[0], l1 = ROWS8 ? 0.f : lacc[2];
+            const float l0 = lacc[0], l1 = lacc[2];
             const float inv0 = l0 > 0.f ? p.out_scale / l0 : 0.f;
             const float inv1 = l1 > 0.f ? p.out_scale / l1 : 0.f;
-            const bool has0 = g < nrow, has1 = !ROWS8 && g + 8 < nrow;
+            const bool has0 = g < nrow, has1 = g + 8 < nrow;
             // lane holds dims 32a + 8t .. 32a + 8t + 7 of rows g and g + 8:
             // o[4a + i][0 / 2] -> dim 32a + 8t + i, o[4a + i][1 / 3] -> + 4
             if (item.part < 0) {
@@ -477,16 +443,22 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             for (int kk = 0; kk < D / 16; ++kk) {
                 const int c = kk * 16 + 2 * t4;
                 qf[kk][0] = g < nrow ? __ldg(reinterpret_cast<const uint32_t *>(q0 + c)) : 0u;
-                qf[kk][1] = !ROWS8 && g + 8 < nrow ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c)) : 0u;
+                qf[kk][1] = g + 8 < nrow ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c)) : 0u;
                 qf[kk][2] = g < nrow ? __ldg(reinterpret_cast<const uint32_t *>(q0 + c + 8)) : 0u;
-                qf[kk][3] = !ROWS8 && g + 8 < nrow ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c + 8)) : 0u;
+                qf[kk][3] = g + 8 < nrow ? __ldg(reinterpret_cast<const uint32_t *>(q1 + c + 8)) : 0u;
             }
             float o[D / 8][4];
 #pragma unroll
             for (int j = 0; j < D / 8; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
             float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-            RowUpdate<D, false> upd;
-            if constexpr (FUSED) upd.begin(p, item, kvh, lane, newrow + warp * 4u * D);
+            if constexpr (FUSED) {
+                const int lp = new_row_page(item);
+                if (lp >= 0) {
+                    store_new_row<D, false>(p, item, lp, kvh, lane);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(row_ready);
+                }
+            }
 
             for (int pg = item.page_begin; pg < item.page_end; ++pg, ++consumed) {
                 const int s = consumed % C::NS;
@@ -498,8 +470,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 }
                 const uint32_t kb = stage(s) + warp * C::NH * C::BOX;
                 const uint32_t vb = kb + C::TSTAGE;
-                const bool new_row = FUSED && pg == upd.last_page;
-                if (new_row) upd.put(kb, (item.key_end - 1) % kBlockSize, newrow + warp * 4u * D, 0, p.cache_k, p.k_scale, lane);
                 // S = Q K^T over this block's 16 keys (two n-tiles of 8 keys)
                 float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
@@ -509,8 +479,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     const int chunk = (kk % 4) * 2 + (mi & 1);
                     uint32_t b0, b1, b2, b3;
                     ldmatrix_x4(sw128(kb + (kk / 4) * C::BOX, key, chunk), b0, b1, b2, b3);
-                    mma_bf16<ROWS8>(sc[0], qf[kk], b0, b1);
-                    mma_bf16<ROWS8>(sc[1], qf[kk], b2, b3);
+                    mma_bf16_16816(sc[0], qf[kk], b0, b1);
+                    mma_bf16_16816(sc[1], qf[kk], b2, b3);
                 }
                 // mask keys past each row's limit, scale to log2 units
                 const int key0 = pg * kBlockSize;
@@ -532,37 +502,31 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 // Rescale only when the running maximum grows by more than 2^8;
                 // otherwise keep the stale reference (weights stay <= 256).
                 const bool need0 = mx0 > m0 + 8.f;
-                const bool need1 = !ROWS8 && mx1 > m1 + 8.f;
+                const bool need1 = mx1 > m1 + 8.f;
                 float a0 = 1.f, a1 = 1.f;
                 if (need0) { a0 = ex2(m0 - mx0); m0 = mx0; l0 *= a0; }
                 if (need1) { a1 = ex2(m1 - mx1); m1 = mx1; l1 *= a1; }
                 if (__any_sync(0xffffffffu, need0 || need1)) {
 #pragma unroll
                     for (int j = 0; j < D / 8; ++j) {
-                        o[j][0] *= a0; o[j][1] *= a0;
-                        if constexpr (!ROWS8) { o[j][2] *= a1; o[j][3] *= a1; }
+                        o[j][0] *= a0; o[j][1] *= a0; o[j][2] *= a1; o[j][3] *= a1;
                     }
                 }
                 const float r0 = m0 == -INFINITY ? 0.f : m0;
                 const float r1 = m1 == -INFINITY ? 0.f : m1;
                 uint32_t pa[4];
                 pa[0] = pack_bf16x2(ex2(sc[0][0] - r0), ex2(sc[0][1] - r0));
+                pa[1] = pack_bf16x2(ex2(sc[0][2] - r1), ex2(sc[0][3] - r1));
                 pa[2] = pack_bf16x2(ex2(sc[1][0] - r0), ex2(sc[1][1] - r0));
+                pa[3] = pack_bf16x2(ex2(sc[1][2] - r1), ex2(sc[1][3] - r1));
                 l0 += bf16_lo(pa[0]) + bf16_hi(pa[0]) + bf16_lo(pa[2]) + bf16_hi(pa[2]);
-                if constexpr (ROWS8) {
-                    pa[1] = pa[3] = 0u;
-                } else {
-                    pa[1] = pack_bf16x2(ex2(sc[0][2] - r1), ex2(sc[0][3] - r1));
-                    pa[3] = pack_bf16x2(ex2(sc[1][2] - r1), ex2(sc[1][3] - r1));
-                    l1 += bf16_lo(pa[1]) + bf16_hi(pa[1]) + bf16_lo(pa[3]) + bf16_hi(pa[3]);
-                }
+                l1 += bf16_lo(pa[1]) + bf16_hi(pa[1]) + bf16_lo(pa[3]) + bf16_hi(pa[3]);
 
                 if (!warp_wait(full_v(s), par, &abort_flag)) {
                     if (lane == 0) raise_abort(&abort_flag, p.err, kErrTimeout);
                     ok = false;
                     break;
                 }
-                if (new_row) upd.put(vb, (item.key_end - 1) % kBlockSize, newrow + warp * 4u * D, 1, p.cache_v, p.v_scale, lane);
                 if (valid_keys < kBlockSize) {
                     // rows past the context may hold anything (even NaN); zero
                     // them so that 0-weight * row stays 0 inside the MMA
@@ -585,8 +549,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     const int chunk = 2 * np + (mi >> 1);
                     uint32_t b0, b1, b2, b3;
                     ldmatrix_x4_trans(sw128(vb + (chunk / 8) * C::BOX, key, chunk % 8), b0, b1, b2, b3);
-                    mma_bf16<ROWS8>(o[2 * np], pa, b0, b1);
-                    mma_bf16<ROWS8>(o[2 * np + 1], pa, b2, b3);
+                    mma_bf16_16816(o[2 * np], pa, b0, b1);
+                    mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty(s));
@@ -599,7 +563,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
             const float inv0 = l0 > 0.f ? p.out_scale / l0 : 0.f;
             const float inv1 = l1 > 0.f ? p.out_scale / l1 : 0.f;
-            const bool has0 = g < nrow, has1 = !ROWS8 && g + 8 < nrow;
+            const bool has0 = g < nrow, has1 = g + 8 < nrow;
             if (item.part < 0) {
                 uint16_t *orow0 = p.out + (static_cast<int64_t>(item.token + tok0) * p.num_heads_q + head0) * D;
                 uint16_t *orow1 = p.out + (static_cast<int64_t>(item.token + tok1) * p.num_heads_q + head1) * D;
@@ -634,7 +598,7 @@ template <int D, int HG, bool KV8, bool FUSED>
 cudaError_t configure() {
     static bool configured = false;  // attribute is per function, set once per process
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, HG, KV8, FUSED, PA_DECODE_ROWS8 != 0>,
+        cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, HG, KV8, FUSED>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, DecodeCfg<D, HG, KV8>::SMEM);
         if (e != cudaSuccess) return e;
         configured = true;
@@ -655,9 +619,9 @@ cudaError_t launch_t(int num_ctas, const CUtensorMap &tm_k, const CUtensorMap &t
     cudaError_t e = configure_both<D, HG, KV8>();
     if (e != cudaSuccess) return e;
     if (p.new_k != nullptr)
-        return launch_pdl(decode_kernel<D, HG, KV8, true, PA_DECODE_ROWS8 != 0>, dim3(num_ctas), dim3(C::THREADS),
+        return launch_pdl(decode_kernel<D, HG, KV8, true>, dim3(num_ctas), dim3(C::THREADS),
                           C::SMEM, stream, tm_k, tm_v, p);
-    return launch_pdl(decode_kernel<D, HG, KV8, false, PA_DECODE_ROWS8 != 0>, dim3(num_ctas), dim3(C::THREADS),
+    return launch_pdl(decode_kernel<D, HG, KV8, false>, dim3(num_ctas), dim3(C::THREADS),
                       C::SMEM, stream, tm_k, tm_v, p);
 }
 
@@ -667,7 +631,7 @@ cudaError_t launch_t(int num_ctas, const CUtensorMap &tm_k, const CUtensorMap &t
     X(64, 1, false) X(64, 2, false) X(64, 4, false) X(64, 8, false) X(128, 1, false) X(128, 2, false)      \
     X(128, 4, false) X(128, 8, false) X(128, 1, true) X(128, 2, true) X(128, 4, true) X(128, 8, true)
 
-cudaError_t PA_DECODE_NAME(prepare_decode)(int head_dim, int hg, bool kv8) {
+cudaError_t prepare_decode(int head_dim, int hg, bool kv8) {
 #define X(d, h, f) \
     if (head_dim == d && hg == h && kv8 == f) return configure_both<d, h, f>();
     PA_DECODE_CASES(X)
@@ -675,7 +639,7 @@ cudaError_t PA_DECODE_NAME(prepare_decode)(int head_dim, int hg, bool kv8) {
     return cudaErrorInvalidValue;
 }
 
-cudaError_t PA_DECODE_NAME(launch_decode)(int head_dim, int hg, bool kv8, int num_ctas, const CUtensorMap &tm_k,
+cudaError_t launch_decode(int head_dim, int hg, bool kv8, int num_ctas, const CUtensorMap &tm_k,
                                           const CUtensorMap &tm_v, const DecodeParams &p, cudaStream_t stream) {
     if (num_ctas <= 0) return cudaSuccess;
 #define X(d, h, f) \

@@ -448,12 +448,6 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
             units.push_back({r, qsl[r] + j, n, d->num_computed_tokens[r] + j + n});
         }
     }
-    // decode items of at most 8 (query token, head) rows run on kernels that
-    // drop MMA rows 8..15; a fixed-shape plan decides from its shape alone
-    // (rows of several tokens possible when max_tokens > max_reqs)
-    P->rows8 = P->G <= 8;
-    if (P->fixed) P->rows8 = P->rows8 && shape->max_tokens <= shape->max_reqs;
-    for (const DecodeUnit &u : units) P->rows8 = P->rows8 && u.n_tok * P->G <= 8;
     std::vector<int32_t> pieces, item_unit;
     const int cps = std::max(1, decode_ctas_per_sm_static(P->D, P->HG, P->kv8));
     plan_decode(P, units, pieces, item_unit, P->fixed ? static_cast<int64_t>(P->num_sms) * cps : 0);
@@ -649,8 +643,7 @@ namespace pa {
 
 pa_status prepare_plan(pa_plan_s *P) {
     if (P->prepared) return PA_OK;
-    if (P->ncta > 0 && (P->rows8 ? prepare_decode_rows8 : prepare_decode)(P->D, P->HG, P->kv8) != cudaSuccess)
-        return PA_ERR_CUDA;
+    if (P->ncta > 0 && prepare_decode(P->D, P->HG, P->kv8) != cudaSuccess) return PA_ERR_CUDA;
     if (P->cap_tiles > 0 && prepare_extend(P->D) != cudaSuccess) return PA_ERR_CUDA;
     P->prepared = true;
     return PA_OK;
@@ -777,9 +770,7 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
         dp.k_scale = P->k_scale;
         dp.v_scale = P->v_scale;
         if (rec(0, true, stream) != cudaSuccess) return PA_ERR_CUDA;
-        if ((P->rows8 ? launch_decode_rows8 : launch_decode)(P->D, P->HG, P->kv8, P->ncta, tm_k, tm_v, dp, stream) !=
-            cudaSuccess)
-            return PA_ERR_CUDA;
+        if (launch_decode(P->D, P->HG, P->kv8, P->ncta, tm_k, tm_v, dp, stream) != cudaSuccess) return PA_ERR_CUDA;
         if (rec(0, false, stream) != cudaSuccess) return PA_ERR_CUDA;
     }
     if (P->cap_merges > 0) {

@@ -29,11 +29,11 @@ constexpr int decode_stages(int d, int hg, bool kv8) {
                                                                        : 2);
 }
 constexpr int decode_threads(int hg) { return (hg + 1) * 32; }
-// per-warp buffer of a decode row's new K and V rows (bf16) for the fused update
-constexpr int decode_newrow_bytes(int d, int hg) { return hg * 4 * d; }
+// stages, their full_k / full_v / empty barriers and the fused update's
+// row_ready barrier, plus 1024-byte alignment slack
 constexpr int decode_smem_bytes(int d, int hg, bool kv8) {
-    return decode_stages(d, hg, kv8) * decode_stage_bytes(d, hg, kv8) + decode_newrow_bytes(d, hg) +
-           3 * decode_stages(d, hg, kv8) * 8 + 1024;
+    return decode_stages(d, hg, kv8) * decode_stage_bytes(d, hg, kv8) + (3 * decode_stages(d, hg, kv8) + 1) * 8 +
+           1024;
 }
 constexpr int kSmemPerSm = 233472;  // 228 KiB of shared memory per SM
 constexpr int decode_ctas_per_sm_static(int d, int hg, bool kv8) {
@@ -254,9 +254,6 @@ cudaError_t launch_dequant(int grid, const DequantParams &p, cudaStream_t stream
 // cudaErrorInvalidValue for an unsupported combination.
 cudaError_t launch_decode(int head_dim, int hg, bool kv8, int num_ctas, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const DecodeParams &p, cudaStream_t stream);
-// The same kernels for launches whose items all have at most 8 MMA rows.
-cudaError_t launch_decode_rows8(int head_dim, int hg, bool kv8, int num_ctas, const CUtensorMap &tm_k,
-                                const CUtensorMap &tm_v, const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_extend(int head_dim, int grid, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const ExtendParams &p, cudaStream_t stream);
 cudaError_t launch_merge(int head_dim, int grid, const MergeParams &p, cudaStream_t stream);
@@ -271,7 +268,6 @@ cudaError_t launch_zero_blocks(const int32_t *ids, int32_t num_ids, int32_t num_
 // One-time per-process kernel attributes (dynamic shared memory sizes) of the
 // kernels a plan launches, so that later launches can be captured.
 cudaError_t prepare_decode(int head_dim, int hg, bool kv8);
-cudaError_t prepare_decode_rows8(int head_dim, int hg, bool kv8);
 cudaError_t prepare_extend(int head_dim);
 
 }  // namespace pa

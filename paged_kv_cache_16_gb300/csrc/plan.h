@@ -16,7 +16,6 @@ struct pa_plan_s {
     int32_t prefix_splits = 0;
     float scale_log2 = 0.f;     // softmax_scale * k_scale * log2(e)
     bool kv8 = false;           // E4M3 caches
-    bool rows8 = false;         // every decode item has at most 8 MMA rows (ROWS8 kernels)
     float out_scale = 1.f;      // v_scale for E4M3 caches
     float k_scale = 1.f, v_scale = 1.f;   // E4M3 quantisation scales of the fused write
     // work lists
