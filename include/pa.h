@@ -335,7 +335,7 @@ pa_status pa_attention_launch(const pa_plan_t *plan, const void *q, const void *
  * exactly as pa_slot_mapping + pa_write_kv (bf16) or pa_write_kv_fp8 (E4M3,
  * with the plan's k_scale / v_scale) would leave them, and out is the result
  * pa_attention computes over those caches.  A decode row's new K/V row is
- * stored by the decode kernel itself (and used from on-chip memory); the new
+ * stored by the decode kernel itself (before it loads the row's last page); the new
  * rows of extend rows are stored by one kernel before the tensor-core tiles
  * read them.  No separate slot-mapping or write launch is needed.
  *   key, value     DEVICE bf16 [T][Hkv][D] (16-byte aligned): the new rows
