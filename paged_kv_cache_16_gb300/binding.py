@@ -54,10 +54,10 @@ class BatchDesc(ctypes.Structure):
         ("block_size", ctypes.c_int32),
         ("num_blocks", ctypes.c_int32),
         ("max_blocks_per_req", ctypes.c_int32),
-        ("query_start_loc", ctypes.POINTER(ctypes.c_int32)),
-        ("seq_lens", ctypes.POINTER(ctypes.c_int32)),
-        ("num_computed_tokens", ctypes.POINTER(ctypes.c_int32)),
-        ("block_table_host", ctypes.POINTER(ctypes.c_int32)),
+        ("query_start_loc", ctypes.c_void_p),      # const int32_t * (host)
+        ("seq_lens", ctypes.c_void_p),
+        ("num_computed_tokens", ctypes.c_void_p),
+        ("block_table_host", ctypes.c_void_p),
         ("num_common_prefix_blocks", ctypes.c_int32),
         ("softmax_scale", ctypes.c_float),
         ("num_sms", ctypes.c_int32),
@@ -240,25 +240,10 @@ def make_desc(*, num_heads_q, num_heads_kv, head_dim, num_blocks, query_start_lo
     bt = None if block_table_host is None else np.ascontiguousarray(block_table_host, dtype=np.int32)
     if max_blocks_per_req is None:
         max_blocks_per_req = bt.shape[1] if bt is not None else 1
-    i32p = ctypes.POINTER(ctypes.c_int32)
-    d = BatchDesc()
-    d.num_reqs = len(sl)
-    d.num_heads_q = num_heads_q
-    d.num_heads_kv = num_heads_kv
-    d.head_dim = head_dim
-    d.block_size = block_size
-    d.num_blocks = num_blocks
-    d.max_blocks_per_req = int(max_blocks_per_req)
-    d.query_start_loc = qsl.ctypes.data_as(i32p)
-    d.seq_lens = sl.ctypes.data_as(i32p)
-    d.num_computed_tokens = nc.ctypes.data_as(i32p)
-    d.block_table_host = bt.ctypes.data_as(i32p) if bt is not None else ctypes.cast(None, i32p)
-    d.num_common_prefix_blocks = int(num_common_prefix_blocks)
-    d.softmax_scale = float(softmax_scale)
-    d.num_sms = int(num_sms)
-    d.kv_cache_dtype = int(kv_cache_dtype)
-    d.k_scale = float(k_scale)
-    d.v_scale = float(v_scale)
+    d = BatchDesc(len(sl), num_heads_q, num_heads_kv, head_dim, block_size, num_blocks, int(max_blocks_per_req),
+                  qsl.ctypes.data, sl.ctypes.data, nc.ctypes.data, bt.ctypes.data if bt is not None else None,
+                  int(num_common_prefix_blocks), float(softmax_scale), int(num_sms), int(kv_cache_dtype),
+                  float(k_scale), float(v_scale))
     return d, (qsl, sl, nc, bt)
 
 
