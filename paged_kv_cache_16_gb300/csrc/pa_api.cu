@@ -508,10 +508,16 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     P->ncta = static_cast<int32_t>(P->cta_begin.size()) - 1;
     const int32_t scr_rows = P->max_blocks > 0 ? static_cast<int32_t>(P->scratch_table.size() / P->max_blocks) : 0;
     if (P->fixed) {
-        // every decode unit holds at least one token
-        const int64_t items_cap = static_cast<int64_t>(P->ncta) + static_cast<int64_t>(shape->max_tokens) * P->n_groups;
+        // decode units: at least one token each, and a request of at most
+        // kMaxSmallQ tokens makes at most ceil(kMaxSmallQ / tg) of them; the
+        // equal cut adds at most one item per CTA
+        const int64_t max_units = std::min<int64_t>(shape->max_tokens, static_cast<int64_t>(shape->max_reqs) *
+                                                                            ((kMaxSmallQ + tg - 1) / tg));
+        const int64_t items_cap = static_cast<int64_t>(P->ncta) + max_units * P->n_groups;
         const int64_t merges_cap = static_cast<int64_t>(shape->max_tokens) * P->n_groups;
-        const int64_t slots_cap = shape->max_partial_slots > 0 ? shape->max_partial_slots : items_cap + merges_cap;
+        const int64_t slots_cap = shape->max_partial_slots > 0
+                                      ? shape->max_partial_slots
+                                      : static_cast<int64_t>(P->ncta) + 2 * merges_cap;
         if (items_cap > INT32_MAX || merges_cap > INT32_MAX || slots_cap > INT32_MAX) return PA_ERR_UNSUPPORTED;
         P->cap_tokens = shape->max_tokens;
         P->cap_items = static_cast<int32_t>(items_cap);

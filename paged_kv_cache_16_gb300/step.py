@@ -206,14 +206,23 @@ class GraphStep:
         self.turn = 0
         self.caches = (key_cache.data_ptr(), value_cache.data_ptr())
 
-    def replay(self, plan: binding.Plan):
-        """Write the plan's metadata image and replay the graph that uploads it."""
+    def prepare_replay(self, plan: binding.Plan):
+        """Write the plan's metadata image for the next replay (host work)."""
         i = self.turn
         self.done[i].synchronize()   # the replay that last read image i has run
         binding.pa_plan_copy_metadata(plan, self.images[i])
+
+    def launch_replay(self):
+        """Replay the graph that uploads the prepared image."""
+        i = self.turn
         self.graphs[i].replay()
         self.done[i].record()
         self.turn = 1 - i
+
+    def replay(self, plan: binding.Plan):
+        """Write the plan's metadata image and replay the graph that uploads it."""
+        self.prepare_replay(plan)
+        self.launch_replay()
 
     def run(self, batch: Batch, q, key, value, key_cache, value_cache) -> torch.Tensor:
         """One step: plan, copy in, replay (capturing on first use)."""
