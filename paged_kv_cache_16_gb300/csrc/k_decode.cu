@@ -197,7 +197,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         const int g = lane >> 2;
         const int t4 = lane & 3;
         const int G = p.group;
-        const int gsh = __ffs(G) - 1;   // G is a power of two; MMA row r = (token r / G, head r % G)
+        // MMA row r = (token r / G, head r % G)
         constexpr uint32_t kOnes = 0x3C003C00u;  // f16x2 (1, 1)
         const uint32_t k_lane = g * 128u + 4u * t4;   // key g at +0, key g + 8 at +1024
         const uint32_t va_lane = 256u * t4 + 16u * (g >> 2) + 4u * (g & 3);             // key 2t
@@ -209,8 +209,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const DecodeItem item = p.items[it];
             const int kvh = item.head_group * HG + warp;
             const int nrow = item.n_tok * G;
-            const int tok0 = g >> gsh, tok1 = (g + 8) >> gsh;
-            const int head0 = kvh * G + (g & (G - 1)), head1 = kvh * G + ((g + 8) & (G - 1));
+            const int tok0 = g / G, tok1 = (g + 8) / G;
+            const int head0 = kvh * G + g % G, head1 = kvh * G + (g + 8) % G;
             const uint16_t *q0 = p.q + (static_cast<int64_t>(item.token + tok0) * p.num_heads_q + head0) * D;
             const uint16_t *q1 = p.q + (static_cast<int64_t>(item.token + tok1) * p.num_heads_q + head1) * D;
             // causal limit of each row: token i sees keys < key_end - (n_tok - 1 - i)
@@ -424,15 +424,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         const int g = lane >> 2;
         const int t4 = lane & 3;
         const int G = p.group;
-        const int gsh = __ffs(G) - 1;   // G is a power of two
         int consumed = 0;
         bool ok = true;
         for (int it = item_begin; it < item_end && ok; ++it) {
             const DecodeItem item = p.items[it];
             const int kvh = item.head_group * HG + warp;
             const int nrow = item.n_tok * G;
-            const int tok0 = g >> gsh, tok1 = (g + 8) >> gsh;
-            const int head0 = kvh * G + (g & (G - 1)), head1 = kvh * G + ((g + 8) & (G - 1));
+            const int tok0 = g / G, tok1 = (g + 8) / G;
+            const int head0 = kvh * G + g % G, head1 = kvh * G + (g + 8) % G;
             const uint16_t *q0 = p.q + (static_cast<int64_t>(item.token + tok0) * p.num_heads_q + head0) * D;
             const uint16_t *q1 = p.q + (static_cast<int64_t>(item.token + tok1) * p.num_heads_q + head1) * D;
             // causal limit of each row: token i sees keys < key_end - (n_tok - 1 - i)

@@ -184,7 +184,9 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 break;
             }
             const int n_q = sh.n_sub[1] > 0 ? 2 : 1;
-            if (lane == 0) mbar_arrive_expect_tx(bar(B_QFULL), n_q * C::QB);
+            // each box is tpt tokens x G heads x 64 dims: tpt * G rows of
+            // 128 bytes (128 rows unless G does not divide 128)
+            if (lane == 0) mbar_arrive_expect_tx(bar(B_QFULL), n_q * C::NH * tpt * G * 128);
             __syncwarp();
             if (lane < n_q * C::NH) {
                 const int t = lane / C::NH, half = lane % C::NH;
@@ -353,7 +355,8 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const TileShape sh = tile_shape(tile, tpt);
             const int i = t * tpt + row / G;         // token of this row within the tile
             const int gq = row % G;
-            const bool tok_valid = i < tile.n_tok;
+            // rows past tpt * G (when G does not divide 128) are padding
+            const bool tok_valid = row < tpt * G && i < tile.n_tok;
             const int pos_lim = tile.causal ? tile.pos0 + i + 1 : 0x7fffffff;  // keys < pos_lim
             const int row_end = min(tile.key_end, pos_lim);
             const int n_mine = t ? sh.n_sub[1] : sh.n_sub[0];

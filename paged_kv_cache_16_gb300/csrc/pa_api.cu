@@ -126,7 +126,6 @@ StagingPool &staging() {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 int heads_per_group(int hkv) {
     for (int hg = kMaxDecodeHeads; hg > 1; hg >>= 1)
@@ -188,7 +187,7 @@ pa_status validate(const pa_batch_desc *d) {
     if (d->kv_cache_dtype == PA_KV_FP8_E4M3 && d->head_dim != 128) return PA_ERR_UNSUPPORTED;
     if (d->head_dim != 64 && d->head_dim != 128) return PA_ERR_UNSUPPORTED;
     const int G = d->num_heads_q / d->num_heads_kv;
-    if (!is_pow2(G) || G > 16) return PA_ERR_UNSUPPORTED;
+    if (G > kTileRows) return PA_ERR_UNSUPPORTED;   // a tensor-core sub-tile holds at least one token
     if (static_cast<int64_t>(d->num_blocks) * d->block_size > INT32_MAX) return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
@@ -293,11 +292,15 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     // needs several units (each re-reads the row's keys) but the tensor-core
     // tiles of all such rows would not fill the GPU; else, and for longer
     // rows, tensor-core tiles.
+    // A decode unit is one MMA tile of 16 (token, head) rows, so the decode
+    // kernel takes groups of at most 16 query heads; larger groups (e.g. a
+    // single kv head shared by 32 query heads) run every row on the tiles.
     const int32_t tg = std::max(1, kMmaRows / P->G);   // tokens per decode unit
     std::vector<int32_t> decode_rows, small_rows, extend_rows, multi_unit;
     for (int32_t r = 0; r < P->R; ++r) {
         const int32_t q_len = qsl[r + 1] - qsl[r];
-        if (q_len == 1) decode_rows.push_back(r);
+        if (q_len > 0 && P->G > kMmaRows) extend_rows.push_back(r);
+        else if (q_len == 1) decode_rows.push_back(r);
         else if (q_len > 1 && q_len <= tg) small_rows.push_back(r);
         else if (q_len > 1 && q_len <= kMaxSmallQ) multi_unit.push_back(r);
         else if (q_len > 1) extend_rows.push_back(r);

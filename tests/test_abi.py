@@ -106,14 +106,30 @@ def test_invalid_metadata(lib, tiny, case):
     assert binding.pa_plan_status(**kw) == binding.PA_ERR_INVALID_ARGUMENT
 
 
-@pytest.mark.parametrize("over", [dict(head_dim=96), dict(block_size=32), dict(num_heads_q=6, num_heads_kv=2),
-                                  dict(num_heads_q=64, num_heads_kv=2)])
+@pytest.mark.parametrize("over", [dict(head_dim=96), dict(block_size=32), dict(num_heads_q=256, num_heads_kv=1)])
 def test_unsupported_shapes(lib, tiny, over):
     kw = desc(tiny, **over)
     if "block_size" in over:
         # keep the metadata consistent with 32-token blocks
         kw["block_table_host"] = tiny.block_table[:, :2]
     assert binding.pa_plan_status(**kw) == binding.PA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("hq,hkv", [(6, 2), (28, 4), (64, 2), (32, 1), (128, 1)])
+def test_any_group_size_plans(lib, hq, hkv):
+    """Any Hq % Hkv == 0 up to 128 query heads per kv head: groups of at most
+    16 keep decode rows on the split-KV kernel, larger ones run every row on
+    the tensor-core tiles (a sub-tile holds 128 // G tokens)."""
+    G = hq // hkv
+    b = workloads.make_batch(name="g", num_heads_q=hq, num_heads_kv=hkv, head_dim=64, q_lens=[1, 5, 1, 40],
+                             seq_lens=[30, 70, 200, 90], num_blocks=80, seed=G)
+    info = binding.pa_plan(**desc(b)).info()
+    if G <= 16:
+        assert info["num_decode_rows"] == 2 and info["num_extend_rows"] + info["num_small_q_rows"] == 2
+    else:
+        assert info["num_decode_rows"] == 0 and info["num_small_q_rows"] == 0 and info["num_extend_rows"] == 4
+        tpt = 2 * (128 // G)
+        assert info["num_extend_tiles"] == hkv * sum(-(-q // tpt) for q in (1, 5, 1, 40))
 
 
 def test_mixed_batch_example_metadata(lib):

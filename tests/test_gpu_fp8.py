@@ -89,7 +89,8 @@ def test_fp8_cascade_small(use_cascade):
                             use_cascade=use_cascade, kv_cache_dtype="fp8"))
 
 
-@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (16, 4), (64, 4), (4, 1), (32, 16), (48, 3)])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (16, 4), (64, 4), (4, 1), (32, 16), (48, 3), (28, 4), (40, 8),
+                                     (32, 1)])
 def test_fp8_head_shapes(hq, hkv):
     q_lens = [1, 1, 37, 1, 129, 3, 1]
     seq = [1, 77, 37, 300, 400, 19, 64]

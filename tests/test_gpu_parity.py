@@ -83,10 +83,14 @@ def test_cascade_with_extend_rows():
 
 
 @pytest.mark.parametrize("hq,hkv,d", [(8, 8, 128), (16, 8, 64), (16, 4, 128), (32, 4, 64), (64, 4, 128),
-                                      (4, 1, 128), (16, 1, 64), (32, 16, 128), (48, 3, 64), (6, 6, 64)])
+                                      (4, 1, 128), (16, 1, 64), (32, 16, 128), (48, 3, 64), (6, 6, 64),
+                                      (28, 4, 128), (24, 8, 64), (12, 2, 128), (40, 8, 128), (80, 8, 64),
+                                      (32, 1, 128), (64, 1, 64), (128, 1, 128)])
 def test_head_shapes(hq, hkv, d):
-    """Group sizes 1..16, head dims 64/128, kv-head counts that are not a
-    power of two and more than 8 kv heads (several decode head groups)."""
+    """Group sizes 1..16 (powers of two and 3, 5, 6, 7, 10: 128 not a multiple
+    of G leaves padding rows in the tiles), 32..128 (every row on the tiles),
+    head dims 64/128, kv-head counts that are not a power of two and more
+    than 8 kv heads (several decode head groups)."""
     q_lens = [1, 1, 37, 1, 129, 3, 1]
     seq = [1, 77, 37, 300, 400, 19, 64]
     b = make_batch(name=f"heads-{hq}-{hkv}-{d}", num_heads_q=hq, num_heads_kv=hkv, head_dim=d, q_lens=q_lens,
