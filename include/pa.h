@@ -37,8 +37,9 @@
  * 0..position (bottom-right causal alignment).
  *
  * Supported: head_dim 64 or 128 (128 only with FP8 caches), block_size 16,
- * Hq % Hkv == 0 with the group size Hq/Hkv a power of two up to 16,
- * num_blocks * 16 < 2^31.  Other shapes return PA_ERR_UNSUPPORTED.
+ * Hq % Hkv == 0 with the group size G = Hq/Hkv at most 128 (groups of more
+ * than 16 query heads run every row on the tensor-core tiles), num_blocks *
+ * 16 < 2^31.  Other shapes return PA_ERR_UNSUPPORTED.
  *
  * Ownership: the caller allocates and owns every device buffer (q, caches,
  * block table, out, slot mapping, workspace).  A plan is host memory owned by
