@@ -72,9 +72,9 @@ TRAFFIC = {
     # (kernel, workload, kv dtype, source sha) -> bytes per launch (fused-write variant, the one the
     # default step runs); profiles/decode_kernel_decode-workload.md, profiles/extend_kernel_prefill-workload.md,
     # profiles/decode_kernel_e4m3_decode-workload.md
-    ("decode", "decode", "bf16", "3a8b6428f720c2bb"): 645_146_624,
-    ("decode", "decode", "fp8", "3a8b6428f720c2bb"): 325_626_880,
-    ("extend", "prefill", "bf16", "059d9582423e486a"): 73_212_672,
+    ("decode", "decode", "bf16", "92b11a045f4b2f7c"): 645_422_592,
+    ("decode", "decode", "fp8", "92b11a045f4b2f7c"): 325_470_720,
+    ("extend", "prefill", "bf16", "b45c1014dd07eddd"): 73_937_408,
 }
 KERNEL_SOURCES = {"decode": "paged_kv_cache_16_gb300/csrc/k_decode.cu",
                   "extend": "paged_kv_cache_16_gb300/csrc/k_extend.cu"}
