@@ -158,3 +158,14 @@ def test_write_kv_out_of_range_slot_reported():
         if s is not None:
             assert torch.equal(flat[s], key[t])
     assert binding.pa_check_device_errors(err) == 0  # cleared by the read
+
+
+@pytest.mark.parametrize("q_gain", [8.0, 40.0])
+def test_extend_wide_score_range(q_gain):
+    """Queries scaled up so that a row's scores span hundreds of powers of
+    two: most weights underflow to zero and the running max moves many
+    times along a row."""
+    b = make_batch(name="wide", num_heads_q=32, num_heads_kv=8, head_dim=128, q_lens=[300, 1, 77, 2],
+                   seq_lens=[700, 900, 77, 260], num_blocks=200, seed=11)
+    b.q = (b.q.float() * q_gain).to(torch.bfloat16)
+    check_batch(b, what=f"wide x{q_gain}")
