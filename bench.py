@@ -32,7 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from paged_kv_cache_16_gb300 import binding, build, workloads  # noqa: E402
-from paged_kv_cache_16_gb300.step import DeviceStep, GraphStep  # noqa: E402
+from paged_kv_cache_16_gb300.step import DeviceStep, GraphStep, NativeGraphStep  # noqa: E402
 from paged_kv_cache_16_gb300.workloads import bf16_bits  # noqa: E402
 
 METRIC = "paged-attn step tokens/s; decode KV GB/s & prefill TFLOPS as % GB300 roofline"
@@ -400,12 +400,13 @@ def run_ours(args, world, rank, local):
     # Capacities are this workload's own sizes; the eager plan and the
     # fixed-shape plan cut the work identically, so the kernels (timed per
     # launch above) are the same ones the graph replays.
-    gs = GraphStep(num_heads_q=batch.num_heads_q, num_heads_kv=batch.num_heads_kv, head_dim=batch.head_dim,
+    gs_args = dict(num_heads_q=batch.num_heads_q, num_heads_kv=batch.num_heads_kv, head_dim=batch.head_dim,
                    num_blocks=batch.num_blocks, max_blocks_per_req=batch.block_table.shape[1],
                    softmax_scale=batch.softmax_scale, max_tokens=max(T, 1), max_reqs=max(batch.num_reqs, 1),
                    max_extend_tiles=info["num_extend_tiles"], max_dequant_blocks=info["num_dequant_blocks"],
                    max_partial_slots=max(info["num_partial_slots"], 1), kv_cache_dtype=batch.kv_cache_dtype,
                    k_scale=batch.k_scale, v_scale=batch.v_scale, device=dev, fused=fused)
+    gs = GraphStep(**gs_args)
     first = gs.make_plan(batch)
     gs.load(batch, first, q, key, value)
     gs.capture(first, kc, vc)
@@ -447,30 +448,42 @@ def run_ours(args, world, rank, local):
         ms_all, clocks = g_ms_all, g_clocks
 
     # ---- end to end through the C ABI with host buffers ----
-    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-    q_h, key_h, val_h = pin(batch.q), pin(batch.key), pin(batch.value)
-    meta_h = [pin(torch.as_tensor(a)) for a in (batch.query_start_loc, batch.num_computed, batch.block_table)]
-    meta_d = [st.qsl, st.num_computed, st.block_table]
-    out_h = torch.empty((max(T, 1), batch.num_heads_q, batch.head_dim), dtype=torch.bfloat16).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, key_h, val_h, *meta_h))
-    d2h = T * batch.num_heads_q * batch.head_dim * 2
     e2e_steps = max(3, min(args.steps, 200))
     e2e_times = []
-    for i in range(e2e_steps + 2):
-        flush_l2()
-        torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()
-        if graph_mode:
-            gs.q[:T].copy_(q_h, non_blocking=True)
-            gs.key[:T].copy_(key_h, non_blocking=True)
-            gs.value[:T].copy_(val_h, non_blocking=True)
-            gs.qsl[:batch.num_reqs + 1].copy_(meta_h[0], non_blocking=True)
-            gs.num_computed[:batch.num_reqs].copy_(meta_h[1], non_blocking=True)
-            gs.block_table[:batch.num_reqs].copy_(meta_h[2], non_blocking=True)
-            plan = gs.make_plan(batch)
-            gs.replay(plan)
-            out_h[:T].copy_(gs.out[:T], non_blocking=True)
-        else:
+    if graph_mode:
+        # the step's inputs sit in a page-locked image (q, key, value and the
+        # request metadata in one layout); each replay copies it in, runs the
+        # step and copies the output back to page-locked memory
+        gh = NativeGraphStep(**gs_args, key_cache=kc, value_cache=vc, host_io=True)
+        for i in (0, 1):
+            gh.fill_host_image(i, batch, batch.q, batch.key, batch.value)
+        h2d = gh.host_in[0].numel()
+        d2h = gh.host_out[0].numel() * 2
+        R = batch.num_reqs
+        for i in range(e2e_steps + 2):
+            flush_l2()
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            gh.launch(R, batch.num_common_prefix_blocks)
+            out_host = gh.output(T)
+            if i >= 2:
+                e2e_times.append(time.perf_counter() - t0)
+        if not torch.equal(out_host, gs.out[:T].cpu()):
+            raise SystemExit("host-to-host step differs from the device-resident replay")
+        bits |= gh.check_errors()
+        gh.destroy()
+    else:
+        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+        q_h, key_h, val_h = pin(batch.q), pin(batch.key), pin(batch.value)
+        meta_h = [pin(torch.as_tensor(a)) for a in (batch.query_start_loc, batch.num_computed, batch.block_table)]
+        meta_d = [st.qsl, st.num_computed, st.block_table]
+        out_h = torch.empty((max(T, 1), batch.num_heads_q, batch.head_dim), dtype=torch.bfloat16).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (q_h, key_h, val_h, *meta_h))
+        d2h = T * batch.num_heads_q * batch.head_dim * 2
+        for i in range(e2e_steps + 2):
+            flush_l2()
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
             q.copy_(q_h, non_blocking=True)
             key.copy_(key_h, non_blocking=True)
             value.copy_(val_h, non_blocking=True)
@@ -484,13 +497,19 @@ def run_ours(args, world, rank, local):
                 st.write(key, value, kc, vc, stream)
                 st.attend(q, kc, vc, stream, plan=plan)
             out_h[:T].copy_(st.out[:T], non_blocking=True)
-        torch.cuda.synchronize(dev)
-        if i >= 2:
-            e2e_times.append(time.perf_counter() - t0)
-        plan.destroy()
+            torch.cuda.synchronize(dev)
+            if i >= 2:
+                e2e_times.append(time.perf_counter() - t0)
+            plan.destroy()
     e2e_s = max_over_ranks(world, statistics.mean(e2e_times), dev)
     e2e = {"value": tokens_all / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "ms_per_step": e2e_s * 1e3}
+           "ms_per_step": e2e_s * 1e3,
+           "path": ("pa_graph_step (the library's graph executor, one C call: fixed plan from the host metadata, "
+                    "metadata image, graph launch); the graph copies the page-locked input image to the device, "
+                    "uploads the metadata, runs the step kernels and copies the output to page-locked memory; "
+                    "wall clock to the output's arrival" if graph_mode else
+                    "per-tensor copies from page-locked memory, host plan, eager launches, output copy back; "
+                    "wall clock to the output's arrival")}
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1) ----
     cpu = None

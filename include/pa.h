@@ -439,6 +439,93 @@ pa_status pa_attention_no_alloc(const pa_plan_t *plan, const void *q, const void
                                 const void *value_cache, const int32_t *block_table, void *out,
                                 int32_t *device_error_word, void *stream);
 
+/*
+ * Native graph executor: graph mode of "vLLM 源码完全拆解（十六）" (fourth
+ * walk-through: capture a stable shape once; per step copy the new data to
+ * fixed addresses and replay) without a framework around it.  A pa_graph_t
+ * holds two instantiated CUDA graphs of one fixed shape, each made of
+ *   [copy of a page-locked input image to the device]   (optional host I/O)
+ *   pa_upload_metadata_from(its own page-locked metadata image)
+ *   the step: pa_attention_with_kv_update_launch (fused), or pa_slot_mapping
+ *             + pa_write_kv / pa_write_kv_fp8 + pa_attention_launch
+ *   [copy of out back to a page-locked output buffer]   (optional host I/O)
+ * and alternates between them, so the host prepares one step while the
+ * previous one may still run.  It owns its workspace (error word included),
+ * its slot buffer, both metadata images, two events and a capture stream; the
+ * caller owns every buffer listed in pa_graph_buffers and must keep them (and
+ * their addresses) for the graph's lifetime.  pa_graph_step costs one fixed
+ * plan (host), one copy of its metadata image (host) and one graph launch.
+ */
+typedef struct pa_graph_s pa_graph_t;
+
+typedef struct {
+    /* DEVICE buffers sized for the fixed shape (16-byte aligned). */
+    void *q;                         /* bf16 [max_tokens][Hq][D]          */
+    void *key;                       /* bf16 [max_tokens][Hkv][D]         */
+    void *value;                     /* bf16 [max_tokens][Hkv][D]         */
+    void *out;                       /* bf16 [max_tokens][Hq][D]          */
+    int32_t *query_start_loc;        /* [max_reqs + 1]                     */
+    int32_t *num_computed;           /* [max_reqs]                         */
+    int32_t *block_table;            /* [max_reqs][max_blocks_per_req]     */
+    void *key_cache;                 /* [num_blocks][16][Hkv][D] of the    */
+    void *value_cache;               /*   desc's kv_cache_dtype            */
+    int32_t fused;                   /* 1: write + attention in one call   */
+    /* Optional host I/O (all NULL / 0 for none).  host_in[i] (page-locked
+     * HOST, in_bytes) is copied to device_in (DEVICE, in_bytes) at the start
+     * of graph i; out (out_bytes from its start) is copied to host_out[i]
+     * (page-locked HOST) at its end.  device_in normally spans the device
+     * buffers above, so that one copy brings a whole step's inputs in. */
+    const void *host_in[2];
+    void *device_in;
+    size_t in_bytes;
+    void *host_out[2];
+    size_t out_bytes;
+} pa_graph_buffers;
+
+/*
+ * Capture the two graphs.  desc is any step the shape accepts (its model
+ * fields fix the graph's: head counts, head_dim, block_size, num_blocks,
+ * max_blocks_per_req, softmax_scale, num_sms, kv_cache_dtype, k_scale,
+ * v_scale); it is planned with pa_plan_fixed and its metadata uploaded
+ * eagerly on the capture stream, which also prepares the kernels.  The
+ * device buffers are not read during this call.
+ * Errors: as pa_plan_fixed; PA_ERR_INVALID_ARGUMENT for a NULL or misaligned
+ * buffer, host I/O given in part, or a host buffer that is not page-locked;
+ * PA_ERR_CUDA when an allocation, the capture or the instantiation fails.
+ */
+pa_status pa_graph_create(const pa_batch_desc *desc, const pa_fixed_shape *shape, const pa_graph_buffers *bufs,
+                          pa_graph_t **out);
+
+/*
+ * One step: wait until the graph that next runs (pa_graph_turn) has finished
+ * its previous launch, plan desc with the graph's fixed shape, copy the
+ * plan's metadata into that graph's image, launch it on stream and flip the
+ * turn.  With host I/O, host_in[pa_graph_turn(g)] must hold the step's inputs
+ * before the call (write them after pa_graph_wait of that turn), and the
+ * output is in host_out[that turn] once pa_graph_wait returns for it.
+ * Errors: PA_ERR_INVALID_ARGUMENT (NULL, or desc's model fields differ from
+ * the graph's), the errors of pa_plan_fixed (nothing is launched then),
+ * PA_ERR_CUDA.
+ */
+pa_status pa_graph_step(pa_graph_t *g, const pa_batch_desc *desc, void *stream);
+
+/* Index (0 or 1) of the graph the next pa_graph_step launches. */
+int32_t pa_graph_turn(const pa_graph_t *g);
+
+/* Block until graph `turn`'s last launch (if any) has completed. */
+pa_status pa_graph_wait(pa_graph_t *g, int32_t turn);
+
+/* The graph's workspace: its first 4 bytes are the device error word (read
+ * it with pa_check_device_errors). */
+void *pa_graph_workspace(const pa_graph_t *g);
+
+/* The graph's DEVICE slot buffer (int64 [max_tokens]): every token's slot
+ * after a step (fused or not). */
+int64_t *pa_graph_slot_mapping(const pa_graph_t *g);
+
+/* Waits for both graphs, then frees everything the graph owns.  NULL is a no-op. */
+void pa_graph_destroy(pa_graph_t *g);
+
 /* Static description of a status code. */
 const char *pa_status_string(pa_status status);
 

@@ -36,7 +36,8 @@ EXPORTED = ("pa_plan", "pa_plan_destroy", "pa_plan_get_info", "pa_slot_mapping",
             "pa_plan_kernel_times", "pa_status_string", "pa_attention_no_alloc", "pa_write_kv_fp8",
             "pa_plan_fixed", "pa_upload_metadata", "pa_attention_launch", "pa_zero_blocks",
             "pa_attention_with_kv_update", "pa_attention_with_kv_update_launch", "pa_plan_metadata_bytes",
-            "pa_plan_copy_metadata", "pa_upload_metadata_from")
+            "pa_plan_copy_metadata", "pa_upload_metadata_from", "pa_graph_create", "pa_graph_step",
+            "pa_graph_turn", "pa_graph_wait", "pa_graph_workspace", "pa_graph_slot_mapping", "pa_graph_destroy")
 
 
 class PaError(RuntimeError):
@@ -104,6 +105,26 @@ class FixedShape(ctypes.Structure):
     ]
 
 
+class GraphBuffers(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p),
+        ("key", ctypes.c_void_p),
+        ("value", ctypes.c_void_p),
+        ("out", ctypes.c_void_p),
+        ("query_start_loc", ctypes.c_void_p),
+        ("num_computed", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p),
+        ("key_cache", ctypes.c_void_p),
+        ("value_cache", ctypes.c_void_p),
+        ("fused", ctypes.c_int32),
+        ("host_in", ctypes.c_void_p * 2),
+        ("device_in", ctypes.c_void_p),
+        ("in_bytes", ctypes.c_size_t),
+        ("host_out", ctypes.c_void_p * 2),
+        ("out_bytes", ctypes.c_size_t),
+    ]
+
+
 def library_path() -> str:
     return _build.LIBRARY
 
@@ -137,6 +158,20 @@ def load(path: str | None = None, build_if_missing: bool = False) -> ctypes.CDLL
     lib.pa_plan_copy_metadata.argtypes = [vp, vp, sz]
     lib.pa_upload_metadata_from.restype = ctypes.c_int
     lib.pa_upload_metadata_from.argtypes = [vp, sz, vp, sz, vp]
+    lib.pa_graph_create.restype = ctypes.c_int
+    lib.pa_graph_create.argtypes = [vp, vp, vp, ctypes.POINTER(vp)]
+    lib.pa_graph_step.restype = ctypes.c_int
+    lib.pa_graph_step.argtypes = [vp, vp, vp]
+    lib.pa_graph_turn.restype = i32
+    lib.pa_graph_turn.argtypes = [vp]
+    lib.pa_graph_wait.restype = ctypes.c_int
+    lib.pa_graph_wait.argtypes = [vp, i32]
+    lib.pa_graph_workspace.restype = vp
+    lib.pa_graph_workspace.argtypes = [vp]
+    lib.pa_graph_slot_mapping.restype = vp
+    lib.pa_graph_slot_mapping.argtypes = [vp]
+    lib.pa_graph_destroy.restype = None
+    lib.pa_graph_destroy.argtypes = [vp]
     lib.pa_attention_launch.restype = ctypes.c_int
     lib.pa_attention_launch.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.pa_attention_with_kv_update.restype = ctypes.c_int
@@ -183,9 +218,11 @@ def _check(status: int, what: str):
 
 
 def _ptr(t) -> int | None:
-    """Raw device/host address of a tensor (or None)."""
+    """Raw device/host address of a tensor or an address (or None)."""
     if t is None:
         return None
+    if isinstance(t, int):
+        return t
     return int(t.data_ptr())
 
 
@@ -413,3 +450,90 @@ def pa_check_device_errors(word, stream=None) -> int:
     if st not in (PA_OK, PA_ERR_DEVICE_CHECK):
         raise PaError(st, "pa_check_device_errors")
     return int(bits.value)
+
+
+class NativeGraph:
+    """pa_graph_t: the two captured step graphs of one fixed shape (see pa.h).
+
+    ``host``: the step's metadata arrays the planner reads each step
+    (query_start_loc [max_reqs+1], seq_lens [max_reqs], num_computed
+    [max_reqs], block_table [max_reqs][max_blocks_per_req], int32 numpy
+    arrays kept by the caller and rewritten in place), or a pair of such sets,
+    one per graph (step n reads set ``turn``); ``num_reqs`` is set per step.
+    ``buffers``: the device (and optional page-locked host I/O) buffers of
+    pa_graph_buffers, as tensors or raw addresses.
+    """
+
+    def __init__(self, *, shape: dict, host: dict, buffers: dict, num_reqs: int, fused: bool, **model):
+        sets = list(host) if isinstance(host, (list, tuple)) else [host, host]
+        self._host = sets
+        self._descs = []
+        for hs in sets:
+            for k in ("query_start_loc", "seq_lens", "num_computed", "block_table"):
+                a = hs[k]
+                if not (isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous):
+                    raise ValueError(f"host[{k!r}] must be a C-contiguous int32 numpy array")
+            d, _ = make_desc(query_start_loc=hs["query_start_loc"], seq_lens=hs["seq_lens"],
+                             num_computed_tokens=hs["num_computed"], block_table_host=hs["block_table"], **model)
+            # the descriptor points into the caller's arrays, rewritten each step
+            d.query_start_loc = hs["query_start_loc"].ctypes.data
+            d.seq_lens = hs["seq_lens"].ctypes.data
+            d.num_computed_tokens = hs["num_computed"].ctypes.data
+            d.block_table_host = hs["block_table"].ctypes.data
+            d.num_reqs = int(num_reqs)
+            self._descs.append(d)
+        self._shape = _fixed_shape(**shape)
+        addr = lambda t: None if t is None else (t if isinstance(t, int) else int(t.data_ptr()))  # noqa: E731
+        b = GraphBuffers()
+        for k in ("q", "key", "value", "out", "query_start_loc", "num_computed", "block_table", "key_cache",
+                  "value_cache", "device_in"):
+            setattr(b, k, addr(buffers.get(k)))
+        b.fused = 1 if fused else 0
+        for k, n in (("host_in", "in_bytes"), ("host_out", "out_bytes")):
+            pair = buffers.get(k)
+            if pair is not None:
+                getattr(b, k)[0] = addr(pair[0])
+                getattr(b, k)[1] = addr(pair[1])
+                setattr(b, n, int(buffers[n]))
+        self._buffers = buffers
+        h = ctypes.c_void_p()
+        self.handle = None
+        _check(load().pa_graph_create(ctypes.byref(self._descs[0]), ctypes.byref(self._shape), ctypes.byref(b),
+                                      ctypes.byref(h)), "pa_graph_create")
+        self.handle = h.value
+        self._step = load().pa_graph_step
+        self._turn = 0
+
+    def step(self, num_reqs: int, stream=None, num_common_prefix_blocks: int = 0):
+        """Plan the step now in the host arrays (set ``turn``) and launch the
+        next graph (num_common_prefix_blocks > 0: the cascade route)."""
+        d = self._descs[self._turn]
+        d.num_reqs = num_reqs
+        d.num_common_prefix_blocks = num_common_prefix_blocks
+        _check(self._step(self.handle, ctypes.byref(d), _stream(stream)), "pa_graph_step")
+        self._turn = 1 - self._turn
+
+    @property
+    def turn(self) -> int:
+        """Graph (and host set / I/O buffers) the next step uses."""
+        return int(load().pa_graph_turn(self.handle))
+
+    def wait(self, turn: int):
+        _check(load().pa_graph_wait(self.handle, int(turn)), "pa_graph_wait")
+
+    def workspace_ptr(self) -> int:
+        return int(load().pa_graph_workspace(self.handle))
+
+    def slot_mapping_ptr(self) -> int:
+        return int(load().pa_graph_slot_mapping(self.handle))
+
+    def destroy(self):
+        if self.handle:
+            load().pa_graph_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass

@@ -80,6 +80,65 @@ class DeviceStep:
         return binding.pa_check_device_errors(self.error_word, stream)
 
 
+def _device_view(ptr: int, n: int, dtype, device) -> torch.Tensor:
+    """A tensor over n elements of library-owned device memory (no copy)."""
+    typestr = {torch.int64: "<i8", torch.int32: "<i4"}[dtype]
+
+    class _Array:
+        __cuda_array_interface__ = {"shape": (n,), "typestr": typestr, "data": (ptr, False), "version": 3}
+    return torch.as_tensor(_Array(), device=device)
+
+
+def _input_layout(max_tokens, max_reqs, hq, hkv, d, mb):
+    """Byte offsets of the step's inputs in one block (256-byte aligned)."""
+    sizes = [("q", max_tokens * hq * d * 2), ("key", max_tokens * hkv * d * 2), ("value", max_tokens * hkv * d * 2),
+             ("qsl", (max_reqs + 1) * 4), ("num_computed", max_reqs * 4), ("block_table", max_reqs * mb * 4),
+             ("seq_lens", max_reqs * 4)]
+    lay, off = {}, 0
+    for name, n in sizes:
+        lay[name] = (off, n)
+        off += (n + 255) // 256 * 256
+    lay["bytes"] = off
+    lay["dims"] = (max_tokens, max_reqs, hq, hkv, d, mb)
+    return lay
+
+
+def _input_views(block: torch.Tensor, lay) -> dict:
+    """Typed views of an input block (device or page-locked host)."""
+    t, r, hq, hkv, d, mb = lay["dims"]
+
+    def view(name, dtype, shape):
+        off, n = lay[name]
+        return block[off:off + n].view(dtype).view(*shape)
+    return {"q": view("q", torch.bfloat16, (t, hq, d)), "key": view("key", torch.bfloat16, (t, hkv, d)),
+            "value": view("value", torch.bfloat16, (t, hkv, d)), "qsl": view("qsl", torch.int32, (r + 1,)),
+            "num_computed": view("num_computed", torch.int32, (r,)),
+            "block_table": view("block_table", torch.int32, (r, mb)), "seq_lens": view("seq_lens", torch.int32, (r,))}
+
+
+def _fill(views: dict, batch: Batch, q=None, key=None, value=None):
+    """Write a step's metadata (padded to the static shapes: spare requests
+    get no tokens) and, if given, its new rows into a set of input views."""
+    R, T = batch.num_reqs, batch.num_tokens
+    mr, mb = views["num_computed"].numel(), views["block_table"].shape[1]
+    qsl = np.full(mr + 1, T, dtype=np.int32)
+    qsl[:R + 1] = batch.query_start_loc
+    nc = np.zeros(mr, dtype=np.int32)
+    nc[:R] = batch.num_computed
+    bt = np.zeros((mr, mb), dtype=np.int32)
+    bt[:R, :batch.block_table.shape[1]] = batch.block_table
+    views["qsl"].copy_(torch.from_numpy(qsl))
+    views["num_computed"].copy_(torch.from_numpy(nc))
+    views["block_table"].copy_(torch.from_numpy(bt))
+    if "seq_lens" in views:
+        sl = np.zeros(mr, dtype=np.int32)
+        sl[:R] = batch.seq_lens
+        views["seq_lens"].copy_(torch.from_numpy(sl))
+    for name, src in (("q", q), ("key", key), ("value", value)):
+        if src is not None:
+            views[name][:T].copy_(src)
+
+
 class GraphStep:
     """Engine steps replayed from one CUDA graph (fixed-shape plans).
 
@@ -94,12 +153,17 @@ class GraphStep:
     and the attention kernels (fused: pa_attention_with_kv_update_launch; else
     slot mapping, pa_write_kv and pa_attention_launch).  Two images and two
     graphs alternate, so the host writes one step's image while the previous
-    step's graph may still be reading the other.
+    step's graph may still be reading the other.  With ``host_io`` each graph
+    also brings the step's inputs in from a page-locked input image (one copy:
+    q, key, value and the request metadata share one layout) and copies the
+    output back to page-locked memory, so a replay goes from host memory to
+    host memory.
     """
 
     def __init__(self, *, num_heads_q, num_heads_kv, head_dim, num_blocks, max_blocks_per_req, softmax_scale,
                  max_tokens, max_reqs, max_extend_tiles=0, max_dequant_blocks=0, max_partial_slots=0,
-                 kv_cache_dtype="bf16", k_scale=1.0, v_scale=1.0, num_sms=0, device="cuda", fused=True):
+                 kv_cache_dtype="bf16", k_scale=1.0, v_scale=1.0, num_sms=0, device="cuda", fused=True,
+                 host_io=False):
         dev = torch.device(device)
         self.device = dev
         self.fused = fused
@@ -112,14 +176,25 @@ class GraphStep:
                           max_dequant_blocks=max_dequant_blocks, max_partial_slots=max_partial_slots)
         self.fp8 = kv_cache_dtype == "fp8"
         self.k_scale, self.v_scale = k_scale, v_scale
-        self.q = torch.zeros(max_tokens, num_heads_q, head_dim, dtype=torch.bfloat16, device=dev)
-        self.key = torch.zeros(max_tokens, num_heads_kv, head_dim, dtype=torch.bfloat16, device=dev)
-        self.value = torch.zeros_like(self.key)
+        # the step's inputs (q, key, value, query_start_loc, num_computed,
+        # block_table) are views of one device block, so that one copy from a
+        # page-locked image of the same layout brings a whole step in
+        self._in_layout = _input_layout(max_tokens, max_reqs, num_heads_q, num_heads_kv, head_dim,
+                                        max_blocks_per_req)
+        self._in = torch.zeros(self._in_layout["bytes"], dtype=torch.uint8, device=dev)
+        views = _input_views(self._in, self._in_layout)
+        self.q, self.key, self.value = views["q"], views["key"], views["value"]
+        self.qsl, self.num_computed, self.block_table = views["qsl"], views["num_computed"], views["block_table"]
         self.out = torch.zeros_like(self.q)
-        self.qsl = torch.zeros(max_reqs + 1, dtype=torch.int32, device=dev)
-        self.num_computed = torch.zeros(max_reqs, dtype=torch.int32, device=dev)
-        self.block_table = torch.zeros(max_reqs, max_blocks_per_req, dtype=torch.int32, device=dev)
         self.slots = torch.zeros(max_tokens, dtype=torch.int64, device=dev)
+        # host_io: each graph also copies a page-locked input image (the
+        # layout above) to the device first and the output back last, so a
+        # replay is a whole step from host memory to host memory
+        self.host_in = None
+        self.host_out = None
+        if host_io:
+            self.host_in = [torch.zeros(self._in_layout["bytes"], dtype=torch.uint8).pin_memory() for _ in range(2)]
+            self.host_out = [torch.zeros(self.out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
         self.workspace = None
         self.graphs = None       # two captures, one per metadata image
         self.images = None       # page-locked metadata images
@@ -152,20 +227,25 @@ class GraphStep:
 
     def stage(self, batch: Batch, q=None, key=None, value=None):
         """Copy a step's request metadata and new rows into the static buffers."""
-        R, T = batch.num_reqs, batch.num_tokens
-        mr, mb = self.num_computed.numel(), self.block_table.shape[1]
-        qsl = np.full(mr + 1, T, dtype=np.int32)
-        qsl[:R + 1] = batch.query_start_loc
-        nc = np.zeros(mr, dtype=np.int32)
-        nc[:R] = batch.num_computed
-        bt = np.zeros((mr, mb), dtype=np.int32)
-        bt[:R, :batch.block_table.shape[1]] = batch.block_table
-        self.qsl.copy_(torch.from_numpy(qsl))
-        self.num_computed.copy_(torch.from_numpy(nc))
-        self.block_table.copy_(torch.from_numpy(bt))
-        for dst, src in ((self.q, q), (self.key, key), (self.value, value)):
-            if src is not None:
-                dst[:T].copy_(src)
+        _fill({"q": self.q, "key": self.key, "value": self.value, "qsl": self.qsl,
+               "num_computed": self.num_computed, "block_table": self.block_table}, batch, q, key, value)
+
+    def host_inputs(self, i=None) -> dict:
+        """Views of page-locked input image i (default: the one the next
+        replay copies in): q, key, value, qsl, num_computed, block_table."""
+        return _input_views(self.host_in[self.turn if i is None else i], self._in_layout)
+
+    def stage_host(self, batch: Batch, q=None, key=None, value=None, i=None):
+        """Write a step's metadata and new rows into page-locked input image i."""
+        if i is None and self.done is not None:
+            self.done[self.turn].synchronize()   # the replay that last read it has run
+        _fill(self.host_inputs(i), batch, q, key, value)
+
+    def host_output(self, num_tokens: int) -> torch.Tensor:
+        """The last replay's output in page-locked host memory (waits for it)."""
+        i = 1 - self.turn
+        self.done[i].synchronize()
+        return self.host_out[i][:num_tokens]
 
     def enqueue(self, plan: binding.Plan, key_cache, value_cache, stream=None):
         """Slot mapping, cache write and attention over the static buffers
@@ -199,8 +279,12 @@ class GraphStep:
         for img in self.images:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
+                if self.host_in is not None:
+                    self._in.copy_(self.host_in[len(self.graphs)], non_blocking=True)
                 binding.pa_upload_metadata_from(img, nbytes, self.workspace)
                 self.enqueue(plan, key_cache, value_cache)
+                if self.host_out is not None:
+                    self.host_out[len(self.graphs)].copy_(self.out, non_blocking=True)
             self.graphs.append(g)
         self.done = [torch.cuda.Event(), torch.cuda.Event()]
         self.turn = 0
@@ -237,3 +321,109 @@ class GraphStep:
 
     def check_errors(self, stream=None) -> int:
         return binding.pa_check_device_errors(self.error_word, stream)
+
+
+class NativeGraphStep:
+    """Engine steps through the library's own graph executor (pa_graph_*).
+
+    The same graph mode as GraphStep (two graphs of one fixed shape, each
+    uploading its own page-locked metadata image, alternating), but captured,
+    planned and launched inside the library: a step is one C call
+    (pa_graph_step: fixed plan from the host metadata, copy of its metadata
+    image, graph launch).  The inputs share one layout (q, key, value,
+    query_start_loc, num_computed, block_table, seq_lens).  With ``host_io``
+    the graphs copy a page-locked input image in first and the output back
+    last, and the planner reads the metadata from that same image; without
+    it the caller stages device inputs (``prepare``) and host metadata.
+    """
+
+    def __init__(self, *, num_heads_q, num_heads_kv, head_dim, num_blocks, max_blocks_per_req, softmax_scale,
+                 max_tokens, max_reqs, key_cache, value_cache, max_extend_tiles=0, max_dequant_blocks=0,
+                 max_partial_slots=0, kv_cache_dtype="bf16", k_scale=1.0, v_scale=1.0, num_sms=0, device="cuda",
+                 fused=True, host_io=False):
+        dev = torch.device(device)
+        self.device = dev
+        self.host_io = host_io
+        lay = _input_layout(max_tokens, max_reqs, num_heads_q, num_heads_kv, head_dim, max_blocks_per_req)
+        self._lay = lay
+        self._in = torch.zeros(lay["bytes"], dtype=torch.uint8, device=dev)
+        self.inputs = _input_views(self._in, lay)
+        self.out = torch.zeros(max_tokens, num_heads_q, head_dim, dtype=torch.bfloat16, device=dev)
+        bufs = {"q": self.inputs["q"], "key": self.inputs["key"], "value": self.inputs["value"], "out": self.out,
+                "query_start_loc": self.inputs["qsl"], "num_computed": self.inputs["num_computed"],
+                "block_table": self.inputs["block_table"], "key_cache": key_cache, "value_cache": value_cache}
+        if host_io:
+            self.host_in = [torch.zeros(lay["bytes"], dtype=torch.uint8).pin_memory() for _ in range(2)]
+            self.host_out = [torch.zeros(self.out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+            views = [_input_views(t, lay) for t in self.host_in]
+            bufs.update(host_in=self.host_in, device_in=self._in, in_bytes=lay["bytes"], host_out=self.host_out,
+                        out_bytes=self.out.numel() * 2)
+        else:
+            self.host_in = self.host_out = None
+            meta = {"qsl": np.zeros(max_reqs + 1, dtype=np.int32), "seq_lens": np.zeros(max_reqs, dtype=np.int32),
+                    "num_computed": np.zeros(max_reqs, dtype=np.int32),
+                    "block_table": np.zeros((max_reqs, max_blocks_per_req), dtype=np.int32)}
+            views = [{k: torch.from_numpy(v) for k, v in meta.items()}] * 2
+        self._host_views = views
+        host = [{"query_start_loc": v["qsl"].numpy(), "seq_lens": v["seq_lens"].numpy(),
+                 "num_computed": v["num_computed"].numpy(), "block_table": v["block_table"].numpy()} for v in views]
+        self.graph = binding.NativeGraph(
+            shape=dict(max_tokens=max_tokens, max_reqs=max_reqs, max_extend_tiles=max_extend_tiles,
+                       max_dequant_blocks=max_dequant_blocks, max_partial_slots=max_partial_slots),
+            host=host, buffers=bufs, num_reqs=0, fused=fused, num_heads_q=num_heads_q, num_heads_kv=num_heads_kv,
+            head_dim=head_dim, num_blocks=num_blocks, softmax_scale=softmax_scale, num_sms=num_sms,
+            kv_cache_dtype=binding.PA_KV_FP8_E4M3 if kv_cache_dtype == "fp8" else binding.PA_KV_BF16,
+            k_scale=k_scale, v_scale=v_scale)
+        self._last = None   # graph index of the last step launched
+        self._keep = (key_cache, value_cache)
+
+    def prepare(self, batch: Batch, q=None, key=None, value=None):
+        """Write the step's metadata and new rows where the next graph reads
+        them: its page-locked input image (host_io; after that graph's last
+        run finished) or the device inputs and host metadata (after the last
+        step finished)."""
+        i = self.graph.turn
+        if self.host_io:
+            self.graph.wait(i)
+            _fill(self._host_views[i], batch, q, key, value)
+            return
+        if self._last is not None:
+            self.graph.wait(self._last)
+        _fill(self._host_views[0], batch)
+        _fill(self.inputs, batch, q, key, value)
+
+    def fill_host_image(self, i: int, batch: Batch, q=None, key=None, value=None):
+        """Write a step into page-locked input image i (host_io), after graph
+        i's last run finished."""
+        self.graph.wait(i)
+        _fill(self._host_views[i], batch, q, key, value)
+
+    def launch(self, num_reqs: int, num_common_prefix_blocks: int = 0, stream=None):
+        """One step: plan (host), metadata image, graph launch (one C call)."""
+        turn = self.graph.turn
+        self.graph.step(num_reqs, stream, num_common_prefix_blocks)
+        self._last = turn
+
+    def output(self, num_tokens: int) -> torch.Tensor:
+        """The last step's output: page-locked host memory (host_io, after
+        waiting for it) or the device buffer (stream ordered)."""
+        if self.host_io:
+            self.graph.wait(self._last)
+            return self.host_out[self._last][:num_tokens]
+        return self.out[:num_tokens]
+
+    def run(self, batch: Batch, q, key, value) -> torch.Tensor:
+        self.prepare(batch, q, key, value)
+        self.launch(batch.num_reqs, batch.num_common_prefix_blocks)
+        return self.output(batch.num_tokens)
+
+    @property
+    def slot_mapping(self) -> torch.Tensor:
+        """Device slot buffer of the executor (int64 [max_tokens]), as a tensor view."""
+        return _device_view(self.graph.slot_mapping_ptr(), self.out.shape[0], torch.int64, self.device)
+
+    def check_errors(self, stream=None) -> int:
+        return binding.pa_check_device_errors(self.graph.workspace_ptr(), stream)
+
+    def destroy(self):
+        self.graph.destroy()

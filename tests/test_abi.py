@@ -357,3 +357,33 @@ def test_small_q_routing_by_parallelism(lib):
     assert plan(18, 8)["num_small_q_rows"] == 18                      # 18 x 8 tiles < 152 SMs
     i = plan(64, 8)                                                   # 512 tile CTAs: tiles read keys once
     assert i["num_small_q_rows"] == 0 and i["num_extend_rows"] == 64
+
+
+def test_graph_executor_rejects_bad_arguments(lib):
+    """pa_graph_*: NULL and partial arguments are refused before any CUDA
+    call (host only)."""
+    import ctypes
+    b = workloads.tiny("1A")
+    d, keep = binding.make_desc(**desc(b))
+    fs = binding._fixed_shape(8, 4)
+    bufs = binding.GraphBuffers()
+    h = ctypes.c_void_p(123)
+    assert lib.pa_graph_create(None, ctypes.byref(fs), ctypes.byref(bufs), ctypes.byref(h)) == binding.PA_ERR_INVALID_ARGUMENT
+    assert h.value is None
+    assert lib.pa_graph_create(ctypes.byref(d), ctypes.byref(fs), ctypes.byref(bufs), ctypes.byref(h)) == \
+        binding.PA_ERR_INVALID_ARGUMENT   # every device buffer NULL
+    for name in ("q", "key", "value", "out", "query_start_loc", "num_computed", "block_table", "key_cache",
+                 "value_cache"):
+        setattr(bufs, name, 4096)
+    bufs.in_bytes = 64                    # host input copy given in part
+    assert lib.pa_graph_create(ctypes.byref(d), ctypes.byref(fs), ctypes.byref(bufs), ctypes.byref(h)) == \
+        binding.PA_ERR_INVALID_ARGUMENT
+    bufs.in_bytes = 0
+    bufs.q = 4097                         # misaligned
+    assert lib.pa_graph_create(ctypes.byref(d), ctypes.byref(fs), ctypes.byref(bufs), ctypes.byref(h)) == \
+        binding.PA_ERR_INVALID_ARGUMENT
+    assert lib.pa_graph_step(None, ctypes.byref(d), None) == binding.PA_ERR_INVALID_ARGUMENT
+    assert lib.pa_graph_wait(None, 0) == binding.PA_ERR_INVALID_ARGUMENT
+    assert lib.pa_graph_turn(None) == 0
+    assert lib.pa_graph_workspace(None) is None and lib.pa_graph_slot_mapping(None) is None
+    lib.pa_graph_destroy(None)

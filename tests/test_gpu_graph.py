@@ -30,10 +30,14 @@ def _gpu():
     ensure_library()
 
 
+def graph_args(b, max_blocks):
+    return dict(num_heads_q=b.num_heads_q, num_heads_kv=b.num_heads_kv, head_dim=b.head_dim,
+                num_blocks=b.num_blocks, max_blocks_per_req=max_blocks, softmax_scale=b.softmax_scale,
+                kv_cache_dtype=b.kv_cache_dtype, k_scale=b.k_scale, v_scale=b.v_scale)
+
+
 def graph_for(b, max_blocks, fused=False, **shape):
-    return GraphStep(fused=fused, num_heads_q=b.num_heads_q, num_heads_kv=b.num_heads_kv, head_dim=b.head_dim,
-                     num_blocks=b.num_blocks, max_blocks_per_req=max_blocks, softmax_scale=b.softmax_scale,
-                     kv_cache_dtype=b.kv_cache_dtype, k_scale=b.k_scale, v_scale=b.v_scale, **shape)
+    return GraphStep(fused=fused, **graph_args(b, max_blocks), **shape)
 
 
 def replay_steps(batches, fused=False, **shape):
@@ -181,3 +185,123 @@ def test_zero_blocks(kv):
     binding.pa_zero_blocks(bad, gkc, gvc, err)
     assert binding.pa_check_device_errors(err) & binding.PA_DEVERR_BLOCK_RANGE
     assert not gkc[3].any() and not gvc[3].any()
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_graph_replay_host_io(fused):
+    """Graphs that also copy a page-locked input image in and the output back
+    (host memory to host memory): steps of changing size, each equal bit for
+    bit to the device-resident graph on the same caches and to the eager path,
+    and within tolerance of the oracle; the two images alternate."""
+    dev = torch.device("cuda")
+    batches = decode_steps()
+    mb = max(b.block_table.shape[1] for b in batches)
+    shape = dict(max_tokens=48, max_reqs=48)
+    gh = GraphStep(host_io=True, fused=fused, **{**graph_args(batches[0], mb), **shape})
+    gd = GraphStep(fused=fused, **{**graph_args(batches[0], mb), **shape})
+    kc = batches[0].key_cache.to(dev, copy=True)
+    vc = batches[0].value_cache.to(dev, copy=True)
+    kc2, vc2 = kc.clone(), vc.clone()
+    for n, b in enumerate(batches):
+        before = replace(b, key_cache=kc.cpu(), value_cache=vc.cpu())
+        plan = gh.make_plan(b)
+        if gh.graphs is None:
+            gh.load(b, plan, b.q.to(dev), b.key.to(dev), b.value.to(dev))
+            gh.capture(plan, kc, vc)
+        turn = gh.turn
+        gh.stage_host(b, b.q, b.key, b.value)
+        gh.replay(plan)
+        view = gh.host_output(b.num_tokens)
+        assert gh.turn != turn
+        assert view.device.type == "cpu" and view.is_pinned()
+        out = view.clone()
+        ref = gd.run(b, b.q.to(dev), b.key.to(dev), b.value.to(dev), kc2, vc2)
+        torch.cuda.synchronize()
+        assert gh.check_errors() == 0 and gd.check_errors() == 0, b.name
+        assert torch.equal(out, ref.cpu()), f"{b.name}: host-io replay differs from the device replay"
+        assert torch.equal(kc, kc2) and torch.equal(vc, vc2), b.name
+        _, _, _, oout = run_oracle(before)
+        assert_close(out, oout, what=b.name)
+        eager = run_gpu(before)
+        assert torch.equal(eager.out.cpu(), out), f"{b.name}: host-io replay differs from the eager path"
+
+
+def native_steps(batches, fused, host_io, **shape):
+    """Every batch through the library's graph executor (pa_graph_*) on one
+    cache pool: caches and slots against the oracle bit for bit, output within
+    tolerance of the oracle and equal bit for bit to the eager path."""
+    from paged_kv_cache_16_gb300.step import NativeGraphStep
+    dev = torch.device("cuda")
+    mb = max(b.block_table.shape[1] for b in batches)
+    kc = batches[0].key_cache.to(dev, copy=True)
+    vc = batches[0].value_cache.to(dev, copy=True)
+    ns = NativeGraphStep(fused=fused, host_io=host_io, key_cache=kc, value_cache=vc, device=dev,
+                         **graph_args(batches[0], mb), **shape)
+    turns = []
+    for b in batches:
+        before = replace(b, key_cache=kc.cpu(), value_cache=vc.cpu())
+        turns.append(ns.graph.turn)
+        out = ns.run(b, b.q, b.key, b.value) if host_io else ns.run(b, b.q.to(dev), b.key.to(dev), b.value.to(dev))
+        out = out.clone()
+        torch.cuda.synchronize()
+        assert ns.check_errors() == 0, b.name
+        assert out.device.type == ("cpu" if host_io else "cuda")
+        okc, ovc, oslots, oout = run_oracle(before)
+        assert np.array_equal(cache_bits(kc), okc) and np.array_equal(cache_bits(vc), ovc), b.name
+        if b.num_tokens:
+            assert np.array_equal(ns.slot_mapping[:b.num_tokens].cpu().numpy(), oslots), b.name
+            assert_close(out, oout, what=b.name)
+            eager = run_gpu(before)
+            assert eager.bits == 0
+            assert torch.equal(eager.out.cpu(), out.cpu()), f"{b.name}: native graph differs from the eager path"
+    assert turns == [i % 2 for i in range(len(batches))]
+    ns.destroy()
+
+
+@pytest.mark.parametrize("host_io", [False, True])
+@pytest.mark.parametrize("fused", [False, True])
+def test_native_graph_decode_steps(fused, host_io):
+    native_steps(decode_steps() + decode_steps(), fused, host_io, max_tokens=48, max_reqs=48)
+
+
+@pytest.mark.parametrize("host_io", [False, True])
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_native_graph_mixed_steps(kv, host_io):
+    native_steps(mixed_steps(kv), True, host_io, max_tokens=512, max_reqs=8, max_extend_tiles=64,
+                 max_dequant_blocks=256 if kv == "fp8" else 0)
+
+
+def test_native_graph_cascade_steps():
+    steps = []
+    for i, (n, nb) in enumerate(((24, 16), (9, 8))):
+        steps.append(replace(workloads.cascade(batch=n, prefix_tokens=16 * nb, lo=1, hi=200, num_blocks=700,
+                                               seed=80 + i), name=f"cascade-step{i}"))
+    native_steps(steps, False, True, max_tokens=24, max_reqs=24, max_extend_tiles=256, max_partial_slots=24 * 160)
+
+
+def test_native_graph_rejects_other_model_and_capacity():
+    """A step whose model fields differ from the graph's, or that needs more
+    than its shape holds, is refused and launches nothing."""
+    from paged_kv_cache_16_gb300.step import NativeGraphStep
+    dev = torch.device("cuda")
+    b = mixed_steps()[0]                    # has extend rows
+    kc, vc = b.key_cache.to(dev, copy=True), b.value_cache.to(dev, copy=True)
+    ns = NativeGraphStep(key_cache=kc, value_cache=vc, device=dev, **graph_args(b, b.block_table.shape[1]),
+                         max_tokens=512, max_reqs=8)   # no tensor-core tiles
+    ns.prepare(b, b.q.to(dev), b.key.to(dev), b.value.to(dev))
+    with pytest.raises(binding.PaError) as e:
+        ns.launch(b.num_reqs)
+    assert e.value.status == binding.PA_ERR_CAPACITY
+    d = ns.graph._descs[0]
+    d.num_reqs = 0
+    d.softmax_scale *= 2
+    with pytest.raises(binding.PaError) as e:
+        ns.graph.step(0)
+    assert e.value.status == binding.PA_ERR_INVALID_ARGUMENT
+    d.softmax_scale /= 2
+    assert ns.graph.turn == 0
+    decode = replace(workloads.decode(batch=8, lo=1, hi=300, num_blocks=600, seed=91), name="decode-after")
+    ns.run(decode, decode.q.to(dev), decode.key.to(dev), decode.value.to(dev))
+    torch.cuda.synchronize()
+    assert ns.check_errors() == 0 and ns.graph.turn == 1
+    ns.destroy()
