@@ -74,7 +74,7 @@ TRAFFIC = {
     # profiles/decode_kernel_e4m3_decode-workload.md
     ("decode", "decode", "bf16", "92b11a045f4b2f7c"): 645_422_592,
     ("decode", "decode", "fp8", "92b11a045f4b2f7c"): 325_470_720,
-    ("extend", "prefill", "bf16", "b45c1014dd07eddd"): 73_937_408,
+    ("extend", "prefill", "bf16", "e6cbabdc09e6bede"): 74_034_176,
 }
 KERNEL_SOURCES = {"decode": "paged_kv_cache_16_gb300/csrc/k_decode.cu",
                   "extend": "paged_kv_cache_16_gb300/csrc/k_extend.cu"}

@@ -23,7 +23,10 @@
 // warpgroup 0 gives its registers to the softmax warpgroups), warps 4-7
 // softmax of sub-tile 0, warps 8-11 softmax of sub-tile 1.  The MMA thread
 // alternates between the sub-tiles, so the tensor core works on one while
-// the other's softmax runs.  The running max only moves (and O is rescaled) when it
+// the other's softmax runs.  Its issue blocks at the pipe's rate (about one
+// M128 N128 K16 MMA per 64 cycles), so a wait between two MMA groups idles
+// the pipe: the barriers it needs next (the next K and V tiles, the other
+// sub-tile's P) are tested once in the middle of each group instead.  The running max only moves (and O is rescaled) when it
 // grows by more than 2^8, which keeps every weight <= 256.
 //
 // Tensor memory (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256)
@@ -258,7 +261,13 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const uint64_t q_desc[2] = {sdesc_sw128(q_s(0), 16, 1024), sdesc_sw128(q_s(1), 16, 1024)};
             const uint64_t k_desc0 = sdesc_sw128(k_s(0), 16, 1024);
             const uint64_t v_desc0 = sdesc_sw128(v_s(0), C::HALF, 1024);
-            auto qk = [&](int t, int s) {
+            // readiness of the barriers the thread needs next, polled (one
+            // test each) between MMAs, where the pipe still holds queued work
+            bool p_ready[2] = {false, false}, k_ready = false, v_ready = false;
+            auto poll = [&](bool &flag, int b, int parity) {
+                if (!flag) flag = mbar_test_wait(bar(b), static_cast<uint32_t>(parity));
+            };
+            auto qk = [&](int t, int s, auto mid) {
                 const uint64_t a0 = q_desc[t];
                 const uint64_t b0 = sdesc_advance(k_desc0, static_cast<uint32_t>(s) * C::KVB);
                 const uint32_t d = tmem + col_s(t);
@@ -266,20 +275,25 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk / 4) * C::HALF + (kk % 4) * 32;
                     tc_mma(d, sdesc_advance(a0, off), sdesc_advance(b0, off), C::IDESC_QK, kk > 0 ? 1u : 0u);
+                    if (kk == D / 32 - 1) mid();
                 }
                 tc_commit(bar(B_SFULL + t));
             };
-            auto pv = [&](int t, int sv, bool first) -> bool {
-                if (!mbar_wait_spin(bar(B_PFULL + t), pc[t] & 1, &abort_flag)) return false;
+            auto pv = [&](int t, int sv, bool first, auto mid) -> bool {
+                if (!p_ready[t] && !mbar_wait_spin(bar(B_PFULL + t), pc[t] & 1, &abort_flag)) return false;
+                p_ready[t] = false;
                 ++pc[t];
                 tc_fence_after();
                 const uint64_t b0 = sdesc_advance(v_desc0, static_cast<uint32_t>(sv) * C::KVB);
                 const uint32_t d = tmem + col_o(t), a = tmem + col_s(t);
 #pragma unroll
-                for (int kk = 0; kk < kTileKeys / 16; ++kk)
+                for (int kk = 0; kk < kTileKeys / 16; ++kk) {
                     tc_mma_ts(d, a + kk * 8, sdesc_advance(b0, kk * 2048), C::IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+                    if (kk == 3) mid();
+                }
                 return true;
             };
+            auto nothing = [] {};
             for (int ti = tile_begin; ti < tile_end && ok; ++ti) {
                 const ExtendTile tile = p.tiles[p.cta_tiles[ti]];
                 const TileShape sh = tile_shape(tile, tpt);
@@ -297,7 +311,7 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
                 for (int t = 0; t < 2; ++t)
                     if (sh.n_sub[t] > 0) {
-                        qk(t, kc % C::NSK);
+                        qk(t, kc % C::NSK, nothing);
                         if (--q_left == 0) tc_commit(bar(B_QEMPTY));
                     }
                 tc_commit(bar(B_KEMPTY + kc % C::NSK));   // K tile 0 read by both QK^T
@@ -305,30 +319,43 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 for (int j = 0; j < sh.n_tiles && ok; ++j) {
                     const int sv = vc % C::NSV;
                     const int t_last = j < sh.n_sub[1] ? 1 : 0;   // last sub-tile that reads V tile j
-                    bool k_next_ready = false;
-                    ok = mbar_wait_spin(bar(B_VFULL + sv), (vc / C::NSV) & 1, &abort_flag);
+                    const bool k_next = j + 1 < sh.n_tiles;
+                    bool k_used = false;
+                    if (!v_ready) ok = mbar_wait_spin(bar(B_VFULL + sv), (vc / C::NSV) & 1, &abort_flag);
+                    v_ready = false;
 #pragma unroll
                     for (int t = 0; t < 2 && ok; ++t) {
                         if (j >= sh.n_sub[t]) continue;
-                        ok = pv(t, sv, j == 0);
+                        // during PV_0: the next K tile; during PV_1: the next V tile
+                        if (t == 0)
+                            ok = pv(0, sv, j == 0, [&] { if (k_next) poll(k_ready, B_KFULL + kc % C::NSK, (kc / C::NSK) & 1); });
+                        else
+                            ok = pv(1, sv, j == 0, [&] { poll(v_ready, B_VFULL + (vc + 1) % C::NSV, ((vc + 1) / C::NSV) & 1); });
                         if (!ok) break;
                         if (t == t_last) tc_commit(bar(B_VEMPTY + sv));   // V tile j read by both PV
                         if (j + 1 < sh.n_sub[t]) {
-                            if (!k_next_ready) {
+                            if (!k_ready) {
                                 ok = mbar_wait_spin(bar(B_KFULL + kc % C::NSK), (kc / C::NSK) & 1, &abort_flag);
                                 if (!ok) break;
-                                k_next_ready = true;
+                                k_ready = true;
                             }
+                            k_used = true;
                             tc_fence_after();
-                            qk(t, kc % C::NSK);   // overwrites S_t: issued after the PV that reads P_t
+                            // overwrites S_t: issued after the PV that reads P_t.
+                            // During QK_0 poll P_1 of this step, during QK_1 P_0 of the next
+                            if (t == 0)
+                                qk(0, kc % C::NSK, [&] { if (j < sh.n_sub[1]) poll(p_ready[1], B_PFULL + 1, pc[1] & 1); });
+                            else
+                                qk(1, kc % C::NSK, [&] { poll(p_ready[0], B_PFULL + 0, pc[0] & 1); });
                             if (--q_left == 0) tc_commit(bar(B_QEMPTY));
                         } else {
                             tc_commit(bar(B_ODONE + t));
                         }
                     }
-                    if (ok && k_next_ready) {
+                    if (ok && k_used) {
                         tc_commit(bar(B_KEMPTY + kc % C::NSK));   // K tile j+1 read by both QK^T
                         ++kc;
+                        k_ready = false;
                     }
                     ++vc;
                 }
