@@ -154,9 +154,13 @@ pa_status validate(const pa_batch_desc *d) {
         const int64_t need = (static_cast<int64_t>(d->seq_lens[r]) + d->block_size - 1) / d->block_size;
         if (need > d->max_blocks_per_req) return PA_ERR_INVALID_ARGUMENT;
         if (d->block_table_host) {
+            // one unsigned compare per id (negative ids wrap to large ones),
+            // branch-free so that the compiler vectorises it
             const int32_t *row = d->block_table_host + static_cast<int64_t>(r) * d->max_blocks_per_req;
-            for (int64_t b = 0; b < need; ++b)
-                if (row[b] < 0 || row[b] >= d->num_blocks) return PA_ERR_INVALID_ARGUMENT;
+            const uint32_t nb = static_cast<uint32_t>(d->num_blocks);
+            uint32_t bad = 0;
+            for (int64_t b = 0; b < need; ++b) bad |= static_cast<uint32_t>(row[b]) >= nb ? 1u : 0u;
+            if (bad) return PA_ERR_INVALID_ARGUMENT;
         }
     }
     const int32_t n = d->num_common_prefix_blocks;
@@ -208,6 +212,7 @@ void plan_decode(pa_plan_s *P, const std::vector<DecodeUnit> &units, std::vector
                  std::vector<int32_t> &item_unit, int64_t fixed_ncta) {
     struct Run { int32_t u, grp, pb, pe; };
     std::vector<Run> runs;
+    runs.reserve(units.size() * P->n_groups);
     const int32_t kb = P->n_prefix;  // first block of the suffix work
     int64_t total = 0;
     for (int grp = 0; grp < P->n_groups; ++grp)
@@ -229,6 +234,10 @@ void plan_decode(pa_plan_s *P, const std::vector<DecodeUnit> &units, std::vector
     int64_t ncta = std::min<int64_t>(static_cast<int64_t>(P->num_sms) * cps, (total + min_pages - 1) / min_pages);
     ncta = std::max<int64_t>(ncta, 1);
     if (fixed_ncta > 0) ncta = std::min(ncta, fixed_ncta);
+    // an equal cut makes at most one item per run plus one per CTA
+    P->items.reserve(runs.size() + static_cast<size_t>(ncta));
+    item_unit.reserve(runs.size() + static_cast<size_t>(ncta));
+    P->cta_begin.reserve(static_cast<size_t>(std::max(ncta, fixed_ncta)) + 1);
     size_t run = 0;
     int32_t cursor = runs.empty() ? 0 : runs[0].pb;
     for (int64_t c = 0; c < ncta; ++c) {
@@ -297,6 +306,7 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     // single kv head shared by 32 query heads) run every row on the tiles.
     const int32_t tg = std::max(1, kMmaRows / P->G);   // tokens per decode unit
     std::vector<int32_t> decode_rows, small_rows, extend_rows, multi_unit;
+    decode_rows.reserve(static_cast<size_t>(P->R));
     for (int32_t r = 0; r < P->R; ++r) {
         const int32_t q_len = qsl[r + 1] - qsl[r];
         if (q_len > 0 && P->G > kMmaRows) extend_rows.push_back(r);
@@ -345,6 +355,11 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
                     P->tiles.push_back(t);
                 }
         P->info.num_prefix_tiles = static_cast<int32_t>(P->tiles.size());
+    }
+    {
+        size_t n = P->tiles.size();
+        for (int32_t r : extend_rows) n += static_cast<size_t>(P->Hkv) * ((qsl[r + 1] - qsl[r] + tpt - 1) / tpt);
+        P->tiles.reserve(n);
     }
     for (int32_t r : extend_rows) {
         const int32_t q_len = qsl[r + 1] - qsl[r];
@@ -404,10 +419,14 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
         const int64_t max_ctas = P->fixed ? std::min<int64_t>(shape->max_extend_tiles, P->num_sms)
                                           : std::min<int64_t>(static_cast<int64_t>(P->tiles.size()), P->num_sms);
         P->ext_ctas = static_cast<int32_t>(std::max<int64_t>(max_ctas, 0));
-        std::vector<std::vector<int32_t>> lists(static_cast<size_t>(P->ext_ctas));
+        // counts per CTA, then the tiles in assignment order (a counting
+        // sort: no per-CTA lists to grow)
+        P->cta_tile_begin.assign(static_cast<size_t>(P->ext_ctas) + 1, 0);
+        P->cta_tiles.clear();
         if (P->ext_ctas > 0) {
             const int tpt_rows = kTileRows / P->G;
             std::vector<std::pair<int64_t, int32_t>> cost;
+            cost.reserve(P->tiles.size());
             for (size_t i = 0; i < P->tiles.size(); ++i) {
                 const ExtendTile &t = P->tiles[i];
                 int n_tiles = 0;
@@ -425,24 +444,29 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
                                  return a.first > b.first;
                              });
             using Load = std::pair<int64_t, int32_t>;   // (work so far, CTA)
-            std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+            std::vector<Load> heap_store;
+            heap_store.reserve(static_cast<size_t>(P->ext_ctas));
+            std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap(std::greater<Load>(),
+                                                                                 std::move(heap_store));
             for (int32_t c = 0; c < P->ext_ctas; ++c) heap.push({0, c});
-            for (const auto &ct : cost) {
+            std::vector<int32_t> cta_of(cost.size());
+            for (size_t k = 0; k < cost.size(); ++k) {
                 Load ld = heap.top();
                 heap.pop();
-                lists[ld.second].push_back(ct.second);
-                heap.push({ld.first + ct.first, ld.second});
+                cta_of[k] = ld.second;
+                ++P->cta_tile_begin[static_cast<size_t>(ld.second) + 1];
+                heap.push({ld.first + cost[k].first, ld.second});
             }
-        }
-        P->cta_tile_begin.assign(1, 0);
-        for (const auto &l : lists) {
-            P->cta_tiles.insert(P->cta_tiles.end(), l.begin(), l.end());
-            P->cta_tile_begin.push_back(static_cast<int32_t>(P->cta_tiles.size()));
+            for (size_t c = 1; c < P->cta_tile_begin.size(); ++c) P->cta_tile_begin[c] += P->cta_tile_begin[c - 1];
+            P->cta_tiles.resize(cost.size());
+            std::vector<int32_t> pos(P->cta_tile_begin.begin(), P->cta_tile_begin.end() - 1);
+            for (size_t k = 0; k < cost.size(); ++k) P->cta_tiles[pos[cta_of[k]]++] = cost[k].second;
         }
     }
 
     // ------------------------------------------------------------- decode
     std::vector<DecodeUnit> units;
+    units.reserve(decode_rows.size() + small_rows.size() * 2);
     for (int32_t r = 0; r < P->R; ++r) {
         const int32_t q_len = qsl[r + 1] - qsl[r];
         if (!on_decode[r]) continue;
@@ -490,6 +514,7 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
         else if (k == 1) it.part = -1;
     }
     P->part_offset.assign(count.size(), 0);
+    P->merges.reserve(units.size() * P->n_groups + (cascade ? count.size() : 0));
     int64_t slots = 0;
     for (size_t i = 0; i < count.size(); ++i) {
         P->part_offset[i] = static_cast<int32_t>(slots);
@@ -616,10 +641,10 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     const int64_t row_bytes = static_cast<int64_t>(P->Hkv) * P->D * 2 * (P->kv8 ? 1 : 2);   // K and V
     for (const DecodeUnit &u : units) I.decode_kv_bytes += std::max(0, u.key_end - kb_keys) * row_bytes;
     I.prefix_kv_bytes = cascade ? kb_keys * row_bytes : 0;
-    double pairs = 0.0;
+    double pairs = 0.0;   // sum over the row's queries i of (num_computed + i + 1 - prefix keys)
     for (int32_t r : extend_rows) {
-        const int32_t q_len = qsl[r + 1] - qsl[r];
-        for (int32_t i = 0; i < q_len; ++i) pairs += d->num_computed_tokens[r] + i + 1 - kb_keys;
+        const double q_len = qsl[r + 1] - qsl[r];
+        pairs += q_len * (d->num_computed_tokens[r] + 1 - kb_keys) + q_len * (q_len - 1) / 2;
     }
     I.extend_flops = 4.0 * P->D * P->Hq * pairs;
     I.prefix_flops = cascade ? 4.0 * P->D * P->Hq * static_cast<double>(P->T) * kb_keys : 0.0;
