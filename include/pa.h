@@ -21,7 +21,9 @@
  * Fixed-shape plans (pa_plan_fixed) make the attention launches of a step a
  * function of capacities only, so that they can be captured once in a CUDA
  * graph and replayed for later steps: pa_upload_metadata then replay (or
- * pa_attention_launch).
+ * pa_attention_launch).  pa_graph_create / pa_graph_step do that inside the
+ * library: two captured graphs of one fixed shape, one C call per step,
+ * optionally with the step's host inputs and output copied inside the graph.
  *
  * Data types: every tensor element is IEEE bfloat16, passed as raw 16-bit
  * patterns; metadata is int32 except slot_mapping (int64).  All layouts are
@@ -42,8 +44,9 @@
  * 16 < 2^31.  Other shapes return PA_ERR_UNSUPPORTED.
  *
  * Ownership: the caller allocates and owns every device buffer (q, caches,
- * block table, out, slot mapping, workspace).  A plan is host memory owned by
- * the library from pa_plan until pa_plan_destroy.  Device entry points only
+ * block table, out, slot mapping, workspace), except the workspace, slot
+ * buffer, metadata images and streams a pa_graph_t allocates for itself.  A
+ * plan is host memory owned by the library from pa_plan until pa_plan_destroy.  Device entry points only
  * enqueue work on the given stream (a cudaStream_t; NULL = the legacy default
  * stream) and never synchronise, except pa_check_device_errors.  Errors come
  * back as a status; nothing aborts, traps or throws across the ABI.
@@ -455,6 +458,8 @@ pa_status pa_attention_no_alloc(const pa_plan_t *plan, const void *q, const void
  * caller owns every buffer listed in pa_graph_buffers and must keep them (and
  * their addresses) for the graph's lifetime.  pa_graph_step costs one fixed
  * plan (host), one copy of its metadata image (host) and one graph launch.
+ * A pa_graph_t is not thread-safe: one host thread at a time may call
+ * pa_graph_step / pa_graph_wait on it (different graphs are independent).
  */
 typedef struct pa_graph_s pa_graph_t;
 

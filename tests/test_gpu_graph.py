@@ -305,3 +305,29 @@ def test_native_graph_rejects_other_model_and_capacity():
     torch.cuda.synchronize()
     assert ns.check_errors() == 0 and ns.graph.turn == 1
     ns.destroy()
+
+
+def test_native_graph_refuses_pageable_host_io():
+    """Host I/O buffers must be page-locked: pageable ones are refused at
+    creation, before anything is captured."""
+    from paged_kv_cache_16_gb300.step import _input_layout
+    dev = torch.device("cuda")
+    b = decode_steps()[0]
+    kc, vc = b.key_cache.to(dev, copy=True), b.value_cache.to(dev, copy=True)
+    lay = _input_layout(b.num_tokens, b.num_reqs, b.num_heads_q, b.num_heads_kv, b.head_dim, b.block_table.shape[1])
+    dev_in = torch.zeros(lay["bytes"], dtype=torch.uint8, device=dev)
+    out = torch.zeros(b.num_tokens, b.num_heads_q, b.head_dim, dtype=torch.bfloat16, device=dev)
+    meta = {"query_start_loc": np.zeros(b.num_reqs + 1, np.int32), "seq_lens": np.zeros(b.num_reqs, np.int32),
+            "num_computed": np.zeros(b.num_reqs, np.int32),
+            "block_table": np.zeros((b.num_reqs, b.block_table.shape[1]), np.int32)}
+    bufs = {"q": dev_in, "key": dev_in, "value": dev_in, "out": out, "query_start_loc": dev_in,
+            "num_computed": dev_in, "block_table": dev_in, "key_cache": kc, "value_cache": vc,
+            "device_in": dev_in, "in_bytes": lay["bytes"],
+            "host_in": [torch.zeros(lay["bytes"], dtype=torch.uint8), torch.zeros(lay["bytes"], dtype=torch.uint8)]}
+    ga = graph_args(b, b.block_table.shape[1])
+    ga.pop("max_blocks_per_req")
+    ga["kv_cache_dtype"] = binding.PA_KV_BF16
+    with pytest.raises(binding.PaError) as e:
+        binding.NativeGraph(shape=dict(max_tokens=b.num_tokens, max_reqs=b.num_reqs), host=meta, buffers=bufs,
+                            num_reqs=0, fused=True, **ga)
+    assert e.value.status == binding.PA_ERR_INVALID_ARGUMENT
