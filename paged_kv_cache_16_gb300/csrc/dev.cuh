@@ -3,6 +3,7 @@
 // tensor core + tensor memory) instructions, all as inline PTX.
 #pragma once
 #include <cstdint>
+#include <type_traits>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -350,12 +351,26 @@ template <int D>
 __device__ __forceinline__ void merge_head(uint16_t *out_row, const float *o_part, const float2 *ml_part,
                                            int64_t slot0, int count, int num_heads_q, int h, int lane) {
     constexpr int V = D / 32;
-    // lane s holds (m, l) of partial s of each group of 32: the loads are
-    // independent, so the merge costs a few round trips whatever the count
-    // (L2 loads: partials written by other SMs in this same launch must not
-    // be served from a stale L1 line)
-    float m = -INFINITY;
-    for (int s0 = 0; s0 < count; s0 += 32) {
+    // The o rows of the first KPRE partials are loaded together with the
+    // (m, l) pairs, before the weights are known, so that a merge of up to
+    // KPRE partials costs one round trip to L2 instead of three; a partial
+    // whose l is 0 was never written and its o is skipped (not multiplied
+    // by 0: it may hold anything).  L2 loads: partials written by other SMs
+    // in this same launch must not be served from a stale L1 line.
+    constexpr int KPRE = 8;
+    using VecT = typename std::conditional<V == 4, float4, float2>::type;
+    auto o_at = [&](int j) {
+        return reinterpret_cast<const VecT *>(o_part + ((slot0 + j) * num_heads_q + h) * D + lane * V);
+    };
+    VecT pre[KPRE];
+#pragma unroll
+    for (int j = 0; j < KPRE; ++j)
+        if (j < count) pre[j] = __ldcg(o_at(j));
+    // lane s holds (m, l) of partial s of each group of 32
+    float2 ml0 = make_float2(-INFINITY, 0.f);
+    if (lane < count) ml0 = __ldcg(ml_part + (slot0 + lane) * num_heads_q + h);
+    float m = ml0.y > 0.f ? ml0.x : -INFINITY;
+    for (int s0 = 32; s0 < count; s0 += 32) {
         if (s0 + lane < count) {
             const float2 ml = __ldcg(ml_part + (slot0 + s0 + lane) * num_heads_q + h);
             if (ml.y > 0.f) m = fmaxf(m, ml.x);
@@ -366,27 +381,34 @@ __device__ __forceinline__ void merge_head(uint16_t *out_row, const float *o_par
     float acc[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[v] = 0.f;
+    auto add = [&](float wj, const VecT &x) {
+        if constexpr (V == 4) {
+            acc[0] += wj * x.x; acc[1] += wj * x.y; acc[2] += wj * x.z; acc[3] += wj * x.w;
+        } else {
+            acc[0] += wj * x.x; acc[1] += wj * x.y;
+        }
+    };
     float wsum = 0.f;   // this lane's partials' weights
     for (int s0 = 0; s0 < count; s0 += 32) {
         float w = 0.f;
         if (s0 + lane < count) {
-            const float2 ml = __ldcg(ml_part + (slot0 + s0 + lane) * num_heads_q + h);
+            const float2 ml = s0 == 0 ? ml0 : __ldcg(ml_part + (slot0 + s0 + lane) * num_heads_q + h);
             if (ml.y > 0.f) w = ex2(ml.x - m) * ml.y;
         }
         wsum += w;
         const int n = min(32, count - s0);
+        if (s0 == 0) {
+#pragma unroll
+            for (int j = 0; j < KPRE; ++j) {
+                const float wj = __shfl_sync(0xffffffffu, w, j);
+                if (j < n && wj != 0.f) add(wj, pre[j]);
+            }
+        }
 #pragma unroll 4
-        for (int j = 0; j < n; ++j) {
+        for (int j = s0 == 0 ? KPRE : 0; j < n; ++j) {
             const float wj = __shfl_sync(0xffffffffu, w, j);
             if (wj == 0.f) continue;   // empty partial: its o was never written
-            const float *o = o_part + ((slot0 + s0 + j) * num_heads_q + h) * D + lane * V;
-            if constexpr (V == 4) {
-                const float4 x = __ldcg(reinterpret_cast<const float4 *>(o));
-                acc[0] += wj * x.x; acc[1] += wj * x.y; acc[2] += wj * x.z; acc[3] += wj * x.w;
-            } else {
-                const float2 x = __ldcg(reinterpret_cast<const float2 *>(o));
-                acc[0] += wj * x.x; acc[1] += wj * x.y;
-            }
+            add(wj, __ldcg(o_at(s0 + j)));
         }
     }
     float total = wsum;
