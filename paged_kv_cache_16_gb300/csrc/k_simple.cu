@@ -118,9 +118,27 @@ __global__ void dequant_kernel(DequantParams p) {
         }
         const uint4 *ks = reinterpret_cast<const uint4 *>(p.key_cache + static_cast<int64_t>(src) * p.block_elems);
         const uint4 *vs = reinterpret_cast<const uint4 *>(p.value_cache + static_cast<int64_t>(src) * p.block_elems);
-        for (int32_t c = threadIdx.x; c < chunks; c += blockDim.x) {
-            expand16(__ldg(ks + c), kd + 2 * c);
-            expand16(__ldg(vs + c), vd + 2 * c);
+        // a thread's chunks of the block are all loaded before any is
+        // stored: one round trip to memory instead of one per chunk
+        constexpr int U = 4;
+        for (int32_t c0 = threadIdx.x; c0 < chunks; c0 += U * blockDim.x) {
+            uint4 kx[U], vx[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int32_t c = c0 + u * static_cast<int32_t>(blockDim.x);
+                if (c < chunks) {
+                    kx[u] = __ldg(ks + c);
+                    vx[u] = __ldg(vs + c);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int32_t c = c0 + u * static_cast<int32_t>(blockDim.x);
+                if (c < chunks) {
+                    expand16(kx[u], kd + 2 * c);
+                    expand16(vx[u], vd + 2 * c);
+                }
+            }
         }
     }
 }
@@ -149,6 +167,17 @@ __global__ void write_runs_kernel(WriteParams p) {
         const WriteRun run = p.runs[lo];
         const int32_t t = run.t0 + (e - run.wbegin);
         const int32_t pos = run.pos0 + (e - run.wbegin);
+        // the source chunks do not depend on the block id: load them first,
+        // so that they and the block-table read share one round trip
+        const uint4 *k = reinterpret_cast<const uint4 *>(p.key) + static_cast<int64_t>(t) * (p.row_elems / 8);
+        const uint4 *v = reinterpret_cast<const uint4 *>(p.value) + static_cast<int64_t>(t) * (p.row_elems / 8);
+        const int32_t sc = p.kv8 ? 2 * c : c;
+        const uint4 k0 = __ldcs(k + sc), v0 = __ldcs(v + sc);
+        uint4 k1 = make_uint4(0, 0, 0, 0), v1 = k1;
+        if (p.kv8) {
+            k1 = __ldcs(k + sc + 1);
+            v1 = __ldcs(v + sc + 1);
+        }
         const int32_t blk = p.block_table[static_cast<int64_t>(run.req) * p.max_blocks + pos / kBlockSize];
         if (blk < 0 || blk >= p.num_blocks) {
             if (c == 0) atomicOr(p.err, kErrBlockRange);
@@ -156,16 +185,14 @@ __global__ void write_runs_kernel(WriteParams p) {
         }
         const int64_t slot = static_cast<int64_t>(blk) * kBlockSize + pos % kBlockSize;
         if (c == 0 && p.slots_out != nullptr) p.slots_out[t] = slot;
-        const uint4 *k = reinterpret_cast<const uint4 *>(p.key) + static_cast<int64_t>(t) * (p.row_elems / 8);
-        const uint4 *v = reinterpret_cast<const uint4 *>(p.value) + static_cast<int64_t>(t) * (p.row_elems / 8);
         uint4 *kd = static_cast<uint4 *>(p.key_cache) + slot * cpr + c;
         uint4 *vd = static_cast<uint4 *>(p.value_cache) + slot * cpr + c;
         if (p.kv8) {
-            *kd = quantize16(__ldcs(k + 2 * c), __ldcs(k + 2 * c + 1), p.k_scale);
-            *vd = quantize16(__ldcs(v + 2 * c), __ldcs(v + 2 * c + 1), p.v_scale);
+            *kd = quantize16(k0, k1, p.k_scale);
+            *vd = quantize16(v0, v1, p.v_scale);
         } else {
-            *kd = __ldcs(k + c);
-            *vd = __ldcs(v + c);
+            *kd = k0;
+            *vd = v0;
         }
     }
 }
