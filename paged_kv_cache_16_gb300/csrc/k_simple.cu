@@ -41,14 +41,15 @@ __global__ void write_kv_kernel(const uint4 *__restrict__ key, const uint4 *__re
          i < total_chunks; i += stride) {
         const int64_t t = i / chunks_per_row;
         const int32_t c = static_cast<int32_t>(i - t * chunks_per_row);
+        // the source chunks do not depend on the slot: loaded together with it
+        const uint4 kv = __ldcs(key + i);
+        const uint4 vv = __ldcs(value + i);
         const int64_t slot = __ldg(slots + t);
         if (slot < 0) continue;
         if (slot >= num_slots) {
             if (err != nullptr && c == 0) atomicOr(err, kErrSlotRange);
             continue;
         }
-        const uint4 kv = __ldcs(key + i);
-        const uint4 vv = __ldcs(value + i);
         key_cache[slot * chunks_per_row + c] = kv;
         value_cache[slot * chunks_per_row + c] = vv;
     }
@@ -72,15 +73,17 @@ __global__ void write_kv_fp8_kernel(const uint4 *__restrict__ key, const uint4 *
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_chunks; i += stride) {
         const int64_t t = i / chunks_per_row;
         const int32_t c = static_cast<int32_t>(i - t * chunks_per_row);
+        // the source chunks do not depend on the slot: loaded together with it
+        const uint4 k0 = __ldcs(key + 2 * i), k1 = __ldcs(key + 2 * i + 1);
+        const uint4 v0 = __ldcs(value + 2 * i), v1 = __ldcs(value + 2 * i + 1);
         const int64_t slot = __ldg(slots + t);
         if (slot < 0) continue;
         if (slot >= num_slots) {
             if (err != nullptr && c == 0) atomicOr(err, kErrSlotRange);
             continue;
         }
-        key_cache[slot * chunks_per_row + c] = quantize16(__ldcs(key + 2 * i), __ldcs(key + 2 * i + 1), k_scale);
-        value_cache[slot * chunks_per_row + c] =
-            quantize16(__ldcs(value + 2 * i), __ldcs(value + 2 * i + 1), v_scale);
+        key_cache[slot * chunks_per_row + c] = quantize16(k0, k1, k_scale);
+        value_cache[slot * chunks_per_row + c] = quantize16(v0, v1, v_scale);
     }
 }
 
