@@ -141,6 +141,11 @@ typedef struct {
                                       tokens, longer ones only while their tiles
                                       (Hkv per row) would not fill the GPU
                                       (decode_kv_bytes counts each unit's keys)   */
+    int32_t num_extend_ctas;       /* CTAs of the tensor-core kernel that get tiles   */
+    int32_t side_by_side;          /* 1: the tensor-core tiles run on a second stream,
+                                      concurrently with the decode kernel on the
+                                      other SMs (num_extend_ctas of them go to the
+                                      tiles); 0: one after the other              */
 } pa_plan_info;
 
 /*

@@ -212,12 +212,6 @@ int oracle_write_kv_fp8(int32_t num_tokens, int32_t num_heads_kv, int32_t head_d
     return status;
 }
 
-/* Dequantise FP8 caches into the double values attention reads
- * (code_value * scale), so the attention of step 3 applies unchanged. */
-void oracle_dequantize_fp8(int64_t n, const uint8_t *codes, double scale, double *out) {
-    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_value(codes[i]) * scale;
-}
-
 /* Metadata check shared by the attention entry points: q_len from the
  * prefix sums ("vLLM 源码完全拆解（十六）", fourth walk-through: c_i tokens of
  * request i, query_start_loc its prefix sum) and seq_len = num_computed +

@@ -86,6 +86,8 @@ class PlanInfo(ctypes.Structure):
         ("extend_flops", ctypes.c_double),
         ("prefix_flops", ctypes.c_double),
         ("num_small_q_rows", ctypes.c_int32),
+        ("num_extend_ctas", ctypes.c_int32),
+        ("side_by_side", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -12,8 +12,11 @@
 //    every SM streams the same number of bytes (runs that split a request
 //    produce partials for the merge kernel);
 //  * one CTA serves HG kv heads; a producer warp streams each 16-token block
-//    as HG x (D/64) TMA boxes of [16 rows][64 dims] (128-byte swizzle) for K
-//    and for V into an NS-stage mbarrier ring;
+//    as one TMA box per 128-byte column slice ([HG heads][16 rows][128 B],
+//    128-byte swizzle, each head's rows one contiguous tile) for K and for V
+//    into an NS-stage mbarrier ring.  Large boxes matter: the TMA unit's
+//    per-box cost caps an SM at about 54 GB/s with one box per head, while
+//    [8 heads] boxes reach the HBM limit from about 100 SMs on;
 //  * one consumer warp per kv head: the G query heads of the group form the
 //    rows of a 16x16 bf16 MMA tile (G <= 16), so each K/V row loaded from HBM
 //    is used by all G heads; S = Q K^T and O += P V run on the tensor cores
@@ -32,8 +35,9 @@ struct DecodeCfg {
     static constexpr int EB = KV8 ? 1 : 2;                 // bytes per cache element
     static constexpr int NH = D * EB / 128;                // 128-byte boxes per cache row
     static constexpr int CPE = 128 / EB;                   // elements per box row
-    static constexpr int BOX = 16 * 128;                   // one [16 rows][128 B] box
-    static constexpr int TSTAGE = HG * NH * BOX;           // K (or V) bytes per block
+    static constexpr int BOX = 16 * 128;                   // one head's [16 rows][128 B] tile
+    static constexpr int SLICE = HG * BOX;                 // one TMA box: a column slice of all HG heads
+    static constexpr int TSTAGE = NH * SLICE;              // K (or V) bytes per block: [slice][head][row]
     static constexpr int STAGE = decode_stage_bytes(D, HG, KV8);
     static constexpr int NS = decode_stages(D, HG, KV8);
     static constexpr int THREADS = decode_threads(HG);
@@ -163,13 +167,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     }
                 }
                 __syncwarp();
-                if (valid && lane < 2 * HG * C::NH) {
-                    const int tensor = lane / (HG * C::NH);
-                    const int idx = lane % (HG * C::NH);
-                    const uint32_t dst = stage(s) + tensor * C::TSTAGE + idx * C::BOX;
+                if (valid && lane < 2 * C::NH) {
+                    const int tensor = lane / C::NH;
+                    const int slice = lane % C::NH;
+                    const uint32_t dst = stage(s) + tensor * C::TSTAGE + slice * C::SLICE;
                     const uint32_t bar = tensor ? full_v(s) : full_k(s);
-                    tma_load_3d(dst, tensor ? &tm_v : &tm_k, (idx % C::NH) * C::CPE, h0 + idx / C::NH,
-                                blk * kBlockSize, bar);
+                    tma_load_3d(dst, tensor ? &tm_v : &tm_k, slice * C::CPE, blk * kBlockSize, h0, bar);
                 }
                 ++issued;
             }
@@ -467,7 +470,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     ok = false;
                     break;
                 }
-                const uint32_t kb = stage(s) + warp * C::NH * C::BOX;
+                const uint32_t kb = stage(s) + warp * C::BOX;   // this head's tile of slice 0
                 const uint32_t vb = kb + C::TSTAGE;
                 // S = Q K^T over this block's 16 keys (two n-tiles of 8 keys)
                 float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -477,7 +480,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     const int key = (mi >> 1) * 8 + (lane & 7);
                     const int chunk = (kk % 4) * 2 + (mi & 1);
                     uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4(sw128(kb + (kk / 4) * C::BOX, key, chunk), b0, b1, b2, b3);
+                    ldmatrix_x4(sw128(kb + (kk / 4) * C::SLICE, key, chunk), b0, b1, b2, b3);
                     mma_bf16_16816(sc[0], qf[kk], b0, b1);
                     mma_bf16_16816(sc[1], qf[kk], b2, b3);
                 }
@@ -534,7 +537,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                         const int row = valid_keys + i / (C::NH * 8);
                         const int half = (i / 8) % C::NH;
                         const int ch = i % 8;
-                        const uint32_t a = vb + half * C::BOX + row * 128 + ch * 16;
+                        const uint32_t a = vb + half * C::SLICE + row * 128 + ch * 16;
                         asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
                     }
                     fence_proxy_async_smem();
@@ -547,7 +550,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     const int key = (mi & 1) * 8 + (lane & 7);
                     const int chunk = 2 * np + (mi >> 1);
                     uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4_trans(sw128(vb + (chunk / 8) * C::BOX, key, chunk % 8), b0, b1, b2, b3);
+                    ldmatrix_x4_trans(sw128(vb + (chunk / 8) * C::SLICE, key, chunk % 8), b0, b1, b2, b3);
                     mma_bf16_16816(o[2 * np], pa, b0, b1);
                     mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
                 }

@@ -549,11 +549,11 @@ cudaError_t configure() {
 
 template <int D>
 cudaError_t launch_t(int grid, const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                     const ExtendParams &p, cudaStream_t stream) {
+                     const ExtendParams &p, cudaStream_t stream, bool pdl) {
     using C = ExtCfg<D>;
     cudaError_t e = configure<D>();
     if (e != cudaSuccess) return e;
-    return launch_pdl(extend_kernel<D>, dim3(grid), dim3(C::THREADS), C::SMEM, stream, tm_q, tm_k, tm_v, p);
+    return launch_ex(extend_kernel<D>, dim3(grid), dim3(C::THREADS), C::SMEM, stream, pdl, tm_q, tm_k, tm_v, p);
 }
 
 }  // namespace
@@ -565,10 +565,10 @@ cudaError_t prepare_extend(int head_dim) {
 }
 
 cudaError_t launch_extend(int head_dim, int grid, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                          const CUtensorMap &tm_v, const ExtendParams &p, cudaStream_t stream) {
+                          const CUtensorMap &tm_v, const ExtendParams &p, cudaStream_t stream, bool pdl) {
     if (grid <= 0) return cudaSuccess;
-    if (head_dim == 128) return launch_t<128>(grid, tm_q, tm_k, tm_v, p, stream);
-    if (head_dim == 64) return launch_t<64>(grid, tm_q, tm_k, tm_v, p, stream);
+    if (head_dim == 128) return launch_t<128>(grid, tm_q, tm_k, tm_v, p, stream, pdl);
+    if (head_dim == 64) return launch_t<64>(grid, tm_q, tm_k, tm_v, p, stream, pdl);
     return cudaErrorInvalidValue;
 }
 

@@ -299,15 +299,15 @@ cudaError_t launch_write_kv_fp8(const void *key, const void *value, const int64_
     return cudaGetLastError();
 }
 
-cudaError_t launch_dequant(int grid, const DequantParams &p, cudaStream_t stream) {
+cudaError_t launch_dequant(int grid, const DequantParams &p, cudaStream_t stream, bool pdl) {
     if (grid <= 0) return cudaSuccess;
-    return launch_pdl(dequant_kernel, dim3(grid), dim3(256), 0, stream, p);
+    return launch_ex(dequant_kernel, dim3(grid), dim3(256), 0, stream, pdl, p);
 }
 
-cudaError_t launch_merge(int head_dim, int grid, const MergeParams &p, cudaStream_t stream) {
+cudaError_t launch_merge(int head_dim, int grid, const MergeParams &p, cudaStream_t stream, bool pdl) {
     if (grid <= 0) return cudaSuccess;
-    if (head_dim == 128) return launch_pdl(merge_kernel<128>, dim3(grid), dim3(256), 0, stream, p);
-    if (head_dim == 64) return launch_pdl(merge_kernel<64>, dim3(grid), dim3(256), 0, stream, p);
+    if (head_dim == 128) return launch_ex(merge_kernel<128>, dim3(grid), dim3(256), 0, stream, pdl, p);
+    if (head_dim == 64) return launch_ex(merge_kernel<64>, dim3(grid), dim3(256), 0, stream, pdl, p);
     return cudaErrorInvalidValue;
 }
 

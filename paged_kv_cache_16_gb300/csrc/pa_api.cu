@@ -48,17 +48,22 @@ bool make_map(CUtensorMap *tm, const void *ptr, uint64_t d, uint64_t mid, uint64
     return r == CUDA_SUCCESS;
 }
 
-bool make_map_u8(CUtensorMap *tm, const void *ptr, uint64_t d, uint64_t mid, uint64_t outer, uint32_t box_mid,
-                 uint32_t box_outer) {
+// Tensor map of a paged cache for the decode stream: dimensions (element,
+// row, kv head) over [rows][Hkv][D], box [box_heads][16 rows][128 bytes].  One
+// box brings the 16 rows of a block for box_heads kv heads, each head's rows
+// a contiguous, 128-byte-swizzled [16][128 B] tile in shared memory.
+bool make_map_kv(CUtensorMap *tm, const void *ptr, uint64_t d, uint64_t hkv, uint64_t rows, uint32_t box_heads,
+                 bool u8) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[3] = {d, mid, outer};
-    cuuint64_t strides[2] = {d, mid * d};
-    cuuint32_t box[3] = {128, box_mid, box_outer};
+    const uint64_t es = u8 ? 1 : 2;
+    cuuint64_t dims[3] = {d, rows, hkv};
+    cuuint64_t strides[2] = {hkv * d * es, d * es};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(kBlockSize), box_heads};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(tm, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr),
+                    dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -206,10 +211,11 @@ struct DecodeUnit {
 // Cut the concatenated decode runs into ncta equal contiguous shares.
 // pieces[u * n_groups + grp] receives the number of runs unit u was cut into;
 // item_unit[i] the unit of item i.
+// work_ctas: at most that many CTAs get work (0: num_sms x CTAs per SM).
 // fixed_ncta > 0: the grid has exactly that many CTAs; the shares past the
 // ones the work needs are empty.
 void plan_decode(pa_plan_s *P, const std::vector<DecodeUnit> &units, std::vector<int32_t> &pieces,
-                 std::vector<int32_t> &item_unit, int64_t fixed_ncta) {
+                 std::vector<int32_t> &item_unit, int64_t work_ctas, int64_t fixed_ncta) {
     struct Run { int32_t u, grp, pb, pe; };
     std::vector<Run> runs;
     runs.reserve(units.size() * P->n_groups);
@@ -231,7 +237,8 @@ void plan_decode(pa_plan_s *P, const std::vector<DecodeUnit> &units, std::vector
     }
     const int cps = std::max(1, decode_ctas_per_sm_static(P->D, P->HG, P->kv8));
     const int64_t min_pages = 4;
-    int64_t ncta = std::min<int64_t>(static_cast<int64_t>(P->num_sms) * cps, (total + min_pages - 1) / min_pages);
+    const int64_t cap = work_ctas > 0 ? work_ctas : static_cast<int64_t>(P->num_sms) * cps;
+    int64_t ncta = std::min<int64_t>(cap, (total + min_pages - 1) / min_pages);
     ncta = std::max<int64_t>(ncta, 1);
     if (fixed_ncta > 0) ncta = std::min(ncta, fixed_ncta);
     // an equal cut makes at most one item per run plus one per CTA
@@ -268,6 +275,55 @@ void plan_decode(pa_plan_s *P, const std::vector<DecodeUnit> &units, std::vector
     }
     while (static_cast<int64_t>(P->cta_begin.size()) < fixed_ncta + 1)
         P->cta_begin.push_back(static_cast<int32_t>(P->items.size()));
+}
+
+// Step-time model used to split the SMs between the tensor-core tiles and
+// the split-KV decode stream when a step has both (times in microseconds,
+// constants measured on GB300 at full clock).  The tiles are bound by the
+// tensor pipe of the SMs they run on, the decode stream by HBM once it has
+// enough SMs (each SM alone streams about 90 GB/s of bf16 blocks, 40 GB/s of
+// E4M3 codes), so running the two side by side on disjoint SMs costs about
+// the longer of the two instead of their sum.
+// Side by side the two slow each other down a little (the tiles' K/V
+// re-reads and the decode stream share L2 and HBM): both constants below
+// were measured that way.
+constexpr double kTileStepUs = 1.85;          // one 128-key step of a 256-row tile on one SM
+constexpr double kTileStepSideUs = 2.15;      // the same beside the decode stream
+constexpr double kHbmBytesPerUs = 7.0e6;      // decode stream at the HBM limit
+constexpr double kHbmSideBytesPerUs = 6.7e6;  // the same beside the tiles
+constexpr double kSmBf16BytesPerUs = 9.0e4;   // decode stream of one SM, bf16 caches
+constexpr double kSmFp8BytesPerUs = 4.0e4;    // decode stream of one SM, E4M3 caches
+constexpr double kForkUs = 5.0;               // cost of the second stream (fork, join, plain launches)
+
+struct StepModel {
+    double tile_units = 0, tile_max = 0;      // sum and largest tile cost (128-key steps + 1)
+    double decode_bytes = 0, sm_rate = 0;
+    double tiles(int ctas, bool side) const {
+        return ctas <= 0 ? 1e30 : std::max(tile_units / ctas, tile_max) * (side ? kTileStepSideUs : kTileStepUs);
+    }
+    double decode(int sms, bool side) const {
+        return sms <= 0 ? 1e30
+                        : std::max(decode_bytes / (sms * sm_rate),
+                                   decode_bytes / (side ? kHbmSideBytesPerUs : kHbmBytesPerUs));
+    }
+};
+
+// Extend CTAs for a step that runs tiles and decode side by side on
+// num_sms SMs: the split with the shortest modelled step; among near-equal
+// splits the one whose tiles finish with some slack before the decode
+// stream (the model is a few percent off either way).
+int split_sms(const StepModel &m, int num_sms, int max_tile_ctas, double *t_out) {
+    const int hi = std::min(num_sms - 1, max_tile_ctas);
+    double best = 1e30;
+    int arg = 1;
+    for (int e = 1; e <= hi; ++e) {
+        const double t = std::max(m.tiles(e, true), m.decode(num_sms - e, true));
+        if (t < best) { best = t; arg = e; }
+    }
+    for (int e = 1; e <= hi; ++e)
+        if (m.tiles(e, true) <= 0.85 * best && m.decode(num_sms - e, true) <= 1.01 * best) { arg = e; break; }
+    *t_out = best;
+    return arg;
 }
 
 pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape *shape) {
@@ -411,44 +467,98 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
         for (ExtendTile &t : P->tiles) t.req = row_of[t.req];
     }
 
-    // ------------------------------- persistent tensor-core CTAs (LPT)
+    // ------------------------------------------------------ decode units
+    std::vector<DecodeUnit> units;
+    units.reserve(decode_rows.size() + small_rows.size() * 2);
+    for (int32_t r = 0; r < P->R; ++r) {
+        const int32_t q_len = qsl[r + 1] - qsl[r];
+        if (!on_decode[r]) continue;
+        for (int32_t j = 0; j < q_len; j += tg) {
+            const int32_t n = std::min(tg, q_len - j);
+            units.push_back({r, qsl[r] + j, n, d->num_computed_tokens[r] + j + n});
+        }
+    }
+    const int cps = std::max(1, decode_ctas_per_sm_static(P->D, P->HG, P->kv8));
+
+    // ------------------------------------------ tile costs and the SM split
     // cost of a tile: its 128-key steps (as the kernel counts them) plus one
-    // for the Q load and epilogue; each tile goes to the least loaded CTA,
-    // longest tiles first
+    // for the Q load and epilogue
+    std::vector<std::pair<int64_t, int32_t>> cost;
+    cost.reserve(P->tiles.size());
+    StepModel model;
     {
-        const int64_t max_ctas = P->fixed ? std::min<int64_t>(shape->max_extend_tiles, P->num_sms)
-                                          : std::min<int64_t>(static_cast<int64_t>(P->tiles.size()), P->num_sms);
-        P->ext_ctas = static_cast<int32_t>(std::max<int64_t>(max_ctas, 0));
+        const int tpt_rows = kTileRows / P->G;
+        for (size_t i = 0; i < P->tiles.size(); ++i) {
+            const ExtendTile &t = P->tiles[i];
+            int n_tiles = 0;
+            for (int sub = 0; sub < 2; ++sub) {
+                const int first = sub * tpt_rows;
+                if (first >= t.n_tok) continue;
+                const int last = std::min(t.n_tok, first + tpt_rows);
+                const int kend = t.causal ? std::min(t.key_end, t.pos0 + last) : t.key_end;
+                n_tiles = std::max(n_tiles, (kend - t.key_begin + kTileKeys - 1) / kTileKeys);
+            }
+            cost.push_back({n_tiles + 1, static_cast<int32_t>(i)});
+            model.tile_units += n_tiles + 1;
+            model.tile_max = std::max<double>(model.tile_max, n_tiles + 1);
+        }
+        const int64_t row_bytes = static_cast<int64_t>(P->Hkv) * P->D * (P->kv8 ? 1 : 2) * 2;
+        for (const DecodeUnit &u : units)
+            model.decode_bytes += static_cast<double>(std::max(0, u.key_end - kb_keys)) * row_bytes;
+        model.sm_rate = P->kv8 ? kSmFp8BytesPerUs : kSmBf16BytesPerUs;
+    }
+    const int64_t n_tiles_all = static_cast<int64_t>(P->tiles.size());
+    if (P->fixed && n_tiles_all > shape->max_extend_tiles) return PA_ERR_CAPACITY;
+    const bool have_tiles = n_tiles_all > 0, have_decode = model.decode_bytes > 0;
+    // grids: eager plans are sized by the work, fixed-shape plans by their
+    // capacities (the decode grid is always num_sms x CTAs per SM)
+    const int64_t tile_grid_cap = P->fixed ? std::min<int64_t>(shape->max_extend_tiles, P->num_sms)
+                                           : std::min<int64_t>(n_tiles_all, P->num_sms);
+    // The work cut: split the SMs when the model says running the two side
+    // by side pays, else every CTA of both grids gets work.  The cut depends
+    // on the step only, so a fixed-shape plan and a plain plan of the same
+    // step cut (and compute) identically.  The launch topology: plain plans
+    // put the tiles on a second stream exactly when the cut is split;
+    // fixed-shape plans with tiles always do (their launches cannot depend on
+    // the step), and an unsplit step then has both grids compete for the SMs.
+    int64_t tile_work_ctas = std::min<int64_t>(n_tiles_all, P->num_sms);   // CTAs that get tiles
+    int64_t decode_work_ctas = 0;                                           // 0: all
+    bool split = false;
+    if (have_tiles && have_decode && P->num_sms >= 2) {
+        double t_split = 0;
+        const int e = split_sms(model, P->num_sms, static_cast<int>(std::min<int64_t>(n_tiles_all, P->num_sms - 1)),
+                                &t_split);
+        const double t_seq = model.tiles(static_cast<int>(tile_work_ctas), false) + model.decode(P->num_sms, false);
+        if (t_split + kForkUs < t_seq) {
+            split = true;
+            tile_work_ctas = e;
+            decode_work_ctas = P->num_sms - e;
+        }
+    }
+    P->fork = P->fixed ? shape->max_extend_tiles > 0 && P->num_sms >= 2 : split;
+    P->ext_ctas = static_cast<int32_t>(std::max<int64_t>(P->fixed ? tile_grid_cap : tile_work_ctas, 0));
+    P->info.num_extend_ctas = static_cast<int32_t>(have_tiles ? tile_work_ctas : 0);
+    P->info.side_by_side = P->fork ? 1 : 0;
+
+    // ------------------------------- persistent tensor-core CTAs (LPT)
+    // each tile goes to the least loaded of the first tile_work_ctas CTAs,
+    // longest tiles first; the grid's other CTAs get nothing
+    {
         // counts per CTA, then the tiles in assignment order (a counting
         // sort: no per-CTA lists to grow)
         P->cta_tile_begin.assign(static_cast<size_t>(P->ext_ctas) + 1, 0);
         P->cta_tiles.clear();
-        if (P->ext_ctas > 0) {
-            const int tpt_rows = kTileRows / P->G;
-            std::vector<std::pair<int64_t, int32_t>> cost;
-            cost.reserve(P->tiles.size());
-            for (size_t i = 0; i < P->tiles.size(); ++i) {
-                const ExtendTile &t = P->tiles[i];
-                int n_tiles = 0;
-                for (int sub = 0; sub < 2; ++sub) {
-                    const int first = sub * tpt_rows;
-                    if (first >= t.n_tok) continue;
-                    const int last = std::min(t.n_tok, first + tpt_rows);
-                    const int kend = t.causal ? std::min(t.key_end, t.pos0 + last) : t.key_end;
-                    n_tiles = std::max(n_tiles, (kend - t.key_begin + kTileKeys - 1) / kTileKeys);
-                }
-                cost.push_back({n_tiles + 1, static_cast<int32_t>(i)});
-            }
+        if (P->ext_ctas > 0 && have_tiles) {
             std::stable_sort(cost.begin(), cost.end(),
                              [](const std::pair<int64_t, int32_t> &a, const std::pair<int64_t, int32_t> &b) {
                                  return a.first > b.first;
                              });
             using Load = std::pair<int64_t, int32_t>;   // (work so far, CTA)
             std::vector<Load> heap_store;
-            heap_store.reserve(static_cast<size_t>(P->ext_ctas));
+            heap_store.reserve(static_cast<size_t>(tile_work_ctas));
             std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap(std::greater<Load>(),
                                                                                  std::move(heap_store));
-            for (int32_t c = 0; c < P->ext_ctas; ++c) heap.push({0, c});
+            for (int32_t c = 0; c < tile_work_ctas; ++c) heap.push({0, c});
             std::vector<int32_t> cta_of(cost.size());
             for (size_t k = 0; k < cost.size(); ++k) {
                 Load ld = heap.top();
@@ -465,19 +575,8 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     }
 
     // ------------------------------------------------------------- decode
-    std::vector<DecodeUnit> units;
-    units.reserve(decode_rows.size() + small_rows.size() * 2);
-    for (int32_t r = 0; r < P->R; ++r) {
-        const int32_t q_len = qsl[r + 1] - qsl[r];
-        if (!on_decode[r]) continue;
-        for (int32_t j = 0; j < q_len; j += tg) {
-            const int32_t n = std::min(tg, q_len - j);
-            units.push_back({r, qsl[r] + j, n, d->num_computed_tokens[r] + j + n});
-        }
-    }
     std::vector<int32_t> pieces, item_unit;
-    const int cps = std::max(1, decode_ctas_per_sm_static(P->D, P->HG, P->kv8));
-    plan_decode(P, units, pieces, item_unit, P->fixed ? static_cast<int64_t>(P->num_sms) * cps : 0);
+    plan_decode(P, units, pieces, item_unit, decode_work_ctas, P->fixed ? static_cast<int64_t>(P->num_sms) * cps : 0);
 
     // ------------------------------- fused cache update of extend rows
     std::vector<int32_t> multi_rows(small_rows);
@@ -675,17 +774,44 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 namespace pa {
 
+SideStream *side_stream() {
+    // one per host thread and device, created on first use and kept for the
+    // thread's lifetime (never destroyed: a thread may outlive nothing here,
+    // but the CUDA context may be torn down before thread-local destructors)
+    constexpr int kMaxDevices = 64;
+    thread_local SideStream slots[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    SideStream &ss = slots[dev];
+    if (!ss.stream) {
+        cudaStream_t st = nullptr;
+        cudaEvent_t fork = nullptr, join = nullptr;
+        if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+        if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+            if (fork) cudaEventDestroy(fork);
+            cudaStreamDestroy(st);
+            return nullptr;
+        }
+        ss.stream = st;
+        ss.fork = fork;
+        ss.join = join;
+    }
+    return &ss;
+}
+
 pa_status prepare_plan(pa_plan_s *P) {
     if (P->prepared) return PA_OK;
     if (P->ncta > 0 && prepare_decode(P->D, P->HG, P->kv8) != cudaSuccess) return PA_ERR_CUDA;
     if (P->cap_tiles > 0 && prepare_extend(P->D) != cudaSuccess) return PA_ERR_CUDA;
+    if (P->fork && side_stream() == nullptr) return PA_ERR_CUDA;
     P->prepared = true;
     return PA_OK;
 }
 
 pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, const void *value_cache,
                             const int32_t *block_table, void *out, uint8_t *ws, cudaStream_t stream, bool timed,
-                            const KvUpdate &update) {
+                            const KvUpdate &update, bool allow_fork) {
     auto rec = [&](int kind, bool start, cudaStream_t st) { return timed ? record(P, kind, start, st) : cudaSuccess; };
     int32_t *err = reinterpret_cast<int32_t *>(ws);
     const int32_t *counts = reinterpret_cast<const int32_t *>(ws + kHeader);
@@ -695,12 +821,17 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
     uint16_t *out16 = static_cast<uint16_t *>(out);
     const int sms = std::max(1, P->num_sms);
 
-    CUtensorMap tm_k, tm_v;
+    // decode stream: one box per block and 128-byte column slice covers the
+    // CTA's HG kv heads; tensor-core tiles (bf16 caches): one box per block,
+    // kv head and 64-column half
+    CUtensorMap tm_k{}, tm_v{}, tm_dk{}, tm_dv{};
     const uint64_t rows = static_cast<uint64_t>(P->num_blocks) * kBlockSize;
-    if (P->kv8 ? (!make_map_u8(&tm_k, key_cache, P->D, P->Hkv, rows, 1, kBlockSize) ||
-                  !make_map_u8(&tm_v, value_cache, P->D, P->Hkv, rows, 1, kBlockSize))
-               : (!make_map(&tm_k, key_cache, P->D, P->Hkv, rows, 1, kBlockSize) ||
-                  !make_map(&tm_v, value_cache, P->D, P->Hkv, rows, 1, kBlockSize)))
+    if (P->ncta > 0 && (!make_map_kv(&tm_dk, key_cache, P->D, P->Hkv, rows, P->HG, P->kv8) ||
+                        !make_map_kv(&tm_dv, value_cache, P->D, P->Hkv, rows, P->HG, P->kv8)))
+        return PA_ERR_CUDA;
+    if (P->cap_tiles > 0 && !P->kv8 &&
+        (!make_map(&tm_k, key_cache, P->D, P->Hkv, rows, 1, kBlockSize) ||
+         !make_map(&tm_v, value_cache, P->D, P->Hkv, rows, 1, kBlockSize)))
         return PA_ERR_CUDA;
 
     if (update.key != nullptr && P->cap_runs > 0) {
@@ -727,6 +858,20 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
         const int grid = static_cast<int>(std::min<int64_t>((chunks + 255) / 256, 16 * sms));
         if (launch_write_runs(grid, wp, stream) != cudaSuccess) return PA_ERR_CUDA;
     }
+    // Side by side: the tiles (and, for E4M3 caches, the bf16 copies of their
+    // blocks) go to a second stream that starts after everything enqueued so
+    // far (metadata upload, write of the extend rows), while the decode kernel
+    // runs on the other SMs; the merge waits for both.
+    const bool fork = P->fork && allow_fork && P->cap_tiles > 0;
+    cudaStream_t tile_stream = stream;
+    SideStream *side = nullptr;
+    if (fork) {
+        side = side_stream();
+        if (!side || cudaEventRecord(side->fork, stream) != cudaSuccess ||
+            cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
+            return PA_ERR_CUDA;
+        tile_stream = side->stream;
+    }
     if (P->cap_tiles > 0) {
         // E4M3: the tiles read bf16 copies of their blocks, made here
         CUtensorMap tm_tk = tm_k, tm_tv = tm_v;
@@ -745,7 +890,8 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
             qp.max_blocks = P->max_blocks;
             qp.num_blocks = P->num_blocks;
             qp.block_elems = kBlockSize * P->Hkv * P->D;
-            if (launch_dequant(std::min(P->cap_dequant, 8 * sms), qp, stream) != cudaSuccess) return PA_ERR_CUDA;
+            if (launch_dequant(std::min(P->cap_dequant, 8 * sms), qp, tile_stream, !fork) != cudaSuccess)
+                return PA_ERR_CUDA;
             const uint64_t srows = static_cast<uint64_t>(std::max(1, P->cap_dequant)) * kBlockSize;
             if (!make_map(&tm_tk, ws + P->off_kscr, P->D, P->Hkv, srows, 1, kBlockSize) ||
                 !make_map(&tm_tv, ws + P->off_vscr, P->D, P->Hkv, srows, 1, kBlockSize))
@@ -773,9 +919,11 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
         ep.heads_per_group = P->HG;
         ep.scale_log2 = P->scale_log2;
         ep.out_scale = P->out_scale;
-        if (rec(1, true, stream) != cudaSuccess) return PA_ERR_CUDA;
-        if (launch_extend(P->D, P->ext_ctas, tm_q, tm_tk, tm_tv, ep, stream) != cudaSuccess) return PA_ERR_CUDA;
-        if (rec(1, false, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (rec(1, true, tile_stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_extend(P->D, P->ext_ctas, tm_q, tm_tk, tm_tv, ep, tile_stream, !fork) != cudaSuccess)
+            return PA_ERR_CUDA;
+        if (rec(1, false, tile_stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (fork && cudaEventRecord(side->join, tile_stream) != cudaSuccess) return PA_ERR_CUDA;
     }
     if (P->ncta > 0) {
         DecodeParams dp{};
@@ -804,9 +952,10 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
         dp.k_scale = P->k_scale;
         dp.v_scale = P->v_scale;
         if (rec(0, true, stream) != cudaSuccess) return PA_ERR_CUDA;
-        if (launch_decode(P->D, P->HG, P->kv8, P->ncta, tm_k, tm_v, dp, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_decode(P->D, P->HG, P->kv8, P->ncta, tm_dk, tm_dv, dp, stream) != cudaSuccess) return PA_ERR_CUDA;
         if (rec(0, false, stream) != cudaSuccess) return PA_ERR_CUDA;
     }
+    if (fork && cudaStreamWaitEvent(stream, side->join, 0) != cudaSuccess) return PA_ERR_CUDA;
     if (P->cap_merges > 0) {
         MergeParams mp{};
         mp.out = out16;
@@ -819,7 +968,7 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
         const int64_t warps = static_cast<int64_t>(P->cap_merges) * mp.max_heads;   // 8 warps per CTA
         const int grid = static_cast<int>(std::min<int64_t>((warps + 7) / 8, 16 * sms));
         if (rec(2, true, stream) != cudaSuccess) return PA_ERR_CUDA;
-        if (launch_merge(P->D, grid, mp, stream) != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_merge(P->D, grid, mp, stream, !fork) != cudaSuccess) return PA_ERR_CUDA;
         if (rec(2, false, stream) != cudaSuccess) return PA_ERR_CUDA;
     }
     return PA_OK;

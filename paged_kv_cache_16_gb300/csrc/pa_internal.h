@@ -216,11 +216,12 @@ struct WriteParams {
     float k_scale, v_scale;     // E4M3 quantisation (code of x / scale)
 };
 
-// Launch with programmatic stream serialisation (the kernel calls
-// grid_dep_wait before touching data of earlier kernels).
+// Launch with programmatic stream serialisation when `pdl` (the kernel calls
+// grid_dep_wait before touching data of earlier kernels, which is a no-op for
+// a plain launch).  Plain launches follow a wait on another stream's event.
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                              Args &&...args) {
+inline cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             bool pdl, Args &&...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -230,8 +231,14 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args &&...args) {
+    return launch_ex(kernel, grid, block, smem, stream, true, std::forward<Args>(args)...);
 }
 
 // Launchers (each returns the launch's cudaError_t).
@@ -249,14 +256,14 @@ cudaError_t launch_write_kv_fp8(const void *key, const void *value, const int64_
 // The grid-sized launchers take the CTA count to launch; kernels read their
 // real work counts from the device (MetaCount), so a grid sized for a
 // capacity is as correct as an exact one.
-cudaError_t launch_dequant(int grid, const DequantParams &p, cudaStream_t stream);
+cudaError_t launch_dequant(int grid, const DequantParams &p, cudaStream_t stream, bool pdl = true);
 // Decode kernel: head_dim D, heads per CTA hg, E4M3 caches (kv8).  Returns
 // cudaErrorInvalidValue for an unsupported combination.
 cudaError_t launch_decode(int head_dim, int hg, bool kv8, int num_ctas, const CUtensorMap &tm_k,
                           const CUtensorMap &tm_v, const DecodeParams &p, cudaStream_t stream);
 cudaError_t launch_extend(int head_dim, int grid, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                          const CUtensorMap &tm_v, const ExtendParams &p, cudaStream_t stream);
-cudaError_t launch_merge(int head_dim, int grid, const MergeParams &p, cudaStream_t stream);
+                          const CUtensorMap &tm_v, const ExtendParams &p, cudaStream_t stream, bool pdl = true);
+cudaError_t launch_merge(int head_dim, int grid, const MergeParams &p, cudaStream_t stream, bool pdl = true);
 // Copy `bytes` (a multiple of 16) from device-accessible pinned host memory
 // to device memory with a kernel.
 cudaError_t launch_upload(const void *src, void *dst, size_t bytes, cudaStream_t stream);

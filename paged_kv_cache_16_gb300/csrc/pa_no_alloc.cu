@@ -55,7 +55,14 @@ extern "C" pa_status pa_attention_no_alloc(const pa_plan_t *plan, const void *q,
     using namespace pa;
     if (!plan) return PA_ERR_INVALID_ARGUMENT;
     pa_plan_s *P = const_cast<pa_plan_s *>(plan);
-    if (P->T == 0) return PA_OK;
+    if (P->T == 0) {
+        // nothing to attend; the error word still receives this call's bits (none)
+        if (device_error_word && (!aligned(device_error_word, 4) ||
+                                  cudaMemsetAsync(device_error_word, 0, sizeof(int32_t),
+                                                  static_cast<cudaStream_t>(stream_)) != cudaSuccess))
+            return aligned(device_error_word, 4) ? PA_ERR_CUDA : PA_ERR_INVALID_ARGUMENT;
+        return PA_OK;
+    }
     if (!q || !key_cache || !value_cache || !block_table || !out) return PA_ERR_INVALID_ARGUMENT;
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
         !aligned(block_table, 4) || (device_error_word && !aligned(device_error_word, 4)))
@@ -76,7 +83,9 @@ extern "C" pa_status pa_attention_no_alloc(const pa_plan_t *plan, const void *q,
             cudaSuccess)
         return PA_ERR_CUDA;
 
-    const pa_status es = enqueue_attention(P, q, key_cache, value_cache, block_table, out, ws, stream, false);
+    // one stream only: no library stream or event is created for this call
+    const pa_status es = enqueue_attention(P, q, key_cache, value_cache, block_table, out, ws, stream, false,
+                                           KvUpdate{}, false);
     if (es != PA_OK) return es;
     const int32_t *err = reinterpret_cast<const int32_t *>(ws);
     if (device_error_word &&

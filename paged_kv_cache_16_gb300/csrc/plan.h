@@ -26,7 +26,8 @@ struct pa_plan_s {
     std::vector<pa::MergeRow> merges;
     std::vector<int32_t> cta_tile_begin;      // persistent tensor-core CTAs: [ext_ctas + 1]
     std::vector<int32_t> cta_tiles;           // their tile lists
-    int32_t ext_ctas = 0;
+    int32_t ext_ctas = 0;                     // grid of the tensor-core kernel
+    bool fork = false;                        // tiles on a second stream, beside the decode kernel
     std::vector<pa::WriteRun> write_runs;     // extend rows (fused cache update)
     int32_t write_tokens = 0;
     std::vector<int32_t> scratch_table;       // E4M3: [rows][max_blocks] bf16 scratch block ids
@@ -65,9 +66,6 @@ constexpr size_t kWorkspaceHeader = 256;  // error word + reserved, then the met
 // the encoding is rejected).
 bool make_map(CUtensorMap *tm, const void *ptr, uint64_t d, uint64_t mid, uint64_t outer, uint32_t box_mid,
               uint32_t box_outer);
-// The same over one-byte elements (E4M3 caches): box [box_outer][box_mid][128].
-bool make_map_u8(CUtensorMap *tm, const void *ptr, uint64_t d, uint64_t mid, uint64_t outer, uint32_t box_mid,
-                 uint32_t box_outer);
 
 // Enqueue every kernel of one attention call on `stream`; the metadata blob
 // must already be (or be about to be, in stream order) at ws + header.
@@ -81,9 +79,20 @@ struct KvUpdate {
     int64_t *slots_out = nullptr;   // optional [T]
 };
 
+// allow_fork = false keeps every launch on `stream` (a plan whose tiles run
+// side by side with the decode kernel then runs them one after the other,
+// with the same work cut and the same results).
 pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, const void *value_cache,
                             const int32_t *block_table, void *out, uint8_t *ws, cudaStream_t stream, bool timed,
-                            const KvUpdate &update = KvUpdate{});
+                            const KvUpdate &update = KvUpdate{}, bool allow_fork = true);
+
+// The second stream (and its fork / join events) of this host thread on the
+// current device, created on first use; null if creation fails.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideStream *side_stream();
 
 // Set the kernel attributes the plan's launches need (once per plan).
 pa_status prepare_plan(pa_plan_s *P);
