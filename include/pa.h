@@ -50,6 +50,18 @@
  * enqueue work on the given stream (a cudaStream_t; NULL = the legacy default
  * stream) and never synchronise, except pa_check_device_errors.  Errors come
  * back as a status; nothing aborts, traps or throws across the ABI.
+ *
+ * Library-owned host resources: (1) pinned staging buffers for the metadata
+ * upload of pa_attention / pa_upload_metadata, kept in a pool; a buffer is
+ * reused once its last copy has run, and the pool calls cudaMallocHost only
+ * when no such buffer is free (the first calls of a process, and whenever more
+ * plans' uploads are in flight than the pool holds; it keeps up to 32 free
+ * buffers).  The capturable path (pa_plan_copy_metadata +
+ * pa_upload_metadata_from, and pa_graph_*) never uses the pool.  (2) A
+ * second stream with two events per host thread and device, created the
+ * first time that thread prepares a plan whose tensor-core tiles run beside
+ * the decode kernel (pa_plan_info.side_by_side) and kept for the thread's
+ * lifetime.
  */
 #ifndef PA_H
 #define PA_H
@@ -243,6 +255,15 @@ pa_status pa_write_kv_fp8(const void *key, const void *value, const int64_t *slo
  * including NaN).  Returns PA_ERR_WORKSPACE_TOO_SMALL, PA_ERR_INVALID_ARGUMENT
  * (NULL or misaligned pointer) or PA_ERR_CUDA (launch failure).  Equivalent to
  * pa_upload_metadata then pa_attention_launch, plus the optional timing events.
+ *
+ * Side by side (pa_plan_info.side_by_side): when a step has both
+ * tensor-core tiles and decode rows and the planner's step-time model says it
+ * pays, the tiles get a share of the SMs (num_extend_ctas CTAs) and run on
+ * the calling thread's library stream, which first waits for everything
+ * enqueued on `stream` so far; the decode kernel runs on `stream` over the
+ * other SMs, and `stream` waits for the tiles before the merge.  Seen from
+ * `stream` the call stays one ordered unit of work, and under stream capture
+ * the library stream joins and leaves the capture inside the call.
  */
 pa_status pa_attention(const pa_plan_t *plan, const void *q, const void *key_cache,
                        const void *value_cache, const int32_t *block_table, void *out,
@@ -279,7 +300,11 @@ typedef struct {
  * max_reqs must be > 0), and PA_ERR_CAPACITY when this step needs more tokens,
  * requests, tiles, FP8 blocks or partial slots than the shape allows.  The
  * workspace size depends on the shape and model fields only.  The decode
- * kernel always runs on num_sms x (CTAs per SM) CTAs.
+ * kernel always runs on num_sms x (CTAs per SM) CTAs.  With tensor-core tiles
+ * (max_extend_tiles > 0, num_sms >= 2) the tiles always run on the library
+ * stream beside the decode kernel (side_by_side = 1); each step's work cut is
+ * the one pa_plan makes for the same step, so a fixed-shape plan and a plain
+ * plan of one step compute bit-identical results.
  */
 pa_status pa_plan_fixed(const pa_batch_desc *desc, const pa_fixed_shape *shape, pa_plan_t **out,
                         size_t *workspace_bytes);

@@ -66,6 +66,16 @@ int oracle_num_threads(void) {
 #endif
 }
 
+/* Threads of the parallel loops from now on (n >= 1); for timing the oracle
+ * on one core and on all of them. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /*
  * Step 1 -- slot_mapping ("vLLM 推理流程分析" §5.1.2, compute_slot_mapping;
  * also "vLLM 源码完全拆解（十六）", third walk-through: logical position p

@@ -79,6 +79,8 @@ class Oracle:
         L.oracle_bf16_value.restype = ctypes.c_double
         L.oracle_bf16_value.argtypes = [ctypes.c_uint16]
         L.oracle_num_threads.restype = ctypes.c_int
+        L.oracle_set_num_threads.restype = None
+        L.oracle_set_num_threads.argtypes = [ctypes.c_int]
         L.oracle_slot_mapping.restype = ctypes.c_int
         L.oracle_slot_mapping.argtypes = [ctypes.c_int32, _i32p, _i32p, _i32p, ctypes.c_int32,
                                           ctypes.c_int32, _i64p]
@@ -120,6 +122,10 @@ class Oracle:
 
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())
+
+    def set_num_threads(self, n: int) -> None:
+        """Threads the oracle's parallel loops use from now on (n >= 1)."""
+        self.lib.oracle_set_num_threads(int(n))
 
     # -- step 1: slot mapping --------------------------------------------
     def slot_mapping(self, query_start_loc, num_computed, block_table, block_size: int):

@@ -126,6 +126,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // ------------------------------------------------------ producer --
         int issued = 0;
         int rows_waited = 0;            // fused update: row_ready phases consumed
+        // the stream is read once: its lines go first when L2 needs room, so
+        // it does not push out what other kernels of the step (tensor-core
+        // tiles beside it, partials, metadata) keep re-reading
+        const uint64_t evict_first = policy_evict_first();
         bool ok = true;
         for (int it = item_begin; it < item_end && ok; ++it) {
             const DecodeItem item = p.items[it];
@@ -172,7 +176,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     const int slice = lane % C::NH;
                     const uint32_t dst = stage(s) + tensor * C::TSTAGE + slice * C::SLICE;
                     const uint32_t bar = tensor ? full_v(s) : full_k(s);
-                    tma_load_3d(dst, tensor ? &tm_v : &tm_k, slice * C::CPE, blk * kBlockSize, h0, bar);
+                    tma_load_3d_hint(dst, tensor ? &tm_v : &tm_k, slice * C::CPE, blk * kBlockSize, h0, bar, evict_first);
                 }
                 ++issued;
             }
