@@ -297,6 +297,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 const uint32_t par0 = (consumed / C::NS) & 1, par1 = ((consumed + 1) / C::NS) & 1;
                 if (!warp_wait(full_k(s0), par0, &abort_flag) || (TWO && !warp_wait(full_k(s1), par1, &abort_flag)))
                     return false;
+                // the round's V blocks too (they land with the K blocks): one
+                // scheduling region per round, so value loads and conversions
+                // can interleave with the softmax
+                if (!warp_wait(full_v(s0), par0, &abort_flag) || (TWO && !warp_wait(full_v(s1), par1, &abort_flag)))
+                    return false;
                 float sc[4][4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
@@ -348,8 +353,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     pa[b][2] = pack_f16x2(ex2(fmaf(sc[2 * b + 1][0], sl2, -r0)), ex2(fmaf(sc[2 * b + 1][1], sl2, -r0)));
                     pa[b][3] = pack_f16x2(ex2(fmaf(sc[2 * b + 1][2], sl2, -r1)), ex2(fmaf(sc[2 * b + 1][3], sl2, -r1)));
                 }
-                if (!warp_wait(full_v(s0), par0, &abort_flag) || (TWO && !warp_wait(full_v(s1), par1, &abort_flag)))
-                    return false;
                 const uint32_t vb0 = stage(s0) + C::TSTAGE + warp * C::BOX;
                 if (valid_keys < kBlockSize) pv(std::true_type{}, vb0, pa[0], valid_keys);
                 else pv(std::false_type{}, vb0, pa[0], kBlockSize);
