@@ -83,7 +83,13 @@ PER_CONFIG = [("tiny-1A", "tiny-1A", "bf16"), ("tiny-1B", "tiny", "bf16"), ("dec
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of a
 # kernel from one ncu capture, valid only while the kernel source is
 # unchanged (sha256 prefix of the file); the summaries are under profiles/.
-TRAFFIC = {}
+TRAFFIC = {
+    # profiles/decode_kernel_decode-workload.md, profiles/decode_kernel_e4m3_decode-workload.md,
+    # profiles/extend_kernel_prefill-workload.md
+    ("decode", "decode", "bf16", "6e96feda8bb7b62c"): 643_273_216,
+    ("decode", "decode", "fp8", "6e96feda8bb7b62c"): 323_813_376,
+    ("extend", "prefill", "bf16", "2ba182621aa642af"): 73_638_144,
+}
 KERNEL_SOURCES = {"decode": "paged_kv_cache_16_gb300/csrc/k_decode.cu",
                   "extend": "paged_kv_cache_16_gb300/csrc/k_extend.cu"}
 
