@@ -88,7 +88,7 @@ TRAFFIC = {
     # profiles/extend_kernel_prefill-workload.md
     ("decode", "decode", "bf16", "6e96feda8bb7b62c"): 643_273_216,
     ("decode", "decode", "fp8", "6e96feda8bb7b62c"): 323_813_376,
-    ("extend", "prefill", "bf16", "2ba182621aa642af"): 73_638_144,
+    ("extend", "prefill", "bf16", "e69a77fd500c5bc0"): 73_888_256,
 }
 KERNEL_SOURCES = {"decode": "paged_kv_cache_16_gb300/csrc/k_decode.cu",
                   "extend": "paged_kv_cache_16_gb300/csrc/k_extend.cu"}

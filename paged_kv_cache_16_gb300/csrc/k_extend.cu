@@ -198,13 +198,24 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             ++n_q_loads;
             const int32_t *bt = p.block_table + static_cast<int64_t>(tile.req) * p.max_blocks;
+            // block ids of 32 pages (4 key tiles) per load: the producer's
+            // dependent block-table read happens once per window, not per tile
+            const int pg_end = (tile.key_end + kBlockSize - 1) / kBlockSize;
+            int32_t win = 0;
+            int win0 = -64;
             for (int j = 0; j < sh.n_tiles; ++j) {
                 const int kt0 = tile.key_begin + j * kTileKeys;
+                const int pg0 = kt0 / kBlockSize;
                 const int pages = min(8, (tile.key_end - kt0 + kBlockSize - 1) / kBlockSize);
+                if (pg0 + 8 > win0 + 32) {
+                    win0 = pg0;
+                    win = pg0 + lane < pg_end ? bt[pg0 + lane] : 0;
+                }
+                const int32_t mine_blk = __shfl_sync(0xffffffffu, win, (pg0 - win0 + (lane & 7)) & 31);
                 int32_t blk = 0;
                 bool valid = false;
                 if (lane < pages) {
-                    blk = bt[kt0 / kBlockSize + lane];
+                    blk = mine_blk;
                     valid = blk >= 0 && blk < p.num_blocks;
                 }
                 const unsigned vmask = __ballot_sync(0xffffffffu, valid);
