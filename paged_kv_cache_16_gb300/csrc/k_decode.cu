@@ -216,6 +216,230 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const DecodeItem item = p.items[it];
             const int kvh = item.head_group * HG + warp;
             const int nrow = item.n_tok * G;
+            if (nrow <= 8) {
+                // Items of at most 8 query rows (decode rows): the transposed
+                // products S^T = K Q^T and O^T += V^T P^T.  The 16 keys of a
+                // block are the MMA rows and the query rows its 8 columns, so
+                // a block takes half the MMAs of the row-major form (whose 16
+                // rows would be mostly empty for one query token).  Lane
+                // (g, t) holds the scores of keys g and g + 8 for query rows
+                // n0 = 2t and n1 = 2t + 1.  The K codes as loaded above are
+                // the A fragments (same contraction order, so Q^T is row g's
+                // q); P^T reaches the B fragment of the value MMA through an
+                // 8x8 transpose per half block.  O^T m-tile 4h + i holds the
+                // dims 64h + 4r + i (r = 0..15 its row), so one 32-bit load
+                // of a value row feeds four m-tiles.
+                const int n0 = 2 * t4, n1 = 2 * t4 + 1;
+                const uint16_t *qg =
+                    p.q + (static_cast<int64_t>(item.token + g / G) * p.num_heads_q + kvh * G + g % G) * D;
+                uint32_t qt[D / 16][2];
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int c = kk * 16 + 4 * t4;
+                    qt[kk][0] = g < nrow ? bf16x2_to_f16x2(__ldg(reinterpret_cast<const uint32_t *>(qg + c))) : 0u;
+                    qt[kk][1] = g < nrow ? bf16x2_to_f16x2(__ldg(reinterpret_cast<const uint32_t *>(qg + c + 2))) : 0u;
+                }
+                float ot[D / 16][4];
+#pragma unroll
+                for (int j = 0; j < D / 16; ++j) ot[j][0] = ot[j][1] = ot[j][2] = ot[j][3] = 0.f;
+                float lt[4] = {0.f, 0.f, 0.f, 0.f};
+                float ma = -INFINITY, mb = -INFINITY;   // running maxima of rows n0 and n1 (scaled)
+                // causal limits of rows n0 and n1: token i sees keys < key_end - (n_tok - 1 - i)
+                const int lim_a = min(item.key_end, item.key_end - (item.n_tok - 1 - n0 / G));
+                const int lim_b = min(item.key_end, item.key_end - (item.n_tok - 1 - n1 / G));
+                const int lim_lo = item.key_end - (item.n_tok - 1);
+                if constexpr (FUSED) {
+                    const int lp = new_row_page(item);
+                    if (lp >= 0) {
+                        store_new_row<D, true>(p, item, lp, kvh, lane);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(row_ready);
+                    }
+                }
+                auto qk_t = [&](uint32_t kb, float (&s)[4]) {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t x = kb + k_lane + (static_cast<uint32_t>(kk ^ g) << 4);
+                        uint32_t a[4];
+                        e4m3x4_to_f16x2x2(lds_u32(x), a[0], a[2]);
+                        e4m3x4_to_f16x2x2(lds_u32(x + 1024u), a[1], a[3]);
+                        mma_f16_16816(s, a, qt[kk][0], qt[kk][1]);
+                    }
+                };
+                // O^T += V^T P^T for one block: lane (g, t) loads the value
+                // rows of keys 2t, 2t + 1, 2t + 8, 2t + 9 at the logical bytes
+                // 64h + 32jr + 4g (dims of rows g + 8jr of m-tiles 4h + i);
+                // MASKED zeroes the codes of rows at or past `valid`
+                auto pv_t = [&](auto masked, uint32_t vb, uint32_t b0, uint32_t b1, int valid) {
+                    const uint32_t r0 = vb + 256u * t4;
+                    uint32_t mA = ~0u, mB = ~0u, mC = ~0u, mD = ~0u;
+                    if constexpr (decltype(masked)::value) {
+                        mA = 2 * t4 < valid ? ~0u : 0u;
+                        mB = 2 * t4 + 1 < valid ? ~0u : 0u;
+                        mC = 2 * t4 + 8 < valid ? ~0u : 0u;
+                        mD = 2 * t4 + 9 < valid ? ~0u : 0u;
+                    }
+#pragma unroll
+                    for (int h = 0; h < D / 64; ++h) {
+                        uint32_t a[4][4];
+#pragma unroll
+                        for (int jr = 0; jr < 2; ++jr) {
+                            const uint32_t chunk = 4u * h + 2u * jr + static_cast<uint32_t>(g >> 2);
+                            const uint32_t ce = ((chunk ^ (2u * t4)) << 4) + 4u * (g & 3);        // rows 2t, 2t + 8
+                            const uint32_t co = ((chunk ^ (2u * t4 + 1u)) << 4) + 4u * (g & 3);   // rows 2t + 1, 2t + 9
+                            uint32_t wA = lds_u32(r0 + ce), wB = lds_u32(r0 + 128u + co);
+                            uint32_t wC = lds_u32(r0 + 1024u + ce), wD = lds_u32(r0 + 1152u + co);
+                            if constexpr (decltype(masked)::value) {
+                                wA &= mA; wB &= mB; wC &= mC; wD &= mD;
+                            }
+                            e4m3x4_to_f16x2x2(prmt(wA, wB, 0x5140u), a[0][jr], a[1][jr]);
+                            e4m3x4_to_f16x2x2(prmt(wA, wB, 0x7362u), a[2][jr], a[3][jr]);
+                            e4m3x4_to_f16x2x2(prmt(wC, wD, 0x5140u), a[0][2 + jr], a[1][2 + jr]);
+                            e4m3x4_to_f16x2x2(prmt(wC, wD, 0x7362u), a[2][2 + jr], a[3][2 + jr]);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) mma_f16_16816(ot[4 * h + i], a[i], b0, b1);
+                    }
+                    const uint32_t ones[4] = {kOnes, kOnes, kOnes, kOnes};
+                    mma_f16_16816(lt, ones, b0, b1);   // every row: the f16 weights' sums of n0, n1
+                };
+                auto round_t = [&](auto two_c, int pg) -> bool {
+                    constexpr bool TWO = decltype(two_c)::value;
+                    const int s0 = consumed % C::NS, s1 = (consumed + 1) % C::NS;
+                    const uint32_t par0 = (consumed / C::NS) & 1, par1 = ((consumed + 1) / C::NS) & 1;
+                    if (!warp_wait(full_k(s0), par0, &abort_flag) || (TWO && !warp_wait(full_k(s1), par1, &abort_flag)))
+                        return false;
+                    if (!warp_wait(full_v(s0), par0, &abort_flag) || (TWO && !warp_wait(full_v(s1), par1, &abort_flag)))
+                        return false;
+                    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+                    qk_t(stage(s0) + warp * C::BOX, sa);
+                    if constexpr (TWO) qk_t(stage(s1) + warp * C::BOX, sb);
+                    const int loaded = TWO ? 2 * kBlockSize : kBlockSize;
+                    const int valid_keys = min(item.key_end - pg * kBlockSize, loaded);   // V rows past it may be anything
+                    if (!TWO || lim_lo - pg * kBlockSize < 2 * kBlockSize) {
+                        // keys past the context or a row's causal limit drop out
+                        const int va = min(lim_a - pg * kBlockSize, loaded), vb = min(lim_b - pg * kBlockSize, loaded);
+                        if (g >= va) sa[0] = -INFINITY;
+                        if (g >= vb) sa[1] = -INFINITY;
+                        if (g + 8 >= va) sa[2] = -INFINITY;
+                        if (g + 8 >= vb) sa[3] = -INFINITY;
+                        if constexpr (TWO) {
+                            if (g + 16 >= va) sb[0] = -INFINITY;
+                            if (g + 16 >= vb) sb[1] = -INFINITY;
+                            if (g + 24 >= va) sb[2] = -INFINITY;
+                            if (g + 24 >= vb) sb[3] = -INFINITY;
+                        }
+                    }
+                    float mx0 = fmaxf(sa[0], sa[2]), mx1 = fmaxf(sa[1], sa[3]);
+                    if constexpr (TWO) {
+                        mx0 = max3(mx0, sb[0], sb[2]);
+                        mx1 = max3(mx1, sb[1], sb[3]);
+                    }
+#pragma unroll
+                    for (int o = 4; o < 32; o <<= 1) {   // over the keys: lanes of the same t
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                    }
+                    mx0 *= sl2;
+                    mx1 *= sl2;
+                    // rescale only when the running maximum grows by more than 2^8
+                    const bool need0 = mx0 > ma + 8.f;
+                    const bool need1 = mx1 > mb + 8.f;
+                    if (__any_sync(0xffffffffu, need0 || need1)) {
+                        float a0 = 1.f, a1 = 1.f;
+                        if (need0) { a0 = ex2(ma - mx0); ma = mx0; }
+                        if (need1) { a1 = ex2(mb - mx1); mb = mx1; }
+#pragma unroll
+                        for (int j = 0; j < D / 16; ++j) {
+                            ot[j][0] *= a0; ot[j][1] *= a1; ot[j][2] *= a0; ot[j][3] *= a1;
+                        }
+                        lt[0] *= a0; lt[1] *= a1; lt[2] *= a0; lt[3] *= a1;
+                    }
+                    const float ra = ma == -INFINITY ? 0.f : ma;
+                    const float rb = mb == -INFINITY ? 0.f : mb;
+                    // P^T of a block as B fragments: the packed weights of keys
+                    // g (and g + 8) x rows (n0, n1), transposed 8x8
+                    auto weights = [&](const float (&s)[4], uint32_t &b0, uint32_t &b1) {
+                        b0 = movmatrix_trans(pack_f16x2(ex2(fmaf(s[0], sl2, -ra)), ex2(fmaf(s[1], sl2, -rb))));
+                        b1 = movmatrix_trans(pack_f16x2(ex2(fmaf(s[2], sl2, -ra)), ex2(fmaf(s[3], sl2, -rb))));
+                    };
+                    uint32_t pa0, pa1;
+                    weights(sa, pa0, pa1);
+                    const uint32_t vb0 = stage(s0) + C::TSTAGE + warp * C::BOX;
+                    if (valid_keys < kBlockSize) pv_t(std::true_type{}, vb0, pa0, pa1, valid_keys);
+                    else pv_t(std::false_type{}, vb0, pa0, pa1, kBlockSize);
+                    if constexpr (TWO) {
+                        uint32_t pb0, pb1;
+                        weights(sb, pb0, pb1);
+                        const uint32_t vb1 = stage(s1) + C::TSTAGE + warp * C::BOX;
+                        if (valid_keys < 2 * kBlockSize) pv_t(std::true_type{}, vb1, pb0, pb1, valid_keys - kBlockSize);
+                        else pv_t(std::false_type{}, vb1, pb0, pb1, kBlockSize);
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(empty(s0));
+                        if constexpr (TWO) mbar_arrive(empty(s1));
+                    }
+                    consumed += TWO ? 2 : 1;
+                    return true;
+                };
+                int pg = item.page_begin;
+                for (; ok && pg + 1 < item.page_end; pg += 2) ok = round_t(std::true_type{}, pg);
+                if (ok && pg < item.page_end) ok = round_t(std::false_type{}, pg);
+                if (!ok) {
+                    if (lane == 0) raise_abort(&abort_flag, p.err, kErrTimeout);
+                    break;
+                }
+                // rows n0 and n1: lane holds dims 64h + 32jr + 4g + i in
+                // ot[4h + i][2jr] (row n0) and ot[4h + i][2jr + 1] (row n1)
+                const float inv0 = lt[0] > 0.f ? p.out_scale / lt[0] : 0.f;
+                const float inv1 = lt[1] > 0.f ? p.out_scale / lt[1] : 0.f;
+                const bool has0 = n0 < nrow, has1 = n1 < nrow;
+                const int tokA = n0 / G, tokB = n1 / G;
+                const int headA = kvh * G + n0 % G, headB = kvh * G + n1 % G;
+                if (item.part < 0) {
+                    uint16_t *oa = p.out + (static_cast<int64_t>(item.token + tokA) * p.num_heads_q + headA) * D;
+                    uint16_t *ob = p.out + (static_cast<int64_t>(item.token + tokB) * p.num_heads_q + headB) * D;
+#pragma unroll
+                    for (int h = 0; h < D / 64; ++h)
+#pragma unroll
+                        for (int jr = 0; jr < 2; ++jr) {
+                            const int d = 64 * h + 32 * jr + 4 * g;
+                            if (has0)
+                                *reinterpret_cast<uint2 *>(oa + d) =
+                                    make_uint2(pack_bf16x2(ot[4 * h][2 * jr] * inv0, ot[4 * h + 1][2 * jr] * inv0),
+                                               pack_bf16x2(ot[4 * h + 2][2 * jr] * inv0, ot[4 * h + 3][2 * jr] * inv0));
+                            if (has1)
+                                *reinterpret_cast<uint2 *>(ob + d) =
+                                    make_uint2(pack_bf16x2(ot[4 * h][2 * jr + 1] * inv1, ot[4 * h + 1][2 * jr + 1] * inv1),
+                                               pack_bf16x2(ot[4 * h + 2][2 * jr + 1] * inv1, ot[4 * h + 3][2 * jr + 1] * inv1));
+                        }
+                } else {
+                    const int64_t slotA = has0 ? static_cast<int64_t>(p.part_offset[(item.token + tokA) * p.n_groups + item.head_group]) + item.part : 0;
+                    const int64_t slotB = has1 ? static_cast<int64_t>(p.part_offset[(item.token + tokB) * p.n_groups + item.head_group]) + item.part : 0;
+                    float *opa = p.o_part + (slotA * p.num_heads_q + headA) * D;
+                    float *opb = p.o_part + (slotB * p.num_heads_q + headB) * D;
+#pragma unroll
+                    for (int h = 0; h < D / 64; ++h)
+#pragma unroll
+                        for (int jr = 0; jr < 2; ++jr) {
+                            const int d = 64 * h + 32 * jr + 4 * g;
+                            if (has0)
+                                *reinterpret_cast<float4 *>(opa + d) =
+                                    make_float4(ot[4 * h][2 * jr] * inv0, ot[4 * h + 1][2 * jr] * inv0,
+                                                ot[4 * h + 2][2 * jr] * inv0, ot[4 * h + 3][2 * jr] * inv0);
+                            if (has1)
+                                *reinterpret_cast<float4 *>(opb + d) =
+                                    make_float4(ot[4 * h][2 * jr + 1] * inv1, ot[4 * h + 1][2 * jr + 1] * inv1,
+                                                ot[4 * h + 2][2 * jr + 1] * inv1, ot[4 * h + 3][2 * jr + 1] * inv1);
+                        }
+                    if (g == 0) {
+                        if (has0) p.ml_part[slotA * p.num_heads_q + headA] = make_float2(ma, lt[0]);
+                        if (has1) p.ml_part[slotB * p.num_heads_q + headB] = make_float2(mb, lt[1]);
+                    }
+                }
+                continue;
+            }
             const int tok0 = g / G, tok1 = (g + 8) / G;
             const int head0 = kvh * G + g % G, head1 = kvh * G + (g + 8) % G;
             const uint16_t *q0 = p.q + (static_cast<int64_t>(item.token + tok0) * p.num_heads_q + head0) * D;
