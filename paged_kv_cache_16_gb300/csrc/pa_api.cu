@@ -214,6 +214,13 @@ struct DecodeUnit {
 // work_ctas: at most that many CTAs get work (0: num_sms x CTAs per SM).
 // fixed_ncta > 0: the grid has exactly that many CTAs; the shares past the
 // ones the work needs are empty.
+// Decode cut costs in quarters of one block's streaming time.  The fixed
+// cost of an item (about 1 us on GB300) is what one SM streams meanwhile
+// when the whole GPU streams (about 45 GB/s per SM): 48 KB, 1.5 blocks of
+// E4M3 codes or 0.75 blocks of bf16 rows for 8 kv heads of 128 dims.
+constexpr int64_t kPageCost = 4;
+constexpr int64_t kItemBytes = 48 * 1024;
+
 void plan_decode(pa_plan_s *P, const std::vector<DecodeUnit> &units, std::vector<int32_t> &pieces,
                  std::vector<int32_t> &item_unit, int64_t work_ctas, int64_t fixed_ncta) {
     struct Run { int32_t u, grp, pb, pe; };
@@ -241,18 +248,30 @@ void plan_decode(pa_plan_s *P, const std::vector<DecodeUnit> &units, std::vector
     int64_t ncta = std::min<int64_t>(cap, (total + min_pages - 1) / min_pages);
     ncta = std::max<int64_t>(ncta, 1);
     if (fixed_ncta > 0) ncta = std::min(ncta, fixed_ncta);
-    // an equal cut makes at most one item per run plus one per CTA
+    // The cut is equal in cost, not in pages: an item costs its pages plus a
+    // fixed start-up and finish (q loads, the fused row store, the epilogue),
+    // so a CTA that holds the end of one run and the start of the next gets
+    // fewer pages.  Costs are in quarter blocks.  Cutting a run at a CTA
+    // boundary makes at most one item per run plus one per CTA.
+    const int64_t page_bytes = 2LL * kBlockSize * P->HG * P->D * (P->kv8 ? 1 : 2);   // K and V
+    const int64_t item_cost = (kPageCost * kItemBytes + page_bytes / 2) / page_bytes;
+    const int64_t total_cost =
+        kPageCost * total + item_cost * (static_cast<int64_t>(runs.size()) + ncta - 1);
     P->items.reserve(runs.size() + static_cast<size_t>(ncta));
     item_unit.reserve(runs.size() + static_cast<size_t>(ncta));
     P->cta_begin.reserve(static_cast<size_t>(std::max(ncta, fixed_ncta)) + 1);
     size_t run = 0;
     int32_t cursor = runs.empty() ? 0 : runs[0].pb;
+    int64_t spent = 0;   // cost given to the CTAs so far
     for (int64_t c = 0; c < ncta; ++c) {
-        int64_t quota = total / ncta + (c < total % ncta ? 1 : 0);
-        while (quota > 0 && run < runs.size()) {
+        const bool last = c + 1 == ncta;
+        const int64_t target = total_cost * (c + 1) / ncta;   // cumulative cost at this CTA's end
+        while (run < runs.size()) {
             const Run &R = runs[run];
             const DecodeUnit &U = units[R.u];
-            const int32_t take = static_cast<int32_t>(std::min<int64_t>(quota, R.pe - cursor));
+            const int64_t room = last ? R.pe - cursor : (target - spent - item_cost) / kPageCost;   // pages
+            if (room <= 0) break;
+            const int32_t take = static_cast<int32_t>(std::min<int64_t>(room, R.pe - cursor));
             DecodeItem it{};
             it.token = U.t0;
             it.req = U.r;
@@ -265,7 +284,7 @@ void plan_decode(pa_plan_s *P, const std::vector<DecodeUnit> &units, std::vector
             P->items.push_back(it);
             item_unit.push_back(R.u);
             cursor += take;
-            quota -= take;
+            spent += item_cost + kPageCost * take;
             if (cursor >= R.pe) {
                 ++run;
                 if (run < runs.size()) cursor = runs[run].pb;
@@ -281,7 +300,7 @@ void plan_decode(pa_plan_s *P, const std::vector<DecodeUnit> &units, std::vector
 // the split-KV decode stream when a step has both (times in microseconds,
 // constants measured on GB300 at full clock).  The tiles are bound by the
 // tensor pipe of the SMs they run on, the decode stream by HBM once it has
-// enough SMs (each SM alone streams about 90 GB/s of bf16 blocks, 40 GB/s of
+// enough SMs (each SM alone streams about 90 GB/s of bf16 blocks, 52 GB/s of
 // E4M3 codes), so running the two side by side on disjoint SMs costs about
 // the longer of the two instead of their sum.
 // Side by side the two slow each other down a little (the tiles' K/V
@@ -292,7 +311,7 @@ constexpr double kTileStepSideUs = 2.15;      // the same beside the decode stre
 constexpr double kHbmBytesPerUs = 7.0e6;      // decode stream at the HBM limit
 constexpr double kHbmSideBytesPerUs = 6.7e6;  // the same beside the tiles
 constexpr double kSmBf16BytesPerUs = 9.0e4;   // decode stream of one SM, bf16 caches
-constexpr double kSmFp8BytesPerUs = 4.0e4;    // decode stream of one SM, E4M3 caches
+constexpr double kSmFp8BytesPerUs = 5.2e4;    // decode stream of one SM, E4M3 caches
 constexpr double kForkUs = 5.0;               // cost of the second stream (fork, join, plain launches)
 
 struct StepModel {
