@@ -86,8 +86,8 @@ PER_CONFIG = [("tiny-1A", "tiny-1A", "bf16"), ("tiny-1B", "tiny", "bf16"), ("dec
 TRAFFIC = {
     # profiles/decode_kernel_decode-workload.md, profiles/decode_kernel_e4m3_decode-workload.md,
     # profiles/extend_kernel_prefill-workload.md
-    ("decode", "decode", "bf16", "6e96feda8bb7b62c"): 643_273_216,
-    ("decode", "decode", "fp8", "6e96feda8bb7b62c"): 323_813_376,
+    ("decode", "decode", "bf16", "72d7bcb5f44d1173"): 643_443_456,
+    ("decode", "decode", "fp8", "72d7bcb5f44d1173"): 323_953_920,
     ("extend", "prefill", "bf16", "e69a77fd500c5bc0"): 73_888_256,
 }
 KERNEL_SOURCES = {"decode": "paged_kv_cache_16_gb300/csrc/k_decode.cu",

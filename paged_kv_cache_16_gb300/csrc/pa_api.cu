@@ -217,7 +217,10 @@ struct DecodeUnit {
 // Decode cut costs in quarters of one block's streaming time.  The fixed
 // cost of an item (about 1 us on GB300) is what one SM streams meanwhile
 // when the whole GPU streams (about 45 GB/s per SM): 48 KB, 1.5 blocks of
-// E4M3 codes or 0.75 blocks of bf16 rows for 8 kv heads of 128 dims.
+// E4M3 codes for 8 kv heads of 128 dims.  It counts for E4M3 caches only,
+// whose consumers run close to their per-SM limit (about 52 GB/s); a bf16
+// SM streams twice what the HBM share needs and absorbs it (an item cost
+// there made the decode workload 1.3% slower).
 constexpr int64_t kPageCost = 4;
 constexpr int64_t kItemBytes = 48 * 1024;
 
@@ -254,7 +257,7 @@ void plan_decode(pa_plan_s *P, const std::vector<DecodeUnit> &units, std::vector
     // fewer pages.  Costs are in quarter blocks.  Cutting a run at a CTA
     // boundary makes at most one item per run plus one per CTA.
     const int64_t page_bytes = 2LL * kBlockSize * P->HG * P->D * (P->kv8 ? 1 : 2);   // K and V
-    const int64_t item_cost = (kPageCost * kItemBytes + page_bytes / 2) / page_bytes;
+    const int64_t item_cost = P->kv8 ? (kPageCost * kItemBytes + page_bytes / 2) / page_bytes : 0;
     const int64_t total_cost =
         kPageCost * total + item_cost * (static_cast<int64_t>(runs.size()) + ncta - 1);
     P->items.reserve(runs.size() + static_cast<size_t>(ncta));
