@@ -78,16 +78,18 @@ WORKLOADS = {
 # The configurations measured beside the main workload: (entry, workload, kv dtype).
 PER_CONFIG = [("tiny-1A", "tiny-1A", "bf16"), ("tiny-1B", "tiny", "bf16"), ("decode", "decode", "bf16"),
               ("decode-e4m3", "decode", "fp8"), ("long", "long", "bf16"), ("cascade", "cascade", "bf16"),
-              ("cascade-off", "cascade-off", "bf16"), ("prefill", "prefill", "bf16"), ("mixed-e4m3", "mixed", "fp8")]
+              ("cascade-off", "cascade-off", "bf16"), ("prefill", "prefill", "bf16"), ("mixed-e4m3", "mixed", "fp8"),
+              ("long-e4m3", "long", "fp8")]
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of a
 # kernel from one ncu capture, valid only while the kernel source is
 # unchanged (sha256 prefix of the file); the summaries are under profiles/.
 TRAFFIC = {
     # profiles/decode_kernel_decode-workload.md, profiles/decode_kernel_e4m3_decode-workload.md,
-    # profiles/extend_kernel_prefill-workload.md
+    # profiles/step_launches_mixed-workload.md, profiles/extend_kernel_prefill-workload.md
     ("decode", "decode", "bf16", "72d7bcb5f44d1173"): 643_443_456,
     ("decode", "decode", "fp8", "72d7bcb5f44d1173"): 323_953_920,
+    ("decode", "mixed", "bf16", "72d7bcb5f44d1173"): 4_681_763_584,
     ("extend", "prefill", "bf16", "e69a77fd500c5bc0"): 73_888_256,
 }
 KERNEL_SOURCES = {"decode": "paged_kv_cache_16_gb300/csrc/k_decode.cu",
