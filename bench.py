@@ -662,8 +662,9 @@ def run_ours(args, world, rank, local):
                                              "metadata image copy (not on the e2e path, which plans in C)"},
            "path": "pa_graph_step (the library's graph executor, one C call: fixed plan from the host metadata, "
                    "metadata image, graph launch); the graph copies the page-locked input image to the device, "
-                   "uploads the metadata, runs the step kernels and copies the output to page-locked memory; "
-                   "wall clock to the output's arrival"}
+                   "uploads the metadata and runs the step kernels, which store the output rows straight into "
+                   "page-locked host memory through its device mapping (d2h bytes: the output); wall clock to "
+                   "the output's arrival"}
     roof = m["roofline"]
     dominant = roof.get("decode") or roof.get("extend")
 

@@ -507,9 +507,13 @@ typedef struct {
     int32_t fused;                   /* 1: write + attention in one call   */
     /* Optional host I/O (all NULL / 0 for none).  host_in[i] (page-locked
      * HOST, in_bytes) is copied to device_in (DEVICE, in_bytes) at the start
-     * of graph i; out (out_bytes from its start) is copied to host_out[i]
-     * (page-locked HOST) at its end.  device_in normally spans the device
-     * buffers above, so that one copy brings a whole step's inputs in. */
+     * of graph i; device_in normally spans the device buffers above, so that
+     * one copy brings a whole step's inputs in.  Output: when out_bytes
+     * covers the whole out buffer (max_tokens * Hq * D * 2), graph i's
+     * kernels store the output rows straight into host_out[i] through its
+     * device mapping, during the step (device `out` is then not written);
+     * with a smaller out_bytes, out (out_bytes from its start) is copied to
+     * host_out[i] (page-locked HOST) at the end of graph i. */
     const void *host_in[2];
     void *device_in;
     size_t in_bytes;

@@ -77,12 +77,13 @@ pa_status check_buffers(const pa_graph_buffers &b) {
 }
 
 // The step's launches over the graph's buffers, as a caller would enqueue
-// them: fused write + attention, or slot mapping, cache write, attention.
-pa_status enqueue_step(const pa_graph_s *g, const pa_plan_t *plan, cudaStream_t s) {
+// them: fused write + attention, or slot mapping, cache write, attention;
+// the output rows go to `out`.
+pa_status enqueue_step(const pa_graph_s *g, const pa_plan_t *plan, void *out, cudaStream_t s) {
     const pa_graph_buffers &b = g->bufs;
     if (b.fused)
         return pa_attention_with_kv_update_launch(plan, b.q, b.key, b.value, b.key_cache, b.value_cache,
-                                                  b.block_table, g->slots, b.out, g->workspace, g->ws_bytes, s);
+                                                  b.block_table, g->slots, out, g->workspace, g->ws_bytes, s);
     const pa_batch_desc &m = g->model;
     pa_status st = pa_slot_mapping(b.query_start_loc, b.num_computed, b.block_table, g->shape.max_reqs,
                                    g->shape.max_tokens, m.max_blocks_per_req, m.block_size, g->slots, s);
@@ -96,8 +97,25 @@ pa_status enqueue_step(const pa_graph_s *g, const pa_plan_t *plan, cudaStream_t 
         st = pa_write_kv(b.key, b.value, g->slots, g->shape.max_tokens, m.num_heads_kv, m.head_dim, b.key_cache,
                          b.value_cache, num_slots, err, s);
     if (st != PA_OK) return st;
-    return pa_attention_launch(plan, b.q, b.key_cache, b.value_cache, b.block_table, b.out, g->workspace,
+    return pa_attention_launch(plan, b.q, b.key_cache, b.value_cache, b.block_table, out, g->workspace,
                                g->ws_bytes, s);
+}
+
+// The device address of host_out[i] when the kernels can store the output
+// straight into it: out_bytes spans the whole output buffer, so every row a
+// step can write lies inside it.  The stores cross the host link while the
+// step runs (the tiles' rows while the decode stream still streams) instead
+// of one copy after it.  nullptr: copy device `out` back at the end.
+void *direct_host_out(const pa_graph_s *g, int i) {
+    const pa_graph_buffers &b = g->bufs;
+    if (!b.out_bytes) return nullptr;
+    const size_t full = static_cast<size_t>(g->shape.max_tokens) * g->model.num_heads_q * g->model.head_dim * 2;
+    void *dptr = nullptr;
+    if (b.out_bytes < full || cudaHostGetDevicePointer(&dptr, b.host_out[i], 0) != cudaSuccess || !aligned16(dptr)) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return dptr;
 }
 
 // Capture graph i on the capture stream.  The capture is always ended, also
@@ -111,8 +129,9 @@ pa_status capture(pa_graph_s *g, int i) {
                           cudaSuccess)
         st = PA_ERR_CUDA;
     if (st == PA_OK) st = pa_upload_metadata_from(g->image[i], g->image_bytes, g->workspace, g->ws_bytes, g->cap);
-    if (st == PA_OK) st = enqueue_step(g, g->capture_plan, g->cap);
-    if (st == PA_OK && b.out_bytes &&
+    void *direct = direct_host_out(g, i);
+    if (st == PA_OK) st = enqueue_step(g, g->capture_plan, direct ? direct : b.out, g->cap);
+    if (st == PA_OK && b.out_bytes && !direct &&
         cudaMemcpyAsync(b.host_out[i], b.out, b.out_bytes, cudaMemcpyDeviceToHost, g->cap) != cudaSuccess)
         st = PA_ERR_CUDA;
     cudaGraph_t graph = nullptr;
