@@ -340,7 +340,7 @@ class NativeGraphStep:
     def __init__(self, *, num_heads_q, num_heads_kv, head_dim, num_blocks, max_blocks_per_req, softmax_scale,
                  max_tokens, max_reqs, key_cache, value_cache, max_extend_tiles=0, max_dequant_blocks=0,
                  max_partial_slots=0, kv_cache_dtype="bf16", k_scale=1.0, v_scale=1.0, num_sms=0, device="cuda",
-                 fused=True, host_io=False):
+                 fused=True, host_io=False, out_rows=None):
         dev = torch.device(device)
         self.device = dev
         self.host_io = host_io
@@ -354,10 +354,15 @@ class NativeGraphStep:
                 "block_table": self.inputs["block_table"], "key_cache": key_cache, "value_cache": value_cache}
         if host_io:
             self.host_in = [torch.zeros(lay["bytes"], dtype=torch.uint8).pin_memory() for _ in range(2)]
-            self.host_out = [torch.zeros(self.out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+            # out_rows < max_tokens: host buffers for the first out_rows rows
+            # only, which the graph copies back at its end (a whole-output
+            # buffer is stored into by the kernels instead)
+            rows = max_tokens if out_rows is None else out_rows
+            self.host_out = [torch.zeros((rows,) + tuple(self.out.shape[1:]), dtype=torch.bfloat16).pin_memory()
+                             for _ in range(2)]
             views = [_input_views(t, lay) for t in self.host_in]
             bufs.update(host_in=self.host_in, device_in=self._in, in_bytes=lay["bytes"], host_out=self.host_out,
-                        out_bytes=self.out.numel() * 2)
+                        out_bytes=self.host_out[0].numel() * 2)
         else:
             self.host_in = self.host_out = None
             meta = {"qsl": np.zeros(max_reqs + 1, dtype=np.int32), "seq_lens": np.zeros(max_reqs, dtype=np.int32),

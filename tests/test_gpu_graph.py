@@ -271,6 +271,17 @@ def test_native_graph_mixed_steps(kv, host_io):
                  max_dequant_blocks=256 if kv == "fp8" else 0)
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_native_graph_host_out_copy(kv):
+    """A host output buffer for fewer rows than the shape holds: the graph
+    copies those rows back at its end (a whole-output buffer is stored into
+    by the kernels instead); every step's rows fit in it."""
+    steps = mixed_steps(kv)
+    assert max(b.num_tokens for b in steps) <= 384
+    native_steps(steps, True, True, out_rows=384, max_tokens=512, max_reqs=8, max_extend_tiles=64,
+                 max_dequant_blocks=256 if kv == "fp8" else 0)
+
+
 def test_native_graph_cascade_steps():
     steps = []
     for i, (n, nb) in enumerate(((24, 16), (9, 8))):
