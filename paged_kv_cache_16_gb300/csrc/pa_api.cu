@@ -215,14 +215,16 @@ struct DecodeUnit {
 // fixed_ncta > 0: the grid has exactly that many CTAs; the shares past the
 // ones the work needs are empty.
 // Decode cut costs in quarters of one block's streaming time.  The fixed
-// cost of an item (about 1 us on GB300) is what one SM streams meanwhile
-// when the whole GPU streams (about 45 GB/s per SM): 48 KB, 1.5 blocks of
-// E4M3 codes for 8 kv heads of 128 dims.  It counts for E4M3 caches only,
+// cost of an item (about 1.3 us on GB300, fitted: 32-96 KB all cut the
+// E4M3 decode workload's kernel time by 5-6% against an equal cut, 64 KB
+// the most) is what one SM streams meanwhile when the whole GPU streams
+// (about 45 GB/s per SM): 64 KB, 2 blocks of E4M3 codes for 8 kv heads of
+// 128 dims.  It counts for E4M3 caches only,
 // whose consumers run close to their per-SM limit (about 52 GB/s); a bf16
 // SM streams twice what the HBM share needs and absorbs it (an item cost
 // there made the decode workload 1.3% slower).
 constexpr int64_t kPageCost = 4;
-constexpr int64_t kItemBytes = 48 * 1024;
+constexpr int64_t kItemBytes = 64 * 1024;
 
 void plan_decode(pa_plan_s *P, const std::vector<DecodeUnit> &units, std::vector<int32_t> &pieces,
                  std::vector<int32_t> &item_unit, int64_t work_ctas, int64_t fixed_ncta) {
