@@ -8,9 +8,10 @@
 //
 // GB300 mapping:
 //  * persistent CTAs, one per SM; the planner cuts the concatenation of all
-//    decode requests' key blocks into equal contiguous runs, one per CTA, so
-//    every SM streams the same number of bytes (runs that split a request
-//    produce partials for the merge kernel);
+//    decode requests' key blocks into contiguous runs, one per CTA, equal in
+//    bytes (E4M3 caches: equal in bytes plus a fixed cost per item), so every
+//    SM streams about the same (runs that split a request produce partials
+//    for the merge kernel);
 //  * one CTA serves HG kv heads; a producer warp streams each 16-token block
 //    as one TMA box per 128-byte column slice ([HG heads][16 rows][128 B],
 //    128-byte swizzle, each head's rows one contiguous tile) for K and for V
@@ -21,6 +22,9 @@
 //    rows of a 16x16 bf16 MMA tile (G <= 16), so each K/V row loaded from HBM
 //    is used by all G heads; S = Q K^T and O += P V run on the tensor cores
 //    (mma.sync), the online softmax in fp32 registers with quad shuffles.
+//    E4M3 caches: codes converted in registers to f16 MMA operands; items of
+//    at most 8 query rows compute the transposed products (keys as MMA rows),
+//    which halves their MMAs.
 #include <type_traits>
 
 #include "dev.cuh"
