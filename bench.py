@@ -87,9 +87,9 @@ PER_CONFIG = [("tiny-1A", "tiny-1A", "bf16"), ("tiny-1B", "tiny", "bf16"), ("dec
 TRAFFIC = {
     # profiles/decode_kernel_decode-workload.md, profiles/decode_kernel_e4m3_decode-workload.md,
     # profiles/step_launches_mixed-workload.md, profiles/extend_kernel_prefill-workload.md
-    ("decode", "decode", "bf16", "72d7bcb5f44d1173"): 643_443_456,
-    ("decode", "decode", "fp8", "72d7bcb5f44d1173"): 323_953_920,
-    ("decode", "mixed", "bf16", "72d7bcb5f44d1173"): 4_681_763_584,
+    ("decode", "decode", "bf16", "d98510bbbb11bb79"): 643_372_032,
+    ("decode", "decode", "fp8", "d98510bbbb11bb79"): 323_800_832,
+    ("decode", "mixed", "bf16", "d98510bbbb11bb79"): 4_686_585_600,
     ("extend", "prefill", "bf16", "e69a77fd500c5bc0"): 73_888_256,
 }
 KERNEL_SOURCES = {"decode": "paged_kv_cache_16_gb300/csrc/k_decode.cu",
