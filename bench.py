@@ -79,7 +79,7 @@ WORKLOADS = {
 PER_CONFIG = [("tiny-1A", "tiny-1A", "bf16"), ("tiny-1B", "tiny", "bf16"), ("decode", "decode", "bf16"),
               ("decode-e4m3", "decode", "fp8"), ("long", "long", "bf16"), ("cascade", "cascade", "bf16"),
               ("cascade-off", "cascade-off", "bf16"), ("prefill", "prefill", "bf16"), ("mixed-e4m3", "mixed", "fp8"),
-              ("long-e4m3", "long", "fp8")]
+              ("long-e4m3", "long", "fp8"), ("verify", "verify", "bf16"), ("verify-e4m3", "verify", "fp8")]
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of a
 # kernel from one ncu capture, valid only while the kernel source is

@@ -308,14 +308,17 @@ void plan_decode(pa_plan_s *P, const std::vector<DecodeUnit> &units, std::vector
 // the split-KV decode stream when a step has both (times in microseconds,
 // constants measured on GB300 at full clock).  The tiles are bound by the
 // tensor pipe of the SMs they run on, the decode stream by HBM once it has
-// enough SMs (each SM alone streams about 90 GB/s of bf16 blocks, 52 GB/s of
-// E4M3 codes), so running the two side by side on disjoint SMs costs about
+// enough SMs (each SM streams about 90 GB/s of bf16 blocks, 52 GB/s of E4M3
+// codes), so running the two side by side on disjoint SMs costs about
 // the longer of the two instead of their sum.
 // Side by side the two slow each other down a little (the tiles' K/V
-// re-reads and the decode stream share L2 and HBM): both constants below
-// were measured that way.
+// re-reads and the decode stream share L2 and HBM): the side constants below
+// were measured that way.  With E4M3 caches the tile stream first makes the
+// bf16 copies of the tiles' blocks (three bytes moved per code).
 constexpr double kTileStepUs = 1.85;          // one 128-key step of a 256-row tile on one SM
-constexpr double kTileStepSideUs = 2.15;      // the same beside the decode stream
+constexpr double kTileStepSideUs = 2.15;      // the same beside the bf16 decode stream
+constexpr double kTileStepSideFp8Us = 1.80;   // the same beside the E4M3 decode stream
+constexpr double kDequantUsPerBlock = 0.05;   // bf16 copy of one E4M3 block (K and V, all kv heads)
 constexpr double kHbmBytesPerUs = 7.0e6;      // decode stream at the HBM limit
 constexpr double kHbmSideBytesPerUs = 6.7e6;  // the same beside the tiles
 constexpr double kSmBf16BytesPerUs = 9.0e4;   // decode stream of one SM, bf16 caches
@@ -325,8 +328,11 @@ constexpr double kForkUs = 5.0;               // cost of the second stream (fork
 struct StepModel {
     double tile_units = 0, tile_max = 0;      // sum and largest tile cost (128-key steps + 1)
     double decode_bytes = 0, sm_rate = 0;
+    double side_step = kTileStepSideUs;       // tile step beside the decode stream
+    double tile_lead = 0;                     // tile-stream work before the tiles (E4M3 copies)
     double tiles(int ctas, bool side) const {
-        return ctas <= 0 ? 1e30 : std::max(tile_units / ctas, tile_max) * (side ? kTileStepSideUs : kTileStepUs);
+        return ctas <= 0 ? 1e30
+                         : tile_lead + std::max(tile_units / ctas, tile_max) * (side ? side_step : kTileStepUs);
     }
     double decode(int sms, bool side) const {
         return sms <= 0 ? 1e30
@@ -537,6 +543,10 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
         for (const DecodeUnit &u : units)
             model.decode_bytes += static_cast<double>(std::max(0, u.key_end - kb_keys)) * row_bytes;
         model.sm_rate = P->kv8 ? kSmFp8BytesPerUs : kSmBf16BytesPerUs;
+        if (P->kv8) {
+            model.side_step = kTileStepSideFp8Us;
+            model.tile_lead = kDequantUsPerBlock * P->num_scratch_blocks;
+        }
     }
     const int64_t n_tiles_all = static_cast<int64_t>(P->tiles.size());
     if (P->fixed && n_tiles_all > shape->max_extend_tiles) return PA_ERR_CAPACITY;
