@@ -551,7 +551,13 @@ def measure(name, batch, dev, steps, warmup, fused, world=1, clocks=None, e2e_st
 
     # ---- end to end through the C ABI with host buffers ----
     if e2e_steps:
-        gh = NativeGraphStep(**gs_args, key_cache=kc, value_cache=vc, host_io=True)
+        # the leading one-token and short rows (the decode stream's) come in
+        # first; the chunks' rows after them, while the decode stream runs
+        q_lens = np.diff(batch.query_start_loc)
+        lead = int(np.argmax(q_lens > 8)) if (q_lens > 8).any() else len(q_lens)
+        prefix = int(batch.query_start_loc[lead])
+        staged = prefix if 0 < prefix < T and not (q_lens[lead:] <= 8).any() else 0
+        gh = NativeGraphStep(**gs_args, key_cache=kc, value_cache=vc, host_io=True, decode_prefix_tokens=staged)
         for i in (0, 1):
             gh.fill_host_image(i, batch, batch.q, batch.key, batch.value)
         h2d = gh.host_in[0].numel()
@@ -566,11 +572,14 @@ def measure(name, batch, dev, steps, warmup, fused, world=1, clocks=None, e2e_st
             out_host = gh.output(T)
             if i >= 2:
                 times.append(time.perf_counter() - t0)
-        if not torch.equal(out_host, gs.out[:T].cpu()):
-            raise SystemExit(f"{name}: host-to-host step differs from the device-resident replay")
+        # a staged plan's SM split (and so its decode cut and merge rounding)
+        # may differ from the device-resident plan's; otherwise bit for bit
+        diff = float((out_host.float() - gs.out[:T].cpu().float()).abs().max()) if T else 0.0
+        if (diff > 0.05) if staged else not torch.equal(out_host, gs.out[:T].cpu()):
+            raise SystemExit(f"{name}: host-to-host step differs from the device-resident replay ({diff})")
         out["bits"] |= gh.check_errors()
         gh.destroy()
-        out["e2e"] = {"s": statistics.mean(times), "h2d": h2d, "d2h": d2h}
+        out["e2e"] = {"s": statistics.mean(times), "h2d": h2d, "d2h": d2h, "decode_prefix_tokens": staged}
     del gs, st
     return out
 
@@ -660,11 +669,13 @@ def run_ours(args, world, rank, local):
                                      "what": "c_planner: pa_plan_fixed alone on one host core; python_step_prep: "
                                              "the bench's per-step plan through the Python binding plus the "
                                              "metadata image copy (not on the e2e path, which plans in C)"},
+           "decode_prefix_tokens": m["e2e"]["decode_prefix_tokens"],
            "path": "pa_graph_step (the library's graph executor, one C call: fixed plan from the host metadata, "
-                   "metadata image, graph launch); the graph copies the page-locked input image to the device, "
-                   "uploads the metadata and runs the step kernels, which store the output rows straight into "
-                   "page-locked host memory through its device mapping (d2h bytes: the output); wall clock to "
-                   "the output's arrival"}
+                   "metadata image, graph launch); the graph copies the page-locked input image to the device "
+                   "(with decode_prefix_tokens > 0: the decode rows and metadata first, the chunk rows after "
+                   "them on a second stream, the decode stream starting in between), uploads the metadata and "
+                   "runs the step kernels, which store the output rows straight into page-locked host memory "
+                   "through its device mapping (d2h bytes: the output); wall clock to the output's arrival"}
     roof = m["roofline"]
     dominant = roof.get("decode") or roof.get("extend")
 

@@ -292,13 +292,27 @@ typedef struct {
     int32_t max_dequant_blocks;  /* FP8 caches: blocks those tiles read; 0 if none  */
     int32_t max_partial_slots;   /* partial results; 0 = room for every decode
                                     split plus one slot per (token, head group)    */
+    int32_t decode_prefix_tokens;/* 0, or P > 0: every query row of the decode
+                                    stream (one-token decode rows and the small
+                                    multi-token rows it also takes) lies in token
+                                    rows [0, P), and no row from P on is split
+                                    (merged from partials, as cascade steps with
+                                    chunk rows are), so rows from P on may arrive
+                                    later and are final when the tiles finish
+                                    (pa_attention_with_kv_update_launch_staged);
+                                    steps that break it are rejected with
+                                    PA_ERR_CAPACITY.  The SM split then assumes
+                                    those rows' q/key/value cross the host link
+                                    (~200 GB/s) before the tiles start and their
+                                    output rows cross it back after them       */
 } pa_fixed_shape;
 
 /*
  * pa_plan with a fixed shape (see pa_fixed_shape).  As pa_plan, plus
  * PA_ERR_INVALID_ARGUMENT for a NULL shape or a capacity < 0 (max_tokens and
  * max_reqs must be > 0), and PA_ERR_CAPACITY when this step needs more tokens,
- * requests, tiles, FP8 blocks or partial slots than the shape allows.  The
+ * requests, tiles, FP8 blocks or partial slots than the shape allows, or
+ * breaks the shape's decode_prefix_tokens.  The
  * workspace size depends on the shape and model fields only.  The decode
  * kernel always runs on num_sms x (CTAs per SM) CTAs.  With tensor-core tiles
  * (max_extend_tiles > 0, num_sms >= 2) the tiles always run on the library
@@ -390,6 +404,33 @@ pa_status pa_attention_with_kv_update_launch(const pa_plan_t *plan, const void *
                                              const void *value, void *key_cache, void *value_cache,
                                              const int32_t *block_table, int64_t *slot_mapping, void *out,
                                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Staged inputs: as pa_attention_with_kv_update_launch, for a fixed-shape
+ * plan with decode_prefix_tokens = P > 0, when rows P.. of q, key and value
+ * are still being written as the call's work starts on `stream` (a host copy
+ * in flight on another stream, say).  Rows [0, P) and everything else the
+ * call reads must be complete in stream order as usual; rows P.. must be
+ * complete once late_rows (a cudaEvent_t, recorded before this call) has
+ * fired.  The decode stream, which reads rows below P only, starts at once;
+ * the cache write of the rows from P on and the tensor-core tiles wait for
+ * late_rows on the library stream.  Without tiles beside the decode stream
+ * (no max_extend_tiles, or num_sms < 2) the whole step waits for late_rows.
+ * Results are those of pa_attention_with_kv_update_launch.
+ *   late_rows       cudaEvent_t (not NULL)
+ *   late_out_ready  optional cudaEvent_t: recorded once rows P.. of out are
+ *                   final (after the tiles, on the library stream; after the
+ *                   whole step when there is no second stream), so that the
+ *                   caller can copy them out while the decode stream runs on.
+ *                   Rows [0, P) are final in stream order at the call's end.
+ * Errors: as pa_attention_with_kv_update_launch, plus PA_ERR_INVALID_ARGUMENT
+ * for a NULL late_rows or a plan that is not fixed-shape with P > 0.
+ */
+pa_status pa_attention_with_kv_update_launch_staged(const pa_plan_t *plan, const void *q, const void *key,
+                                                    const void *value, void *key_cache, void *value_cache,
+                                                    const int32_t *block_table, int64_t *slot_mapping, void *out,
+                                                    void *workspace, size_t workspace_bytes, void *stream,
+                                                    void *late_rows, void *late_out_ready);
 
 /*
  * Zero newly allocated cache blocks ("vLLM 推理流程分析" §4: the scheduler

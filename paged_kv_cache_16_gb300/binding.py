@@ -37,7 +37,8 @@ EXPORTED = ("pa_plan", "pa_plan_destroy", "pa_plan_get_info", "pa_slot_mapping",
             "pa_plan_fixed", "pa_upload_metadata", "pa_attention_launch", "pa_zero_blocks",
             "pa_attention_with_kv_update", "pa_attention_with_kv_update_launch", "pa_plan_metadata_bytes",
             "pa_plan_copy_metadata", "pa_upload_metadata_from", "pa_graph_create", "pa_graph_step",
-            "pa_graph_turn", "pa_graph_wait", "pa_graph_workspace", "pa_graph_slot_mapping", "pa_graph_destroy")
+            "pa_graph_turn", "pa_graph_wait", "pa_graph_workspace", "pa_graph_slot_mapping", "pa_graph_destroy",
+            "pa_attention_with_kv_update_launch_staged")
 
 
 class PaError(RuntimeError):
@@ -104,6 +105,7 @@ class FixedShape(ctypes.Structure):
         ("max_extend_tiles", ctypes.c_int32),
         ("max_dequant_blocks", ctypes.c_int32),
         ("max_partial_slots", ctypes.c_int32),
+        ("decode_prefix_tokens", ctypes.c_int32),
     ]
 
 
@@ -180,6 +182,8 @@ def load(path: str | None = None, build_if_missing: bool = False) -> ctypes.CDLL
     lib.pa_attention_with_kv_update.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.pa_attention_with_kv_update_launch.restype = ctypes.c_int
     lib.pa_attention_with_kv_update_launch.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.pa_attention_with_kv_update_launch_staged.restype = ctypes.c_int
+    lib.pa_attention_with_kv_update_launch_staged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     lib.pa_zero_blocks.restype = ctypes.c_int
     lib.pa_zero_blocks.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp]
     lib.pa_plan_destroy.restype = None
@@ -295,19 +299,22 @@ def pa_plan(**kw) -> Plan:
     return Plan(handle.value, ws.value, keep)
 
 
-def _fixed_shape(max_tokens, max_reqs, max_extend_tiles=0, max_dequant_blocks=0, max_partial_slots=0):
+def _fixed_shape(max_tokens, max_reqs, max_extend_tiles=0, max_dequant_blocks=0, max_partial_slots=0,
+                 decode_prefix_tokens=0):
     fs = FixedShape()
     fs.max_tokens, fs.max_reqs = int(max_tokens), int(max_reqs)
     fs.max_extend_tiles, fs.max_dequant_blocks = int(max_extend_tiles), int(max_dequant_blocks)
     fs.max_partial_slots = int(max_partial_slots)
+    fs.decode_prefix_tokens = int(decode_prefix_tokens)
     return fs
 
 
 def pa_plan_fixed(*, max_tokens, max_reqs, max_extend_tiles=0, max_dequant_blocks=0, max_partial_slots=0,
-                  **kw) -> Plan:
+                  decode_prefix_tokens=0, **kw) -> Plan:
     """A fixed-shape plan (graph-capturable launches, see pa.h)."""
     d, keep = make_desc(**kw)
-    fs = _fixed_shape(max_tokens, max_reqs, max_extend_tiles, max_dequant_blocks, max_partial_slots)
+    fs = _fixed_shape(max_tokens, max_reqs, max_extend_tiles, max_dequant_blocks, max_partial_slots,
+                      decode_prefix_tokens)
     handle = ctypes.c_void_p()
     ws = ctypes.c_size_t()
     _check(load().pa_plan_fixed(ctypes.byref(d), ctypes.byref(fs), ctypes.byref(handle), ctypes.byref(ws)),
@@ -316,10 +323,11 @@ def pa_plan_fixed(*, max_tokens, max_reqs, max_extend_tiles=0, max_dequant_block
 
 
 def pa_plan_fixed_status(*, max_tokens, max_reqs, max_extend_tiles=0, max_dequant_blocks=0, max_partial_slots=0,
-                         **kw) -> int:
+                         decode_prefix_tokens=0, **kw) -> int:
     """Status code pa_plan_fixed returns (plan discarded)."""
     d, keep = make_desc(**kw)
-    fs = _fixed_shape(max_tokens, max_reqs, max_extend_tiles, max_dequant_blocks, max_partial_slots)
+    fs = _fixed_shape(max_tokens, max_reqs, max_extend_tiles, max_dequant_blocks, max_partial_slots,
+                      decode_prefix_tokens)
     handle = ctypes.c_void_p()
     ws = ctypes.c_size_t()
     st = load().pa_plan_fixed(ctypes.byref(d), ctypes.byref(fs), ctypes.byref(handle), ctypes.byref(ws))
@@ -423,6 +431,24 @@ def pa_attention_with_kv_update_launch(plan: Plan, q, key, value, key_cache, val
                                                      _ptr(value_cache), _ptr(block_table), _ptr(slot_mapping),
                                                      _ptr(out), _ptr(workspace), nbytes, _stream(stream)),
            "pa_attention_with_kv_update_launch")
+
+
+def pa_attention_with_kv_update_launch_staged(plan: Plan, q, key, value, key_cache, value_cache, block_table, out,
+                                              workspace, late_rows, slot_mapping=None, stream=None,
+                                              late_out_ready=None):
+    """As pa_attention_with_kv_update_launch; rows from the plan's decode
+    prefix on may still be written until late_rows (a torch.cuda.Event,
+    already recorded) fires.  late_out_ready (a torch.cuda.Event) is recorded
+    once out's rows from the prefix on are final."""
+    nbytes = workspace.numel() * workspace.element_size()
+    if late_out_ready is not None and not late_out_ready.cuda_event:
+        late_out_ready.record()   # torch creates the CUDA event at its first record
+    _check(load().pa_attention_with_kv_update_launch_staged(
+        plan.handle, _ptr(q), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache), _ptr(block_table),
+        _ptr(slot_mapping), _ptr(out), _ptr(workspace), nbytes, _stream(stream),
+        ctypes.c_void_p(late_rows.cuda_event if late_rows is not None else 0),
+        ctypes.c_void_p(late_out_ready.cuda_event if late_out_ready is not None else 0)),
+        "pa_attention_with_kv_update_launch_staged")
 
 
 def pa_zero_blocks(block_ids, key_cache, value_cache, device_error_word=None, stream=None):

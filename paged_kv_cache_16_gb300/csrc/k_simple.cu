@@ -154,15 +154,23 @@ __global__ void dequant_kernel(DequantParams p) {
 __global__ void write_runs_kernel(WriteParams p) {
     dev::grid_launch_dependents();
     dev::grid_dep_wait();
-    const int32_t nruns = p.counts[kCountWriteRuns];
-    const int64_t ntok = p.counts[kCountWriteTokens];
+    // runs [r0, nruns) and their tokens [e0, ntok)
+    int32_t r0 = 0, nruns = p.counts[kCountWriteRuns];
+    int64_t e0 = 0, ntok = p.counts[kCountWriteTokens];
+    if (p.part == 1) {
+        nruns = p.counts[kCountWriteRunsEarly];
+        ntok = p.counts[kCountWriteTokensEarly];
+    } else if (p.part == 2) {
+        r0 = p.counts[kCountWriteRunsEarly];
+        e0 = p.counts[kCountWriteTokensEarly];
+    }
     const int32_t cpr = p.kv8 ? p.row_elems / 16 : p.row_elems / 8;   // output chunks per row
-    const int64_t total = ntok * cpr;
+    const int64_t total = (ntok - e0) * cpr;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const int32_t e = static_cast<int32_t>(i / cpr);
-        const int32_t c = static_cast<int32_t>(i - static_cast<int64_t>(e) * cpr);
-        int32_t lo = 0, hi = nruns - 1;
+        const int32_t e = static_cast<int32_t>(e0 + i / cpr);
+        const int32_t c = static_cast<int32_t>(i % cpr);
+        int32_t lo = r0, hi = nruns - 1;
         while (lo < hi) {
             const int32_t mid = (lo + hi + 1) >> 1;
             if (p.runs[mid].wbegin <= e) lo = mid; else hi = mid - 1;
@@ -323,9 +331,9 @@ cudaError_t launch_upload(const void *src, void *dst, size_t bytes, cudaStream_t
     return cudaGetLastError();
 }
 
-cudaError_t launch_write_runs(int grid, const WriteParams &p, cudaStream_t stream) {
+cudaError_t launch_write_runs(int grid, const WriteParams &p, cudaStream_t stream, bool pdl) {
     if (grid <= 0) return cudaSuccess;
-    return launch_pdl(write_runs_kernel, dim3(grid), dim3(256), 0, stream, p);
+    return launch_ex(write_runs_kernel, dim3(grid), dim3(256), 0, stream, pdl, p);
 }
 
 cudaError_t launch_zero_blocks(const int32_t *ids, int32_t num_ids, int32_t num_blocks, int64_t block_bytes,

@@ -324,6 +324,12 @@ constexpr double kHbmSideBytesPerUs = 6.7e6;  // the same beside the tiles
 constexpr double kSmBf16BytesPerUs = 9.0e4;   // decode stream of one SM, bf16 caches
 constexpr double kSmFp8BytesPerUs = 5.2e4;    // decode stream of one SM, E4M3 caches
 constexpr double kForkUs = 5.0;               // cost of the second stream (fork, join, plain launches)
+constexpr double kHostLinkBytesPerUs = 2.0e5;  // page-locked host <-> device copy (staged inputs)
+// Share of the tiles' output copy-back counted on their path: the copy
+// overlaps the decode stream's tail, so only part of it lengthens the step
+// (mixed step from host memory to host memory: 1.018 / 0.997 / 1.059 ms
+// for 0 / 0.25 / 0.5, 1.100 ms for all of it).
+constexpr double kOutLeadWeight = 0.25;
 
 struct StepModel {
     double tile_units = 0, tile_max = 0;      // sum and largest tile cost (128-key steps + 1)
@@ -515,6 +521,12 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
             units.push_back({r, qsl[r] + j, n, d->num_computed_tokens[r] + j + n});
         }
     }
+    // staged inputs: the decode stream may read rows below the shape's
+    // decode prefix only
+    P->decode_prefix = P->fixed ? shape->decode_prefix_tokens : 0;
+    if (P->decode_prefix > 0)
+        for (const DecodeUnit &u : units)
+            if (u.t0 + u.n_tok > P->decode_prefix) return PA_ERR_CAPACITY;
     const int cps = std::max(1, decode_ctas_per_sm_static(P->D, P->HG, P->kv8));
 
     // ------------------------------------------ tile costs and the SM split
@@ -547,6 +559,12 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
             model.side_step = kTileStepSideFp8Us;
             model.tile_lead = kDequantUsPerBlock * P->num_scratch_blocks;
         }
+        // staged inputs: the tiles start once the rows from the decode prefix
+        // on (q, key, value) have crossed the host link, and their output
+        // rows cross it back after them
+        if (P->decode_prefix > 0 && P->decode_prefix < P->T)
+            model.tile_lead += static_cast<double>(P->T - P->decode_prefix) *
+                               (P->Hq + 2 * P->Hkv + kOutLeadWeight * P->Hq) * P->D * 2 / kHostLinkBytesPerUs;
     }
     const int64_t n_tiles_all = static_cast<int64_t>(P->tiles.size());
     if (P->fixed && n_tiles_all > shape->max_extend_tiles) return PA_ERR_CAPACITY;
@@ -633,6 +651,13 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
         P->write_tokens += w.n_tok;
         P->write_runs.push_back(w);
     }
+    // the leading runs that lie wholly below the decode prefix (the runs
+    // follow the token order) are stored before the decode stream starts
+    for (const WriteRun &w : P->write_runs) {
+        if (P->decode_prefix <= 0 || w.t0 + w.n_tok > P->decode_prefix) break;
+        ++P->write_runs_early;
+        P->write_tokens_early += w.n_tok;
+    }
 
     // ----------------------------------------------------- partial slots
     std::vector<int32_t> count(static_cast<size_t>(P->T) * P->n_groups, 0);
@@ -666,6 +691,9 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
             m.count = count[i];
             m.hq_begin = static_cast<int32_t>(i % P->n_groups) * P->HG * P->G;
             m.hq_count = P->HG * P->G;
+            // staged inputs: rows from the decode prefix on are final when
+            // the tiles finish, so none of them may be merged
+            if (P->decode_prefix > 0 && m.token >= P->decode_prefix) return PA_ERR_CAPACITY;
             P->merges.push_back(m);
         }
     }
@@ -752,6 +780,8 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     counts[kCountTokens] = P->T;
     counts[kCountWriteRuns] = static_cast<int32_t>(P->write_runs.size());
     counts[kCountWriteTokens] = P->write_tokens;
+    counts[kCountWriteRunsEarly] = P->write_runs_early;
+    counts[kCountWriteTokensEarly] = P->write_tokens_early;
     put(off_counts, counts, sizeof counts);
     put(P->off_part, P->part_offset.data(), P->part_offset.size() * sizeof(int32_t));
     put(P->off_cta, P->cta_begin.data(), P->cta_begin.size() * sizeof(int32_t));
@@ -875,10 +905,16 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
          !make_map(&tm_v, value_cache, P->D, P->Hkv, rows, 1, kBlockSize)))
         return PA_ERR_CUDA;
 
+    const bool fork = P->fork && allow_fork && P->cap_tiles > 0;
+    // staged inputs (rows from the decode prefix on complete at late_rows):
+    // with a second stream only the tiles' side waits; without one, all
+    const bool staged = update.late_rows != nullptr;
+    if (staged && !fork && cudaStreamWaitEvent(stream, update.late_rows, 0) != cudaSuccess) return PA_ERR_CUDA;
+    WriteParams wp{};
+    int write_grid = 0;
     if (update.key != nullptr && P->cap_runs > 0) {
         // fused cache update: extend rows' new tokens first (the tiles read
         // them); decode rows' are stored by the decode kernel itself
-        WriteParams wp{};
         wp.key = static_cast<const uint16_t *>(update.key);
         wp.value = static_cast<const uint16_t *>(update.value);
         wp.key_cache = const_cast<void *>(key_cache);
@@ -896,14 +932,16 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
         wp.v_scale = P->v_scale;
         const int64_t chunks = static_cast<int64_t>(std::max(1, P->fixed ? P->cap_tokens : P->write_tokens)) *
                                (P->kv8 ? wp.row_elems / 16 : wp.row_elems / 8);
-        const int grid = static_cast<int>(std::min<int64_t>((chunks + 255) / 256, 16 * sms));
-        if (launch_write_runs(grid, wp, stream) != cudaSuccess) return PA_ERR_CUDA;
+        write_grid = static_cast<int>(std::min<int64_t>((chunks + 255) / 256, 16 * sms));
+        // staged: here the runs below the decode prefix (small rows the
+        // decode stream reads), the rest on the tile stream after late_rows
+        wp.part = staged && fork ? 1 : 0;
+        if (launch_write_runs(write_grid, wp, stream) != cudaSuccess) return PA_ERR_CUDA;
     }
     // Side by side: the tiles (and, for E4M3 caches, the bf16 copies of their
     // blocks) go to a second stream that starts after everything enqueued so
     // far (metadata upload, write of the extend rows), while the decode kernel
     // runs on the other SMs; the merge waits for both.
-    const bool fork = P->fork && allow_fork && P->cap_tiles > 0;
     cudaStream_t tile_stream = stream;
     SideStream *side = nullptr;
     if (fork) {
@@ -912,6 +950,12 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
             cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
             return PA_ERR_CUDA;
         tile_stream = side->stream;
+        if (staged) {
+            if (cudaStreamWaitEvent(tile_stream, update.late_rows, 0) != cudaSuccess) return PA_ERR_CUDA;
+            wp.part = 2;
+            if (write_grid > 0 && launch_write_runs(write_grid, wp, tile_stream, false) != cudaSuccess)
+                return PA_ERR_CUDA;
+        }
     }
     if (P->cap_tiles > 0) {
         // E4M3: the tiles read bf16 copies of their blocks, made here
@@ -964,6 +1008,10 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
         if (launch_extend(P->D, P->ext_ctas, tm_q, tm_tk, tm_tv, ep, tile_stream, !fork) != cudaSuccess)
             return PA_ERR_CUDA;
         if (rec(1, false, tile_stream) != cudaSuccess) return PA_ERR_CUDA;
+        // staged: the rows from the decode prefix on are the tiles' alone
+        // (no merge row), final here
+        if (fork && update.late_out_ready && cudaEventRecord(update.late_out_ready, tile_stream) != cudaSuccess)
+            return PA_ERR_CUDA;
         if (fork && cudaEventRecord(side->join, tile_stream) != cudaSuccess) return PA_ERR_CUDA;
     }
     if (P->ncta > 0) {
@@ -1012,6 +1060,8 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
         if (launch_merge(P->D, grid, mp, stream, !fork) != cudaSuccess) return PA_ERR_CUDA;
         if (rec(2, false, stream) != cudaSuccess) return PA_ERR_CUDA;
     }
+    if (!fork && update.late_out_ready && cudaEventRecord(update.late_out_ready, stream) != cudaSuccess)
+        return PA_ERR_CUDA;
     return PA_OK;
 }
 
@@ -1055,7 +1105,7 @@ pa_status pa_plan_fixed(const pa_batch_desc *desc, const pa_fixed_shape *shape, 
     if (desc == nullptr || shape == nullptr || out == nullptr || workspace_bytes == nullptr)
         return PA_ERR_INVALID_ARGUMENT;
     if (shape->max_tokens <= 0 || shape->max_reqs <= 0 || shape->max_extend_tiles < 0 ||
-        shape->max_dequant_blocks < 0 || shape->max_partial_slots < 0)
+        shape->max_dequant_blocks < 0 || shape->max_partial_slots < 0 || shape->decode_prefix_tokens < 0)
         return PA_ERR_INVALID_ARGUMENT;
     pa_status st = validate(desc);
     if (st != PA_OK) return st;
@@ -1271,6 +1321,29 @@ pa_status pa_attention_with_kv_update_launch(const pa_plan_t *plan, const void *
     u.key = key;
     u.value = value;
     u.slots_out = slot_mapping;
+    return enqueue_attention(P, q, key_cache, value_cache, block_table, out, static_cast<uint8_t *>(workspace),
+                             static_cast<cudaStream_t>(stream_), false, u);
+}
+
+pa_status pa_attention_with_kv_update_launch_staged(const pa_plan_t *plan, const void *q, const void *key,
+                                                    const void *value, void *key_cache, void *value_cache,
+                                                    const int32_t *block_table, int64_t *slot_mapping, void *out,
+                                                    void *workspace, size_t workspace_bytes, void *stream_,
+                                                    void *late_rows, void *late_out_ready) {
+    if (!plan || !late_rows || !plan->fixed || plan->decode_prefix <= 0) return PA_ERR_INVALID_ARGUMENT;
+    pa_plan_s *P = const_cast<pa_plan_s *>(plan);
+    pa_status st = check_launch_args(P, q, key_cache, value_cache, block_table, out, workspace, workspace_bytes);
+    if (st != PA_OK) return st;
+    if (!key || !value || !aligned(key, 16) || !aligned(value, 16) || (slot_mapping && !aligned(slot_mapping, 8)))
+        return PA_ERR_INVALID_ARGUMENT;
+    std::lock_guard<std::mutex> lock(P->mu);
+    if ((st = prepare_plan(P)) != PA_OK) return st;
+    KvUpdate u;
+    u.key = key;
+    u.value = value;
+    u.slots_out = slot_mapping;
+    u.late_rows = static_cast<cudaEvent_t>(late_rows);
+    u.late_out_ready = static_cast<cudaEvent_t>(late_out_ready);
     return enqueue_attention(P, q, key_cache, value_cache, block_table, out, static_cast<uint8_t *>(workspace),
                              static_cast<cudaStream_t>(stream_), false, u);
 }

@@ -10,9 +10,12 @@
 // Built on the public C ABI only (pa_plan_fixed, pa_upload_metadata[_from],
 // pa_slot_mapping, pa_write_kv[_fp8], pa_attention[_with_kv_update]_launch):
 // the graphs hold exactly the launches a caller capturing by hand would get.
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <new>
+#include <utility>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -33,6 +36,15 @@ struct pa_graph_s {
     bool launched[2] = {false, false};
     cudaStream_t cap = nullptr;
     int turn = 0;
+    // staged host input (shape.decode_prefix_tokens > 0): the bytes of the
+    // input image the decode stream needs are copied first, the rows from the
+    // prefix on after them on a second stream, and only the work that reads
+    // those rows waits for them
+    bool staged = false;
+    std::vector<std::pair<size_t, size_t>> early, late;   // [begin, end) byte ranges of the image
+    cudaStream_t cap_late = nullptr;
+    cudaEvent_t early_in = nullptr, late_in = nullptr;
+    cudaEvent_t late_out = nullptr, late_copied = nullptr;   // rows from the prefix on: final, copied back
 };
 
 namespace {
@@ -108,7 +120,7 @@ pa_status enqueue_step(const pa_graph_s *g, const pa_plan_t *plan, void *out, cu
 // of one copy after it.  nullptr: copy device `out` back at the end.
 void *direct_host_out(const pa_graph_s *g, int i) {
     const pa_graph_buffers &b = g->bufs;
-    if (!b.out_bytes) return nullptr;
+    if (!b.out_bytes || g->staged) return nullptr;
     const size_t full = static_cast<size_t>(g->shape.max_tokens) * g->model.num_heads_q * g->model.head_dim * 2;
     void *dptr = nullptr;
     if (b.out_bytes < full || cudaHostGetDevicePointer(&dptr, b.host_out[i], 0) != cudaSuccess || !aligned16(dptr)) {
@@ -118,22 +130,93 @@ void *direct_host_out(const pa_graph_s *g, int i) {
     return dptr;
 }
 
+// Staging of the host input: the rows from decode_prefix_tokens on of q, key
+// and value, where those buffers lie inside device_in, are copied late;
+// everything else in the image (the other rows, the metadata arrays) first.
+void plan_staging(pa_graph_s *g) {
+    const pa_graph_buffers &b = g->bufs;
+    const int64_t P = g->shape.decode_prefix_tokens, T = g->shape.max_tokens;
+    if (!b.fused || !b.in_bytes || P <= 0 || P >= T) return;
+    const size_t dq = static_cast<size_t>(g->model.num_heads_q) * g->model.head_dim * 2;
+    const size_t dkv = static_cast<size_t>(g->model.num_heads_kv) * g->model.head_dim * 2;
+    const uintptr_t base = reinterpret_cast<uintptr_t>(b.device_in);
+    std::vector<std::pair<size_t, size_t>> late;
+    for (const auto &buf : {std::make_pair(b.q, dq), std::make_pair(b.key, dkv), std::make_pair(b.value, dkv)}) {
+        const uintptr_t p = reinterpret_cast<uintptr_t>(buf.first);
+        if (p < base || p + buf.second * T > base + b.in_bytes) return;   // not inside the image: one copy
+        late.emplace_back(p - base + buf.second * P, p - base + buf.second * T);
+    }
+    std::sort(late.begin(), late.end());
+    for (size_t k = 1; k < late.size(); ++k)
+        if (late[k].first < late[k - 1].second) return;                  // overlapping buffers: one copy
+    size_t at = 0;
+    for (const auto &r : late) {
+        if (r.first > at) g->early.emplace_back(at, r.first);
+        at = r.second;
+    }
+    if (at < b.in_bytes) g->early.emplace_back(at, b.in_bytes);
+    g->late = late;
+    g->staged = true;
+}
+
+cudaError_t copy_ranges(const std::vector<std::pair<size_t, size_t>> &ranges, void *dst, const void *src,
+                        cudaStream_t s) {
+    for (const auto &r : ranges) {
+        const cudaError_t e = cudaMemcpyAsync(static_cast<char *>(dst) + r.first, static_cast<const char *>(src) + r.first,
+                                              r.second - r.first, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 // Capture graph i on the capture stream.  The capture is always ended, also
 // after a failed call inside it.
 pa_status capture(pa_graph_s *g, int i) {
     const pa_graph_buffers &b = g->bufs;
     if (cudaStreamBeginCapture(g->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return PA_ERR_CUDA;
     pa_status st = PA_OK;
-    // one copy each way (splitting them over parallel streams measured slower)
-    if (b.in_bytes && cudaMemcpyAsync(b.device_in, b.host_in[i], b.in_bytes, cudaMemcpyHostToDevice, g->cap) !=
-                          cudaSuccess)
+    // one copy each way (splitting them over parallel streams measured
+    // slower), or, staged, the early part and then the late rows
+    if (g->staged) {
+        if (copy_ranges(g->early, b.device_in, b.host_in[i], g->cap) != cudaSuccess ||
+            cudaEventRecord(g->early_in, g->cap) != cudaSuccess ||
+            cudaStreamWaitEvent(g->cap_late, g->early_in, 0) != cudaSuccess ||
+            copy_ranges(g->late, b.device_in, b.host_in[i], g->cap_late) != cudaSuccess ||
+            cudaEventRecord(g->late_in, g->cap_late) != cudaSuccess)
+            st = PA_ERR_CUDA;
+    } else if (b.in_bytes && cudaMemcpyAsync(b.device_in, b.host_in[i], b.in_bytes, cudaMemcpyHostToDevice,
+                                             g->cap) != cudaSuccess) {
         st = PA_ERR_CUDA;
+    }
     if (st == PA_OK) st = pa_upload_metadata_from(g->image[i], g->image_bytes, g->workspace, g->ws_bytes, g->cap);
     void *direct = direct_host_out(g, i);
-    if (st == PA_OK) st = enqueue_step(g, g->capture_plan, direct ? direct : b.out, g->cap);
-    if (st == PA_OK && b.out_bytes && !direct &&
-        cudaMemcpyAsync(b.host_out[i], b.out, b.out_bytes, cudaMemcpyDeviceToHost, g->cap) != cudaSuccess)
+    void *out = direct ? direct : b.out;
+    // staged with a whole-output host buffer: the rows from the prefix on are
+    // copied back on the second stream as soon as the tiles have written
+    // them, while the decode stream still runs; rows [0, P) after the step
+    const size_t row_bytes = static_cast<size_t>(g->model.num_heads_q) * g->model.head_dim * 2;
+    const size_t full = static_cast<size_t>(g->shape.max_tokens) * row_bytes;
+    const bool split_back = g->staged && b.out_bytes >= full;
+    if (st == PA_OK && g->staged)
+        st = pa_attention_with_kv_update_launch_staged(g->capture_plan, b.q, b.key, b.value, b.key_cache,
+                                                        b.value_cache, b.block_table, g->slots, out, g->workspace,
+                                                        g->ws_bytes, g->cap, g->late_in,
+                                                        split_back ? g->late_out : nullptr);
+    else if (st == PA_OK)
+        st = enqueue_step(g, g->capture_plan, out, g->cap);
+    if (st == PA_OK && split_back) {
+        const size_t early = static_cast<size_t>(g->shape.decode_prefix_tokens) * row_bytes;
+        if (cudaStreamWaitEvent(g->cap_late, g->late_out, 0) != cudaSuccess ||
+            cudaMemcpyAsync(static_cast<char *>(b.host_out[i]) + early, static_cast<const char *>(b.out) + early,
+                            full - early, cudaMemcpyDeviceToHost, g->cap_late) != cudaSuccess ||
+            cudaEventRecord(g->late_copied, g->cap_late) != cudaSuccess ||
+            cudaMemcpyAsync(b.host_out[i], b.out, early, cudaMemcpyDeviceToHost, g->cap) != cudaSuccess ||
+            cudaStreamWaitEvent(g->cap, g->late_copied, 0) != cudaSuccess)
+            st = PA_ERR_CUDA;
+    } else if (st == PA_OK && b.out_bytes && !direct &&
+               cudaMemcpyAsync(b.host_out[i], b.out, b.out_bytes, cudaMemcpyDeviceToHost, g->cap) != cudaSuccess) {
         st = PA_ERR_CUDA;
+    }
     cudaGraph_t graph = nullptr;
     const cudaError_t end = cudaStreamEndCapture(g->cap, &graph);
     if (st == PA_OK && (end != cudaSuccess || graph == nullptr)) st = PA_ERR_CUDA;
@@ -177,6 +260,13 @@ pa_status pa_graph_create(const pa_batch_desc *desc, const pa_fixed_shape *shape
     for (int i = 0; ok && i < 2; ++i)
         ok = cudaHostAlloc(&g->image[i], g->image_bytes, cudaHostAllocMapped) == cudaSuccess &&
              cudaEventCreateWithFlags(&g->done[i], cudaEventDisableTiming) == cudaSuccess;
+    plan_staging(g);
+    if (ok && g->staged)
+        ok = cudaStreamCreateWithFlags(&g->cap_late, cudaStreamNonBlocking) == cudaSuccess &&
+             cudaEventCreateWithFlags(&g->early_in, cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&g->late_in, cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&g->late_out, cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&g->late_copied, cudaEventDisableTiming) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
         pa_graph_destroy(g);
@@ -243,6 +333,14 @@ void pa_graph_destroy(pa_graph_t *g) {
         cudaStreamSynchronize(g->cap);
         cudaStreamDestroy(g->cap);
     }
+    if (g->cap_late) {
+        cudaStreamSynchronize(g->cap_late);
+        cudaStreamDestroy(g->cap_late);
+    }
+    if (g->early_in) cudaEventDestroy(g->early_in);
+    if (g->late_in) cudaEventDestroy(g->late_in);
+    if (g->late_out) cudaEventDestroy(g->late_out);
+    if (g->late_copied) cudaEventDestroy(g->late_copied);
     if (g->workspace) cudaFree(g->workspace);
     if (g->slots) cudaFree(g->slots);
     if (g->capture_plan) pa_plan_destroy(g->capture_plan);

@@ -183,6 +183,8 @@ enum MetaCount : int {
     kCountTokens = 3,
     kCountWriteRuns = 4,     // extend rows whose new K/V the fused write kernel stores
     kCountWriteTokens = 5,   // their tokens in total
+    kCountWriteRunsEarly = 6,    // leading runs wholly below the decode prefix (staged inputs)
+    kCountWriteTokensEarly = 7,  // their tokens
     kNumCounts = 8
 };
 
@@ -214,6 +216,7 @@ struct WriteParams {
     int32_t num_blocks;
     int32_t kv8;
     float k_scale, v_scale;     // E4M3 quantisation (code of x / scale)
+    int32_t part;               // runs to store: 0 all, 1 the early ones, 2 the rest
 };
 
 // Launch with programmatic stream serialisation when `pdl` (the kernel calls
@@ -268,7 +271,7 @@ cudaError_t launch_merge(int head_dim, int grid, const MergeParams &p, cudaStrea
 // to device memory with a kernel.
 cudaError_t launch_upload(const void *src, void *dst, size_t bytes, cudaStream_t stream);
 // Fused write of extend-row tokens: grid-stride over their 16-element chunks.
-cudaError_t launch_write_runs(int grid, const WriteParams &p, cudaStream_t stream);
+cudaError_t launch_write_runs(int grid, const WriteParams &p, cudaStream_t stream, bool pdl = true);
 // Zero the K and V entries of the listed blocks (ids < 0 skipped).
 cudaError_t launch_zero_blocks(const int32_t *ids, int32_t num_ids, int32_t num_blocks, int64_t block_bytes,
                                void *key_cache, void *value_cache, int32_t *err, cudaStream_t stream);

@@ -30,6 +30,9 @@ struct pa_plan_s {
     bool fork = false;                        // tiles on a second stream, beside the decode kernel
     std::vector<pa::WriteRun> write_runs;     // extend rows (fused cache update)
     int32_t write_tokens = 0;
+    int32_t decode_prefix = 0;                // fixed shapes: decode-stream rows lie below it (0: no bound)
+    int32_t write_runs_early = 0;             // leading runs wholly below decode_prefix
+    int32_t write_tokens_early = 0;           // and their tokens
     std::vector<int32_t> scratch_table;       // E4M3: [rows][max_blocks] bf16 scratch block ids
     std::vector<pa::DequantItem> dequant;     // E4M3: blocks to expand each call
     int32_t num_scratch_blocks = 0;
@@ -77,6 +80,11 @@ struct KvUpdate {
     const void *key = nullptr;      // [T][Hkv][D] bf16; null = no update
     const void *value = nullptr;
     int64_t *slots_out = nullptr;   // optional [T]
+    // staged inputs: rows from P->decode_prefix on are complete once this
+    // event fires; their cache write and the tiles wait for it on the side
+    // stream (null: every input is complete in stream order)
+    cudaEvent_t late_rows = nullptr;
+    cudaEvent_t late_out_ready = nullptr;   // optional: recorded once out rows from the prefix on are final
 };
 
 // allow_fork = false keeps every launch on `stream` (a plan whose tiles run

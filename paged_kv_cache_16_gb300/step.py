@@ -340,7 +340,7 @@ class NativeGraphStep:
     def __init__(self, *, num_heads_q, num_heads_kv, head_dim, num_blocks, max_blocks_per_req, softmax_scale,
                  max_tokens, max_reqs, key_cache, value_cache, max_extend_tiles=0, max_dequant_blocks=0,
                  max_partial_slots=0, kv_cache_dtype="bf16", k_scale=1.0, v_scale=1.0, num_sms=0, device="cuda",
-                 fused=True, host_io=False, out_rows=None):
+                 fused=True, host_io=False, out_rows=None, decode_prefix_tokens=0):
         dev = torch.device(device)
         self.device = dev
         self.host_io = host_io
@@ -374,7 +374,8 @@ class NativeGraphStep:
                  "num_computed": v["num_computed"].numpy(), "block_table": v["block_table"].numpy()} for v in views]
         self.graph = binding.NativeGraph(
             shape=dict(max_tokens=max_tokens, max_reqs=max_reqs, max_extend_tiles=max_extend_tiles,
-                       max_dequant_blocks=max_dequant_blocks, max_partial_slots=max_partial_slots),
+                       max_dequant_blocks=max_dequant_blocks, max_partial_slots=max_partial_slots,
+                       decode_prefix_tokens=decode_prefix_tokens),
             host=host, buffers=bufs, num_reqs=0, fused=fused, num_heads_q=num_heads_q, num_heads_kv=num_heads_kv,
             head_dim=head_dim, num_blocks=num_blocks, softmax_scale=softmax_scale, num_sms=num_sms,
             kv_cache_dtype=binding.PA_KV_FP8_E4M3 if kv_cache_dtype == "fp8" else binding.PA_KV_BF16,

@@ -8,6 +8,7 @@ import numpy as np
 import pytest
 
 from paged_kv_cache_16_gb300 import binding, build, workloads
+from paged_kv_cache_16_gb300.workloads import make_batch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "pa.h")
@@ -311,6 +312,55 @@ def test_fixed_plan_tile_capacity(lib):
                                         max_dequant_blocks=4, **fp8) == binding.PA_ERR_CAPACITY
     assert binding.pa_plan_fixed_status(max_tokens=1024, max_reqs=64, max_extend_tiles=128,
                                         max_dequant_blocks=4096, **fp8) == binding.PA_OK
+
+
+def test_fixed_plan_decode_prefix(lib):
+    """decode_prefix_tokens bounds the rows the decode stream reads: a step
+    whose decode or small multi-token rows reach past it is refused; the
+    chunk rows may lie anywhere."""
+    make = lambda ql, sl: make_batch(name="prefix", num_heads_q=32, num_heads_kv=8, head_dim=128, q_lens=ql,
+                                     seq_lens=sl, num_blocks=600, seed=5, max_blocks_per_req=64)
+    shape = dict(max_tokens=512, max_reqs=8, max_extend_tiles=64)
+    first = make([1, 3, 1, 200], [90, 40, 700, 260])          # decode-stream rows: tokens 0..4
+    assert binding.pa_plan_fixed_status(**shape, decode_prefix_tokens=5, **desc(first)) == binding.PA_OK
+    assert binding.pa_plan_fixed_status(**shape, decode_prefix_tokens=4, **desc(first)) == binding.PA_ERR_CAPACITY
+    assert binding.pa_plan_fixed_status(**shape, decode_prefix_tokens=-1, **desc(first)) == \
+        binding.PA_ERR_INVALID_ARGUMENT
+    late = make([200, 1], [260, 90])                           # the decode row is token 200
+    assert binding.pa_plan_fixed_status(**shape, decode_prefix_tokens=16, **desc(late)) == binding.PA_ERR_CAPACITY
+    assert binding.pa_plan_fixed_status(**shape, decode_prefix_tokens=201, **desc(late)) == binding.PA_OK
+    assert binding.pa_plan_fixed_status(**shape, **desc(late)) == binding.PA_OK
+
+
+def test_fixed_plan_decode_prefix_no_merged_late_rows(lib):
+    """Rows from the decode prefix on must be final when the tiles finish: a
+    cascade step with a chunk row (whose rows are merged from prefix and
+    suffix partials) is refused when that row lies past the prefix."""
+    b = make_batch(name="cascade-chunk", num_heads_q=32, num_heads_kv=8, head_dim=128, q_lens=[1, 1, 40],
+                   seq_lens=[300, 300, 400], num_blocks=600, seed=6, max_blocks_per_req=64,
+                   shared_prefix=[([0, 1, 2], 4)], num_common_prefix_blocks=4)
+    shape = dict(max_tokens=512, max_reqs=8, max_extend_tiles=64, max_partial_slots=4096)
+    assert binding.pa_plan_fixed_status(**shape, **desc(b)) == binding.PA_OK
+    assert binding.pa_plan_fixed_status(**shape, decode_prefix_tokens=2, **desc(b)) == binding.PA_ERR_CAPACITY
+    assert binding.pa_plan_fixed_status(**shape, decode_prefix_tokens=42, **desc(b)) == binding.PA_OK
+
+
+def test_staged_launch_argument_checks(lib):
+    """The staged launch needs a fixed-shape plan with a decode prefix and an
+    event; both are checked before anything is enqueued."""
+    b = make_batch(name="prefix", num_heads_q=32, num_heads_kv=8, head_dim=128, q_lens=[1, 200],
+                   seq_lens=[90, 260], num_blocks=600, seed=5, max_blocks_per_req=64)
+    shape = dict(max_tokens=512, max_reqs=8, max_extend_tiles=64)
+    f = binding.load().pa_attention_with_kv_update_launch_staged
+    fake = 1 << 20   # aligned, never dereferenced on these paths
+    plain = binding.pa_plan_fixed(**shape, **desc(b))
+    staged = binding.pa_plan_fixed(**shape, decode_prefix_tokens=1, **desc(b))
+    eager = binding.pa_plan(**desc(b))
+    args = lambda plan, ev: (plan.handle, fake, fake, fake, fake, fake, fake, None, fake, fake, 1 << 40, None, ev,
+                             None)
+    assert f(*args(plain, fake)) == binding.PA_ERR_INVALID_ARGUMENT
+    assert f(*args(eager, fake)) == binding.PA_ERR_INVALID_ARGUMENT
+    assert f(*args(staged, None)) == binding.PA_ERR_INVALID_ARGUMENT
 
 
 def test_zero_blocks_argument_checks(lib):
