@@ -638,9 +638,10 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     plan_decode(P, units, pieces, item_unit, decode_work_ctas, P->fixed ? static_cast<int64_t>(P->num_sms) * cps : 0);
 
     // ------------------------------- fused cache update of extend rows
+    // the small rows (read by the decode stream) first, then the extend rows
+    // (read by the tiles only), each in token order
     std::vector<int32_t> multi_rows(small_rows);
     multi_rows.insert(multi_rows.end(), extend_rows.begin(), extend_rows.end());
-    std::sort(multi_rows.begin(), multi_rows.end());
     for (int32_t r : multi_rows) {
         WriteRun w{};
         w.t0 = qsl[r];
@@ -651,13 +652,10 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
         P->write_tokens += w.n_tok;
         P->write_runs.push_back(w);
     }
-    // the leading runs that lie wholly below the decode prefix (the runs
-    // follow the token order) are stored before the decode stream starts
-    for (const WriteRun &w : P->write_runs) {
-        if (P->decode_prefix <= 0 || w.t0 + w.n_tok > P->decode_prefix) break;
-        ++P->write_runs_early;
-        P->write_tokens_early += w.n_tok;
-    }
+    // the small rows' runs are stored before the decode stream starts; with a
+    // second stream the extend rows' runs are stored there, before the tiles
+    P->write_runs_early = static_cast<int32_t>(small_rows.size());
+    for (int32_t k = 0; k < P->write_runs_early; ++k) P->write_tokens_early += P->write_runs[k].n_tok;
 
     // ----------------------------------------------------- partial slots
     std::vector<int32_t> count(static_cast<size_t>(P->T) * P->n_groups, 0);
@@ -913,8 +911,9 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
     WriteParams wp{};
     int write_grid = 0;
     if (update.key != nullptr && P->cap_runs > 0) {
-        // fused cache update: extend rows' new tokens first (the tiles read
-        // them); decode rows' are stored by the decode kernel itself
+        // fused cache update of the small and extend rows' new tokens (the
+        // decode stream and the tiles read them); one-token decode rows' are
+        // stored by the decode kernel itself
         wp.key = static_cast<const uint16_t *>(update.key);
         wp.value = static_cast<const uint16_t *>(update.value);
         wp.key_cache = const_cast<void *>(key_cache);
@@ -933,10 +932,13 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
         const int64_t chunks = static_cast<int64_t>(std::max(1, P->fixed ? P->cap_tokens : P->write_tokens)) *
                                (P->kv8 ? wp.row_elems / 16 : wp.row_elems / 8);
         write_grid = static_cast<int>(std::min<int64_t>((chunks + 255) / 256, 16 * sms));
-        // staged: here the runs below the decode prefix (small rows the
-        // decode stream reads), the rest on the tile stream after late_rows
-        wp.part = staged && fork ? 1 : 0;
-        if (launch_write_runs(write_grid, wp, stream) != cudaSuccess) return PA_ERR_CUDA;
+        // with a second stream: here the small rows' runs (the decode stream
+        // reads them), the extend rows' on the tile stream before the tiles
+        // (after late_rows when staged); without one, all of them here
+        wp.part = fork ? 1 : 0;
+        if ((!fork || P->fixed || P->write_runs_early > 0) &&
+            launch_write_runs(write_grid, wp, stream) != cudaSuccess)
+            return PA_ERR_CUDA;
     }
     // Side by side: the tiles (and, for E4M3 caches, the bf16 copies of their
     // blocks) go to a second stream that starts after everything enqueued so
@@ -950,12 +952,10 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
             cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
             return PA_ERR_CUDA;
         tile_stream = side->stream;
-        if (staged) {
-            if (cudaStreamWaitEvent(tile_stream, update.late_rows, 0) != cudaSuccess) return PA_ERR_CUDA;
-            wp.part = 2;
-            if (write_grid > 0 && launch_write_runs(write_grid, wp, tile_stream, false) != cudaSuccess)
-                return PA_ERR_CUDA;
-        }
+        if (staged && cudaStreamWaitEvent(tile_stream, update.late_rows, 0) != cudaSuccess) return PA_ERR_CUDA;
+        wp.part = 2;
+        if (write_grid > 0 && launch_write_runs(write_grid, wp, tile_stream, false) != cudaSuccess)
+            return PA_ERR_CUDA;
     }
     if (P->cap_tiles > 0) {
         // E4M3: the tiles read bf16 copies of their blocks, made here

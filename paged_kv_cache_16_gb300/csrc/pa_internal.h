@@ -183,14 +183,15 @@ enum MetaCount : int {
     kCountTokens = 3,
     kCountWriteRuns = 4,     // extend rows whose new K/V the fused write kernel stores
     kCountWriteTokens = 5,   // their tokens in total
-    kCountWriteRunsEarly = 6,    // leading runs wholly below the decode prefix (staged inputs)
+    kCountWriteRunsEarly = 6,    // leading runs: the small rows' (read by the decode stream)
     kCountWriteTokensEarly = 7,  // their tokens
     kNumCounts = 8
 };
 
-// Fused cache update: the new tokens of one extend row, stored by the write
-// kernel before the tensor-core tiles read them (decode rows are stored by
-// the decode kernel itself).
+// Fused cache update: the new tokens of one small or extend row, stored by
+// the write kernel before the decode stream or the tensor-core tiles read
+// them (one-token decode rows are stored by the decode kernel itself).  The
+// small rows' runs come first.
 struct WriteRun {
     int32_t t0;          // first token row
     int32_t n_tok;       // tokens

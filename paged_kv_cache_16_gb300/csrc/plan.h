@@ -28,10 +28,10 @@ struct pa_plan_s {
     std::vector<int32_t> cta_tiles;           // their tile lists
     int32_t ext_ctas = 0;                     // grid of the tensor-core kernel
     bool fork = false;                        // tiles on a second stream, beside the decode kernel
-    std::vector<pa::WriteRun> write_runs;     // extend rows (fused cache update)
+    std::vector<pa::WriteRun> write_runs;     // small, then extend rows (fused cache update)
     int32_t write_tokens = 0;
     int32_t decode_prefix = 0;                // fixed shapes: decode-stream rows lie below it (0: no bound)
-    int32_t write_runs_early = 0;             // leading runs wholly below decode_prefix
+    int32_t write_runs_early = 0;             // leading runs: the small rows' (the decode stream reads them)
     int32_t write_tokens_early = 0;           // and their tokens
     std::vector<int32_t> scratch_table;       // E4M3: [rows][max_blocks] bf16 scratch block ids
     std::vector<pa::DequantItem> dequant;     // E4M3: blocks to expand each call
