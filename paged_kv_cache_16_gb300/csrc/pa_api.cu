@@ -477,10 +477,17 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
                 P->tiles.push_back(t);
             }
     }
-    // longest key ranges first: the last wave is made of short tiles
-    std::stable_sort(P->tiles.begin(), P->tiles.end(), [](const ExtendTile &a, const ExtendTile &b) {
-        return (a.key_end - a.key_begin) > (b.key_end - b.key_begin);
-    });
+    // longest key ranges first: the last wave is made of short tiles (a
+    // stable order: keys (INT32_MAX - range, index) sorted, then one move)
+    {
+        std::vector<uint64_t> key(P->tiles.size());
+        for (size_t i = 0; i < key.size(); ++i)
+            key[i] = (static_cast<uint64_t>(INT32_MAX - (P->tiles[i].key_end - P->tiles[i].key_begin)) << 32) | i;
+        std::sort(key.begin(), key.end());
+        std::vector<ExtendTile> sorted(key.size());
+        for (size_t i = 0; i < key.size(); ++i) sorted[i] = P->tiles[static_cast<uint32_t>(key[i])];
+        P->tiles.swap(sorted);
+    }
 
     // E4M3 caches: the tiles read bf16 copies of the blocks they touch, one
     // scratch block-table row per request the tiles read through
@@ -608,24 +615,39 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
         P->cta_tile_begin.assign(static_cast<size_t>(P->ext_ctas) + 1, 0);
         P->cta_tiles.clear();
         if (P->ext_ctas > 0 && have_tiles) {
-            std::stable_sort(cost.begin(), cost.end(),
-                             [](const std::pair<int64_t, int32_t> &a, const std::pair<int64_t, int32_t> &b) {
-                                 return a.first > b.first;
-                             });
-            using Load = std::pair<int64_t, int32_t>;   // (work so far, CTA)
-            std::vector<Load> heap_store;
-            heap_store.reserve(static_cast<size_t>(tile_work_ctas));
-            std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap(std::greater<Load>(),
-                                                                                 std::move(heap_store));
-            for (int32_t c = 0; c < tile_work_ctas; ++c) heap.push({0, c});
+            // costs in descending order, equal costs by index (stable)
+            std::vector<uint64_t> order(cost.size());
+            for (size_t k = 0; k < cost.size(); ++k)
+                order[k] = (static_cast<uint64_t>(INT32_MAX - cost[k].first) << 32) | static_cast<uint32_t>(k);
+            std::sort(order.begin(), order.end());
+            // min-heap of (work so far, CTA) packed as work << 32 | CTA (the
+            // work of all tiles, in steps, is far below 2^32)
+            if (model.tile_units >= 4294967296.0) return PA_ERR_UNSUPPORTED;
+            std::vector<uint64_t> heap(static_cast<size_t>(tile_work_ctas));
+            for (int32_t c = 0; c < tile_work_ctas; ++c) heap[static_cast<size_t>(c)] = static_cast<uint64_t>(c);
             std::vector<int32_t> cta_of(cost.size());
+            std::vector<std::pair<int64_t, int32_t>> by_cost(cost.size());
             for (size_t k = 0; k < cost.size(); ++k) {
-                Load ld = heap.top();
-                heap.pop();
-                cta_of[k] = ld.second;
-                ++P->cta_tile_begin[static_cast<size_t>(ld.second) + 1];
-                heap.push({ld.first + cost[k].first, ld.second});
+                by_cost[k] = cost[static_cast<uint32_t>(order[k])];
+                const uint64_t top = heap.front();   // least loaded, lowest index among equals
+                const int32_t c = static_cast<int32_t>(top & 0xFFFFFFFFu);
+                cta_of[k] = c;
+                ++P->cta_tile_begin[static_cast<size_t>(c) + 1];
+                // replace the root and sift it down
+                const uint64_t v = top + (static_cast<uint64_t>(by_cost[k].first) << 32);
+                size_t i = 0;
+                const size_t n = heap.size();
+                for (;;) {
+                    size_t l = 2 * i + 1;
+                    if (l >= n) break;
+                    if (l + 1 < n && heap[l + 1] < heap[l]) ++l;
+                    if (heap[l] >= v) break;
+                    heap[i] = heap[l];
+                    i = l;
+                }
+                heap[i] = v;
             }
+            cost.swap(by_cost);
             for (size_t c = 1; c < P->cta_tile_begin.size(); ++c) P->cta_tile_begin[c] += P->cta_tile_begin[c - 1];
             P->cta_tiles.resize(cost.size());
             std::vector<int32_t> pos(P->cta_tile_begin.begin(), P->cta_tile_begin.end() - 1);
