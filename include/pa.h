@@ -554,7 +554,15 @@ typedef struct {
      * kernels store the output rows straight into host_out[i] through its
      * device mapping, during the step (device `out` is then not written);
      * with a smaller out_bytes, out (out_bytes from its start) is copied to
-     * host_out[i] (page-locked HOST) at the end of graph i. */
+     * host_out[i] (page-locked HOST) at the end of graph i.
+     * Staged (fused, shape.decode_prefix_tokens = P with 0 < P < max_tokens,
+     * and q, key, value inside device_in): the image is copied in two parts,
+     * everything but rows P.. of q, key and value first and those rows after
+     * it on a second stream, through pa_attention_with_kv_update_launch_
+     * staged, so the decode stream starts after the first part; with a
+     * whole-output host buffer, out is written on the device and rows
+     * P..max_tokens are copied back as soon as the tiles are done, rows
+     * [0, P) after the step (no direct stores). */
     const void *host_in[2];
     void *device_in;
     size_t in_bytes;
