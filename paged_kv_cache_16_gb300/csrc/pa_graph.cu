@@ -176,19 +176,22 @@ pa_status capture(pa_graph_s *g, int i) {
     if (cudaStreamBeginCapture(g->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return PA_ERR_CUDA;
     pa_status st = PA_OK;
     // one copy each way (splitting them over parallel streams measured
-    // slower), or, staged, the early part and then the late rows
+    // slower), or, staged, the early part and the metadata upload (which
+    // reads its image over the same host link) and only then the late rows
     if (g->staged) {
-        if (copy_ranges(g->early, b.device_in, b.host_in[i], g->cap) != cudaSuccess ||
-            cudaEventRecord(g->early_in, g->cap) != cudaSuccess ||
-            cudaStreamWaitEvent(g->cap_late, g->early_in, 0) != cudaSuccess ||
-            copy_ranges(g->late, b.device_in, b.host_in[i], g->cap_late) != cudaSuccess ||
-            cudaEventRecord(g->late_in, g->cap_late) != cudaSuccess)
+        if (copy_ranges(g->early, b.device_in, b.host_in[i], g->cap) != cudaSuccess) st = PA_ERR_CUDA;
+        if (st == PA_OK) st = pa_upload_metadata_from(g->image[i], g->image_bytes, g->workspace, g->ws_bytes, g->cap);
+        if (st == PA_OK && (cudaEventRecord(g->early_in, g->cap) != cudaSuccess ||
+                            cudaStreamWaitEvent(g->cap_late, g->early_in, 0) != cudaSuccess ||
+                            copy_ranges(g->late, b.device_in, b.host_in[i], g->cap_late) != cudaSuccess ||
+                            cudaEventRecord(g->late_in, g->cap_late) != cudaSuccess))
             st = PA_ERR_CUDA;
-    } else if (b.in_bytes && cudaMemcpyAsync(b.device_in, b.host_in[i], b.in_bytes, cudaMemcpyHostToDevice,
-                                             g->cap) != cudaSuccess) {
-        st = PA_ERR_CUDA;
+    } else {
+        if (b.in_bytes && cudaMemcpyAsync(b.device_in, b.host_in[i], b.in_bytes, cudaMemcpyHostToDevice, g->cap) !=
+                              cudaSuccess)
+            st = PA_ERR_CUDA;
+        if (st == PA_OK) st = pa_upload_metadata_from(g->image[i], g->image_bytes, g->workspace, g->ws_bytes, g->cap);
     }
-    if (st == PA_OK) st = pa_upload_metadata_from(g->image[i], g->image_bytes, g->workspace, g->ws_bytes, g->cap);
     void *direct = direct_host_out(g, i);
     void *out = direct ? direct : b.out;
     // staged with a whole-output host buffer: the rows from the prefix on are
