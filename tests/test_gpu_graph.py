@@ -324,6 +324,19 @@ def test_native_graph_staged_host_io(kv):
                  max_extend_tiles=64, max_dequant_blocks=256 if kv == "fp8" else 0, decode_prefix_tokens=16)
 
 
+def test_native_graph_staged_cascade():
+    """Cascade steps (decode rows only, all below the decode prefix) through a
+    staged host-I/O graph: the prefix tiles wait for the late copy on the
+    library stream and the merge of prefix and suffix partials (rows below
+    the prefix) runs after the join."""
+    steps = []
+    for i, (n, nb) in enumerate(((24, 16), (9, 8))):
+        steps.append(replace(workloads.cascade(batch=n, prefix_tokens=16 * nb, lo=1, hi=200, num_blocks=700,
+                                               seed=80 + i), name=f"staged-cascade-step{i}"))
+    native_steps(steps, True, True, own_pool=True, eager_exact=False, max_tokens=32, max_reqs=24,
+                 max_extend_tiles=256, max_partial_slots=32 * 160, decode_prefix_tokens=24)
+
+
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
 def test_staged_launch_waits_for_late_rows(kv):
     """pa_attention_with_kv_update_launch_staged with rows 16.. copied in on
