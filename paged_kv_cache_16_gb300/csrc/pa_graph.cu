@@ -140,15 +140,17 @@ void plan_staging(pa_graph_s *g) {
     const size_t dq = static_cast<size_t>(g->model.num_heads_q) * g->model.head_dim * 2;
     const size_t dkv = static_cast<size_t>(g->model.num_heads_kv) * g->model.head_dim * 2;
     const uintptr_t base = reinterpret_cast<uintptr_t>(b.device_in);
-    std::vector<std::pair<size_t, size_t>> late;
+    std::vector<std::pair<size_t, size_t>> span, late;
     for (const auto &buf : {std::make_pair(b.q, dq), std::make_pair(b.key, dkv), std::make_pair(b.value, dkv)}) {
         const uintptr_t p = reinterpret_cast<uintptr_t>(buf.first);
         if (p < base || p + buf.second * T > base + b.in_bytes) return;   // not inside the image: one copy
+        span.emplace_back(p - base, p - base + buf.second * T);
         late.emplace_back(p - base + buf.second * P, p - base + buf.second * T);
     }
+    std::sort(span.begin(), span.end());
+    for (size_t k = 1; k < span.size(); ++k)
+        if (span[k].first < span[k - 1].second) return;                  // overlapping buffers: one copy
     std::sort(late.begin(), late.end());
-    for (size_t k = 1; k < late.size(); ++k)
-        if (late[k].first < late[k - 1].second) return;                  // overlapping buffers: one copy
     size_t at = 0;
     for (const auto &r : late) {
         if (r.first > at) g->early.emplace_back(at, r.first);
