@@ -659,7 +659,7 @@ pa_status build_plan(pa_plan_s *P, const pa_batch_desc *d, const pa_fixed_shape 
     std::vector<int32_t> pieces, item_unit;
     plan_decode(P, units, pieces, item_unit, decode_work_ctas, P->fixed ? static_cast<int64_t>(P->num_sms) * cps : 0);
 
-    // ------------------------------- fused cache update of extend rows
+    // ----------------------- fused cache update of small and extend rows
     // the small rows (read by the decode stream) first, then the extend rows
     // (read by the tiles only), each in token order
     std::vector<int32_t> multi_rows(small_rows);
@@ -962,10 +962,11 @@ pa_status enqueue_attention(pa_plan_s *P, const void *q, const void *key_cache, 
             launch_write_runs(write_grid, wp, stream) != cudaSuccess)
             return PA_ERR_CUDA;
     }
-    // Side by side: the tiles (and, for E4M3 caches, the bf16 copies of their
-    // blocks) go to a second stream that starts after everything enqueued so
-    // far (metadata upload, write of the extend rows), while the decode kernel
-    // runs on the other SMs; the merge waits for both.
+    // Side by side: the write of the extend rows, the tiles (and, for E4M3
+    // caches, the bf16 copies of their blocks) go to a second stream that
+    // starts after everything enqueued so far (metadata upload, write of the
+    // small rows), while the decode kernel runs on the other SMs; the merge
+    // waits for both.
     cudaStream_t tile_stream = stream;
     SideStream *side = nullptr;
     if (fork) {
