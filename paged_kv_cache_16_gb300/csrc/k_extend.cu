@@ -516,22 +516,28 @@ extend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 tmem_wait_ld();
                 if (!tok_valid) continue;
                 if (tile.part < 0) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + (static_cast<int64_t>(tok) * p.num_heads_q + h) * D + c);
+                    uint16_t *dst = p.out + (static_cast<int64_t>(tok) * p.num_heads_q + h) * D + c;
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(orr[q4 * 8 + 0]) * inv, __uint_as_float(orr[q4 * 8 + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(orr[q4 * 8 + 2]) * inv, __uint_as_float(orr[q4 * 8 + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(orr[q4 * 8 + 4]) * inv, __uint_as_float(orr[q4 * 8 + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(orr[q4 * 8 + 6]) * inv, __uint_as_float(orr[q4 * 8 + 7]) * inv);
-                        dst[q4] = w;
+                    for (int q8 = 0; q8 < 2; ++q8) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            w[e] = pack_bf16x2(__uint_as_float(orr[q8 * 16 + 2 * e]) * inv,
+                                               __uint_as_float(orr[q8 * 16 + 2 * e + 1]) * inv);
+                        st_global_v8(dst + q8 * 16, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
                     }
                 } else {
-                    float4 *dst = reinterpret_cast<float4 *>(p.o_part + (slot * p.num_heads_q + h) * D + c);
+                    float *dst = p.o_part + (slot * p.num_heads_q + h) * D + c;
 #pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4)
-                        dst[q4] = make_float4(__uint_as_float(orr[q4 * 4 + 0]) * inv, __uint_as_float(orr[q4 * 4 + 1]) * inv,
-                                              __uint_as_float(orr[q4 * 4 + 2]) * inv, __uint_as_float(orr[q4 * 4 + 3]) * inv);
+                    for (int q8 = 0; q8 < 4; ++q8)
+                        st_global_v8(dst + q8 * 8, __float_as_uint(__uint_as_float(orr[q8 * 8 + 0]) * inv),
+                                     __float_as_uint(__uint_as_float(orr[q8 * 8 + 1]) * inv),
+                                     __float_as_uint(__uint_as_float(orr[q8 * 8 + 2]) * inv),
+                                     __float_as_uint(__uint_as_float(orr[q8 * 8 + 3]) * inv),
+                                     __float_as_uint(__uint_as_float(orr[q8 * 8 + 4]) * inv),
+                                     __float_as_uint(__uint_as_float(orr[q8 * 8 + 5]) * inv),
+                                     __float_as_uint(__uint_as_float(orr[q8 * 8 + 6]) * inv),
+                                     __float_as_uint(__uint_as_float(orr[q8 * 8 + 7]) * inv));
                 }
             }
             if (tok_valid && tile.part >= 0) p.ml_part[slot * p.num_heads_q + h] = make_float2(m, l);
