@@ -90,7 +90,7 @@ TRAFFIC = {
     ("decode", "decode", "bf16", "d98510bbbb11bb79"): 643_372_032,
     ("decode", "decode", "fp8", "d98510bbbb11bb79"): 323_800_832,
     ("decode", "mixed", "bf16", "d98510bbbb11bb79"): 4_686_585_600,
-    ("extend", "prefill", "bf16", "e69a77fd500c5bc0"): 73_888_256,
+    ("extend", "prefill", "bf16", "8be8aea7e2cb901b"): 76_740_864,
 }
 KERNEL_SOURCES = {"decode": "paged_kv_cache_16_gb300/csrc/k_decode.cu",
                   "extend": "paged_kv_cache_16_gb300/csrc/k_extend.cu"}
