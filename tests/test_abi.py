@@ -332,6 +332,23 @@ def test_fixed_plan_decode_prefix(lib):
     assert binding.pa_plan_fixed_status(**shape, **desc(late)) == binding.PA_OK
 
 
+def test_fixed_plan_decode_prefix_moves_the_split(lib):
+    """With staged inputs the tiles start after the late rows' copy, so the
+    planner gives them more SMs (and the decode stream fewer) than for the
+    same step with every input resident; the decode grid stays the shape's."""
+    b = workloads.mixed()
+    kw = desc(b)
+    info = binding.pa_plan(**kw).info()
+    shape = dict(max_tokens=b.num_tokens, max_reqs=b.num_reqs, max_extend_tiles=info["num_extend_tiles"],
+                 max_partial_slots=max(info["num_partial_slots"], 1))
+    plain = binding.pa_plan_fixed(**shape, **kw).info()
+    staged = binding.pa_plan_fixed(**shape, decode_prefix_tokens=256, **kw).info()
+    assert plain["side_by_side"] == staged["side_by_side"] == 1
+    assert plain["num_extend_ctas"] == info["num_extend_ctas"]
+    assert staged["num_extend_ctas"] > plain["num_extend_ctas"]
+    assert staged["num_decode_ctas"] == plain["num_decode_ctas"]
+
+
 def test_fixed_plan_decode_prefix_no_merged_late_rows(lib):
     """Rows from the decode prefix on must be final when the tiles finish: a
     cascade step with a chunk row (whose rows are merged from prefix and
