@@ -91,6 +91,16 @@ TRAFFIC = {
     ("decode", "decode", "fp8", "d98510bbbb11bb79"): 323_800_832,
     ("decode", "mixed", "bf16", "d98510bbbb11bb79"): 4_686_585_600,
     ("extend", "prefill", "bf16", "8be8aea7e2cb901b"): 76_740_864,
+    # profiles/dram_traffic_decode-and-extend_per-workload.md
+    ("decode", "long", "bf16", "d98510bbbb11bb79"): 4_299_878_400,
+    ("decode", "long", "fp8", "d98510bbbb11bb79"): 2_150_972_416,
+    ("decode", "cascade", "bf16", "d98510bbbb11bb79"): 316_145_408,
+    ("extend", "cascade", "bf16", "8be8aea7e2cb901b"): 17_895_424,
+    ("decode", "cascade-off", "bf16", "d98510bbbb11bb79"): 334_178_560,
+    ("decode", "verify", "bf16", "d98510bbbb11bb79"): 674_436_608,
+    ("decode", "verify", "fp8", "d98510bbbb11bb79"): 341_064_704,
+    ("decode", "mixed", "fp8", "d98510bbbb11bb79"): 2_336_910_080,
+    ("extend", "mixed", "bf16", "8be8aea7e2cb901b"): 78_454_272,
 }
 KERNEL_SOURCES = {"decode": "paged_kv_cache_16_gb300/csrc/k_decode.cu",
                   "extend": "paged_kv_cache_16_gb300/csrc/k_extend.cu"}
